@@ -1,0 +1,588 @@
+/*
+ * oracle.c -- plain CPU reference of the DSA lightning-indexer hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's CPU-baseline
+ * leg are its only users; the product path never calls it. It shares no code with the
+ * CUDA library. Build: C11, -O2 -ffp-contract=off, no fast-math, so that every float
+ * operation below is one correctly rounded IEEE binary32 operation, in the order written.
+ *
+ * What it computes, and where the pages define it:
+ *   K store   -- LayerNorm -> RoPE on dims 0..63 -> MXFP4 (4 blocks of 32 e2m1 + one
+ *                E8M0 scale each, 68 B/token) or FP8 e4m3 + per-token fp32 scale
+ *                (132 B/token), written to slot_mapping[row] of a paged pool.
+ *                [P3] "Purpose", the five pre-processing steps (LayerNorm on k; RoPE on
+ *                the leading rope dims; FP8 quantisation of k plus the paged cache write);
+ *                [P2] "Purpose" (68 B vs 132 B per token) and "Changes / K write".
+ *   Q quant   -- RoPE -> MXFP4, or per-token-group (group 128) FP8 with the q scale folded
+ *                into the head weights; softmax and head scales folded into fp32 weights.
+ *                [P2] "Changes / Q quant"; [P3] "Purpose" steps 2-4.
+ *   Scorer    -- logits[t,s] = sum_h w[t,h] * ReLU(q[t,h] . k[s]) over the dequantised
+ *                operands, K read through the page table. [P1] "Purpose" and
+ *                "Performance and accuracy" (scores compared with the exact FP4-dequant
+ *                reference); [P2] "Purpose" (in-place paged scoring, no gather).
+ *   Top-k     -- per query, indices of the k largest logits among its visible keys.
+ *                [P2] "Test Result / GPQA Diamond" (sparse selection of top-k 1024 once
+ *                the context passes top-k x compress ratio).
+ *
+ * Readings taken where the pages are silent (each is repeated at its function):
+ *   R1 no bf16 rounding between norm, RoPE and quantisation (fp32 throughout);
+ *   R2 LayerNorm: biased variance, rstd = 1/sqrt(var+eps) correctly rounded, a fixed
+ *      summation tree (16 groups of 8, xor-butterfly 8,4,2,1);
+ *   R3 MX block scale: E = floor(log2 amax) - 2 from the exponent bits, clamped to
+ *      [-127,127]; amax == 0 gives E = -127 (scale byte 0);
+ *   R4 e2m1 sign follows the input sign bit (a negative that rounds to 0 gives code 0x8);
+ *   R5 FP8 scale = max(amax, 1e-10) / 448 in fp32, elements x / scale, RNE, saturate;
+ *   R6 folded weight constant c = fp32(softmax_scale * head_scale), rounded once;
+ *   R7 scoring in fp64 on dequantised operands (exact for these formats);
+ *   R8 top-k: the selected set is unordered; ties broken by lower index here, and the
+ *      tests accept any set that differs only within tolerance of the k-th value.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+
+static float bits_to_f32(uint32_t u) {
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+static uint32_t f32_to_bits(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return u;
+}
+static float bf16_to_f32(uint16_t b) { return bits_to_f32((uint32_t)b << 16); }
+
+/* ------------------------------------------------------------------------------------ */
+/* Element encoders                                                                     */
+/* ------------------------------------------------------------------------------------ */
+
+/* e2m1 magnitudes by code 0..7 (OCP MX FP4: 1 sign, 2 exponent, 1 mantissa bit). */
+static const double kE2M1[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+/* Nearest e2m1 value to v, ties to the even code; anything beyond 6 is nearest to 6,
+ * which is the saturating rule. Sign bit copied from v (reading R4). */
+uint8_t orc_e2m1_encode(float v) {
+    double a = fabs((double)v);
+    int best = 0;
+    double bd = a;
+    for (int c = 1; c < 8; ++c) {
+        double d = fabs(a - kE2M1[c]);
+        if (d < bd || (d == bd && (c & 1) == 0)) {
+            best = c;
+            bd = d;
+        }
+    }
+    return (uint8_t)(best | (signbit(v) ? 8 : 0));
+}
+
+double orc_e2m1_decode(uint8_t code) {
+    double m = kE2M1[code & 7];
+    return (code & 8) ? -m : m;
+}
+
+/* e4m3 "fn" (bias 7, no infinities, 0x7F is NaN, largest finite 448). */
+double orc_e4m3_decode(uint8_t code) {
+    int e = (code >> 3) & 15, m = code & 7;
+    double v = (e == 0) ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return (code & 0x80) ? -v : v;
+}
+
+/* Nearest finite e4m3 value to v (binary search over codes 0x00..0x7E, whose values
+ * increase with the code), ties to the even code; beyond 448 the nearest is 448. */
+uint8_t orc_e4m3_encode(float v) {
+    double a = fabs((double)v);
+    int lo = 0, hi = 0x7E;
+    if (a >= orc_e4m3_decode(0x7E)) {
+        lo = 0x7E;
+    } else {
+        while (hi - lo > 1) { /* invariant: value(lo) <= a < value(hi) */
+            int mid = (lo + hi) / 2;
+            if (orc_e4m3_decode((uint8_t)mid) <= a) lo = mid; else hi = mid;
+        }
+        double dl = a - orc_e4m3_decode((uint8_t)lo), dh = orc_e4m3_decode((uint8_t)hi) - a;
+        if (dh < dl || (dh == dl && (hi & 1) == 0)) lo = hi;
+    }
+    return (uint8_t)(lo | (signbit(v) ? 0x80 : 0));
+}
+
+/* OCP MX shared exponent for a block (reading R3): floor(log2 amax) - 2, where the
+ * floor of log2 is read from the binary32 exponent field (subnormals by the position of
+ * the leading mantissa bit), clamped to the E8M0 range [-127, 127]. */
+int orc_mx_shared_exponent(float amax) {
+    if (amax == 0.0f) return -127;
+    uint32_t u = f32_to_bits(amax) & 0x7fffffffu;
+    int ef = (int)(u >> 23), fl;
+    if (ef > 0) {
+        fl = ef - 127;
+    } else {
+        int msb = 31;
+        while (!((u >> msb) & 1u)) --msb;
+        fl = msb - 149;
+    }
+    int E = fl - 2;
+    if (E < -127) E = -127;
+    if (E > 127) E = 127;
+    return E;
+}
+
+void orc_e2m1_encode_n(const float* v, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_e2m1_encode(v[i]);
+}
+
+void orc_e4m3_encode_n(const float* v, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_encode(v[i]);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Row steps                                                                            */
+/* ------------------------------------------------------------------------------------ */
+
+/* Fixed summation tree over 128 values (reading R2): 16 groups of 8 consecutive values,
+ * each ((e0+e1)+(e2+e3))+((e4+e5)+(e6+e7)); then four butterfly rounds g_j <- g_j +
+ * g_{j xor off} for off = 8, 4, 2, 1; the result is g_0 (all g_j are equal). */
+static float tree_sum128(const float* v) {
+    float g[16], n[16];
+    for (int j = 0; j < 16; ++j) {
+        const float* e = v + 8 * j;
+        float a = e[0] + e[1];
+        float b = e[2] + e[3];
+        float c = e[4] + e[5];
+        float d = e[6] + e[7];
+        float ab = a + b;
+        float cd = c + d;
+        g[j] = ab + cd;
+    }
+    for (int off = 8; off >= 1; off >>= 1) {
+        for (int j = 0; j < 16; ++j) n[j] = g[j] + g[j ^ off];
+        memcpy(g, n, sizeof g);
+    }
+    return g[0];
+}
+
+/* LayerNorm over D = 128 ([P3] "Purpose", step 1 "LayerNorm on k"), reading R2:
+ * mean = S(x)/128; d = x - mean; var = S(d*d)/128 (biased); rstd = 1/sqrt(var + eps);
+ * y = (d*rstd)*gamma + beta; every operation rounded separately. */
+void orc_layernorm128(const float* x, const float* gamma, const float* beta, float eps,
+                      float* y) {
+    const float inv_d = 0.0078125f; /* 1/128, exact */
+    float mean = tree_sum128(x) * inv_d;
+    float d[128], sq[128];
+    for (int i = 0; i < 128; ++i) {
+        d[i] = x[i] - mean;
+        sq[i] = d[i] * d[i];
+    }
+    float var = tree_sum128(sq) * inv_d;
+    float t = var + eps;
+    float s = sqrtf(t);
+    float rstd = 1.0f / s;
+    for (int i = 0; i < 128; ++i) {
+        float a = d[i] * rstd;
+        float b = a * gamma[i];
+        y[i] = b + beta[i];
+    }
+}
+
+/* RoPE on the leading 64 dims ([P3] "Purpose", step 2; "Test Plan / Op test" lists both
+ * the NeoX and the interleaved pairing). cos_sin_row = [cos f_0..f_31, sin f_0..f_31] for
+ * this position. Pair i rotates (a, b) -> (a*c - b*s, b*c + a*s); NeoX pairs dims
+ * (i, i+32), interleaved pairs (2i, 2i+1). Dims 64..127 pass through. */
+void orc_rope128(float* x, const float* cos_sin_row, int mode) {
+    if (mode == ORC_ROPE_NONE) return;
+    for (int i = 0; i < 32; ++i) {
+        int ia = (mode == ORC_ROPE_NEOX) ? i : 2 * i;
+        int ib = (mode == ORC_ROPE_NEOX) ? i + 32 : 2 * i + 1;
+        float a = x[ia], b = x[ib];
+        float c = cos_sin_row[i], s = cos_sin_row[32 + i];
+        float ac = a * c, bs = b * s, bc = b * c, as = a * s;
+        x[ia] = ac - bs;
+        x[ib] = bc + as;
+    }
+}
+
+/* MXFP4 quantisation of one 128-value row: four blocks of 32 share one E8M0 scale
+ * ([P2] "Purpose": 68 B per token = 64 B of e2m1 codes + 4 scale bytes). Per block:
+ * E = orc_mx_shared_exponent(max |x|); scale byte = E + 127; element v = x * 2^-E
+ * (one rounded multiply) encoded by orc_e2m1_encode. Packing: byte j holds element 2j in
+ * its low nibble and element 2j+1 in its high nibble. */
+void orc_mxfp4_quant128(const float* x, uint8_t* codes64, uint8_t* scales4) {
+    for (int b = 0; b < 4; ++b) {
+        float amax = 0.0f;
+        for (int i = 0; i < 32; ++i) {
+            float a = fabsf(x[32 * b + i]);
+            if (a > amax) amax = a;
+        }
+        int E = orc_mx_shared_exponent(amax);
+        scales4[b] = (uint8_t)(E + 127);
+        float inv = (float)ldexp(1.0, -E); /* 2^-E, exactly representable for E in range */
+        for (int i = 0; i < 32; i += 2) {
+            float v0 = x[32 * b + i] * inv;
+            float v1 = x[32 * b + i + 1] * inv;
+            uint8_t c0 = orc_e2m1_encode(v0), c1 = orc_e2m1_encode(v1);
+            codes64[(32 * b + i) / 2] = (uint8_t)(c0 | (c1 << 4));
+        }
+    }
+}
+
+/* FP8 e4m3 quantisation with one fp32 scale per 128 values (reading R5):
+ * scale = max(amax, 1e-10) / 448; code_i = e4m3(x_i / scale). */
+void orc_fp8_quant128(const float* x, uint8_t* codes128, float* scale) {
+    float amax = 0.0f;
+    for (int i = 0; i < 128; ++i) {
+        float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    float m = amax > 1e-10f ? amax : 1e-10f;
+    float s = m / 448.0f;
+    for (int i = 0; i < 128; ++i) {
+        float v = x[i] / s;
+        codes128[i] = orc_e4m3_encode(v);
+    }
+    *scale = s;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Page layout (this library's own choice; the pages fix only the bytes per token)      */
+/* ------------------------------------------------------------------------------------ */
+/*
+ * MXFP4 page of P tokens: [64*P code bytes][4*P scale bytes], 68*P bytes in all.
+ *   Token s's 64 code bytes are four 16-byte chunks; chunk c holds scale block c
+ *   (elements 32c..32c+31), byte i of the chunk holds elements 32c+2i (low nibble) and
+ *   32c+2i+1 (high nibble).
+ *   P = 128: chunk (s, c) at ((s/8)*4 + c)*128 + (s%8)*16.
+ *            scale (s, b) at 8192 + (s%32)*16 + (s/32)*4 + b.
+ *   P =  64: chunk (s, c) at (s/16)*1024 + ((s/8)%2)*512 + c*128 + (s%8)*16.
+ *            scale (s, b) at 4096 + (s%16)*16 + (s/16)*4 + b.
+ * FP8 page of P tokens: [128*P code bytes][P fp32 scales], 132*P bytes in all.
+ *   element j of token s at (s/8)*1024 + (j/16)*128 + (s%8)*16 + (j%16);
+ *   scale of token s at 128*P + 4*s.
+ */
+int64_t orc_page_bytes(int dtype, int page_size) {
+    return (int64_t)(dtype == ORC_MXFP4 ? 68 : 132) * page_size;
+}
+
+int64_t orc_code_offset(int dtype, int page_size, int s, int j) {
+    if (dtype == ORC_FP8) return (int64_t)(s / 8) * 1024 + (j / 16) * 128 + (s % 8) * 16 + (j % 16);
+    int c = j / 16, i = j % 16;
+    if (page_size == 128) return (int64_t)((s / 8) * 4 + c) * 128 + (s % 8) * 16 + i;
+    return (int64_t)(s / 16) * 1024 + ((s / 8) % 2) * 512 + c * 128 + (s % 8) * 16 + i;
+}
+
+int64_t orc_scale_offset(int dtype, int page_size, int s, int b) {
+    if (dtype == ORC_FP8) return (int64_t)128 * page_size + 4 * s;
+    if (page_size == 128) return 8192 + (s % 32) * 16 + (s / 32) * 4 + b;
+    return 4096 + (s % 16) * 16 + (s / 16) * 4 + b;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* K store                                                                              */
+/* ------------------------------------------------------------------------------------ */
+
+/* Per row: bf16 -> fp32, optional LayerNorm, optional RoPE at positions[row], quantise,
+ * write to slot = slot_mapping[row] (page slot/P, in-page token slot%P). Rows with a
+ * negative slot are skipped ([P3] "Purpose": slot_mapping is PAD_SLOT_ID on rows the
+ * kernel must skip). Returns the number of rows rejected for an out-of-range slot or
+ * position (those rows are not written). */
+int orc_k_store(const uint16_t* k, int64_t n_rows, int64_t k_row_stride,
+                const int64_t* slot_mapping, const int32_t* positions,
+                const float* cos_sin, int32_t max_pos, int rope, int apply_norm,
+                const float* gamma, const float* beta, float eps, int dtype,
+                uint8_t* pool, int64_t num_pages, int32_t page_size, int64_t page_stride) {
+    int bad = 0;
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int64_t slot = slot_mapping[r];
+        if (slot < 0) continue;
+        int64_t page = slot / page_size;
+        int s = (int)(slot % page_size);
+        if (page >= num_pages) { ++bad; continue; }
+        float x[128], y[128];
+        for (int i = 0; i < 128; ++i) x[i] = bf16_to_f32(k[r * k_row_stride + i]);
+        if (apply_norm) {
+            orc_layernorm128(x, gamma, beta, eps, y);
+            memcpy(x, y, sizeof x);
+        }
+        if (rope != ORC_ROPE_NONE) {
+            int32_t pos = positions[r];
+            if (pos < 0 || pos >= max_pos) { ++bad; continue; }
+            orc_rope128(x, cos_sin + (int64_t)pos * 64, rope);
+        }
+        uint8_t* base = pool + page * page_stride;
+        if (dtype == ORC_MXFP4) {
+            uint8_t codes[64], sc[4];
+            orc_mxfp4_quant128(x, codes, sc);
+            for (int j = 0; j < 64; ++j) base[orc_code_offset(dtype, page_size, s, j)] = codes[j];
+            for (int b = 0; b < 4; ++b) base[orc_scale_offset(dtype, page_size, s, b)] = sc[b];
+        } else {
+            uint8_t codes[128];
+            float sc;
+            orc_fp8_quant128(x, codes, &sc);
+            for (int j = 0; j < 128; ++j) base[orc_code_offset(dtype, page_size, s, j)] = codes[j];
+            memcpy(base + orc_scale_offset(dtype, page_size, s, 0), &sc, 4);
+        }
+    }
+    return bad;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Q quant                                                                              */
+/* ------------------------------------------------------------------------------------ */
+
+/* Per (t, h) row of q [T][H][128]: bf16 -> fp32, RoPE at positions[t], quantise.
+ * MXFP4: q_codes [T][H][64] (packed as in orc_mxfp4_quant128), q_scales [T][H][4] E8M0,
+ *        w_out[t,h] = w_in[t,h] * c.
+ * FP8:   q_codes [T][H][128] e4m3, q_scales (optional) [T][H] fp32,
+ *        w_out[t,h] = (w_in[t,h] * c) * q_scale[t,h]  ([P3] "Purpose" step 4, the fold
+ *        of the q scale into the indexer weights).
+ * c = fp32(softmax_scale * head_scale), the product rounded once (reading R6;
+ * [P2] "Changes / Q quant": fp32 weights with softmax and head scales folded in).
+ * Returns the number of rows with an out-of-range position (left unwritten). */
+int orc_q_quant(const uint16_t* q, int64_t T, int32_t H, const int32_t* positions,
+                const float* cos_sin, int32_t max_pos, int rope, const float* w_in,
+                float softmax_scale, float head_scale, int dtype, uint8_t* q_codes,
+                uint8_t* q_scales, float* w_out) {
+    int bad = 0;
+    float c = (float)((double)softmax_scale * (double)head_scale);
+    for (int64_t t = 0; t < T; ++t) {
+        int32_t pos = positions ? positions[t] : 0;
+        if (rope != ORC_ROPE_NONE && (pos < 0 || pos >= max_pos)) { bad += H; continue; }
+        for (int h = 0; h < H; ++h) {
+            int64_t row = t * H + h;
+            float x[128];
+            for (int i = 0; i < 128; ++i) x[i] = bf16_to_f32(q[row * 128 + i]);
+            if (rope != ORC_ROPE_NONE) orc_rope128(x, cos_sin + (int64_t)pos * 64, rope);
+            float wc = w_in[row] * c;
+            if (dtype == ORC_MXFP4) {
+                orc_mxfp4_quant128(x, q_codes + row * 64, q_scales + row * 4);
+                w_out[row] = wc;
+            } else {
+                float sc;
+                orc_fp8_quant128(x, q_codes + row * 128, &sc);
+                if (q_scales) memcpy(q_scales + row * 4, &sc, 4);
+                w_out[row] = wc * sc;
+            }
+        }
+    }
+    return bad;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Scorer                                                                               */
+/* ------------------------------------------------------------------------------------ */
+
+/* Keys visible to query t. Query t is the i-th of n_q queries of sequence b
+ * (cu_seqlens_q[b] <= t < cu_seqlens_q[b+1]); causal: the queries are the last n_q
+ * tokens of the sequence, so query i sees keys 0 .. seq_lens_k[b] - n_q + i;
+ * otherwise it sees all seq_lens_k[b] keys. */
+int64_t orc_visible(int64_t t, const int32_t* seq_lens_k, const int32_t* cu_seqlens_q,
+                    int32_t B, int causal) {
+    for (int32_t b = 0; b < B; ++b) {
+        if (t >= cu_seqlens_q[b] && t < cu_seqlens_q[b + 1]) {
+            int64_t nq = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+            int64_t i = t - cu_seqlens_q[b];
+            int64_t v = causal ? (int64_t)seq_lens_k[b] - nq + i + 1 : seq_lens_k[b];
+            if (v < 0) v = 0;
+            if (v > seq_lens_k[b]) v = seq_lens_k[b];
+            return v;
+        }
+    }
+    return -1;
+}
+
+static int32_t seq_of(int64_t t, const int32_t* cu_seqlens_q, int32_t B) {
+    for (int32_t b = 0; b < B; ++b)
+        if (t >= cu_seqlens_q[b] && t < cu_seqlens_q[b + 1]) return b;
+    return -1;
+}
+
+/* Dequantised key row (in fp64) of token s of sequence b, read through the page table. */
+static void dequant_k(const uint8_t* pool, int dtype, int32_t P, int64_t page_stride,
+                      const int32_t* page_table, int32_t pt_stride, int32_t b, int64_t s,
+                      double* kd, double* kscale) {
+    int32_t page = page_table[(int64_t)b * pt_stride + s / P];
+    const uint8_t* base = pool + (int64_t)page * page_stride;
+    int r = (int)(s % P);
+    if (dtype == ORC_MXFP4) {
+        for (int j = 0; j < 64; ++j) {
+            uint8_t byte = base[orc_code_offset(dtype, P, r, j)];
+            int blk = (2 * j) / 32;
+            double sc = ldexp(1.0, (int)base[orc_scale_offset(dtype, P, r, blk)] - 127);
+            kd[2 * j] = orc_e2m1_decode(byte & 15) * sc;
+            kd[2 * j + 1] = orc_e2m1_decode(byte >> 4) * sc;
+        }
+        *kscale = 1.0;
+    } else {
+        for (int j = 0; j < 128; ++j) kd[j] = orc_e4m3_decode(base[orc_code_offset(dtype, P, r, j)]);
+        float sc;
+        memcpy(&sc, base + orc_scale_offset(dtype, P, r, 0), 4);
+        *kscale = sc;
+    }
+}
+
+static void dequant_q(const uint8_t* q_codes, const uint8_t* q_scales, int dtype, int64_t row,
+                      double* qd) {
+    if (dtype == ORC_MXFP4) {
+        for (int j = 0; j < 64; ++j) {
+            uint8_t byte = q_codes[row * 64 + j];
+            double sc = ldexp(1.0, (int)q_scales[row * 4 + (2 * j) / 32] - 127);
+            qd[2 * j] = orc_e2m1_decode(byte & 15) * sc;
+            qd[2 * j + 1] = orc_e2m1_decode(byte >> 4) * sc;
+        }
+    } else {
+        for (int j = 0; j < 128; ++j) qd[j] = orc_e4m3_decode(q_codes[row * 128 + j]);
+    }
+}
+
+typedef struct {
+    const uint8_t *q_codes, *q_scales, *pool;
+    const float* w;
+    int64_t T;
+    int32_t H;
+    int dtype;
+    int32_t P;
+    int64_t page_stride;
+    const int32_t *page_table, *seq_lens_k, *cu_seqlens_q;
+    int32_t pt_stride, B;
+    int causal;
+    const int64_t* rows;
+    int64_t n_rows;
+    double* out;
+    int64_t ld;
+    int n_threads, tid;
+} score_job;
+
+/* One query row: for every visible key s,
+ *   logit = sum_h w[t,h] * max(q[t,h] . k[s], 0)      (MXFP4)
+ *   logit = k_scale[s] * sum_h w[t,h] * max(q[t,h] . k[s], 0)      (FP8; w carries the
+ *           q scale, and k_scale > 0 commutes with ReLU)
+ * with the dot products and the head sum in fp64 (reading R7). */
+static void *score_rows(void* arg) {
+    score_job* j = (score_job*)arg;
+    double* qd = (double*)malloc(sizeof(double) * 128 * (size_t)j->H);
+    double kd[128];
+    for (int64_t r = j->tid; r < j->n_rows; r += j->n_threads) {
+        int64_t t = j->rows ? j->rows[r] : r;
+        int32_t b = seq_of(t, j->cu_seqlens_q, j->B);
+        int64_t vis = orc_visible(t, j->seq_lens_k, j->cu_seqlens_q, j->B, j->causal);
+        if (b < 0) continue;
+        for (int h = 0; h < j->H; ++h) dequant_q(j->q_codes, j->q_scales, j->dtype, t * j->H + h, qd + 128 * h);
+        for (int64_t s = 0; s < vis; ++s) {
+            double ks;
+            dequant_k(j->pool, j->dtype, j->P, j->page_stride, j->page_table, j->pt_stride, b, s, kd, &ks);
+            double logit = 0.0;
+            for (int h = 0; h < j->H; ++h) {
+                const double* qh = qd + 128 * h;
+                double dot = 0.0;
+                for (int d = 0; d < 128; ++d) dot += qh[d] * kd[d];
+                logit += (double)j->w[t * j->H + h] * (dot > 0.0 ? dot : 0.0);
+            }
+            j->out[r * j->ld + s] = logit * ks;
+        }
+    }
+    free(qd);
+    return NULL;
+}
+
+int orc_mqa_logits(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
+                   int64_t T, int32_t H, int dtype, const uint8_t* pool, int64_t num_pages,
+                   int32_t page_size, int64_t page_stride, const int32_t* page_table,
+                   int32_t pt_stride, const int32_t* seq_lens_k, const int32_t* cu_seqlens_q,
+                   int32_t B, int causal, const int64_t* rows, int64_t n_rows, double* out,
+                   int64_t ld, int n_threads) {
+    (void)num_pages;
+    if (!rows) n_rows = T;
+    if (n_threads < 1) n_threads = 1;
+    score_job* jobs = (score_job*)calloc((size_t)n_threads, sizeof(score_job));
+    pthread_t* th = (pthread_t*)calloc((size_t)n_threads, sizeof(pthread_t));
+    for (int i = 0; i < n_threads; ++i) {
+        score_job* j = &jobs[i];
+        j->q_codes = q_codes; j->q_scales = q_scales; j->pool = pool; j->w = w;
+        j->T = T; j->H = H; j->dtype = dtype; j->P = page_size; j->page_stride = page_stride;
+        j->page_table = page_table; j->seq_lens_k = seq_lens_k; j->cu_seqlens_q = cu_seqlens_q;
+        j->pt_stride = pt_stride; j->B = B; j->causal = causal; j->rows = rows;
+        j->n_rows = n_rows; j->out = out; j->ld = ld; j->n_threads = n_threads; j->tid = i;
+    }
+    for (int i = 1; i < n_threads; ++i) pthread_create(&th[i], NULL, score_rows, &jobs[i]);
+    score_rows(&jobs[0]);
+    for (int i = 1; i < n_threads; ++i) pthread_join(th[i], NULL);
+    free(jobs);
+    free(th);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Top-k                                                                                */
+/* ------------------------------------------------------------------------------------ */
+
+typedef struct {
+    double v;
+    int32_t i;
+} vi_pair;
+
+/* (value descending, index ascending): a total order, so the sort is deterministic. */
+static int cmp_desc(const void* a, const void* b) {
+    const vi_pair *x = (const vi_pair*)a, *y = (const vi_pair*)b;
+    if (x->v > y->v) return -1;
+    if (x->v < y->v) return 1;
+    return (x->i > y->i) - (x->i < y->i);
+}
+
+typedef struct {
+    const double* logits;
+    int64_t ld;
+    const int32_t *seq_lens_k, *cu_seqlens_q;
+    int32_t B;
+    int causal;
+    const int64_t* rows;
+    int64_t n_rows;
+    int32_t k;
+    int32_t* out;
+    int n_threads, tid;
+} topk_job;
+
+/* Sort the visible logits of the row, keep the first min(k, visible) indices, pad -1. */
+static void *topk_rows(void* arg) {
+    topk_job* j = (topk_job*)arg;
+    vi_pair* buf = NULL;
+    int64_t cap = 0;
+    for (int64_t r = j->tid; r < j->n_rows; r += j->n_threads) {
+        int64_t t = j->rows ? j->rows[r] : r;
+        int64_t vis = orc_visible(t, j->seq_lens_k, j->cu_seqlens_q, j->B, j->causal);
+        if (vis < 0) vis = 0;
+        if (vis > cap) {
+            free(buf);
+            cap = vis;
+            buf = (vi_pair*)malloc(sizeof(vi_pair) * (size_t)cap);
+        }
+        for (int64_t s = 0; s < vis; ++s) {
+            buf[s].v = j->logits[r * j->ld + s];
+            buf[s].i = (int32_t)s;
+        }
+        qsort(buf, (size_t)vis, sizeof(vi_pair), cmp_desc);
+        for (int32_t q = 0; q < j->k; ++q) j->out[r * j->k + q] = (q < vis) ? buf[q].i : -1;
+    }
+    free(buf);
+    return NULL;
+}
+
+int orc_topk(const double* logits, int64_t ld, const int32_t* seq_lens_k,
+             const int32_t* cu_seqlens_q, int32_t B, int causal, const int64_t* rows,
+             int64_t n_rows, int32_t k, int32_t* out_idx, int n_threads) {
+    if (n_threads < 1) n_threads = 1;
+    topk_job* jobs = (topk_job*)calloc((size_t)n_threads, sizeof(topk_job));
+    pthread_t* th = (pthread_t*)calloc((size_t)n_threads, sizeof(pthread_t));
+    for (int i = 0; i < n_threads; ++i) {
+        topk_job* j = &jobs[i];
+        j->logits = logits; j->ld = ld; j->seq_lens_k = seq_lens_k;
+        j->cu_seqlens_q = cu_seqlens_q; j->B = B; j->causal = causal; j->rows = rows;
+        j->n_rows = n_rows; j->k = k; j->out = out_idx; j->n_threads = n_threads; j->tid = i;
+    }
+    for (int i = 1; i < n_threads; ++i) pthread_create(&th[i], NULL, topk_rows, &jobs[i]);
+    topk_rows(&jobs[0]);
+    for (int i = 1; i < n_threads; ++i) pthread_join(th[i], NULL);
+    free(jobs);
+    free(th);
+    return 0;
+}
