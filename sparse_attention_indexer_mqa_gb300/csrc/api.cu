@@ -1,0 +1,155 @@
+// api.cu -- the extern "C" entry points of idx.h: argument validation, then one launch on
+// the caller's stream. Nothing here allocates, frees or synchronises.
+#include <cmath>
+
+#include "../../include/idx.h"
+#include "kernels.h"
+
+namespace {
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline bool valid_dtype(int32_t d) { return d == IDX_MXFP4 || d == IDX_FP8; }
+inline bool valid_rope(int32_t r) {
+    return r == IDX_ROPE_NONE || r == IDX_ROPE_NEOX || r == IDX_ROPE_INTERLEAVED;
+}
+inline int64_t page_bytes(int32_t dtype, int32_t P) { return (dtype == IDX_MXFP4 ? 68 : 132) * (int64_t)P; }
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? IDX_OK : IDX_ECUDA; }
+
+// common pool checks: page size, stride, alignment
+int check_pool(int32_t dtype, const void* pool, int64_t num_pages, int32_t page_size,
+               int64_t page_stride) {
+    if (!valid_dtype(dtype)) return IDX_EINVAL;
+    if (page_size != 64 && page_size != 128) return IDX_EUNSUPPORTED;
+    if (num_pages < 0) return IDX_EINVAL;
+    if (num_pages > 0 && !pool) return IDX_EINVAL;
+    if (!aligned(pool, 16)) return IDX_EINVAL;
+    if (page_stride < page_bytes(dtype, page_size) || page_stride % 16 != 0) return IDX_EINVAL;
+    return IDX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* idx_status_string(int status) {
+    switch (status) {
+        case IDX_OK: return "ok";
+        case IDX_EINVAL: return "invalid argument";
+        case IDX_EUNSUPPORTED: return "unsupported size or mode";
+        case IDX_ECUDA: return "CUDA launch error";
+        default: return "unknown status";
+    }
+}
+
+int idx_cache_layout(int32_t dtype, int32_t page_size, idx_layout* out) {
+    if (!out || !valid_dtype(dtype)) return IDX_EINVAL;
+    if (page_size != 64 && page_size != 128) return IDX_EUNSUPPORTED;
+    const int64_t per_code = dtype == IDX_MXFP4 ? 64 : 128;
+    out->page_size = page_size;
+    out->bytes_per_token = (int32_t)(per_code + 4);
+    out->code_offset = 0;
+    out->code_bytes = per_code * page_size;
+    out->scale_offset = out->code_bytes;
+    out->scale_bytes = 4LL * page_size;
+    out->page_bytes = out->code_bytes + out->scale_bytes;
+    return IDX_OK;
+}
+
+int idx_k_store(const uint16_t* k, int64_t n_rows, int64_t k_row_stride,
+                const int64_t* slot_mapping, const int32_t* positions, const float* cos_sin,
+                int32_t max_pos, int32_t rope, int32_t apply_norm, const float* gamma,
+                const float* beta, float eps, int32_t dtype, void* pool, int64_t num_pages,
+                int32_t page_size, int64_t page_stride, int32_t* dev_status,
+                cudaStream_t stream) {
+    if (n_rows < 0 || !valid_rope(rope)) return IDX_EINVAL;
+    int st = check_pool(dtype, pool, num_pages, page_size, page_stride);
+    if (st != IDX_OK) return st;
+    if (n_rows == 0) return IDX_OK;
+    if (!k || !slot_mapping || !aligned(k, 16) || k_row_stride < 128 || k_row_stride % 8 != 0)
+        return IDX_EINVAL;
+    if (rope != IDX_ROPE_NONE && (!positions || !cos_sin || max_pos <= 0)) return IDX_EINVAL;
+    if (apply_norm && !(eps >= 0.0f && std::isfinite(eps))) return IDX_EINVAL;
+    idx::KStoreArgs a{};
+    a.k = k; a.n_rows = n_rows; a.k_row_stride = k_row_stride; a.slot_mapping = slot_mapping;
+    a.positions = positions; a.cos_sin = cos_sin; a.max_pos = max_pos; a.rope = rope;
+    a.apply_norm = apply_norm != 0; a.dtype = dtype; a.gamma = gamma; a.beta = beta; a.eps = eps;
+    a.pool = static_cast<uint8_t*>(pool); a.num_pages = num_pages; a.page_size = page_size;
+    a.page_stride = page_stride; a.dev_status = dev_status;
+    return cuda_status(idx::launch_k_store(a, stream));
+}
+
+int idx_q_quant(const uint16_t* q, int64_t T, int32_t H, const int32_t* positions,
+                const float* cos_sin, int32_t max_pos, int32_t rope, const float* w_in,
+                float softmax_scale, float head_scale, int32_t dtype, uint8_t* q_codes,
+                void* q_scales, float* w_out, int32_t* dev_status, cudaStream_t stream) {
+    if (T < 0 || !valid_rope(rope) || !valid_dtype(dtype)) return IDX_EINVAL;
+    if (H < 1 || H > 64) return IDX_EUNSUPPORTED;
+    if (T == 0) return IDX_OK;
+    if (!q || !w_in || !q_codes || !w_out || !aligned(q, 16) || !aligned(q_codes, 16))
+        return IDX_EINVAL;
+    if (dtype == IDX_MXFP4 && (!q_scales || !aligned(q_scales, 4))) return IDX_EINVAL;
+    if (q_scales && !aligned(q_scales, 4)) return IDX_EINVAL;
+    if (rope != IDX_ROPE_NONE && (!positions || !cos_sin || max_pos <= 0)) return IDX_EINVAL;
+    idx::QQuantArgs a{};
+    a.q = q; a.n_rows = T * (int64_t)H; a.H = H; a.positions = positions; a.cos_sin = cos_sin;
+    a.max_pos = max_pos; a.rope = rope; a.dtype = dtype; a.w_in = w_in;
+    a.fold = (float)((double)softmax_scale * (double)head_scale);  // one rounding
+    a.q_codes = q_codes; a.q_scales = q_scales; a.w_out = w_out; a.dev_status = dev_status;
+    return cuda_status(idx::launch_q_quant(a, stream));
+}
+
+int idx_mqa_logits_paged(const uint8_t* q_codes, const void* q_scales, const float* w,
+                         int64_t T, int32_t H, int32_t dtype, const void* pool,
+                         int64_t num_pages, int32_t page_size, int64_t page_stride,
+                         const int32_t* page_table, int32_t pt_stride,
+                         const int32_t* seq_lens_k, const int32_t* cu_seqlens_q, int32_t B,
+                         int32_t causal, int32_t max_q_len, int32_t max_seq_len_k,
+                         float* logits, int64_t ld_logits, int32_t* dev_status,
+                         cudaStream_t stream) {
+    int st = check_pool(dtype, pool, num_pages, page_size, page_stride);
+    if (st != IDX_OK) return st;
+    if (T < 0 || B < 0 || max_q_len < 0 || max_seq_len_k < 0 || pt_stride < 0) return IDX_EINVAL;
+    if (H < 1 || H > 64) return IDX_EUNSUPPORTED;
+    if (T == 0 || B == 0) return IDX_OK;
+    if (!q_codes || !w || !page_table || !seq_lens_k || !cu_seqlens_q || !logits) return IDX_EINVAL;
+    if (dtype == IDX_MXFP4 && !q_scales) return IDX_EINVAL;
+    if (!aligned(q_codes, 16) || !aligned(logits, 16) || ld_logits < max_seq_len_k ||
+        ld_logits % 4 != 0)
+        return IDX_EINVAL;
+    if (pt_stride < (max_seq_len_k + page_size - 1) / page_size) return IDX_EINVAL;
+    idx::ScoreArgs a{};
+    a.q_codes = q_codes; a.q_scales = static_cast<const uint8_t*>(q_scales); a.w = w; a.T = T;
+    a.H = H; a.dtype = dtype; a.pool = static_cast<const uint8_t*>(pool); a.num_pages = num_pages;
+    a.page_size = page_size; a.page_stride = page_stride; a.page_table = page_table;
+    a.pt_stride = pt_stride; a.seq_lens_k = seq_lens_k; a.cu_seqlens_q = cu_seqlens_q; a.B = B;
+    a.causal = causal != 0; a.max_q_len = max_q_len; a.max_seq_len_k = max_seq_len_k;
+    a.logits = logits; a.ld = ld_logits; a.dev_status = dev_status;
+    return cuda_status(idx::launch_scorer(a, stream));
+}
+
+int idx_topk(const float* logits, int64_t ld_logits, const int32_t* seq_lens_k,
+             const int32_t* cu_seqlens_q, int32_t B, int64_t T, int32_t causal, int32_t k,
+             int32_t* out_idx, cudaStream_t stream) {
+    if (T < 0 || B < 0 || ld_logits < 0) return IDX_EINVAL;
+    if (k < 1 || k > 4096) return IDX_EUNSUPPORTED;
+    if (T == 0) return IDX_OK;
+    if (!logits || !seq_lens_k || !cu_seqlens_q || !out_idx || B == 0) return IDX_EINVAL;
+    idx::TopkArgs a{};
+    a.logits = logits; a.ld = ld_logits; a.seq_lens_k = seq_lens_k; a.cu_seqlens_q = cu_seqlens_q;
+    a.B = B; a.T = T; a.causal = causal != 0; a.k = k; a.out = out_idx;
+    return cuda_status(idx::launch_topk(a, stream));
+}
+
+int idx_debug_encode(int32_t kind, const float* in, int64_t n, uint8_t* out, cudaStream_t stream) {
+    if ((kind != 0 && kind != 1) || n < 0) return IDX_EINVAL;
+    if (n == 0) return IDX_OK;
+    if (!in || !out) return IDX_EINVAL;
+    return cuda_status(idx::launch_debug_encode(kind, in, n, out, stream));
+}
+
+}  // extern "C"
+
+namespace idx {
+// Scorer dispatch: one kernel family per dtype.
+cudaError_t launch_scorer(const ScoreArgs& a, cudaStream_t st) { return launch_scorer_simt(a, st); }
+}  // namespace idx

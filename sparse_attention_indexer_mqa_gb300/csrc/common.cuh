@@ -1,0 +1,93 @@
+// common.cuh -- device helpers shared by the indexer kernels: bf16 unpacking, the e2m1 /
+// e4m3 element encoders, the MX shared exponent, the paged-cache layout, status bits.
+//
+// Sources: vllm PR 60834 "Purpose" (MXFP4 cache: 4 blocks of 32 e2m1 + one E8M0 scale,
+// 68 B/token; FP8: 132 B/token); vllm PR 53094 "Purpose" (the pre-processing steps).
+#pragma once
+
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/idx.h"
+
+namespace idx {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ void report(int32_t* status, int32_t bit) {
+    if (status) atomicOr(status, bit);
+}
+
+// bf16 pair in a 32-bit word -> two fp32 (exact)
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// e2m1 code of v (|v| < 8 after block scaling): round to nearest, ties to the even code,
+// saturate at 6; the sign bit follows the sign of v. Midpoints of the grid
+// {0, .5, 1, 1.5, 2, 3, 4, 6} are .25 .75 1.25 1.75 2.5 3.5 5; at a midpoint the even code
+// wins, hence "<=" below even codes and "<" below odd ones.
+__device__ __forceinline__ uint32_t e2m1_code(float v) {
+    float a = fabsf(v);
+    uint32_t c = (a <= 0.25f) ? 0u
+               : (a < 0.75f)  ? 1u
+               : (a <= 1.25f) ? 2u
+               : (a < 1.75f)  ? 3u
+               : (a <= 2.5f)  ? 4u
+               : (a < 3.5f)   ? 5u
+               : (a <= 5.0f)  ? 6u
+                              : 7u;
+    return c | ((__float_as_uint(v) >> 31) << 3);
+}
+
+// e4m3 (fn) code of v: the hardware conversion, round to nearest even, saturating at 448.
+__device__ __forceinline__ uint32_t e4m3_code(float v) {
+    return (uint32_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+}
+
+// OCP MX shared exponent: floor(log2 amax) - 2 read from the exponent field (leading
+// mantissa bit for subnormals), clamped to [-127, 127]; amax == 0 gives -127.
+__device__ __forceinline__ int mx_exponent(float amax) {
+    uint32_t u = __float_as_uint(amax) & 0x7fffffffu;
+    if (u == 0) return -127;
+    int ef = (int)(u >> 23);
+    int fl = ef > 0 ? ef - 127 : (31 - __clz((int)u)) - 149;
+    int e = fl - 2;
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// 2^-E as fp32 for E in [-127, 125] (always a normal number).
+__device__ __forceinline__ float pow2_neg(int e) { return __uint_as_float((uint32_t)(127 - e) << 23); }
+
+// ---- paged cache layout (see idx.h) ------------------------------------------------------
+// MXFP4: byte offset in a page of 16-byte chunk c (scale block c) of in-page token s.
+__device__ __forceinline__ int mx_chunk_off(int P, int s, int c) {
+    return P == 128 ? ((s >> 3) * 4 + c) * 128 + (s & 7) * 16
+                    : (s >> 4) * 1024 + ((s >> 3) & 1) * 512 + c * 128 + (s & 7) * 16;
+}
+// MXFP4: byte offset of the 4 scale bytes (blocks 0..3, contiguous) of in-page token s.
+__device__ __forceinline__ int mx_scale_off(int P, int s) {
+    return P == 128 ? 8192 + (s & 31) * 16 + (s >> 5) * 4 : 4096 + (s & 15) * 16 + (s >> 4) * 4;
+}
+// FP8: byte offset of 16-byte chunk c (elements 16c..16c+15) of token s; scale offset.
+__device__ __forceinline__ int f8_chunk_off(int s, int c) { return (s >> 3) * 1024 + c * 128 + (s & 7) * 16; }
+__device__ __forceinline__ int f8_scale_off(int P, int s) { return 128 * P + 4 * s; }
+
+// Keys visible to the i-th of nq queries of a sequence with seq_len keys.
+__device__ __forceinline__ int64_t visible_keys(int64_t seq_len, int64_t nq, int64_t i, int causal) {
+    int64_t v = causal ? seq_len - nq + i + 1 : seq_len;
+    return v < 0 ? 0 : (v > seq_len ? seq_len : v);
+}
+
+// Sequence b owning global query row t (binary search over cu_seqlens_q[0..B]); -1 if none.
+__device__ __forceinline__ int seq_of_query(const int32_t* cu, int B, int64_t t) {
+    int lo = 0, hi = B;  // find b with cu[b] <= t < cu[b+1]
+    if (t < cu[0] || t >= cu[B]) return -1;
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (cu[mid] <= t) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+}  // namespace idx

@@ -1,0 +1,80 @@
+// kernels.h -- internal argument blocks and launchers behind the C ABI (idx.h).
+// The ABI layer validates every argument before it fills one of these.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace idx {
+
+struct KStoreArgs {
+    const uint16_t* k;
+    int64_t n_rows, k_row_stride;
+    const int64_t* slot_mapping;
+    const int32_t* positions;
+    const float* cos_sin;
+    int32_t max_pos, rope, apply_norm, dtype;
+    const float* gamma;
+    const float* beta;
+    float eps;
+    uint8_t* pool;
+    int64_t num_pages;
+    int32_t page_size;
+    int64_t page_stride;
+    int32_t* dev_status;
+};
+
+struct QQuantArgs {
+    const uint16_t* q;
+    int64_t n_rows;  // T * H
+    int32_t H;
+    const int32_t* positions;
+    const float* cos_sin;
+    int32_t max_pos, rope, dtype;
+    const float* w_in;
+    float fold;  // fp32(softmax_scale * head_scale)
+    uint8_t* q_codes;
+    void* q_scales;
+    float* w_out;
+    int32_t* dev_status;
+};
+
+struct ScoreArgs {
+    const uint8_t* q_codes;
+    const uint8_t* q_scales;  // MXFP4: E8M0 [T][H][4]; FP8: unused
+    const float* w;           // [T][H]
+    int64_t T;
+    int32_t H, dtype;
+    const uint8_t* pool;
+    int64_t num_pages;
+    int32_t page_size;
+    int64_t page_stride;
+    const int32_t* page_table;
+    int32_t pt_stride;
+    const int32_t* seq_lens_k;
+    const int32_t* cu_seqlens_q;
+    int32_t B, causal, max_q_len, max_seq_len_k;
+    float* logits;
+    int64_t ld;
+    int32_t* dev_status;
+};
+
+struct TopkArgs {
+    const float* logits;
+    int64_t ld;
+    const int32_t* seq_lens_k;
+    const int32_t* cu_seqlens_q;
+    int32_t B;
+    int64_t T;
+    int32_t causal, k;
+    int32_t* out;
+};
+
+cudaError_t launch_k_store(const KStoreArgs& a, cudaStream_t st);
+cudaError_t launch_q_quant(const QQuantArgs& a, cudaStream_t st);
+cudaError_t launch_debug_encode(int kind, const float* in, int64_t n, uint8_t* out, cudaStream_t st);
+cudaError_t launch_scorer(const ScoreArgs& a, cudaStream_t st);
+cudaError_t launch_scorer_simt(const ScoreArgs& a, cudaStream_t st);
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st);
+
+}  // namespace idx

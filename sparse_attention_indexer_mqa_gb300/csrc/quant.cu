@@ -1,0 +1,272 @@
+// quant.cu -- the fused K store (LayerNorm -> RoPE -> MXFP4/FP8 -> paged store) and the
+// Q quant (RoPE -> MXFP4/FP8, weight fold) kernels.
+//
+// vllm PR 53094 "Purpose" lists the pre-processing of one indexer layer as five launches
+// (LayerNorm on k; RoPE on q and k; per-token-group FP8 quantisation of q; fold of the
+// q scale into the weights; FP8 quantisation of k plus the paged cache write) and replaces
+// them with one fused kernel; vllm PR 60834 "Changes / K write" and "Q quant" do the same
+// for MXFP4 (norm -> RoPE -> MXFP4 -> preshuffled pages; RoPE -> MXFP4 with the softmax
+// and head scales folded into fp32 weights). Here each of the two steps is one launch.
+//
+// Mapping: 16 threads per 128-element row, 8 consecutive elements (one 16-byte load of
+// bf16) per thread; a 256-thread CTA handles 16 rows. Reductions use a fixed tree (group
+// of 8 in registers, then xor-butterfly over the 16 lanes), so the result does not depend
+// on the launch shape. Every float operation is an explicitly rounded intrinsic (no FMA
+// contraction), which makes the bytes reproducible on any IEEE implementation.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace idx {
+
+namespace {
+
+constexpr int kRowsPerCta = 16;
+constexpr int kThreads = 16 * kRowsPerCta;
+
+__device__ __forceinline__ float sum8(const float* e) {
+    float a = __fadd_rn(e[0], e[1]);
+    float b = __fadd_rn(e[2], e[3]);
+    float c = __fadd_rn(e[4], e[5]);
+    float d = __fadd_rn(e[6], e[7]);
+    return __fadd_rn(__fadd_rn(a, b), __fadd_rn(c, d));
+}
+
+// Sum over the 128 values of a row held 8 per lane by 16 lanes (identical in every lane).
+__device__ __forceinline__ float row_sum(const float* e) {
+    float g = sum8(e);
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1) g = __fadd_rn(g, __shfl_xor_sync(kFull, g, off));
+    return g;
+}
+
+// LayerNorm with biased variance and rstd = 1 / sqrt(var + eps), each op rounded.
+__device__ __forceinline__ void layernorm(float* x, int l16, const float* gamma, const float* beta,
+                                          float eps) {
+    const float inv_d = 0.0078125f;
+    float mean = __fmul_rn(row_sum(x), inv_d);
+    float d[8], sq[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        d[i] = __fsub_rn(x[i], mean);
+        sq[i] = __fmul_rn(d[i], d[i]);
+    }
+    float var = __fmul_rn(row_sum(sq), inv_d);
+    float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float g = gamma ? __ldg(gamma + 8 * l16 + i) : 1.0f;
+        float b = beta ? __ldg(beta + 8 * l16 + i) : 0.0f;
+        x[i] = __fadd_rn(__fmul_rn(__fmul_rn(d[i], rstd), g), b);
+    }
+}
+
+// RoPE on dims 0..63 (lanes 0..7 of the row). NeoX pairs dims (i, i+32): lane l < 4 holds
+// the first element of its pairs, lane l+4 the second. Interleaved pairs (2i, 2i+1) lie
+// inside one lane. cs = the table row [cos f0..f31, sin f0..f31].
+__device__ __forceinline__ void rope(float* x, int l16, const float* cs, int mode) {
+    if (mode == IDX_ROPE_NEOX) {
+        float p[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) p[i] = __shfl_xor_sync(kFull, x[i], 4);
+        if (l16 < 8) {
+            const int f0 = (8 * l16) & 31;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float c = __ldg(cs + f0 + i), s = __ldg(cs + 32 + f0 + i);
+                if (l16 < 4) x[i] = __fsub_rn(__fmul_rn(x[i], c), __fmul_rn(p[i], s));  // a' = ac - bs
+                else         x[i] = __fadd_rn(__fmul_rn(x[i], c), __fmul_rn(p[i], s));  // b' = bc + as
+            }
+        }
+    } else if (mode == IDX_ROPE_INTERLEAVED) {
+        if (l16 < 8) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int f = 4 * l16 + q;
+                float c = __ldg(cs + f), s = __ldg(cs + 32 + f);
+                float a = x[2 * q], b = x[2 * q + 1];
+                x[2 * q] = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s));
+                x[2 * q + 1] = __fadd_rn(__fmul_rn(b, c), __fmul_rn(a, s));
+            }
+        }
+    }
+}
+
+// MXFP4: this lane's 8 elements -> one 32-bit word of nibbles (element 2m low, 2m+1 high
+// of byte m) and the E8M0 byte of its 32-element block (lanes 4b..4b+3 = block b).
+__device__ __forceinline__ void mx_quant(const float* x, uint32_t& word, uint32_t& sbyte) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+    const int e = mx_exponent(amax);
+    const float inv = pow2_neg(e);
+    word = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) word |= e2m1_code(__fmul_rn(x[i], inv)) << (4 * i);
+    sbyte = (uint32_t)(e + 127);
+}
+
+// FP8: scale = max(amax, 1e-10) / 448 over the 128 values; codes e4m3(x / scale).
+__device__ __forceinline__ void f8_quant(const float* x, uint32_t& lo, uint32_t& hi, float& scale) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+    for (int off = 1; off <= 8; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
+    scale = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+    lo = hi = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) lo |= e4m3_code(__fdiv_rn(x[i], scale)) << (8 * i);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) hi |= e4m3_code(__fdiv_rn(x[4 + i], scale)) << (8 * i);
+}
+
+__device__ __forceinline__ void load_row8(const uint16_t* src, bool ok, float* x) {
+    uint4 v = ok ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0, 0, 0, 0);
+    x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x);
+    x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+    x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z);
+    x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+}
+
+template <int kDtype>
+__global__ void __launch_bounds__(kThreads) k_store_kernel(KStoreArgs a) {
+    const int l16 = threadIdx.x & 15;
+    const int64_t row = (int64_t)blockIdx.x * kRowsPerCta + (threadIdx.x >> 4);
+    bool ok = row < a.n_rows;
+    int64_t slot = ok ? __ldg(a.slot_mapping + row) : -1;
+    ok = ok && slot >= 0;
+    const int64_t page = ok ? slot / a.page_size : 0;
+    const int s = ok ? (int)(slot - page * a.page_size) : 0;
+    if (ok && page >= a.num_pages) {
+        if (l16 == 0) report(a.dev_status, IDX_STATUS_BAD_SLOT);
+        ok = false;
+    }
+    int32_t pos = 0;
+    if (a.rope != IDX_ROPE_NONE && ok) {
+        pos = __ldg(a.positions + row);
+        if (pos < 0 || pos >= a.max_pos) {
+            if (l16 == 0) report(a.dev_status, IDX_STATUS_BAD_POS);
+            ok = false;
+            pos = 0;
+        }
+    }
+    // every lane keeps going (zeros for skipped rows) so that the shuffles stay converged
+    float x[8];
+    load_row8(a.k + (ok ? row : 0) * a.k_row_stride + 8 * l16, ok, x);
+    if (a.apply_norm) layernorm(x, l16, a.gamma, a.beta, a.eps);
+    if (a.rope != IDX_ROPE_NONE) rope(x, l16, a.cos_sin + (int64_t)pos * 64, a.rope);
+
+    uint8_t* base = a.pool + page * a.page_stride;  // 64-bit page rebasing
+    if (kDtype == IDX_MXFP4) {
+        uint32_t word, sbyte;
+        mx_quant(x, word, sbyte);
+        // gather the 4 words of a 16-byte chunk (= one scale block) into its first lane
+        uint32_t w1 = __shfl_down_sync(kFull, word, 1);
+        uint32_t w2 = __shfl_down_sync(kFull, word, 2);
+        uint32_t w3 = __shfl_down_sync(kFull, word, 3);
+        uint32_t s1 = __shfl_down_sync(kFull, sbyte, 4);
+        uint32_t s2 = __shfl_down_sync(kFull, sbyte, 8);
+        uint32_t s3 = __shfl_down_sync(kFull, sbyte, 12);
+        if (ok && (l16 & 3) == 0) {
+            *reinterpret_cast<uint4*>(base + mx_chunk_off(a.page_size, s, l16 >> 2)) =
+                make_uint4(word, w1, w2, w3);
+        }
+        if (ok && l16 == 0) {
+            *reinterpret_cast<uint32_t*>(base + mx_scale_off(a.page_size, s)) =
+                sbyte | (s1 << 8) | (s2 << 16) | (s3 << 24);
+        }
+    } else {
+        uint32_t lo, hi;
+        float scale;
+        f8_quant(x, lo, hi, scale);
+        uint32_t plo = __shfl_down_sync(kFull, lo, 1);
+        uint32_t phi = __shfl_down_sync(kFull, hi, 1);
+        if (ok && (l16 & 1) == 0) {
+            *reinterpret_cast<uint4*>(base + f8_chunk_off(s, l16 >> 1)) = make_uint4(lo, hi, plo, phi);
+        }
+        if (ok && l16 == 0) *reinterpret_cast<float*>(base + f8_scale_off(a.page_size, s)) = scale;
+    }
+}
+
+template <int kDtype>
+__global__ void __launch_bounds__(kThreads) q_quant_kernel(QQuantArgs a) {
+    const int l16 = threadIdx.x & 15;
+    const int64_t row = (int64_t)blockIdx.x * kRowsPerCta + (threadIdx.x >> 4);  // t*H + h
+    bool ok = row < a.n_rows;
+    const int64_t t = ok ? row / a.H : 0;
+    int32_t pos = 0;
+    if (a.rope != IDX_ROPE_NONE && ok) {
+        pos = __ldg(a.positions + t);
+        if (pos < 0 || pos >= a.max_pos) {
+            if (l16 == 0) report(a.dev_status, IDX_STATUS_BAD_POS);
+            ok = false;
+            pos = 0;
+        }
+    }
+    float x[8];
+    load_row8(a.q + (ok ? row : 0) * 128 + 8 * l16, ok, x);
+    if (a.rope != IDX_ROPE_NONE) rope(x, l16, a.cos_sin + (int64_t)pos * 64, a.rope);
+    if (kDtype == IDX_MXFP4) {
+        uint32_t word, sbyte;
+        mx_quant(x, word, sbyte);
+        uint32_t s1 = __shfl_down_sync(kFull, sbyte, 4);
+        uint32_t s2 = __shfl_down_sync(kFull, sbyte, 8);
+        uint32_t s3 = __shfl_down_sync(kFull, sbyte, 12);
+        if (ok) {
+            reinterpret_cast<uint32_t*>(a.q_codes + row * 64)[l16] = word;
+            if (l16 == 0) {
+                reinterpret_cast<uint32_t*>(a.q_scales)[row] = sbyte | (s1 << 8) | (s2 << 16) | (s3 << 24);
+                a.w_out[row] = __fmul_rn(__ldg(a.w_in + row), a.fold);
+            }
+        }
+    } else {
+        uint32_t lo, hi;
+        float scale;
+        f8_quant(x, lo, hi, scale);
+        if (ok) {
+            reinterpret_cast<uint2*>(a.q_codes + row * 128)[l16] = make_uint2(lo, hi);
+            if (l16 == 0) {
+                if (a.q_scales) reinterpret_cast<float*>(a.q_scales)[row] = scale;
+                a.w_out[row] = __fmul_rn(__fmul_rn(__ldg(a.w_in + row), a.fold), scale);
+            }
+        }
+    }
+}
+
+__global__ void debug_encode_kernel(int kind, const float* in, int64_t n, uint8_t* out) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        float v = in[i];
+        out[i] = (uint8_t)(kind == 0 ? e2m1_code(v) : e4m3_code(v));
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_k_store(const KStoreArgs& a, cudaStream_t st) {
+    if (a.n_rows == 0) return cudaSuccess;
+    const int64_t grid = (a.n_rows + kRowsPerCta - 1) / kRowsPerCta;
+    if (a.dtype == IDX_MXFP4) k_store_kernel<IDX_MXFP4><<<(unsigned)grid, kThreads, 0, st>>>(a);
+    else k_store_kernel<IDX_FP8><<<(unsigned)grid, kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_q_quant(const QQuantArgs& a, cudaStream_t st) {
+    if (a.n_rows == 0) return cudaSuccess;
+    const int64_t grid = (a.n_rows + kRowsPerCta - 1) / kRowsPerCta;
+    if (a.dtype == IDX_MXFP4) q_quant_kernel<IDX_MXFP4><<<(unsigned)grid, kThreads, 0, st>>>(a);
+    else q_quant_kernel<IDX_FP8><<<(unsigned)grid, kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_debug_encode(int kind, const float* in, int64_t n, uint8_t* out, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 152 * 64) blocks = 152 * 64;
+    debug_encode_kernel<<<(unsigned)blocks, 256, 0, st>>>(kind, in, n, out);
+    return cudaGetLastError();
+}
+
+}  // namespace idx

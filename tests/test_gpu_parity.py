@@ -1,0 +1,297 @@
+"""GPU parity: the CUDA library against the CPU oracle, through the C ABI.
+
+Bit-exact: packed cache bytes (codes and scales), quantised Q, folded weights, element
+encoders. Tolerance: logits within 1e-4 * max |exact logit| of the row with cosine >=
+0.999999; top-k sets equal up to ties within that tolerance of the k-th value.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+from sparse_attention_indexer_mqa_gb300 import workloads as W
+
+from helpers import (Dev, assert_logits_close, assert_topk_valid, oracle_logits, oracle_q,
+                     oracle_store, oracle_topk)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch as T
+    from sparse_attention_indexer_mqa_gb300 import binding
+    binding.load()
+    return T
+
+
+# ------------------------------------------------------------------ element encoders
+
+def _sweep_values():
+    b = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    v = W.bf16_to_f32(b)
+    v = v[np.isfinite(v)]
+    rng = np.random.default_rng(20)
+    r = np.concatenate([(rng.standard_normal(2_000_000) * 3).astype(np.float32),
+                        (rng.random(1_000_000) * 16 - 8).astype(np.float32),
+                        (rng.standard_normal(1_000_000) * 200).astype(np.float32)])
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0, 448.0, 464.0], np.float32)
+    near = np.concatenate([np.nextafter(mids, 0), np.nextafter(mids, 1e9), mids])
+    return np.concatenate([v, r, near, -near, np.array([0.0, -0.0], np.float32)])
+
+
+def test_e2m1_encoder_matches_oracle(torch):
+    from sparse_attention_indexer_mqa_gb300 import binding as Bn
+    v = _sweep_values()
+    v = v[np.abs(v) < 8]
+    x = torch.from_numpy(v).cuda()
+    out = torch.empty(v.shape[0], dtype=torch.uint8, device="cuda")
+    Bn.idx_debug_encode(0, x, out)
+    np.testing.assert_array_equal(out.cpu().numpy(), O.e2m1_encode_n(v))
+
+
+def test_e4m3_encoder_matches_oracle(torch):
+    from sparse_attention_indexer_mqa_gb300 import binding as Bn
+    v = _sweep_values()
+    x = torch.from_numpy(v).cuda()
+    out = torch.empty(v.shape[0], dtype=torch.uint8, device="cuda")
+    Bn.idx_debug_encode(1, x, out)
+    np.testing.assert_array_equal(out.cpu().numpy(), O.e4m3_encode_n(v))
+
+
+# ------------------------------------------------------------------ K store / Q quant
+
+def _check_store_and_quant(wl, label):
+    d = Dev(wl)
+    d.store()
+    d.quant()
+    pool_gpu = d.host("pool_buf")
+    pool_ref = oracle_store(wl)
+    assert d.host("status")[0] == 0
+    diff = np.nonzero(pool_gpu != pool_ref)[0]
+    assert diff.size == 0, f"{label}: {diff.size} cache bytes differ, first at {diff[:8]}"
+    qc, qs, w = oracle_q(wl)
+    np.testing.assert_array_equal(d.host("q_codes"), qc, err_msg=label)
+    np.testing.assert_array_equal(d.host("q_scales").view(np.uint8), qs.view(np.uint8), err_msg=label)
+    np.testing.assert_array_equal(d.host("w").view(np.uint32), w.view(np.uint32), err_msg=label)
+    return d, pool_ref, (qc, qs, w)
+
+
+def test_store_quant_tiny_decode(torch):
+    wl = W.make("tiny_decode")
+    d, pool_ref, _ = _check_store_and_quant(wl, "tiny")
+    # the page of slack in front of the pool view stays untouched
+    assert not d.host("pool_buf")[:wl.page_stride].any()
+
+
+@pytest.mark.parametrize("n", [1, 7, 32, 257, 1023])
+@pytest.mark.parametrize("P", [64, 128])
+@pytest.mark.parametrize("rope", [W.ROPE_NEOX, W.ROPE_INTERLEAVED])
+@pytest.mark.parametrize("dtype", [W.MXFP4, W.FP8])
+def test_store_quant_grid(torch, n, P, rope, dtype):
+    """Token-count x page-size x RoPE-layout grid of the fused pre-processing op test
+    (vllm PR 53094 "Test Plan / Op test"), here bit-exact against the oracle."""
+    rng = np.random.default_rng(1000 + n)
+    pages = (n + P - 1) // P + 3
+    perm = rng.permutation(pages).astype(np.int32)
+    slots = (perm[np.arange(n) // P].astype(np.int64) * P + np.arange(n) % P)
+    slots[rng.random(n) < 0.1] = -1  # padded rows are skipped
+    H = 4
+    wl = W.Workload(
+        name="grid", dtype=dtype, B=1, H=H, page_size=P, pool_pages=pages, base_offset_pages=1,
+        page_stride=W.page_bytes(dtype, P) + 16 * int(rng.integers(0, 3)),
+        seq_lens_k=np.array([n], np.int32), cu_seqlens_q=np.array([0, n], np.int32),
+        page_table=perm[None, :], causal=1, topk=8,
+        k=W.bf16_bits((rng.standard_normal((n, 128)) * rng.uniform(0.1, 30)).astype(np.float32)),
+        slot_mapping=slots, k_positions=rng.integers(0, 4000, n).astype(np.int32), k_rope=rope,
+        k_norm=1, step_rows=np.arange(n), q=W.bf16_bits(rng.standard_normal((n, H, 128)).astype(np.float32)),
+        q_positions=rng.integers(0, 4000, n).astype(np.int32), q_rope=rope,
+        w_in=rng.standard_normal((n, H)).astype(np.float32), softmax_scale=0.088388,
+        head_scale=0.5, cos_sin=W.rope_table(4000), ld_logits=n)
+    _check_store_and_quant(wl, f"grid n={n} P={P} rope={rope} dtype={dtype}")
+
+
+def test_store_quant_only_mode_outliers(torch):
+    wl = W.make("decode_b64", B=4, ctx=1000)
+    _check_store_and_quant(wl, "quant-only")
+
+
+def test_store_quant_compressed_full(torch):
+    _check_store_and_quant(W.make("decode_compressed"), "compressed decode, full size")
+
+
+def test_store_quant_fp8_full(torch):
+    _check_store_and_quant(W.make("prefill_fp8"), "fp8 prefill, full size")
+
+
+def test_store_bad_rows_set_status(torch):
+    from sparse_attention_indexer_mqa_gb300 import binding as Bn
+    wl = W.make("tiny_decode")
+    d = Dev(wl)
+    slot = d.slot.clone()
+    slot[3] = wl.pool_pages * wl.page_size + 5  # beyond the pool
+    pos = d.kpos.clone()
+    pos[5] = 10 ** 6                            # beyond the RoPE table
+    Bn.idx_k_store(d.k, slot, pos, d.cos_sin, wl.k_rope, 1, wl.dtype, d.pool, wl.pool_pages,
+                   wl.page_size, wl.page_stride, dev_status=d.status)
+    st = int(d.host("status")[0])
+    assert st & Bn.IDX_STATUS_BAD_SLOT and st & Bn.IDX_STATUS_BAD_POS
+    ref = oracle_store(wl, rows=np.setdiff1d(np.arange(wl.n_k_rows), [3, 5]))
+    np.testing.assert_array_equal(d.host("pool_buf"), ref)
+
+
+# ------------------------------------------------------------------ scorer + top-k
+
+def torch_rows(rows):
+    import torch as T
+    return T.from_numpy(np.asarray(rows, np.int64)).cuda()
+
+
+def _full_path(wl, rows=None, label=""):
+    d = Dev(wl)
+    d.run_all()
+    assert d.host("status")[0] == 0
+    pool_ref = oracle_store(wl)
+    np.testing.assert_array_equal(d.host("pool_buf"), pool_ref)
+    qc, qs, w = oracle_q(wl)
+    exact = oracle_logits(wl, pool_ref, qc, qs, w, rows=rows)
+    vis = wl.visible()
+    if rows is not None:
+        r = torch_rows(rows)
+        got, tk, vis = d.logits[r].cpu().numpy(), d.topk[r].cpu().numpy(), vis[rows]
+    else:
+        got, tk = d.host("logits"), d.host("topk")
+    worst = assert_logits_close(got, exact, vis, label=label)
+    assert_topk_valid(tk, exact, got, vis, wl.topk, label=label)
+    # entries past visible(t) are not written
+    for r in range(got.shape[0]):
+        assert np.isnan(got[r, vis[r]:]).all(), f"{label}: wrote past visible in row {r}"
+    return d, worst
+
+
+def test_path_tiny_decode(torch):
+    _full_path(W.make("tiny_decode"), label="tiny")
+
+
+def test_path_decode_b64_full(torch):
+    _full_path(W.make("decode_b64"), label="decode B64/H32/8K")
+
+
+def test_path_decode_compressed_full(torch):
+    _full_path(W.make("decode_compressed"), label="decode compressed B256/H64")
+
+
+def test_path_prefill_small_ragged(torch):
+    # several tiles, a ragged tail, causal
+    _full_path(W.make("prefill_8k", T=700), label="prefill 700")
+
+
+def test_path_prefill_8k_sampled(torch):
+    wl = W.make("prefill_8k")
+    rows = np.unique(np.concatenate([np.arange(0, 8), [1022, 1023, 1024, 1025],
+                                     np.linspace(0, 8191, 40).astype(int), np.arange(8184, 8192)]))
+    _full_path(wl, rows=rows, label="prefill 8192 (sampled rows)")
+
+
+def test_path_fp8_small(torch):
+    _full_path(W.make("prefill_fp8", B=2, cached=300, new=200), label="fp8 small")
+
+
+def test_path_fp8_full_sampled(torch):
+    wl = W.make("prefill_fp8")
+    rows = np.concatenate([b * 4096 + np.array([0, 1, 2047, 4094, 4095]) for b in range(8)])
+    _full_path(wl, rows=rows, label="fp8 32K (sampled rows)")
+
+
+def test_shuffled_pages_bitwise(torch):
+    wl = W.make("tiny_decode")
+    d = Dev(wl)
+    d.run_all()
+    base = d.host("logits").copy()
+    rng = np.random.default_rng(30)
+    perm = rng.permutation(wl.pool_pages)
+    pool = d.host("pool").copy()
+    new = np.zeros_like(pool)
+    ps = wl.page_stride
+    for p in range(wl.pool_pages):
+        new[perm[p] * ps:(perm[p] + 1) * ps] = pool[p * ps:(p + 1) * ps]
+    d.pool.copy_(torch.from_numpy(new).cuda())
+    pt = torch.from_numpy(perm[wl.page_table].astype(np.int32)).cuda()
+    d.logits.fill_(float("nan"))
+    d.score(page_table=pt)
+    assert np.array_equal(d.host("logits"), base, equal_nan=True)
+
+
+def test_mutations_break_parity(torch):
+    """Shifted page table, one flipped scale byte: the comparison must fail."""
+    wl = W.make("tiny_decode")
+    d = Dev(wl)
+    d.run_all()
+    pool_ref = oracle_store(wl)
+    qc, qs, w = oracle_q(wl)
+    exact = oracle_logits(wl, pool_ref, qc, qs, w)
+    vis = wl.visible()
+    d.logits.fill_(float("nan"))
+    d.score(page_table=torch.roll(d.page_table, 1, dims=1).contiguous())
+    with pytest.raises(AssertionError):
+        assert_logits_close(d.host("logits"), exact, vis)
+    pg = int(wl.page_table[0, 0])
+    d.pool[pg * wl.page_stride + O.scale_offset(0, wl.page_size, 2, 0)] += 3
+    d.logits.fill_(float("nan"))
+    d.score()
+    with pytest.raises(AssertionError):
+        assert_logits_close(d.host("logits"), exact, vis)
+
+
+def test_bad_page_sets_status(torch):
+    wl = W.make("tiny_decode")
+    d = Dev(wl)
+    d.store(); d.quant()
+    pt = d.page_table.clone()
+    pt[1, 0] = wl.pool_pages + 3
+    d.score(page_table=pt)
+    from sparse_attention_indexer_mqa_gb300 import binding as Bn
+    assert int(d.host("status")[0]) & Bn.IDX_STATUS_BAD_PAGE
+
+
+def test_large_pool_addresses(torch):
+    """Pages placed across the 2^31, 2^32 and 4.608e9-byte offsets of a 4.7 GB pool
+    (the 64-bit page rebasing cases of vllm PR 57517 "Test plan")."""
+    wl = W.make("tiny_decode")
+    ps = wl.page_stride
+    targets = [2 ** 31, 2 ** 32, 4_608_000_000]
+    n_pages = 4_700_000_000 // ps
+    # choose physical page ids whose byte range straddles or follows each target
+    ids = []
+    for tgt in targets:
+        p = tgt // ps
+        ids += [p - 1, p, p + 1]
+    ids = np.array(ids[:8], np.int32)
+    pt = np.full_like(wl.page_table, 0)
+    need0 = (int(wl.seq_lens_k[0]) + wl.page_size - 1) // wl.page_size
+    need1 = (int(wl.seq_lens_k[1]) + wl.page_size - 1) // wl.page_size
+    pt[0, :need0] = ids[:need0]
+    pt[1, :need1] = ids[need0:need0 + need1]
+    slots = []
+    for b, L in enumerate(wl.seq_lens_k):
+        s = np.arange(int(L))
+        slots.append(pt[b, s // wl.page_size].astype(np.int64) * wl.page_size + s % wl.page_size)
+    slots = np.concatenate(slots)
+    big = W.Workload(**{**wl.__dict__, "page_table": pt, "slot_mapping": slots,
+                        "pool_pages": int(n_pages), "base_offset_pages": 0})
+    d = Dev(big)
+    d.run_all()
+    assert d.host("status")[0] == 0
+    # oracle on a compact pool holding only the used pages (same bytes, remapped ids)
+    remap = {int(p): i for i, p in enumerate(sorted(set(ids.tolist())))}
+    pt_c = np.vectorize(lambda p: remap.get(int(p), 0))(pt).astype(np.int32)
+    small = W.Workload(**{**wl.__dict__, "page_table": pt_c, "pool_pages": len(remap),
+                          "base_offset_pages": 0,
+                          "slot_mapping": np.concatenate([pt_c[b, np.arange(int(L)) // wl.page_size].astype(np.int64) * wl.page_size + np.arange(int(L)) % wl.page_size for b, L in enumerate(wl.seq_lens_k)])})
+    pool_ref = oracle_store(small)
+    torch.cuda.synchronize()
+    for p, i in remap.items():
+        np.testing.assert_array_equal(d.pool[p * ps:(p + 1) * ps].cpu().numpy(),
+                                      pool_ref[i * ps:(i + 1) * ps])
+    qc, qs, w = oracle_q(small)
+    exact = oracle_logits(small, pool_ref, qc, qs, w)
+    assert_logits_close(d.host("logits"), exact, wl.visible(), label="large pool")
