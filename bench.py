@@ -1,0 +1,464 @@
+"""Benchmark of the indexer hot path on GB300: one step = K store of the step's new keys,
+Q quant, paged MQA-logits scorer and per-query top-k, through the C ABI.
+
+Default workload: MXFP4 decode, B=64 sequences x 1 query, H=32, D=128, 8192 keys each,
+page size 128 from a permuted pool of 4608 pages, 1% outlier K rows, top-k 1024. Metric:
+K-tokens/s = (query, key) pairs scored per second / 1000 (higher is better).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+Prints one JSON line (rank 0). Timing: W untimed steps, then exactly K steps between a
+barrier + synchronize on both sides, CUDA events on the launching stream, max over ranks.
+The L2 (129 MB) is defeated by rotating over enough independent copies of the K cache and
+Q inputs that consecutive reuses are more than 4x the L2 size apart. Multi-GPU: one
+independent replica per rank (the path needs no exchange), weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_attention_indexer_mqa_gb300 import workloads as W  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+
+# per-config algorithmic bytes of one scorer launch (what the scorer must read + write)
+# and of the other kernels, computed from the workload below
+
+
+def algorithmic_bytes(wl):
+    """Bytes the scorer must move in one launch: every visible key once (68 or 132 B), the
+    quantised Q (64+4 or 128 B per (t,h)), the weights, page table, lengths and the fp32
+    logits it writes."""
+    per_tok = 68 if wl.dtype == W.MXFP4 else 132
+    per_q = 68 if wl.dtype == W.MXFP4 else 128
+    keys = int(wl.seq_lens_k.sum())
+    pt = int(sum((int(L) + wl.page_size - 1) // wl.page_size for L in wl.seq_lens_k)) * 4
+    return {
+        "scorer": keys * per_tok + wl.T * wl.H * (per_q + 4) + pt + 4 * wl.B + 4 * (wl.B + 1)
+        + 4 * wl.pairs(),
+        "k_store": len(wl.step_rows) * (256 + per_tok + 8 + 4),
+        "q_quant": wl.T * wl.H * (256 + per_q + 4 + 4),
+        "topk": 4 * wl.pairs() + 4 * wl.T * wl.topk,
+    }
+
+
+def scorer_flops(wl):
+    return 2.0 * wl.H * 128 * wl.pairs()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def source_sha(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        h.update(open(os.path.join(ROOT, p), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(kernel_key, sources):
+    """dram bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_key)
+    if not d or d.get("source_sha") != source_sha(sources):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except FileNotFoundError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1])); mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------------------
+
+class Replica:
+    """Device state of one workload: R rotating copies of the K cache and Q inputs."""
+
+    def __init__(self, wl, copies, device):
+        import torch
+        from sparse_attention_indexer_mqa_gb300 import binding as Bn
+        self.Bn, self.torch, self.wl = Bn, torch, wl
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        self.cos_sin = t(wl.cos_sin)
+        self.page_table = t(wl.page_table)
+        self.seq_lens_k = t(wl.seq_lens_k)
+        self.cu = t(wl.cu_seqlens_q)
+        self.max_q = int(np.diff(wl.cu_seqlens_q).max())
+        self.max_k = int(wl.seq_lens_k.max())
+        # the step's new keys (their rows of k / slots / positions)
+        sr = wl.step_rows
+        self.k_new = t(wl.k[sr].view(np.int16))
+        self.slot_new = t(wl.slot_mapping[sr])
+        self.pos_new = t(wl.k_positions[sr])
+        self.q = [t(wl.q.view(np.int16)) for _ in range(copies)]
+        self.qpos = t(wl.q_positions)
+        self.w_in = t(wl.w_in)
+        T, H = wl.T, wl.H
+        per_q = 64 if wl.dtype == W.MXFP4 else 128
+        self.q_codes = torch.zeros((T, H, per_q), dtype=torch.uint8, device=device)
+        self.q_scales = (torch.zeros((T, H, 4), dtype=torch.uint8, device=device)
+                         if wl.dtype == W.MXFP4 else None)
+        self.w = torch.zeros((T, H), dtype=torch.float32, device=device)
+        self.logits = torch.empty((T, wl.ld_logits), dtype=torch.float32, device=device)
+        self.topk = torch.empty((T, wl.topk), dtype=torch.int32, device=device)
+        # set-up (untimed): store every key once, then clone the pool R-1 times
+        pool0 = torch.zeros(wl.pool_pages * wl.page_stride, dtype=torch.uint8, device=device)
+        kall = t(wl.k.view(np.int16))
+        Bn.idx_k_store(kall, t(wl.slot_mapping), t(wl.k_positions) if wl.k_rope else None,
+                       self.cos_sin if wl.k_rope else None, wl.k_rope, wl.k_norm, wl.dtype, pool0,
+                       wl.pool_pages, wl.page_size, wl.page_stride)
+        del kall
+        self.pools = [pool0] + [pool0.clone() for _ in range(copies - 1)]
+        torch.cuda.synchronize()
+
+    def step(self, i, ev=None):
+        wl, Bn = self.wl, self.Bn
+        r = i % len(self.pools)
+        pool = self.pools[r]
+
+        def mark(j):
+            if ev is not None:
+                ev[j].record()
+
+        mark(0)
+        Bn.idx_k_store(self.k_new, self.slot_new, self.pos_new if wl.k_rope else None,
+                       self.cos_sin if wl.k_rope else None, wl.k_rope, wl.k_norm, wl.dtype, pool,
+                       wl.pool_pages, wl.page_size, wl.page_stride)
+        mark(1)
+        Bn.idx_q_quant(self.q[r], self.qpos if wl.q_rope else None,
+                       self.cos_sin if wl.q_rope else None, wl.q_rope, self.w_in,
+                       wl.softmax_scale, wl.head_scale, wl.dtype, self.q_codes, self.q_scales,
+                       self.w)
+        mark(2)
+        Bn.idx_mqa_logits_paged(self.q_codes, self.q_scales, self.w, wl.dtype, pool,
+                                wl.pool_pages, wl.page_size, wl.page_stride, self.page_table,
+                                self.seq_lens_k, self.cu, wl.causal, self.max_q, self.max_k,
+                                self.logits)
+        mark(3)
+        Bn.idx_topk(self.logits, self.seq_lens_k, self.cu, wl.causal, wl.topk, self.topk)
+        mark(4)
+
+
+def working_set_bytes(wl):
+    return wl.pool_pages * wl.page_stride + wl.q.nbytes
+
+
+def run_gpu(args, rank, world):
+    import torch
+    from sparse_attention_indexer_mqa_gb300 import binding as Bn
+    Bn.load()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    wl = W.make(args.config, seed=args.seed + rank)
+    copies = max(2, -(-4 * L2_BYTES // working_set_bytes(wl)))
+    if working_set_bytes(wl) > 4 * L2_BYTES:
+        copies = 1 if working_set_bytes(wl) > 16 * L2_BYTES else 2
+    rep = Replica(wl, copies, dev)
+    stream = torch.cuda.current_stream()
+
+    for i in range(args.warmup):
+        rep.step(i)
+    torch.cuda.synchronize()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    start.record(stream)
+    for i in range(args.steps):
+        rep.step(args.warmup + i, ev[i])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    time.sleep(0.2)
+    clk = clocks.stop()
+    ms = start.elapsed_time(stop)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    names = ["k_store", "q_quant", "scorer", "topk"]
+    per_kernel_ms = {n: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)) / args.steps
+                     for j, n in enumerate(names)}
+
+    # end to end through the C ABI with host buffers: H2D of the step's inputs (new K rows,
+    # slots, positions, Q, weights) from pinned memory, the four calls, D2H of the top-k
+    e2e = run_e2e(rep, args, torch)
+
+    pairs = wl.pairs()
+    value = world * pairs / (ms / args.steps / 1e3) / 1e3
+    ab = algorithmic_bytes(wl)
+    peaks, peak_kind = measured_peaks()
+    sc_s = per_kernel_ms["scorer"] / 1e3
+    achieved = ab["scorer"] / sc_s / 1e9
+    traffic = profile_traffic(f"scorer:{args.config}", SCORER_SOURCES)
+    line = {
+        "metric": "indexer decode K-tokens/s (query-key pairs scored per second / 1e3), "
+                  "B64/H32/D128/8K MXFP4, page 128",
+        "value": round(value, 1),
+        "unit": "K-tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "mxfp4" if wl.dtype == W.MXFP4 else "fp8e4m3",
+        "data": "synthetic (seeded numpy PCG64: bf16 N(0,1) q/k with 1% x20 K rows, "
+                "N(0,1/H) weights, permuted pages)",
+        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "D": 128, "seq_len_k": int(wl.seq_lens_k.max()),
+                   "page_size": wl.page_size, "topk": wl.topk, "queries": wl.T, "pairs": pairs,
+                   "l2": f"inputs rotate over {copies} copies of cache+Q "
+                         f"({copies * working_set_bytes(wl) / 2**20:.0f} MiB > 4x L2)",
+                   "step": "k_store(new keys) + q_quant + mqa_logits_paged + topk"},
+        "kernel_us": {n: round(v * 1e3, 3) for n, v in per_kernel_ms.items()},
+        "roofline": {"kernel": "scorer", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                     "algorithmic_bytes": ab["scorer"], "peak_source": peak_kind},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
+    return line
+
+
+def run_e2e(rep, args, torch):
+    wl = rep.wl
+    Bn = rep.Bn
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    sr = wl.step_rows
+    h_k, h_slot, h_pos = pin(wl.k[sr].view(np.int16)), pin(wl.slot_mapping[sr]), pin(wl.k_positions[sr])
+    h_q, h_qpos, h_w = pin(wl.q.view(np.int16)), pin(wl.q_positions), pin(wl.w_in)
+    h_top = torch.empty(tuple(rep.topk.shape), dtype=torch.int32).pin_memory()
+    d_k, d_slot, d_pos = torch.empty_like(rep.k_new), torch.empty_like(rep.slot_new), torch.empty_like(rep.pos_new)
+    d_q, d_qpos, d_w = torch.empty_like(rep.q[0]), torch.empty_like(rep.qpos), torch.empty_like(rep.w_in)
+    h2d = sum(x.numel() * x.element_size() for x in (h_k, h_slot, h_pos, h_q, h_qpos, h_w))
+    d2h = h_top.numel() * 4
+
+    def one(i):
+        r = i % len(rep.pools)
+        pool = rep.pools[r]
+        for d, h in ((d_k, h_k), (d_slot, h_slot), (d_pos, h_pos), (d_q, h_q), (d_qpos, h_qpos), (d_w, h_w)):
+            d.copy_(h, non_blocking=True)
+        Bn.idx_k_store(d_k, d_slot, d_pos if wl.k_rope else None, rep.cos_sin if wl.k_rope else None,
+                       wl.k_rope, wl.k_norm, wl.dtype, pool, wl.pool_pages, wl.page_size, wl.page_stride)
+        Bn.idx_q_quant(d_q, d_qpos if wl.q_rope else None, rep.cos_sin if wl.q_rope else None,
+                       wl.q_rope, d_w, wl.softmax_scale, wl.head_scale, wl.dtype, rep.q_codes,
+                       rep.q_scales, rep.w)
+        Bn.idx_mqa_logits_paged(rep.q_codes, rep.q_scales, rep.w, wl.dtype, pool, wl.pool_pages,
+                                wl.page_size, wl.page_stride, rep.page_table, rep.seq_lens_k, rep.cu,
+                                wl.causal, rep.max_q, rep.max_k, rep.logits)
+        Bn.idx_topk(rep.logits, rep.seq_lens_k, rep.cu, wl.causal, wl.topk, rep.topk)
+        h_top.copy_(rep.topk, non_blocking=True)
+
+    for i in range(args.warmup):
+        one(i)
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for i in range(args.steps):
+        one(args.warmup + i)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / args.steps
+    return {"value": round(wl.pairs() / (ms / 1e3) / 1e3, 1), "unit": "K-tokens/s",
+            "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ----------------------------------------------------------------------------------------
+# CPU side: the oracle as it stands, timed on this host's cores
+
+def oracle_step(wl, pool, rows, n_threads):
+    import oracle as O
+    view = pool
+    sr = wl.step_rows
+    O.k_store(view, wl.k[sr], wl.slot_mapping[sr], wl.k_positions[sr], wl.cos_sin, wl.k_rope,
+              wl.k_norm, wl.dtype, wl.pool_pages, wl.page_size, wl.page_stride)
+    qc, qs, w = O.q_quant(wl.q, wl.q_positions, wl.cos_sin, wl.q_rope, wl.w_in,
+                          wl.softmax_scale, wl.head_scale, wl.dtype)
+    lg = O.mqa_logits(qc, qs, w, wl.dtype, view, wl.pool_pages, wl.page_size, wl.page_stride,
+                      wl.page_table, wl.seq_lens_k, wl.cu_seqlens_q, wl.causal, wl.ld_logits,
+                      rows=rows, n_threads=n_threads)
+    O.topk(np.nan_to_num(lg, nan=-np.inf), wl.seq_lens_k, wl.cu_seqlens_q, wl.causal, wl.topk,
+           rows=rows, n_threads=n_threads)
+    return int(wl.visible()[rows].sum())
+
+
+def oracle_pool(wl):
+    import oracle as O
+    pool = np.zeros(wl.pool_pages * wl.page_stride, np.uint8)
+    O.k_store(pool, wl.k, wl.slot_mapping, wl.k_positions, wl.cos_sin, wl.k_rope, wl.k_norm,
+              wl.dtype, wl.pool_pages, wl.page_size, wl.page_stride)
+    return pool
+
+
+def cpu_baseline(wl, budget_s=15.0, rows_per_step=None):
+    """Oracle step (K store of the new keys, Q quant, scoring + top-k of a sample of query
+    rows) on all host cores; value in K-tokens/s."""
+    n_threads = os.cpu_count() or 1
+    pool = oracle_pool(wl)
+    rows = np.arange(wl.T if rows_per_step is None else min(rows_per_step, wl.T), dtype=np.int64)
+    t0 = time.perf_counter()
+    pairs = 0
+    reps = 0
+    while True:
+        pairs += oracle_step(wl, pool, rows, n_threads)
+        reps += 1
+        if time.perf_counter() - t0 > budget_s or reps >= 50:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(pairs / dt / 1e3, 3), "unit": "K-tokens/s", "cores": n_threads,
+            "kind": "oracle",
+            "sample": f"{reps} oracle step(s): K store of {len(wl.step_rows)} new keys, Q quant "
+                      f"of all {wl.T}x{wl.H} rows, fp64 scoring + top-k of {len(rows)} of {wl.T} "
+                      f"queries ({pairs // reps} pairs per step), {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    wl = W.make(args.config, seed=args.seed)
+    n_threads = os.cpu_count() or 1
+    pool = oracle_pool(wl)
+    rows = np.arange(min(wl.T, args.ref_rows), dtype=np.int64)
+    for _ in range(args.warmup):
+        oracle_step(wl, pool, rows, n_threads)
+    t0 = time.perf_counter()
+    pairs = 0
+    for _ in range(args.steps):
+        pairs += oracle_step(wl, pool, rows, n_threads)
+    dt = time.perf_counter() - t0
+    v = round(pairs / dt / 1e3, 3)
+    return {
+        "impl": "reference",
+        "metric": "indexer decode K-tokens/s (query-key pairs scored per second / 1e3), "
+                  "B64/H32/D128/8K MXFP4, page 128",
+        "value": v, "unit": "K-tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": wl.name, "B": wl.B, "H": wl.H,
+                                        "seq_len_k": int(wl.seq_lens_k.max())},
+        "cpu_baseline": {"value": v, "unit": "K-tokens/s", "cores": n_threads, "kind": "oracle",
+                         "sample": f"each step: K store of {len(wl.step_rows)} new keys, Q quant, "
+                                   f"scoring + top-k of {len(rows)} of {wl.T} queries"},
+        "e2e": {"value": v, "unit": "K-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+SCORER_SOURCES = ["sparse_attention_indexer_mqa_gb300/csrc/scorer_simt.cu",
+                  "sparse_attention_indexer_mqa_gb300/csrc/common.cuh"]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="decode_b64", choices=sorted(W.BUILDERS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-rows", type=int, default=8)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    line = run_gpu(args, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

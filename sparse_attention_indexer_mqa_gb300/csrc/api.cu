@@ -112,7 +112,7 @@ int idx_mqa_logits_paged(const uint8_t* q_codes, const void* q_scales, const flo
     if (H < 1 || H > 64) return IDX_EUNSUPPORTED;
     if (T == 0 || B == 0) return IDX_OK;
     if (!q_codes || !w || !page_table || !seq_lens_k || !cu_seqlens_q || !logits) return IDX_EINVAL;
-    if (dtype == IDX_MXFP4 && !q_scales) return IDX_EINVAL;
+    if (dtype == IDX_MXFP4 && (!q_scales || !aligned(q_scales, 4))) return IDX_EINVAL;
     if (!aligned(q_codes, 16) || !aligned(logits, 16) || ld_logits < max_seq_len_k ||
         ld_logits % 4 != 0)
         return IDX_EINVAL;
@@ -151,5 +151,8 @@ int idx_debug_encode(int32_t kind, const float* in, int64_t n, uint8_t* out, cud
 
 namespace idx {
 // Scorer dispatch: one kernel family per dtype.
-cudaError_t launch_scorer(const ScoreArgs& a, cudaStream_t st) { return launch_scorer_simt(a, st); }
+cudaError_t launch_scorer(const ScoreArgs& a, cudaStream_t st) {
+    if (a.max_q_len <= 1) return launch_scorer_decode(a, st);
+    return launch_scorer_simt(a, st);
+}
 }  // namespace idx

@@ -135,6 +135,11 @@ def _slots(pt, lens, P):
     return np.concatenate(out)
 
 
+def _ld(n):
+    """Logits row stride: the longest row rounded up to 4 floats (16-byte aligned rows)."""
+    return (int(n) + 3) // 4 * 4
+
+
 def _normal_bf16(rng, shape):
     return bf16_bits(rng.standard_normal(shape, dtype=np.float32))
 
@@ -163,7 +168,7 @@ def tiny_decode(seed=0, **over) -> Workload:
         q=_normal_bf16(rq, (B, H, 128)), q_positions=(lens - 1).astype(np.int32),
         q_rope=ROPE_NEOX, w_in=(rw.standard_normal((B, H), dtype=np.float32)
                                  / np.float32(math.sqrt(H))).astype(np.float32),
-        softmax_scale=1.0, head_scale=1.0, cos_sin=rope_table(max_pos), ld_logits=int(lens.max()),
+        softmax_scale=1.0, head_scale=1.0, cos_sin=rope_table(max_pos), ld_logits=_ld(lens.max()),
     )
 
 
@@ -191,7 +196,7 @@ def decode_b64(seed=0, B=64, ctx=8192, H=32, **over) -> Workload:
         step_rows=np.cumsum(lens).astype(np.int64) - 1,
         q=_normal_bf16(rq, (B, H, 128)), q_positions=np.zeros(B, np.int32), q_rope=ROPE_NONE,
         w_in=(rw.standard_normal((B, H), dtype=np.float32) / np.float32(math.sqrt(H))),
-        softmax_scale=1.0, head_scale=1.0, cos_sin=rope_table(1), ld_logits=ctx,
+        softmax_scale=1.0, head_scale=1.0, cos_sin=rope_table(1), ld_logits=_ld(ctx),
     )
 
 
@@ -212,7 +217,7 @@ def prefill_8k(seed=0, T=8192, H=32, **over) -> Workload:
         k_rope=ROPE_NONE, k_norm=0, step_rows=np.arange(T, dtype=np.int64),
         q=_normal_bf16(rq, (T, H, 128)), q_positions=np.zeros(T, np.int32), q_rope=ROPE_NONE,
         w_in=(rw.standard_normal((T, H), dtype=np.float32) / np.float32(math.sqrt(H))),
-        softmax_scale=1.0, head_scale=1.0, cos_sin=rope_table(1), ld_logits=T,
+        softmax_scale=1.0, head_scale=1.0, cos_sin=rope_table(1), ld_logits=_ld(T),
     )
 
 
@@ -241,7 +246,7 @@ def decode_compressed(seed=0, B=256, H=64, **over) -> Workload:
         q_rope=ROPE_NEOX,
         w_in=(rw.standard_normal((B, H), dtype=np.float32) / np.float32(math.sqrt(H))),
         softmax_scale=float(128 ** -0.5), head_scale=1.0, cos_sin=rope_table(max_pos),
-        ld_logits=int(lens.max()),
+        ld_logits=_ld(lens.max()),
     )
 
 
@@ -268,7 +273,7 @@ def prefill_fp8(seed=0, B=8, cached=28672, new=4096, H=32, **over) -> Workload:
         k_rope=ROPE_INTERLEAVED, k_norm=1, step_rows=step_rows,
         q=_normal_bf16(rq, (B * new, H, 128)), q_positions=qpos, q_rope=ROPE_INTERLEAVED,
         w_in=(rw.standard_normal((B * new, H), dtype=np.float32) / np.float32(math.sqrt(H))),
-        softmax_scale=1.0, head_scale=1.0, cos_sin=rope_table(L), ld_logits=L,
+        softmax_scale=1.0, head_scale=1.0, cos_sin=rope_table(L), ld_logits=_ld(L),
     )
 
 

@@ -180,6 +180,16 @@ def test_path_decode_compressed_full(torch):
     _full_path(W.make("decode_compressed"), label="decode compressed B256/H64")
 
 
+def test_path_fp8_decode(torch):
+    # one new query per sequence: the FP8 decode kernel, page 64, ragged lengths
+    _full_path(W.make("prefill_fp8", B=5, cached=3001, new=1), label="fp8 decode")
+
+
+def test_path_decode_h64_p128_ragged(torch):
+    wl = W.make("decode_b64", B=9, ctx=1000, H=64)
+    _full_path(wl, label="decode H64 P128 ragged")
+
+
 def test_path_prefill_small_ragged(torch):
     # several tiles, a ragged tail, causal
     _full_path(W.make("prefill_8k", T=700), label="prefill 700")
