@@ -56,7 +56,35 @@ def algorithmic_bytes(wl):
 
 
 def scorer_flops(wl):
+    """Tensor-core work of one scorer launch: 2 * H * D flops per (query, key) pair."""
     return 2.0 * wl.H * 128 * wl.pairs()
+
+
+def scorer_alu_ops(wl):
+    """Epilogue issue work of one scorer launch: per (query, key) pair and head one ReLU
+    (max) and one fused multiply-add of the head-weighted sum (thread instructions)."""
+    return 2.0 * wl.H * wl.pairs()
+
+
+# issue rate of the GPU in thread instructions per second: 4 schedulers x 32 lanes per SM per
+# clock, 152 SMs, at the measured maximum SM clock (one warp instruction per scheduler per clock)
+def alu_peak_ops(peaks):
+    return 4 * 32 * 152 * peaks.get("sm_max_mhz", 2070.0) * 1e6
+
+
+# nominal dense tensor rates relative to bf16 (2.25 PF bf16, 4.5 PF fp8, 13.5 PF fp4)
+TENSOR_RATIO = {W.MXFP4: 6.0, W.FP8: 2.0}
+
+
+def is_decode(wl):
+    return int(np.diff(wl.cu_seqlens_q).max()) <= 1
+
+
+def metric_name(wl):
+    kind = "decode" if is_decode(wl) else "prefill"
+    dt = "MXFP4" if wl.dtype == W.MXFP4 else "FP8"
+    return (f"indexer {kind} K-tokens/s (query-key pairs scored per second / 1e3), {wl.name} "
+            f"({dt}, H{wl.H}, page {wl.page_size})")
 
 
 def measured_peaks():
@@ -163,9 +191,10 @@ class Replica:
         self.qpos = t(wl.q_positions)
         self.w_in = t(wl.w_in)
         T, H = wl.T, wl.H
+        Hq = (H + 7) // 8 * 8
         per_q = 64 if wl.dtype == W.MXFP4 else 128
-        self.q_codes = torch.zeros((T, H, per_q), dtype=torch.uint8, device=device)
-        self.q_scales = (torch.zeros((T, H, 4), dtype=torch.uint8, device=device)
+        self.q_codes = torch.zeros((T, Hq, per_q), dtype=torch.uint8, device=device)
+        self.q_scales = (torch.zeros((T, 512), dtype=torch.uint8, device=device)
                          if wl.dtype == W.MXFP4 else None)
         self.w = torch.zeros((T, H), dtype=torch.float32, device=device)
         self.logits = torch.empty((T, wl.ld_logits), dtype=torch.float32, device=device)
@@ -180,36 +209,56 @@ class Replica:
         self.pools = [pool0] + [pool0.clone() for _ in range(copies - 1)]
         torch.cuda.synchronize()
 
-    def step(self, i, ev=None):
+    def call(self, name, i, inputs=None):
+        """One library call of the step on rotation copy i % R."""
         wl, Bn = self.wl, self.Bn
         r = i % len(self.pools)
         pool = self.pools[r]
+        inp = inputs or {}
+        if name == "k_store":
+            Bn.idx_k_store(inp.get("k", self.k_new), inp.get("slot", self.slot_new),
+                           inp.get("pos", self.pos_new) if wl.k_rope else None,
+                           self.cos_sin if wl.k_rope else None, wl.k_rope, wl.k_norm, wl.dtype,
+                           pool, wl.pool_pages, wl.page_size, wl.page_stride)
+        elif name == "q_quant":
+            Bn.idx_q_quant(inp.get("q", self.q[r]), inp.get("qpos", self.qpos) if wl.q_rope else None,
+                           self.cos_sin if wl.q_rope else None, wl.q_rope, inp.get("w", self.w_in),
+                           wl.softmax_scale, wl.head_scale, wl.dtype, self.q_codes, self.q_scales,
+                           self.w)
+        elif name == "scorer":
+            Bn.idx_mqa_logits_paged(self.q_codes, self.q_scales, self.w, wl.dtype, pool,
+                                    wl.pool_pages, wl.page_size, wl.page_stride, self.page_table,
+                                    self.seq_lens_k, self.cu, wl.causal, self.max_q, self.max_k,
+                                    self.logits)
+        else:
+            Bn.idx_topk(self.logits, self.seq_lens_k, self.cu, wl.causal, wl.topk, self.topk)
 
-        def mark(j):
-            if ev is not None:
-                ev[j].record()
-
-        mark(0)
-        Bn.idx_k_store(self.k_new, self.slot_new, self.pos_new if wl.k_rope else None,
-                       self.cos_sin if wl.k_rope else None, wl.k_rope, wl.k_norm, wl.dtype, pool,
-                       wl.pool_pages, wl.page_size, wl.page_stride)
-        mark(1)
-        Bn.idx_q_quant(self.q[r], self.qpos if wl.q_rope else None,
-                       self.cos_sin if wl.q_rope else None, wl.q_rope, self.w_in,
-                       wl.softmax_scale, wl.head_scale, wl.dtype, self.q_codes, self.q_scales,
-                       self.w)
-        mark(2)
-        Bn.idx_mqa_logits_paged(self.q_codes, self.q_scales, self.w, wl.dtype, pool,
-                                wl.pool_pages, wl.page_size, wl.page_stride, self.page_table,
-                                self.seq_lens_k, self.cu, wl.causal, self.max_q, self.max_k,
-                                self.logits)
-        mark(3)
-        Bn.idx_topk(self.logits, self.seq_lens_k, self.cu, wl.causal, wl.topk, self.topk)
-        mark(4)
+    def step(self, i, inputs=None):
+        for n in ("k_store", "q_quant", "scorer", "topk"):
+            self.call(n, i, inputs)
 
 
 def working_set_bytes(wl):
+    """Bytes a step reads that a rotation copy can hold: the K cache and the bf16 Q."""
     return wl.pool_pages * wl.page_stride + wl.q.nbytes
+
+
+def capture(torch, fn, n):
+    """One CUDA graph holding n calls fn(i) on the capture stream."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n):
+            fn(i)
+    return g
+
+
+def time_graph(torch, g, stream):
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    g.replay()
+    e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e)
 
 
 def run_gpu(args, rank, world):
@@ -219,56 +268,82 @@ def run_gpu(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     wl = W.make(args.config, seed=args.seed + rank)
-    copies = max(2, -(-4 * L2_BYTES // working_set_bytes(wl)))
-    if working_set_bytes(wl) > 4 * L2_BYTES:
-        copies = 1 if working_set_bytes(wl) > 16 * L2_BYTES else 2
+    ws = working_set_bytes(wl)
+    copies = 1 if ws > 16 * L2_BYTES else (2 if ws > 4 * L2_BYTES else max(2, -(-4 * L2_BYTES // ws)))
     rep = Replica(wl, copies, dev)
     stream = torch.cuda.current_stream()
 
+    # W eager warm-up steps, then the K steps are captured once into a CUDA graph (the
+    # library's calls are asynchronous and capturable) so that host launch overhead does
+    # not gap the device timeline
     for i in range(args.warmup):
         rep.step(i)
     torch.cuda.synchronize()
+    g_step = capture(torch, lambda i: rep.step(args.warmup + i), args.steps)
+    g_step.replay()  # upload, untimed
+    torch.cuda.synchronize()
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(dev.index)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
     clocks.start()
-    time.sleep(0.3)
-    start.record(stream)
-    for i in range(args.steps):
-        rep.step(args.warmup + i, ev[i])
-    stop.record(stream)
-    torch.cuda.synchronize()
+    t_end = time.time() + 0.6
+    while time.time() < t_end:  # keep the GPU loaded while the sampler starts
+        g_step.replay()
+        torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    time.sleep(0.2)
+    torch.cuda.synchronize()
+    ms = time_graph(torch, g_step, stream)  # the timed region: exactly K steps
+    if world > 1:
+        torch.distributed.barrier()
+    t_end = time.time() + 0.3
+    while time.time() < t_end:
+        g_step.replay()
+        torch.cuda.synchronize()
     clk = clocks.stop()
-    ms = start.elapsed_time(stop)
     if world > 1:
         tt = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         ms = float(tt.item())
-    names = ["k_store", "q_quant", "scorer", "topk"]
-    per_kernel_ms = {n: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)) / args.steps
-                     for j, n in enumerate(names)}
+
+    # per-kernel device time: each kernel captured K times (same rotation) and timed alone
+    per_kernel_ms = {}
+    for name in ("k_store", "q_quant", "scorer", "topk"):
+        g = capture(torch, lambda i, n=name: rep.call(n, args.warmup + i), args.steps)
+        g.replay()
+        torch.cuda.synchronize()
+        per_kernel_ms[name] = time_graph(torch, g, stream) / args.steps
 
     # end to end through the C ABI with host buffers: H2D of the step's inputs (new K rows,
     # slots, positions, Q, weights) from pinned memory, the four calls, D2H of the top-k
-    e2e = run_e2e(rep, args, torch)
+    e2e = run_e2e(rep, args, torch, stream)
 
     pairs = wl.pairs()
     value = world * pairs / (ms / args.steps / 1e3) / 1e3
     ab = algorithmic_bytes(wl)
     peaks, peak_kind = measured_peaks()
     sc_s = per_kernel_ms["scorer"] / 1e3
-    achieved = ab["scorer"] / sc_s / 1e9
-    traffic = profile_traffic(f"scorer:{args.config}", SCORER_SOURCES)
+    if is_decode(wl):
+        achieved = ab["scorer"] / sc_s / 1e9
+        roof = {"kernel": "scorer", "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": profile_traffic(f"scorer:{args.config}", SCORER_SOURCES),
+                "algorithmic_bytes": ab["scorer"], "peak_source": f"{peak_kind} (hbm_gbs)"}
+    else:
+        alu = scorer_alu_ops(wl) / sc_s
+        tpeak = peaks["bf16_tflops"] * TENSOR_RATIO[wl.dtype]
+        roof = {"kernel": "scorer", "bound": "alu", "achieved": round(alu / 1e12, 2),
+                "peak": round(alu_peak_ops(peaks) / 1e12, 2), "unit": "T instr/s",
+                "frac": round(alu / alu_peak_ops(peaks), 4),
+                "traffic": profile_traffic(f"scorer:{args.config}", SCORER_SOURCES),
+                "algorithmic_ops": scorer_alu_ops(wl),
+                "peak_source": "issue rate 4x32 lanes x 152 SMs x measured max SM clock",
+                "tensor": {"achieved_tflops": round(scorer_flops(wl) / sc_s / 1e12, 1),
+                           "peak_tflops": round(tpeak, 1),
+                           "frac": round(scorer_flops(wl) / sc_s / 1e12 / tpeak, 4),
+                           "peak_source": f"{peak_kind} bf16 x nominal ratio {TENSOR_RATIO[wl.dtype]:g}"},
+                "hbm_gbs": round(ab["scorer"] / sc_s / 1e9, 1)}
     line = {
-        "metric": "indexer decode K-tokens/s (query-key pairs scored per second / 1e3), "
-                  "B64/H32/D128/8K MXFP4, page 128",
+        "metric": metric_name(wl),
         "value": round(value, 1),
         "unit": "K-tokens/s",
         "n_gpus": world,
@@ -279,87 +354,98 @@ def run_gpu(args, rank, world):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "mxfp4" if wl.dtype == W.MXFP4 else "fp8e4m3",
-        "data": "synthetic (seeded numpy PCG64: bf16 N(0,1) q/k with 1% x20 K rows, "
-                "N(0,1/H) weights, permuted pages)",
-        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "D": 128, "seq_len_k": int(wl.seq_lens_k.max()),
-                   "page_size": wl.page_size, "topk": wl.topk, "queries": wl.T, "pairs": pairs,
+        "data": "synthetic (seeded numpy PCG64: bf16 N(0,1) q/k, N(0,1/H) head weights, "
+                "permuted physical pages)",
+        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "D": 128,
+                   "seq_len_k": int(wl.seq_lens_k.max()), "page_size": wl.page_size,
+                   "topk": wl.topk, "queries": wl.T, "pairs": pairs, "causal": wl.causal,
                    "l2": f"inputs rotate over {copies} copies of cache+Q "
-                         f"({copies * working_set_bytes(wl) / 2**20:.0f} MiB > 4x L2)",
-                   "step": "k_store(new keys) + q_quant + mqa_logits_paged + topk"},
+                         f"({copies * ws / 2**20:.0f} MiB)" if copies > 1 else
+                         f"working set {ws / 2**20:.0f} MiB > 16x L2",
+                   "step": "k_store(step keys) + q_quant + mqa_logits_paged + topk",
+                   "launch": "K steps captured in one CUDA graph, replayed once"},
         "kernel_us": {n: round(v * 1e3, 3) for n, v in per_kernel_ms.items()},
-        "roofline": {"kernel": "scorer", "bound": "hbm", "achieved": round(achieved, 1),
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                     "algorithmic_bytes": ab["scorer"], "peak_source": peak_kind},
+        "roofline": roof,
         "gpu_launches": 4 * args.steps,
         "clocks": clk,
         "e2e": e2e,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget,
+                                            rows_per_step=None if is_decode(wl) else args.ref_rows)
     return line
 
 
-def run_e2e(rep, args, torch):
+def run_e2e(rep, args, torch, stream):
+    """The same step through the C ABI with host buffers: the step's inputs (new K rows,
+    slots, positions, Q, positions, weights) are packed in one pinned host buffer and copied
+    to the device in one H2D copy; the top-k indices come back in one D2H copy."""
     wl = rep.wl
-    Bn = rep.Bn
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
     sr = wl.step_rows
-    h_k, h_slot, h_pos = pin(wl.k[sr].view(np.int16)), pin(wl.slot_mapping[sr]), pin(wl.k_positions[sr])
-    h_q, h_qpos, h_w = pin(wl.q.view(np.int16)), pin(wl.q_positions), pin(wl.w_in)
+    parts = [("k", wl.k[sr].view(np.int16), torch.int16), ("slot", wl.slot_mapping[sr], torch.int64),
+             ("pos", wl.k_positions[sr], torch.int32), ("q", wl.q.view(np.int16), torch.int16),
+             ("qpos", wl.q_positions, torch.int32), ("w", wl.w_in, torch.float32)]
+    offs, o = {}, 0
+    for n, a, _ in parts:
+        offs[n] = o
+        o += (a.nbytes + 255) // 256 * 256
+    h_buf = torch.zeros(o, dtype=torch.uint8).pin_memory()
+    hb = h_buf.numpy()
+    for n, a, _ in parts:
+        hb[offs[n]:offs[n] + a.nbytes] = np.ascontiguousarray(a).view(np.uint8).ravel()
+    d_buf = torch.empty(o, dtype=torch.uint8, device=rep.q[0].device)
+    dev_in = {n: d_buf[offs[n]:offs[n] + a.nbytes].view(dt).view(a.shape) for n, a, dt in parts}
     h_top = torch.empty(tuple(rep.topk.shape), dtype=torch.int32).pin_memory()
-    d_k, d_slot, d_pos = torch.empty_like(rep.k_new), torch.empty_like(rep.slot_new), torch.empty_like(rep.pos_new)
-    d_q, d_qpos, d_w = torch.empty_like(rep.q[0]), torch.empty_like(rep.qpos), torch.empty_like(rep.w_in)
-    h2d = sum(x.numel() * x.element_size() for x in (h_k, h_slot, h_pos, h_q, h_qpos, h_w))
-    d2h = h_top.numel() * 4
+    h2d, d2h = o, h_top.numel() * 4
 
     def one(i):
-        r = i % len(rep.pools)
-        pool = rep.pools[r]
-        for d, h in ((d_k, h_k), (d_slot, h_slot), (d_pos, h_pos), (d_q, h_q), (d_qpos, h_qpos), (d_w, h_w)):
-            d.copy_(h, non_blocking=True)
-        Bn.idx_k_store(d_k, d_slot, d_pos if wl.k_rope else None, rep.cos_sin if wl.k_rope else None,
-                       wl.k_rope, wl.k_norm, wl.dtype, pool, wl.pool_pages, wl.page_size, wl.page_stride)
-        Bn.idx_q_quant(d_q, d_qpos if wl.q_rope else None, rep.cos_sin if wl.q_rope else None,
-                       wl.q_rope, d_w, wl.softmax_scale, wl.head_scale, wl.dtype, rep.q_codes,
-                       rep.q_scales, rep.w)
-        Bn.idx_mqa_logits_paged(rep.q_codes, rep.q_scales, rep.w, wl.dtype, pool, wl.pool_pages,
-                                wl.page_size, wl.page_stride, rep.page_table, rep.seq_lens_k, rep.cu,
-                                wl.causal, rep.max_q, rep.max_k, rep.logits)
-        Bn.idx_topk(rep.logits, rep.seq_lens_k, rep.cu, wl.causal, wl.topk, rep.topk)
+        d_buf.copy_(h_buf, non_blocking=True)
+        rep.step(i, inputs=dev_in)
         h_top.copy_(rep.topk, non_blocking=True)
 
     for i in range(args.warmup):
         one(i)
     torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for i in range(args.steps):
-        one(args.warmup + i)
-    e.record()
+    g = capture(torch, lambda i: one(args.warmup + i), args.steps)
+    g.replay()
     torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / args.steps
+    ms = time_graph(torch, g, stream) / args.steps
     return {"value": round(wl.pairs() / (ms / 1e3) / 1e3, 1), "unit": "K-tokens/s",
-            "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h),
+            "how": "K steps of (one packed H2D from pinned host, 4 library calls, one D2H of "
+                   "the top-k) in one CUDA graph"}
 
 
 # ----------------------------------------------------------------------------------------
 # CPU side: the oracle as it stands, timed on this host's cores
 
 def oracle_step(wl, pool, rows, n_threads):
+    """One oracle step on a sample: K store of the step's new keys, Q quant of the sampled
+    query rows, fp64 scoring and top-k of those rows. Returns the pairs scored."""
     import oracle as O
-    view = pool
     sr = wl.step_rows
-    O.k_store(view, wl.k[sr], wl.slot_mapping[sr], wl.k_positions[sr], wl.cos_sin, wl.k_rope,
+    O.k_store(pool, wl.k[sr], wl.slot_mapping[sr], wl.k_positions[sr], wl.cos_sin, wl.k_rope,
               wl.k_norm, wl.dtype, wl.pool_pages, wl.page_size, wl.page_stride)
-    qc, qs, w = O.q_quant(wl.q, wl.q_positions, wl.cos_sin, wl.q_rope, wl.w_in,
-                          wl.softmax_scale, wl.head_scale, wl.dtype)
-    lg = O.mqa_logits(qc, qs, w, wl.dtype, view, wl.pool_pages, wl.page_size, wl.page_stride,
+    qc_s, qs_s, w_s = O.q_quant(wl.q[rows], wl.q_positions[rows], wl.cos_sin, wl.q_rope,
+                                wl.w_in[rows], wl.softmax_scale, wl.head_scale, wl.dtype)
+    qc = np.zeros((wl.T,) + qc_s.shape[1:], qc_s.dtype)
+    qs = np.zeros((wl.T,) + qs_s.shape[1:], qs_s.dtype)
+    w = np.zeros((wl.T, wl.H), np.float32)
+    qc[rows], qs[rows], w[rows] = qc_s, qs_s, w_s
+    lg = O.mqa_logits(qc, qs, w, wl.dtype, pool, wl.pool_pages, wl.page_size, wl.page_stride,
                       wl.page_table, wl.seq_lens_k, wl.cu_seqlens_q, wl.causal, wl.ld_logits,
                       rows=rows, n_threads=n_threads)
     O.topk(np.nan_to_num(lg, nan=-np.inf), wl.seq_lens_k, wl.cu_seqlens_q, wl.causal, wl.topk,
            rows=rows, n_threads=n_threads)
     return int(wl.visible()[rows].sum())
+
+
+def sample_rows(wl, n):
+    """n query rows spread evenly over all queries (all rows if n >= T)."""
+    if n is None or n >= wl.T:
+        return np.arange(wl.T, dtype=np.int64)
+    return np.unique(np.linspace(0, wl.T - 1, n).round().astype(np.int64))
 
 
 def oracle_pool(wl):
@@ -375,7 +461,7 @@ def cpu_baseline(wl, budget_s=15.0, rows_per_step=None):
     rows) on all host cores; value in K-tokens/s."""
     n_threads = os.cpu_count() or 1
     pool = oracle_pool(wl)
-    rows = np.arange(wl.T if rows_per_step is None else min(rows_per_step, wl.T), dtype=np.int64)
+    rows = sample_rows(wl, rows_per_step)
     t0 = time.perf_counter()
     pairs = 0
     reps = 0
@@ -387,9 +473,9 @@ def cpu_baseline(wl, budget_s=15.0, rows_per_step=None):
     dt = time.perf_counter() - t0
     return {"value": round(pairs / dt / 1e3, 3), "unit": "K-tokens/s", "cores": n_threads,
             "kind": "oracle",
-            "sample": f"{reps} oracle step(s): K store of {len(wl.step_rows)} new keys, Q quant "
-                      f"of all {wl.T}x{wl.H} rows, fp64 scoring + top-k of {len(rows)} of {wl.T} "
-                      f"queries ({pairs // reps} pairs per step), {dt:.1f} s"}
+            "sample": f"{reps} oracle step(s): K store of {len(wl.step_rows)} new keys, Q quant, "
+                      f"fp64 scoring and top-k of {len(rows)} of {wl.T} queries spread evenly "
+                      f"({pairs // reps} pairs per step), {dt:.1f} s"}
 
 
 def run_reference(args, rank, world):
@@ -398,7 +484,7 @@ def run_reference(args, rank, world):
     wl = W.make(args.config, seed=args.seed)
     n_threads = os.cpu_count() or 1
     pool = oracle_pool(wl)
-    rows = np.arange(min(wl.T, args.ref_rows), dtype=np.int64)
+    rows = sample_rows(wl, args.ref_rows)
     for _ in range(args.warmup):
         oracle_step(wl, pool, rows, n_threads)
     t0 = time.perf_counter()
@@ -409,8 +495,7 @@ def run_reference(args, rank, world):
     v = round(pairs / dt / 1e3, 3)
     return {
         "impl": "reference",
-        "metric": "indexer decode K-tokens/s (query-key pairs scored per second / 1e3), "
-                  "B64/H32/D128/8K MXFP4, page 128",
+        "metric": metric_name(wl),
         "value": v, "unit": "K-tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -418,12 +503,14 @@ def run_reference(args, rank, world):
                                         "seq_len_k": int(wl.seq_lens_k.max())},
         "cpu_baseline": {"value": v, "unit": "K-tokens/s", "cores": n_threads, "kind": "oracle",
                          "sample": f"each step: K store of {len(wl.step_rows)} new keys, Q quant, "
-                                   f"scoring + top-k of {len(rows)} of {wl.T} queries"},
+                                   f"scoring + top-k of {len(rows)} of {wl.T} queries spread evenly"},
         "e2e": {"value": v, "unit": "K-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
-SCORER_SOURCES = ["sparse_attention_indexer_mqa_gb300/csrc/scorer_simt.cu",
+SCORER_SOURCES = ["sparse_attention_indexer_mqa_gb300/csrc/scorer_decode.cu",
+                  "sparse_attention_indexer_mqa_gb300/csrc/scorer_prefill.cu",
+                  "sparse_attention_indexer_mqa_gb300/csrc/tc.cuh",
                   "sparse_attention_indexer_mqa_gb300/csrc/common.cuh"]
 
 

@@ -119,13 +119,23 @@ int idx_k_store(const uint16_t* k, int64_t n_rows, int64_t k_row_stride,
 /*
  * Q quant ([P2] "Changes / Q quant"; [P3] "Purpose" steps 2-4):
  * q: bf16 [T][H][128] contiguous; positions: int32 [T] (NULL if rope == NONE);
- * w_in: fp32 [T][H]. For each (t, h): RoPE at positions[t], then
- *   MXFP4: q_codes [T][H][64] bytes (byte i = elements 2i | 2i+1 << 4),
- *          q_scales [T][H][4] E8M0 bytes, w_out[t,h] = w_in[t,h] * c;
- *   FP8:   q_codes [T][H][128] e4m3 (one fp32 scale per 128-element group, i.e. per
- *          (t, h)), q_scales: optional fp32 [T][H] copy of those scales (may be NULL),
- *          w_out[t,h] = (w_in[t,h] * c) * scale[t,h]   (the q-scale fold, [P3] step 4);
- *   c = fp32(softmax_scale * head_scale), one rounding.
+ * w_in: fp32 [T][H]. For each (t, h): RoPE at positions[t], then quantisation.
+ * Output layout (this library's own, the packed Q of [P1] "Purpose"): per query, the
+ * quantised heads form a tensor-core operand image of Hq = roundup(H, 8) rows, K-major,
+ * 8-row groups of 16-byte chunks, so the scorers copy it to shared memory unchanged.
+ *   MXFP4: q_codes [T][Hq][64] bytes; chunk c (scale block c) of head h of query t at
+ *            t*Hq*64 + ((h/8)*4 + c)*128 + (h%8)*16, byte i of the chunk holding elements
+ *            32c+2i (low nibble) and 32c+2i+1 (high nibble);
+ *          q_scales [T][512] bytes (16-byte aligned): the E8M0 scale of block c of head h at
+ *            t*512 + (h%32)*16 + (h/32)*4 + c (the tensor-memory scale-factor order);
+ *          w_out[t,h] = w_in[t,h] * c.
+ *   FP8:   q_codes [T][Hq][128] e4m3; element j of head h at
+ *            t*Hq*128 + ((h/8)*8 + j/16)*128 + (h%8)*16 + j%16 (one fp32 scale per
+ *            128-element group, i.e. per (t, h));
+ *          q_scales: optional fp32 [T][H] copy of those scales (may be NULL);
+ *          w_out[t,h] = (w_in[t,h] * c) * scale[t,h]   (the q-scale fold, [P3] step 4).
+ *   c = fp32(softmax_scale * head_scale), one rounding. Heads h in [H, Hq) are written as
+ *   zero codes with scale bytes 127; the scale bytes of heads >= Hq are not written.
  * Same rounding rules as idx_k_store. H in 1..64.
  */
 int idx_q_quant(const uint16_t* q, int64_t T, int32_t H, const int32_t* positions,

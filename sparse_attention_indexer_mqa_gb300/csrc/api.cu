@@ -87,11 +87,11 @@ int idx_q_quant(const uint16_t* q, int64_t T, int32_t H, const int32_t* position
     if (T == 0) return IDX_OK;
     if (!q || !w_in || !q_codes || !w_out || !aligned(q, 16) || !aligned(q_codes, 16))
         return IDX_EINVAL;
-    if (dtype == IDX_MXFP4 && (!q_scales || !aligned(q_scales, 4))) return IDX_EINVAL;
+    if (dtype == IDX_MXFP4 && (!q_scales || !aligned(q_scales, 16))) return IDX_EINVAL;
     if (q_scales && !aligned(q_scales, 4)) return IDX_EINVAL;
     if (rope != IDX_ROPE_NONE && (!positions || !cos_sin || max_pos <= 0)) return IDX_EINVAL;
     idx::QQuantArgs a{};
-    a.q = q; a.n_rows = T * (int64_t)H; a.H = H; a.positions = positions; a.cos_sin = cos_sin;
+    a.q = q; a.n_rows = T * (int64_t)((H + 7) & ~7); a.H = H; a.positions = positions; a.cos_sin = cos_sin;
     a.max_pos = max_pos; a.rope = rope; a.dtype = dtype; a.w_in = w_in;
     a.fold = (float)((double)softmax_scale * (double)head_scale);  // one rounding
     a.q_codes = q_codes; a.q_scales = q_scales; a.w_out = w_out; a.dev_status = dev_status;
@@ -112,7 +112,7 @@ int idx_mqa_logits_paged(const uint8_t* q_codes, const void* q_scales, const flo
     if (H < 1 || H > 64) return IDX_EUNSUPPORTED;
     if (T == 0 || B == 0) return IDX_OK;
     if (!q_codes || !w || !page_table || !seq_lens_k || !cu_seqlens_q || !logits) return IDX_EINVAL;
-    if (dtype == IDX_MXFP4 && (!q_scales || !aligned(q_scales, 4))) return IDX_EINVAL;
+    if (dtype == IDX_MXFP4 && (!q_scales || !aligned(q_scales, 16))) return IDX_EINVAL;
     if (!aligned(q_codes, 16) || !aligned(logits, 16) || ld_logits < max_seq_len_k ||
         ld_logits % 4 != 0)
         return IDX_EINVAL;
@@ -153,6 +153,6 @@ namespace idx {
 // Scorer dispatch: one kernel family per dtype.
 cudaError_t launch_scorer(const ScoreArgs& a, cudaStream_t st) {
     if (a.max_q_len <= 1) return launch_scorer_decode(a, st);
-    return launch_scorer_simt(a, st);
+    return launch_scorer_prefill(a, st);
 }
 }  // namespace idx

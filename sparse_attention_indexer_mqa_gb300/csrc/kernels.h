@@ -26,7 +26,7 @@ struct KStoreArgs {
 
 struct QQuantArgs {
     const uint16_t* q;
-    int64_t n_rows;  // T * H
+    int64_t n_rows;  // T * Hq (Hq = H rounded up to 8)
     int32_t H;
     const int32_t* positions;
     const float* cos_sin;
@@ -41,7 +41,7 @@ struct QQuantArgs {
 
 struct ScoreArgs {
     const uint8_t* q_codes;
-    const uint8_t* q_scales;  // MXFP4: E8M0 [T][H][4]; FP8: unused
+    const uint8_t* q_scales;  // MXFP4: E8M0 scale atoms [T][512]; FP8: unused
     const float* w;           // [T][H]
     int64_t T;
     int32_t H, dtype;
@@ -76,6 +76,7 @@ cudaError_t launch_debug_encode(int kind, const float* in, int64_t n, uint8_t* o
 cudaError_t launch_scorer(const ScoreArgs& a, cudaStream_t st);
 cudaError_t launch_scorer_simt(const ScoreArgs& a, cudaStream_t st);
 cudaError_t launch_scorer_decode(const ScoreArgs& a, cudaStream_t st);
+cudaError_t launch_scorer_prefill(const ScoreArgs& a, cudaStream_t st);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st);
 
 }  // namespace idx

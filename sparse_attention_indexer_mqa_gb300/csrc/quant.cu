@@ -190,12 +190,18 @@ __global__ void __launch_bounds__(kThreads) k_store_kernel(KStoreArgs a) {
     }
 }
 
+// Q rows are walked over T x Hq "virtual" heads, Hq = H rounded up to 8: heads past H
+// write the zero/neutral padding of the tensor-core image (see idx.h for the layout).
 template <int kDtype>
 __global__ void __launch_bounds__(kThreads) q_quant_kernel(QQuantArgs a) {
     const int l16 = threadIdx.x & 15;
-    const int64_t row = (int64_t)blockIdx.x * kRowsPerCta + (threadIdx.x >> 4);  // t*H + h
-    bool ok = row < a.n_rows;
-    const int64_t t = ok ? row / a.H : 0;
+    const int64_t vrow = (int64_t)blockIdx.x * kRowsPerCta + (threadIdx.x >> 4);  // t*Hq + h
+    const int Hq = (a.H + 7) & ~7;
+    bool live = vrow < a.n_rows;  // n_rows = T * Hq
+    const int64_t t = live ? vrow / Hq : 0;
+    const int h = live ? (int)(vrow - t * Hq) : 0;
+    const bool real = live && h < a.H;
+    bool ok = real;
     int32_t pos = 0;
     if (a.rope != IDX_ROPE_NONE && ok) {
         pos = __ldg(a.positions + t);
@@ -205,6 +211,7 @@ __global__ void __launch_bounds__(kThreads) q_quant_kernel(QQuantArgs a) {
             pos = 0;
         }
     }
+    const int64_t row = t * a.H + h;  // index of (t, h) in q, w_in, w_out
     float x[8];
     load_row8(a.q + (ok ? row : 0) * 128 + 8 * l16, ok, x);
     if (a.rope != IDX_ROPE_NONE) rope(x, l16, a.cos_sin + (int64_t)pos * 64, a.rope);
@@ -214,20 +221,24 @@ __global__ void __launch_bounds__(kThreads) q_quant_kernel(QQuantArgs a) {
         uint32_t s1 = __shfl_down_sync(kFull, sbyte, 4);
         uint32_t s2 = __shfl_down_sync(kFull, sbyte, 8);
         uint32_t s3 = __shfl_down_sync(kFull, sbyte, 12);
-        if (ok) {
-            reinterpret_cast<uint32_t*>(a.q_codes + row * 64)[l16] = word;
+        if (live && (ok || !real)) {
+            // canonical image: 8-head groups of [4 chunks][8 heads][16 B]
+            uint8_t* img = a.q_codes + t * Hq * 64 + ((h >> 3) * 4 + (l16 >> 2)) * 128 + (h & 7) * 16;
+            reinterpret_cast<uint32_t*>(img)[l16 & 3] = real ? word : 0u;
             if (l16 == 0) {
-                reinterpret_cast<uint32_t*>(a.q_scales)[row] = sbyte | (s1 << 8) | (s2 << 16) | (s3 << 24);
-                a.w_out[row] = __fmul_rn(__ldg(a.w_in + row), a.fold);
+                uint8_t* atom = reinterpret_cast<uint8_t*>(a.q_scales) + t * 512 + (h & 31) * 16 + (h >> 5) * 4;
+                *reinterpret_cast<uint32_t*>(atom) = real ? (sbyte | (s1 << 8) | (s2 << 16) | (s3 << 24)) : 0x7f7f7f7fu;
+                if (real) a.w_out[row] = __fmul_rn(__ldg(a.w_in + row), a.fold);
             }
         }
     } else {
         uint32_t lo, hi;
         float scale;
         f8_quant(x, lo, hi, scale);
-        if (ok) {
-            reinterpret_cast<uint2*>(a.q_codes + row * 128)[l16] = make_uint2(lo, hi);
-            if (l16 == 0) {
+        if (live && (ok || !real)) {
+            uint8_t* img = a.q_codes + t * Hq * 128 + ((h >> 3) * 8 + (l16 >> 1)) * 128 + (h & 7) * 16;
+            reinterpret_cast<uint2*>(img)[l16 & 1] = real ? make_uint2(lo, hi) : make_uint2(0, 0);
+            if (l16 == 0 && real) {
                 if (a.q_scales) reinterpret_cast<float*>(a.q_scales)[row] = scale;
                 a.w_out[row] = __fmul_rn(__fmul_rn(__ldg(a.w_in + row), a.fold), scale);
             }

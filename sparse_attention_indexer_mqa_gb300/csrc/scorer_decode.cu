@@ -1,28 +1,36 @@
 // scorer_decode.cu -- paged MQA-logits scorer for decode (one query per sequence) on the
 // 5th-generation tensor cores.
 //
-//   logits[t, s] = sum_h w[t,h] * ReLU(q[t,h] . k[s])          (MXFP4)
+//   logits[t, s] = sum_h w[t,h] * ReLU(q[t,h] . k[s])               (MXFP4)
 //   logits[t, s] = kscale[s] * sum_h w[t,h] * ReLU(q[t,h] . k[s])   (FP8, w carries q's scale)
 //
 // vllm PR 57517 "Purpose" / "Performance and accuracy" (decode B64/H32/D128/8K scorer) and
 // vllm PR 60834 "Purpose" (the MXFP4 cache is scored in place through the page table,
 // without gathering K first).
 //
-// Operand roles: the key tile is the A operand (M = 128 keys = one 128-token page or two
-// 64-token pages), the query's heads are B (N = H rounded up to 16), K = 128. So each
-// tensor-memory lane holds one key and one thread reduces its key's H head scores with
-// no shuffles. The cache pages are laid out in the tensor core's canonical K-major order
-// (see idx.h), so each page is bulk-copied (cp.async.bulk) into shared memory unchanged;
-// its MXFP4 scale bytes are already in the tensor-memory scale-factor order and go to
-// tensor memory with one tcgen05.cp. MXFP4 runs kind::mxf4 block-scaled MMAs (two of
-// K = 64, scale factors by 32-block); FP8 runs kind::f8f6f4 (four of K = 32) and applies the
-// per-token scale in the epilogue.
+// Operands: the key tile is the A operand (M = 128 keys = one 128-token page or two 64-token
+// pages), the query's heads are B (N = H rounded up to 16), K = 128. So each tensor-memory
+// lane holds one key and one thread reduces its key's H head scores with no shuffles. Cache
+// pages and the quantised Q are stored in the tensor core's canonical K-major order (see
+// idx.h): every operand reaches shared memory through cp.async.bulk unchanged, and the
+// MXFP4 E8M0 scale atoms go to tensor memory with one tcgen05.cp each. MXFP4 runs
+// kind::mxf4 block-scaled MMAs (two of K = 64); FP8 runs kind::f8f6f4 (four of K = 32) and
+// applies the per-key scale in the epilogue.
 //
-// A CTA owns up to kTiles consecutive 128-key tiles of one sequence. One thread of warp 4
-// issues every tile's bulk copies at once (all bytes in flight immediately: the step is
-// HBM bound), then the MMAs tile by tile into two tensor-memory accumulators; warps 0-3
-// drain the accumulators (tcgen05.ld), form the ReLU-weighted head sums and write logits.
-// Several CTAs share an SM, so one CTA's epilogue overlaps other CTAs' copies.
+// Persistent, warp-specialised: one CTA per SM takes a contiguous, balanced slice of all
+// (sequence, 128-key tile) units. Tiles move through the pipeline in groups of G (a
+// shared-memory stage holds G tiles and one mbarrier phase covers them), because each
+// mbarrier wait and tcgen05.commit costs hundreds of cycles of the issuing thread: with one
+// tile per phase the MMA thread, not HBM, set the pace.
+//   warp 0   producer: bulk copies of the query images and of the tiles into a ring of
+//            stage groups; each lane of the warp issues one tile, so a batch of tiles goes
+//            out at once (HBM bound: many tiles stay in flight);
+//   warp 1   tensor-memory owner and MMA issuer: scale atoms -> TMEM, G tiles' MMAs into
+//            one of two accumulator groups, one commit to free the stage group, one to
+//            publish the accumulators;
+//   warps 2-5 epilogue (one 32-lane TMEM quadrant each): tcgen05.ld, ReLU-weighted head
+//            sum in fp32, coalesced logits stores.
+// Every role walks the same unit sequence, so no metadata is passed between roles.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -31,19 +39,77 @@ namespace idx {
 
 namespace {
 
-constexpr int kEpi = 128;           // warps 0-3: epilogue (one TMEM lane quadrant each)
-constexpr int kThreads = kEpi + 32;  // warp 4: copies, tensor-memory allocation, MMAs
-constexpr int kIssuer = kEpi;        // the thread that issues copies and MMAs
+constexpr int kWarps = 6;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kEpiThreads = 128;
+constexpr int kAccG = 2;  // accumulator groups in tensor memory
 
-template <int kDtype>
-struct DecodeCfg {
-    static constexpr int kTiles = kDtype == IDX_MXFP4 ? 4 : 2;                // tiles per CTA
-    static constexpr int kTileCode = kDtype == IDX_MXFP4 ? 128 * 64 : 128 * 128;  // bytes
-    static constexpr int kTileAux = 512;     // MXFP4 scale atom / FP8 128 fp32 scales
-    static constexpr int kQRow = kDtype == IDX_MXFP4 ? 64 : 128;  // code bytes per head
-    static constexpr int kKSteps = kDtype == IDX_MXFP4 ? 2 : 4;   // MMAs per tile
-    static constexpr int kStepBytes = 256;   // K advance per MMA in the canonical layout
+template <int kDtype, int NP>
+struct Cfg {
+    // CTAs per SM: for H <= 32, four independent pipelines share an SM (tensor memory <= 128
+    // columns each) so that one CTA's issue, MMA and epilogue latencies overlap the others';
+    // one CTA per SM for 64 heads. Tiles per group G: 1 with four CTAs per SM, else 2-4.
+    static constexpr int kCps = NP <= 32 ? 4 : 1;
+    static constexpr int G = kCps == 4 ? 1 : ((kDtype == IDX_MXFP4 && NP <= 32) ? 4 : 2);
+    static constexpr int kTileCode = kDtype == IDX_MXFP4 ? 128 * 64 : 128 * 128;
+    static constexpr int kTileSf = kDtype == IDX_MXFP4 ? 512 : 0;          // scale atom (MXFP4)
+    static constexpr int kTile = kTileCode + kTileSf;
+    static constexpr int kGroup = G * kTile;
+    static constexpr int kSG = ((kCps == 1 ? 184 : 200 / kCps) * 1024) / kGroup;  // stage groups
+    static constexpr int kQRow = kDtype == IDX_MXFP4 ? 64 : 128;
+    static constexpr int kQImg = NP * kQRow;                               // per Q slot
+    static constexpr int kQSf = kDtype == IDX_MXFP4 ? 512 : 0;
     static constexpr uint32_t kSbo = kDtype == IDX_MXFP4 ? 512 : 1024;
+    static constexpr int kColsUsed = kAccG * G * (NP + 4) + 8;             // acc + SFA + SFB
+    static constexpr uint32_t kCols = kColsUsed <= 64 ? 64 : kColsUsed <= 128 ? 128 : kColsUsed <= 256 ? 256 : 512;
+    static constexpr int kBatch = G * kSG < 32 ? G * kSG : (32 / G) * G;   // tiles per producer batch
+    // shared memory map
+    static constexpr int oStages = 0;
+    static constexpr int oQ = kSG * kGroup;
+    static constexpr int oQSf = oQ + 2 * kQImg;
+    static constexpr int oBars = oQSf + 2 * kQSf;
+    static constexpr int kBars = 2 * kSG + 4 + 2 * kAccG;
+    static constexpr int oMisc = oBars + 8 * kBars;
+    static constexpr int kSmem = oMisc + 64;
+    static_assert(kBatch % G == 0 && kBatch <= G * kSG, "a batch covers whole, distinct stage groups");
+    static_assert(kCols * kCps <= 512, "tensor memory of the CTAs sharing an SM");
+};
+
+// Tile count and first query row of sequence b (0 tiles if it has no query).
+struct SeqInfo {
+    int64_t t, vis, tiles;
+};
+
+__device__ __forceinline__ SeqInfo seq_info(const ScoreArgs& a, int b) {
+    SeqInfo r{0, 0, 0};
+    const int64_t q0 = a.cu_seqlens_q[b], nq = a.cu_seqlens_q[b + 1] - q0;
+    if (nq <= 0) return r;
+    int64_t len = a.seq_lens_k[b];
+    len = len < 0 ? 0 : (len > a.max_seq_len_k ? a.max_seq_len_k : len);
+    r.t = q0;
+    r.vis = visible_keys(len, nq, nq - 1, a.causal);
+    r.tiles = (r.vis + 127) / 128;
+    return r;
+}
+
+// Walks (sequence, tile) units in order from a starting unit.
+struct Walker {
+    int b;
+    int64_t j;
+    SeqInfo si;
+    __device__ __forceinline__ void init(const ScoreArgs& a, int b0, int64_t j0) {
+        b = b0;
+        j = j0;
+        si = seq_info(a, b);
+    }
+    __device__ __forceinline__ void next(const ScoreArgs& a) {
+        if (++j < si.tiles) return;
+        j = 0;
+        do {
+            ++b;
+            si = b < a.B ? seq_info(a, b) : SeqInfo{0, 0, 1};
+        } while (si.tiles == 0);
+    }
 };
 
 template <int NP>
@@ -67,218 +133,372 @@ __device__ __forceinline__ void load_acc(uint32_t taddr, float* v) {
 }
 
 template <int kDtype, int NP>
-__global__ void __launch_bounds__(kThreads) decode_kernel(ScoreArgs a) {
-    using Cfg = DecodeCfg<kDtype>;
-    constexpr int TPC = Cfg::kTiles;
-    constexpr uint32_t kCols = (2 * NP + 4 * TPC + 4) <= 64 ? 64 : ((2 * NP + 4 * TPC + 4) <= 128 ? 128 : 256);
-
+__global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel(ScoreArgs a) {
+    using C = Cfg<kDtype, NP>;
+    constexpr int G = C::G;
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t* sK = smem;                                         // TPC x tile codes
-    uint8_t* sAux = sK + TPC * Cfg::kTileCode;                  // TPC x 512
-    uint8_t* sQ = sAux + TPC * Cfg::kTileAux;                   // NP x kQRow (canonical)
-    uint8_t* sSFB = sQ + NP * Cfg::kQRow;                       // 512
-    float* sW = reinterpret_cast<float*>(sSFB + 512);           // 64
-    uint64_t* bar_load = reinterpret_cast<uint64_t*>(sW + 64);  // TPC
-    uint64_t* bar_full = bar_load + TPC;                        // 2
-    uint64_t* bar_empty = bar_full + 2;                         // 2
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_empty + 2);
-    int32_t* half_ok = reinterpret_cast<int32_t*>(tmem_slot + 1);  // TPC x 2
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::oBars);
+    uint64_t* k_full = bars;              // per stage group: G arrivals (+ bytes)
+    uint64_t* k_empty = k_full + C::kSG;  // per stage group: one commit
+    uint64_t* q_full = k_empty + C::kSG;
+    uint64_t* q_empty = q_full + 2;
+    uint64_t* acc_full = q_empty + 2;
+    uint64_t* acc_empty = acc_full + kAccG;
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::oMisc);
+    // misc[0] tmem base, misc[1] start sequence, misc[2..3] start tile, misc[4..5] unit count,
+    // misc[6] abort flag
+    volatile uint32_t* abort_flag = misc + 6;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.y;
-    const int64_t t = a.cu_seqlens_q[b];
-    if (a.cu_seqlens_q[b + 1] <= t) return;  // sequence without a query
-    int64_t seq_len = a.seq_lens_k[b];
-    if (seq_len > a.max_seq_len_k || seq_len < 0) {
-        if (tid == 0 && blockIdx.x == 0) report(a.dev_status, IDX_STATUS_BAD_LEN);
-        seq_len = seq_len < 0 ? 0 : a.max_seq_len_k;
-    }
-    const int64_t nq = a.cu_seqlens_q[b + 1] - t;
-    const int64_t vis = visible_keys(seq_len, nq, nq - 1, a.causal);  // the last query
-    const int64_t tile0 = (int64_t)blockIdx.x * TPC;
-    const int64_t tiles_total = (vis + 127) / 128;
-    if (tile0 >= tiles_total) return;
-    const int n_tiles = (int)min((int64_t)TPC, tiles_total - tile0);
-    const int H = a.H;
-    const int P = a.page_size;
+    const int H = a.H, P = a.page_size;
+    const int Hq = (H + 7) & ~7;
 
-    if (tid == 0) {
+    // ---- this CTA's slice of the units: two warp-wide scans over the sequences ----------
+    if (warp == 0) {
+        int64_t total = 0;
+        for (int base = 0; base < a.B; base += 32) {
+            const int b = base + lane;
+            int64_t n = b < a.B ? seq_info(a, b).tiles : 0;
 #pragma unroll
-        for (int i = 0; i < TPC; ++i) tc::mbar_init(&bar_load[i], 1);
-        tc::mbar_init(&bar_full[0], 1);
-        tc::mbar_init(&bar_full[1], 1);
-        tc::mbar_init(&bar_empty[0], kEpi);
-        tc::mbar_init(&bar_empty[1], kEpi);
-        tc::fence_mbar_init();
-    }
-    __syncthreads();
-
-    // ---- issuer: every page copy of this CTA, issued at once -------------------------------
-    if (tid == kIssuer) {
-        const int32_t* pt = a.page_table + (int64_t)b * a.pt_stride;
-        for (int i = 0; i < n_tiles; ++i) {
-            const int64_t key0 = (tile0 + i) * 128;
-            const int halves = P == 128 ? 1 : (key0 + 64 < vis ? 2 : 1);
-            int32_t pages[2];
-            uint32_t bytes = 0;
-            for (int h = 0; h < halves; ++h) {
-                const int32_t pg = pt[(key0 + 64 * h) / P];
-                const bool ok = pg >= 0 && pg < a.num_pages;
-                if (!ok) report(a.dev_status, IDX_STATUS_BAD_PAGE);
-                pages[h] = ok ? pg : -1;
-                half_ok[2 * i + h] = ok;
-                if (ok) bytes += (uint32_t)(P * (Cfg::kTileCode / 128 + 4));
+            for (int o = 16; o >= 1; o >>= 1) n += __shfl_xor_sync(kFull, n, o);
+            total += n;
+        }
+        const int64_t u0 = total * blockIdx.x / gridDim.x, u1 = total * (blockIdx.x + 1) / gridDim.x;
+        int64_t acc = 0;
+        int b0 = a.B;
+        int64_t j0 = 0;
+        for (int base = 0; base < a.B && b0 == a.B; base += 32) {
+            const int b = base + lane;
+            const int64_t n = b < a.B ? seq_info(a, b).tiles : 0;
+            int64_t inc = n;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int64_t y = __shfl_up_sync(kFull, inc, o);
+                if (lane >= o) inc += y;
             }
-            if (halves == 1) half_ok[2 * i + 1] = (P == 128) ? half_ok[2 * i] : 0;
-            tc::mbar_arrive_expect_tx(&bar_load[i], bytes);
-            uint8_t* dK = sK + i * Cfg::kTileCode;
-            uint8_t* dA = sAux + i * Cfg::kTileAux;
-            for (int h = 0; h < halves; ++h) {
-                if (pages[h] < 0) continue;
-                const uint8_t* src = a.pool + (int64_t)pages[h] * a.page_stride;
-                if (P == 128) {
-                    tc::bulk_g2s(dK, src, Cfg::kTileCode, &bar_load[i]);
-                    tc::bulk_g2s(dA, src + Cfg::kTileCode, 512, &bar_load[i]);
-                } else if (kDtype == IDX_MXFP4) {
-                    // four 1 KB chunks of 16 keys interleave with the other page's chunks
-                    for (int q = 0; q < 4; ++q)
-                        tc::bulk_g2s(dK + q * 2048 + h * 1024, src + q * 1024, 1024, &bar_load[i]);
-                    tc::bulk_g2s(dA + h * 256, src + 4096, 256, &bar_load[i]);
-                } else {
-                    tc::bulk_g2s(dK + h * 8192, src, 8192, &bar_load[i]);
-                    tc::bulk_g2s(dA + h * 256, src + 8192, 256, &bar_load[i]);
-                }
+            const bool hit = n > 0 && acc + inc - n <= u0 && u0 < acc + inc;
+            const unsigned m = __ballot_sync(kFull, hit);
+            if (m) {
+                const int src = __ffs(m) - 1;
+                b0 = base + src;
+                j0 = u0 - (acc + __shfl_sync(kFull, inc - n, src));
             }
+            acc += __shfl_sync(kFull, inc, 31);
+        }
+        if (lane == 0) {
+            const int64_t n = b0 < a.B ? u1 - u0 : 0;
+            misc[1] = (uint32_t)b0;
+            misc[2] = (uint32_t)j0;
+            misc[3] = (uint32_t)(j0 >> 32);
+            misc[4] = (uint32_t)n;
+            misc[5] = (uint32_t)(n >> 32);
+            misc[6] = 0;
+            for (int i = 0; i < C::kSG; ++i) {
+                tc::mbar_init(&k_full[i], G);
+                tc::mbar_init(&k_empty[i], 1);
+            }
+            for (int i = 0; i < 2; ++i) {
+                tc::mbar_init(&q_full[i], 1);
+                tc::mbar_init(&q_empty[i], 1);
+            }
+            for (int i = 0; i < kAccG; ++i) {
+                tc::mbar_init(&acc_full[i], 1);
+                tc::mbar_init(&acc_empty[i], kEpiThreads);
+            }
+            tc::fence_mbar_init();
         }
     }
-
-    // ---- all threads: Q (canonical image, zero rows past H), its scale atom, weights ------
-    {
-        const uint8_t* qg = a.q_codes + t * H * Cfg::kQRow;
-        constexpr int kChunks = Cfg::kQRow / 16;
-        for (int i = tid; i < NP * kChunks; i += kThreads) {
-            const int h = i / kChunks, c = i % kChunks;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (h < H) v = *reinterpret_cast<const uint4*>(qg + h * Cfg::kQRow + 16 * c);
-            *reinterpret_cast<uint4*>(sQ + ((h >> 3) * kChunks + c) * 128 + (h & 7) * 16) = v;
-        }
-        if (kDtype == IDX_MXFP4) {
-            for (int h = tid; h < 128; h += kThreads) {
-                uint32_t s = 0x7f7f7f7fu;
-                if (h < H) s = *reinterpret_cast<const uint32_t*>(a.q_scales + (t * H + h) * 4);
-                *reinterpret_cast<uint32_t*>(sSFB + (h & 31) * 16 + (h >> 5) * 4) = s;
-            }
-        }
-        if (tid < 64) sW[tid] = tid < H ? a.w[t * H + tid] : 0.0f;
-    }
-    tc::fence_proxy_async();
-    __syncwarp();
-    if (warp == 4) {
-        tc::tmem_alloc(tmem_slot, kCols);
+    if (warp == 1) {
+        tc::tmem_alloc(&misc[0], C::kCols);
         tc::tmem_relinquish();
     }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    const uint32_t tbase = *tmem_slot;
-    const uint32_t t_sfa = tbase + 2 * NP;           // 4 columns per tile
-    const uint32_t t_sfb = t_sfa + 4 * TPC;          // 4 columns
-    bool ok = true;
+    const uint32_t tbase = misc[0];
+    const int b_start = (int)misc[1];
+    const int64_t j_start = (int64_t)misc[2] | ((int64_t)misc[3] << 32);
+    const int64_t n_units = (int64_t)misc[4] | ((int64_t)misc[5] << 32);
+    const int64_t n_groups = (n_units + G - 1) / G;
+    const int64_t n_slots = n_groups * G;  // tile slots incl. the last group's empty ones
 
-    // ---- issuer: MMAs, tile by tile, into accumulator buffer i % 2 --------------------------
-    if (tid == kIssuer) {
-        if (kDtype == IDX_MXFP4) tc::cp_32x128b_warpx4(t_sfb, tc::smem_desc(tc::smem_u32(sSFB), 128, 128));
-        for (int i = 0; i < n_tiles && ok; ++i) {
-            const int buf = i & 1;
-            if (i >= 2) ok = tc::mbar_wait(&bar_empty[buf], ((i - 2) >> 1) & 1);
-            ok = ok && tc::mbar_wait(&bar_load[i], 0);
-            if (!ok) break;
-            tc::tc_fence_after();
-            const uint32_t d = tbase + buf * NP;
-            const uint32_t a0 = tc::smem_u32(sK + i * Cfg::kTileCode), b0 = tc::smem_u32(sQ);
-            if (kDtype == IDX_MXFP4) {
-                tc::cp_32x128b_warpx4(t_sfa + 4 * i, tc::smem_desc(tc::smem_u32(sAux + i * 512), 128, 128));
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    tc::mma_mxf4(d, tc::smem_desc(a0 + j * 256, 128, Cfg::kSbo),
-                                 tc::smem_desc(b0 + j * 256, 128, Cfg::kSbo),
-                                 tc::idesc_mxf4(128, NP, 2 * j, 2 * j), t_sfa + 4 * i, t_sfb, j);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    tc::mma_f8(d, tc::smem_desc(a0 + j * 256, 128, Cfg::kSbo),
-                               tc::smem_desc(b0 + j * 256, 128, Cfg::kSbo), tc::idesc_f8(128, NP), j);
+    if (warp == 0 && n_units > 0) {
+        // ---------------------------------------------------------------- producer warp
+        // Tiles go out in batches of kBatch (whole stage groups, each group once): lane L
+        // owns tile slot i0+L and issues its page lookups, its stage-group wait and its bulk
+        // copies, so the warp issues the batch at once. Every wait of a lane depends only on
+        // earlier batches or on lower lanes, which never wait on it (no warp barrier inside
+        // a batch). Empty slots of the last group arrive without bytes.
+        Walker w;  // position of the batch's first unit (same in every lane)
+        w.init(a, b_start, j_start);
+        int prev_b = -1;     // sequence of the unit before the batch
+        int64_t q_base = 0;  // sequences started before the batch
+        for (int64_t i0 = 0; i0 < n_slots && !__any_sync(kFull, *abort_flag != 0); i0 += C::kBatch) {
+            const int nb = (int)min((int64_t)C::kBatch, n_units - i0);  // real tiles (may be <= 0)
+            const int ns = (int)min((int64_t)C::kBatch, n_slots - i0);  // slots
+            const bool real = lane < nb;
+            Walker my = w;
+            for (int k = 0; k < lane && k + 1 < nb; ++k) my.next(a);
+            const int b_before = __shfl_up_sync(kFull, my.b, 1);
+            const bool newseq = real && my.b != (lane == 0 ? prev_b : b_before);
+            const unsigned starts = __ballot_sync(kFull, newseq);
+            if (lane < ns) {
+                const int64_t i = i0 + lane;
+                const int64_t gi = i / G;
+                const int grp = (int)(gi % C::kSG);
+                int32_t pg[2] = {-1, -1};
+                int halves = 0;
+                if (real) {
+                    if (newseq) {
+                        const int64_t qk = q_base + __popc(starts & ((2u << lane) - 1)) - 1;
+                        const int slot = (int)(qk & 1);
+                        if (!tc::mbar_wait(&q_empty[slot], (uint32_t)(((qk >> 1) & 1) ^ 1))) {
+                            *abort_flag = 1;
+                        } else {
+                            const uint32_t qbytes = (uint32_t)(Hq * C::kQRow);
+                            tc::mbar_arrive_expect_tx(&q_full[slot], qbytes + C::kQSf);
+                            tc::bulk_g2s(smem + C::oQ + slot * C::kQImg, a.q_codes + my.si.t * Hq * C::kQRow,
+                                         qbytes, &q_full[slot]);
+                            if (kDtype == IDX_MXFP4)
+                                tc::bulk_g2s(smem + C::oQSf + slot * C::kQSf, a.q_scales + my.si.t * 512, 512,
+                                             &q_full[slot]);
+                        }
+                    }
+                    const int64_t key0 = my.j * 128;
+                    halves = P == 128 ? 1 : (key0 + 64 < my.si.vis ? 2 : 1);
+                    const int32_t* pt = a.page_table + (int64_t)my.b * a.pt_stride;
+                    pg[0] = __ldg(pt + key0 / P);
+                    if (halves == 2) pg[1] = __ldg(pt + (key0 + 64) / P);
+                }
+                if (*abort_flag || !tc::mbar_wait(&k_empty[grp], (uint32_t)(((gi / C::kSG) & 1) ^ 1))) {
+                    *abort_flag = 1;
+                } else {
+                    uint32_t bytes = 0;
+                    for (int h = 0; h < halves; ++h) {
+                        if (pg[h] >= 0 && pg[h] < a.num_pages) {
+                            bytes += (uint32_t)(P * (C::kTileCode / 128 + C::kTileSf / 128));
+                        } else {
+                            report(a.dev_status, IDX_STATUS_BAD_PAGE);
+                            pg[h] = -1;
+                        }
+                    }
+                    tc::mbar_arrive_expect_tx(&k_full[grp], bytes);
+                    uint8_t* dK = smem + C::oStages + grp * C::kGroup + (int)(i % G) * C::kTile;
+                    uint8_t* dS = dK + C::kTileCode;
+                    for (int h = 0; h < halves; ++h) {
+                        if (pg[h] < 0) continue;
+                        const uint8_t* src = a.pool + (int64_t)pg[h] * a.page_stride;
+                        if (P == 128) {
+                            // codes and scale atom are contiguous in the page and in the stage
+                            tc::bulk_g2s(dK, src, C::kTile, &k_full[grp]);
+                        } else if (kDtype == IDX_MXFP4) {
+                            // four 1 KB chunks of 16 keys interleave with the other page's chunks
+                            for (int q = 0; q < 4; ++q)
+                                tc::bulk_g2s(dK + q * 2048 + h * 1024, src + q * 1024, 1024, &k_full[grp]);
+                            tc::bulk_g2s(dS + h * 256, src + 4096, 256, &k_full[grp]);
+                        } else {
+                            tc::bulk_g2s(dK + h * 8192, src, 8192, &k_full[grp]);
+                        }
+                    }
+                }
             }
-            tc::mma_commit(&bar_full[buf]);
+            __syncwarp();
+            if (nb <= 0) break;
+            // next batch: one unit after this batch's last real unit
+            const int src = (nb < C::kBatch ? nb : C::kBatch) - 1;
+            Walker last = my;
+            last.b = __shfl_sync(kFull, my.b, src);
+            last.j = __shfl_sync(kFull, my.j, src);
+            last.si.t = __shfl_sync(kFull, my.si.t, src);
+            last.si.vis = __shfl_sync(kFull, my.si.vis, src);
+            last.si.tiles = __shfl_sync(kFull, my.si.tiles, src);
+            prev_b = last.b;
+            q_base += __popc(starts);
+            w = last;
+            if (i0 + C::kBatch < n_units) w.next(a);
         }
-        if (!ok) report(a.dev_status, IDX_STATUS_TIMEOUT);
-    }
-
-    // ---- epilogue: lane m of the tile = one key ---------------------------------------------
-    const int m = warp * 32 + lane;
-    const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
-    // key offset of row m inside the tile; for two 64-key pages, rows with m%32 < 16 come from
-    // the first page (its keys s%16 + 16*(m/32)... see the page layout in idx.h)
-    const int half = (P == 64 && kDtype == IDX_MXFP4) ? ((m >> 4) & 1) : (m >> 6);
-    const int koff = (P == 64 && kDtype == IDX_MXFP4) ? (64 * half + (m & 15) + 16 * (m >> 5)) : m;
-    float* out = a.logits + t * a.ld;
-    for (int i = 0; i < n_tiles && tid < kEpi; ++i) {
-        const int buf = i & 1;
-        // warp-uniform, since tcgen05.ld is a warp-collective instruction
-        const bool got = __all_sync(0xffffffffu, tc::mbar_wait(&bar_full[buf], (i >> 1) & 1));
-        tc::tc_fence_after();
-        float v[NP];
-        if (got) load_acc<NP>(lane_addr + buf * NP, v);
-        tc::tc_fence_before();
-        tc::mbar_arrive(&bar_empty[buf]);
-        if (!got) {
-            report(a.dev_status, IDX_STATUS_TIMEOUT);
-            break;
-        }
-        const int64_t key = (tile0 + i) * 128 + koff;
-        const bool row_ok = key < vis && half_ok[2 * i + (P == 128 ? 0 : half)];
-        float logit = 0.0f;
+        if (lane == 0 && *abort_flag) report(a.dev_status, IDX_STATUS_TIMEOUT);
+    } else if (warp == 1 && lane == 0 && n_units > 0) {
+        // ---------------------------------------------------------------- MMA issuer
+        // tensor memory: accumulators [kAccG][G][NP], then A scale slots [kAccG][G][4] (a slot
+        // is rewritten only after the epilogue released its accumulator group, i.e. after the
+        // MMAs that read it ended), then the B scale slot of each Q slot [2][4]
+        const uint32_t t_sfa = tbase + kAccG * G * NP;
+        const uint32_t t_sfb = t_sfa + kAccG * G * 4;
+        // descriptors of stage 0 / Q slot 0; other tiles, slots and K steps add (bytes >> 4)
+        // to the start-address field (shared-memory addresses stay below 256 KB)
+        const uint64_t dA0 = tc::smem_desc(tc::smem_u32(smem + C::oStages), 128, C::kSbo);
+        const uint64_t dB0 = tc::smem_desc(tc::smem_u32(smem + C::oQ), 128, C::kSbo);
+        const uint64_t dSA0 = tc::smem_desc(tc::smem_u32(smem + C::oStages + C::kTileCode), 128, 128);
+        const uint64_t dSB0 = tc::smem_desc(tc::smem_u32(smem + C::oQSf), 128, 128);
+        const uint32_t id0 = kDtype == IDX_MXFP4 ? tc::idesc_mxf4(128, NP, 0, 0) : tc::idesc_f8(128, NP);
+        const uint32_t id1 = kDtype == IDX_MXFP4 ? tc::idesc_mxf4(128, NP, 2, 2) : id0;
+        Walker w;
+        w.init(a, b_start, j_start);
+        int prev_b = -1;
+        int64_t qk = -1;
+        int slot = 0;
+        int grp = 0, ag = 0;
+        uint32_t kph = 0, aph = 1;  // parity to wait for: k_full[grp], acc_empty[ag]
+        for (int64_t gi = 0; gi < n_groups; ++gi) {
+            if (*abort_flag) break;
+            if (!tc::mbar_wait(&k_full[grp], kph) || !tc::mbar_wait(&acc_empty[ag], aph)) {
+                *abort_flag = 1;
+                break;
+            }
+            tc::tc_fence_after();
+            for (int t = 0; t < G; ++t) {
+                const int64_t i = gi * G + t;
+                if (i >= n_units) break;
+                if (w.b != prev_b) {
+                    ++qk;
+                    slot = (int)(qk & 1);
+                    if (!tc::mbar_wait(&q_full[slot], (uint32_t)((qk >> 1) & 1))) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    if (kDtype == IDX_MXFP4)
+                        tc::cp_32x128b_warpx4(t_sfb + 4 * slot, dSB0 + (uint64_t)((slot * C::kQSf) >> 4));
+                    prev_b = w.b;
+                }
+                const int cell = ag * G + t;
+                const uint32_t d = tbase + cell * NP;
+                const int off = grp * C::kGroup + t * C::kTile;
+                const uint64_t da = dA0 + (uint64_t)(off >> 4);
+                const uint64_t db = dB0 + (uint64_t)((slot * C::kQImg) >> 4);
+                if (kDtype == IDX_MXFP4) {
+                    const uint32_t sfa = t_sfa + 4 * cell;
+                    tc::cp_32x128b_warpx4(sfa, dSA0 + (uint64_t)(off >> 4));
+                    tc::mma_mxf4(d, da, db, id0, sfa, t_sfb + 4 * slot, 0);
+                    tc::mma_mxf4(d, da + 16, db + 16, id1, sfa, t_sfb + 4 * slot, 1);
+                } else {
 #pragma unroll
-        for (int h = 0; h < NP; ++h)
-            if (h < H) logit = fmaf(sW[h], fmaxf(v[h], 0.0f), logit);
-        if (kDtype == IDX_FP8) logit *= reinterpret_cast<const float*>(sAux + i * Cfg::kTileAux)[m];
-        if (row_ok) out[key] = logit;
+                    for (int k = 0; k < 4; ++k) tc::mma_f8(d, da + 16 * k, db + 16 * k, id0, k);
+                }
+                const int cur_b = w.b;
+                w.next(a);
+                if (i + 1 == n_units || w.b != cur_b) tc::mma_commit(&q_empty[slot]);
+            }
+            if (*abort_flag) break;
+            tc::mma_commit(&k_empty[grp]);
+            tc::mma_commit(&acc_full[ag]);
+            if (++grp == C::kSG) { grp = 0; kph ^= 1; }
+            if (++ag == kAccG) { ag = 0; aph ^= 1; }
+        }
+        if (*abort_flag) report(a.dev_status, IDX_STATUS_TIMEOUT);
+    } else if (warp >= 2 && n_units > 0) {
+        // ---------------------------------------------------------------- epilogue
+        const int quad = warp & 3;
+        const int m = quad * 32 + lane;
+        const uint32_t lane_addr = tbase + ((uint32_t)(quad * 32) << 16);
+        // key offset of TMEM row m inside its tile: for two 64-key MXFP4 pages, rows with
+        // m % 32 < 16 hold the first page's keys (m % 16) + 16 * (m / 32)
+        const bool split = P == 64 && kDtype == IDX_MXFP4;
+        const int half = split ? ((m >> 4) & 1) : (m >> 6);
+        const int koff = split ? (64 * half + (m & 15) + 16 * (m >> 5)) : m;
+        Walker w;
+        w.init(a, b_start, j_start);
+        int prev_b = -1;
+        float wr[NP];
+        int ag = 0;
+        uint32_t aph = 0;
+        for (int64_t gi = 0; gi < n_groups; ++gi) {
+            // the group's page lookups are issued before the accumulator wait (their latency
+            // hides behind it); their values are used after it
+            int32_t pg[G];
+            Walker wk = w;
+#pragma unroll
+            for (int t = 0; t < G; ++t) {
+                const int64_t i = gi * G + t;
+                const int64_t key = wk.j * 128 + koff;
+                pg[t] = (i < n_units && key < wk.si.vis) ? __ldg(a.page_table + (int64_t)wk.b * a.pt_stride + key / P) : -1;
+                if (i + 1 < n_units) wk.next(a);
+            }
+            const bool got = __all_sync(kFull, tc::mbar_wait(&acc_full[ag], aph));
+            if (!got) {
+                *abort_flag = 1;
+                report(a.dev_status, IDX_STATUS_TIMEOUT);
+                break;
+            }
+            tc::tc_fence_after();
+#pragma unroll
+            for (int t = 0; t < G; ++t) {
+                const int64_t i = gi * G + t;
+                if (i >= n_units) break;
+                if (w.b != prev_b) {
+#pragma unroll
+                    for (int h = 0; h < NP; ++h) wr[h] = h < H ? __ldg(a.w + w.si.t * H + h) : 0.0f;
+                    prev_b = w.b;
+                }
+                const int64_t key = w.j * 128 + koff;
+                const bool key_ok = key < w.si.vis && pg[t] >= 0 && pg[t] < a.num_pages;
+                float kscale = 1.0f;
+                if (kDtype == IDX_FP8 && key_ok)
+                    kscale = __ldg(reinterpret_cast<const float*>(a.pool + (int64_t)pg[t] * a.page_stride + 128 * P +
+                                                                  4 * (key % P)));
+                float v[NP];
+                load_acc<NP>(lane_addr + (ag * G + t) * NP, v);
+                // four independent accumulation chains over the heads
+                float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int h = 0; h < NP; ++h)
+                    if (h < H) part[h & 3] = fmaf(wr[h], fmaxf(v[h], 0.0f), part[h & 3]);
+                const float logit = (part[0] + part[1]) + (part[2] + part[3]);
+                if (key_ok) a.logits[w.si.t * a.ld + key] = logit * kscale;
+                w.next(a);
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(&acc_empty[ag]);
+            if (++ag == kAccG) { ag = 0; aph ^= 1; }
+        }
     }
 
     tc::tc_fence_before();
     __syncthreads();
-    if (warp == 4) {
+    if (warp == 1) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tbase, kCols);
+        tc::tmem_dealloc(tbase, C::kCols);
     }
 }
 
+int sm_count() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 1;
+    }
+    return n;
+}
+
 template <int kDtype, int NP>
-cudaError_t launch_decode_np(const ScoreArgs& a, cudaStream_t st) {
-    using Cfg = DecodeCfg<kDtype>;
-    const size_t smem = Cfg::kTiles * (Cfg::kTileCode + Cfg::kTileAux) + NP * Cfg::kQRow + 512 +
-                        256 + 8 * (Cfg::kTiles + 4) + 4 + 8 * Cfg::kTiles + 64;
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<kDtype, NP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+cudaError_t launch_np(const ScoreArgs& a, cudaStream_t st) {
+    using C = Cfg<kDtype, NP>;
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<kDtype, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmem);
     if (e != cudaSuccess) return e;
-    const int64_t tiles = (a.max_seq_len_k + 127) / 128;
-    dim3 grid((unsigned)((tiles + Cfg::kTiles - 1) / Cfg::kTiles), (unsigned)a.B);
-    decode_kernel<kDtype, NP><<<grid, kThreads, smem, st>>>(a);
+    // an upper bound of the unit count sizes the grid (a CTA with no units exits)
+    const int64_t units_max = (int64_t)a.B * ((a.max_seq_len_k + 127) / 128);
+    const int ctas = C::kCps * sm_count();
+    const int grid = (int)(units_max < ctas ? (units_max > 0 ? units_max : 1) : ctas);
+    decode_kernel<kDtype, NP><<<grid, kThreads, C::kSmem, st>>>(a);
     return cudaGetLastError();
 }
 
 template <int kDtype>
-cudaError_t launch_decode_dt(const ScoreArgs& a, cudaStream_t st) {
-    if (a.H <= 16) return launch_decode_np<kDtype, 16>(a, st);
-    if (a.H <= 32) return launch_decode_np<kDtype, 32>(a, st);
-    return launch_decode_np<kDtype, 64>(a, st);
+cudaError_t launch_dt(const ScoreArgs& a, cudaStream_t st) {
+    if (a.H <= 16) return launch_np<kDtype, 16>(a, st);
+    if (a.H <= 32) return launch_np<kDtype, 32>(a, st);
+    return launch_np<kDtype, 64>(a, st);
 }
 
 }  // namespace
 
 cudaError_t launch_scorer_decode(const ScoreArgs& a, cudaStream_t st) {
     if (a.T == 0 || a.max_seq_len_k == 0 || a.B == 0) return cudaSuccess;
-    return a.dtype == IDX_MXFP4 ? launch_decode_dt<IDX_MXFP4>(a, st) : launch_decode_dt<IDX_FP8>(a, st);
+    return a.dtype == IDX_MXFP4 ? launch_dt<IDX_MXFP4>(a, st) : launch_dt<IDX_FP8>(a, st);
 }
 
 }  // namespace idx

@@ -1,0 +1,453 @@
+// scorer_prefill.cu -- paged MQA-logits scorer for prefill / chunked prefill (many queries
+// per sequence, optionally causal) on the 5th-generation tensor cores.
+//
+//   logits[t, s] = sum_h w[t,h] * ReLU(q[t,h] . k[s])               (MXFP4)
+//   logits[t, s] = kscale[s] * sum_h w[t,h] * ReLU(q[t,h] . k[s])   (FP8)
+//
+// vllm PR 57517 "Performance and accuracy" (prefill scorer, 8192 queries / H32 / 8K) and
+// vllm PR 60834 "Purpose" (the paged cache is scored in place, so prefill no longer gathers
+// K first).
+//
+// Operands: A = a 128-key tile of the sequence's paged cache (as in the decode scorer), B =
+// a block of QB queries x Hq heads = N <= 256 rows of the quantised Q image (consecutive
+// queries' images concatenate into one canonical operand). One block-scaled MMA pair
+// (kind::mxf4, K = 64 each) or four kind::f8f6f4 MMAs (K = 32) give D[key][query, head]
+// in tensor memory. The ReLU-weighted head sum is the epilogue: each thread owns one key
+// and half of the block's queries, so no cross-thread reduction is needed.
+//
+// The work per query block grows with its position (causal), so the persistent CTAs take
+// query blocks heaviest first, in snake order (CTA c gets ranks c, 2G-1-c, 2G+c, ...).
+// Roles: warp 0 = producer (Q block image by bulk copy, its scale atoms assembled by the
+// warp's lanes, K tiles into a ring of stages by bulk copy); warp 1 = tensor-memory owner
+// and MMA issuer; warps 2-9 = epilogue, two warps per 32-lane TMEM quadrant. The single
+// accumulator is drained to registers at once, so the next tile's MMAs run while the
+// epilogue does its (ALU-bound) head sums.
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace idx {
+
+namespace {
+
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kN = 256;  // B rows (query x head) per block, at most
+
+template <int kDtype>
+struct PCfg {
+    static constexpr int kTileCode = kDtype == IDX_MXFP4 ? 128 * 64 : 128 * 128;
+    static constexpr int kTileSf = kDtype == IDX_MXFP4 ? 512 : 0;
+    static constexpr int kStage = kTileCode + kTileSf;
+    static constexpr int kStages = kDtype == IDX_MXFP4 ? 12 : 6;
+    static constexpr int kQRow = kDtype == IDX_MXFP4 ? 64 : 128;
+    static constexpr int kQImg = kN * kQRow;
+    static constexpr int kQSf = kDtype == IDX_MXFP4 ? 1024 : 0;  // two scale atoms
+    static constexpr uint32_t kSbo = kDtype == IDX_MXFP4 ? 512 : 1024;
+    static constexpr uint32_t kCols = 512;  // accumulator 256 + scale factors
+    static constexpr int oStages = 0;
+    static constexpr int oQ = kStages * kStage;   // two Q slots (double-buffered blocks)
+    static constexpr int oQSf = oQ + 2 * kQImg;
+    static constexpr int oBars = oQSf + 2 * kQSf;
+    static constexpr int kBars = 2 * kStages + 6;
+    static constexpr int oMisc = oBars + 8 * kBars;
+    static constexpr int kSmem = oMisc + 64;
+};
+
+// Query block geometry: each query's Hq = roundup(H, 8) image rows are placed HP rows apart
+// in B (HP = the power of two >= Hq, 8..64), QB = 256 / HP queries per block, N = 256.
+struct Geo {
+    int Hq, QB, N;
+};
+template <int HP>
+__device__ __forceinline__ Geo geo(int H) {
+    Geo g;
+    g.Hq = (H + 7) & ~7;
+    g.QB = kN / HP;
+    g.N = kN;
+    return g;
+}
+
+struct Unit {
+    int b;
+    int64_t q0, nq_blk;   // first query (sequence-local) and queries in this block
+    int64_t t0;           // global row of the sequence's first query
+    int64_t nq, len;      // queries and keys of the sequence
+    int64_t tiles;        // 128-key tiles to score
+};
+
+// Unit of virtual rank v: blocks are ranked heaviest first: v -> (jr = v / B, b = v % B),
+// block j = MB - 1 - jr of sequence b (empty if the sequence has fewer blocks).
+__device__ __forceinline__ bool unit_of(const ScoreArgs& a, const Geo& g, int64_t MB, int64_t v, Unit& u) {
+    const int64_t jr = v / a.B;
+    u.b = (int)(v - jr * a.B);
+    const int64_t j = MB - 1 - jr;
+    u.t0 = a.cu_seqlens_q[u.b];
+    u.nq = a.cu_seqlens_q[u.b + 1] - u.t0;
+    u.q0 = j * g.QB;
+    if (u.nq <= 0 || u.q0 >= u.nq) return false;
+    u.nq_blk = min((int64_t)g.QB, u.nq - u.q0);
+    int64_t len = a.seq_lens_k[u.b];
+    u.len = len < 0 ? 0 : (len > a.max_seq_len_k ? a.max_seq_len_k : len);
+    const int64_t vis_last = visible_keys(u.len, u.nq, u.q0 + u.nq_blk - 1, a.causal);
+    u.tiles = (vis_last + 127) / 128;
+    return u.tiles > 0;
+}
+
+// Iterates this CTA's units: ranks c, 2G-1-c, 2G+c, 4G-1-c, ... (snake order).
+struct Sched {
+    int64_t k, V, MB;
+    int c, G;
+    Geo g;
+    __device__ __forceinline__ void init(const ScoreArgs& a, const Geo& gg) {
+        g = gg;
+        MB = ((int64_t)a.max_q_len + g.QB - 1) / g.QB;
+        V = MB * a.B;
+        k = 0;
+        c = blockIdx.x;
+        G = gridDim.x;
+    }
+    __device__ __forceinline__ bool next(const ScoreArgs& a, Unit& u) {
+        for (;;) {
+            const int64_t v = k * G + ((k & 1) ? (G - 1 - c) : c);
+            if (k * G >= V) return false;
+            ++k;
+            if (v < V && unit_of(a, g, MB, v, u)) return true;
+        }
+    }
+};
+
+template <int kDtype, int HP>
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
+    using C = PCfg<kDtype>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::oBars);
+    uint64_t* k_full = bars;
+    uint64_t* k_empty = k_full + C::kStages;
+    uint64_t* q_full = k_empty + C::kStages;   // 2
+    uint64_t* q_empty = q_full + 2;            // 2
+    uint64_t* acc_full = q_empty + 2;
+    uint64_t* acc_empty = acc_full + 1;
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::oMisc);
+    volatile uint32_t* abort_flag = misc + 1;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = a.H, P = a.page_size;
+    const Geo g = geo<HP>(H);
+    constexpr int QB = kN / HP;
+
+    if (tid == 0) {
+        misc[1] = 0;
+        for (int i = 0; i < C::kStages; ++i) {
+            tc::mbar_init(&k_full[i], 1);
+            tc::mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&q_full[i], 1);
+            tc::mbar_init(&q_empty[i], 1);
+        }
+        tc::mbar_init(acc_full, 1);
+        tc::mbar_init(acc_empty, kEpiThreads);
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(&misc[0], C::kCols);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tbase = misc[0];
+    const uint32_t t_sfa = tbase + kN;       // 2 x 4 columns (alternating tiles)
+    const uint32_t t_sfb = t_sfa + 8;        // per Q slot: 2 atoms x 4 columns
+
+    Sched sch;
+    sch.init(a, g);
+    Unit u;
+
+    if (warp == 0) {
+        // -------------------------------------------------------------- producer warp
+        int64_t n_units = 0, kt = 0;  // units and tiles issued so far
+        while (sch.next(a, u)) {
+            if (__any_sync(kFull, *abort_flag != 0)) break;  // warp-uniform exit
+            // Q block into slot n % 2, once the MMAs of block n-2 are done with that slot
+            const int slot = (int)(n_units & 1);
+            if (!__all_sync(kFull, tc::mbar_wait(&q_empty[slot], (uint32_t)(((n_units >> 1) & 1) ^ 1)))) {
+                if (lane == 0) *abort_flag = 1;
+                break;
+            }
+            const uint32_t qrow_bytes = (uint32_t)(g.Hq * C::kQRow);  // one query's image
+            const uint32_t qbytes = (uint32_t)u.nq_blk * qrow_bytes;
+            if (kDtype == IDX_MXFP4) {
+                // scale atoms of B: row n = q*Hq + h -> byte (n%32)*16 + ((n/32)%4)*4 of atom n/128,
+                // from query q's own atom (head h at (h%32)*16 + (h/32)*4)
+                uint8_t* sf = smem + C::oQSf + slot * C::kQSf;
+                for (int n = lane; n < kN; n += 32) {
+                    const int q = n / HP, h = n % HP;
+                    uint32_t v = 0x7f7f7f7fu;
+                    if (q < u.nq_blk && h < g.Hq)
+                        v = *reinterpret_cast<const uint32_t*>(a.q_scales + (u.t0 + u.q0 + q) * 512 +
+                                                               (h & 31) * 16 + (h >> 5) * 4);
+                    *reinterpret_cast<uint32_t*>(sf + (n >> 7) * 512 + (n & 31) * 16 + ((n >> 5) & 3) * 4) = v;
+                }
+                tc::fence_proxy_async();
+            }
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive_expect_tx(&q_full[slot], qbytes);
+                const uint8_t* qsrc = a.q_codes + (u.t0 + u.q0) * g.Hq * C::kQRow;
+                uint8_t* qdst = smem + C::oQ + slot * C::kQImg;
+                if (g.Hq == HP) {
+                    tc::bulk_g2s(qdst, qsrc, qbytes, &q_full[slot]);
+                } else {  // padded spacing: one copy per query (padding rows are never summed)
+                    for (int q = 0; q < u.nq_blk; ++q)
+                        tc::bulk_g2s(qdst + q * HP * C::kQRow, qsrc + q * qrow_bytes, qrow_bytes, &q_full[slot]);
+                }
+            }
+            // K tiles in batches: lane L owns tile j0+L (page lookup, stage wait, copies), so
+            // the warp issues a batch at once; a batch never reuses a stage, and each lane's
+            // wait depends only on tiles of earlier batches
+            constexpr int kBatch = C::kStages < 16 ? C::kStages : 16;
+            const int32_t* pt = a.page_table + (int64_t)u.b * a.pt_stride;
+            for (int64_t j0 = 0; j0 < u.tiles && !__any_sync(kFull, *abort_flag != 0); j0 += kBatch) {
+                const int nb = (int)min((int64_t)kBatch, u.tiles - j0);
+                if (lane < nb) {
+                    const int64_t j = j0 + lane, k = kt + lane;
+                    const int64_t key0 = j * 128;
+                    const int halves = P == 128 ? 1 : (key0 + 64 < u.len ? 2 : 1);
+                    int32_t pg[2] = {__ldg(pt + key0 / P), halves == 2 ? __ldg(pt + (key0 + 64) / P) : -1};
+                    const int s = (int)(k % C::kStages);
+                    if (!tc::mbar_wait(&k_empty[s], (uint32_t)(((k / C::kStages) & 1) ^ 1))) {
+                        *abort_flag = 1;
+                    } else {
+                        uint32_t bytes = 0;
+                        for (int hh = 0; hh < halves; ++hh) {
+                            if (pg[hh] >= 0 && pg[hh] < a.num_pages) {
+                                bytes += (uint32_t)(P * (C::kTileCode / 128 + C::kTileSf / 128));
+                            } else {
+                                report(a.dev_status, IDX_STATUS_BAD_PAGE);
+                                pg[hh] = -1;
+                            }
+                        }
+                        tc::mbar_arrive_expect_tx(&k_full[s], bytes);
+                        uint8_t* dK = smem + C::oStages + s * C::kStage;
+                        uint8_t* dS = dK + C::kTileCode;
+                        for (int hh = 0; hh < halves; ++hh) {
+                            if (pg[hh] < 0) continue;
+                            const uint8_t* src = a.pool + (int64_t)pg[hh] * a.page_stride;
+                            if (P == 128) {
+                                tc::bulk_g2s(dK, src, C::kTileCode, &k_full[s]);
+                                if (kDtype == IDX_MXFP4) tc::bulk_g2s(dS, src + C::kTileCode, 512, &k_full[s]);
+                            } else if (kDtype == IDX_MXFP4) {
+                                for (int q = 0; q < 4; ++q)
+                                    tc::bulk_g2s(dK + q * 2048 + hh * 1024, src + q * 1024, 1024, &k_full[s]);
+                                tc::bulk_g2s(dS + hh * 256, src + 4096, 256, &k_full[s]);
+                            } else {
+                                tc::bulk_g2s(dK + hh * 8192, src, 8192, &k_full[s]);
+                            }
+                        }
+                    }
+                }
+                kt += nb;
+                __syncwarp();
+            }
+            ++n_units;
+            __syncwarp();
+        }
+        if (lane == 0 && *abort_flag) report(a.dev_status, IDX_STATUS_TIMEOUT);
+    } else if (warp == 1) {
+        // -------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            // descriptors of stage 0 / Q slot 0; stages, slots and K steps add (bytes >> 4)
+            // to the start-address field (shared-memory addresses stay below 256 KB)
+            const uint64_t dA0 = tc::smem_desc(tc::smem_u32(smem + C::oStages), 128, C::kSbo);
+            const uint64_t dB0 = tc::smem_desc(tc::smem_u32(smem + C::oQ), 128, C::kSbo);
+            const uint64_t dSA0 = tc::smem_desc(tc::smem_u32(smem + C::oStages + C::kTileCode), 128, 128);
+            const uint64_t dSB0 = tc::smem_desc(tc::smem_u32(smem + C::oQSf), 128, 128);
+            const uint32_t id0 = kDtype == IDX_MXFP4 ? tc::idesc_mxf4(128, kN, 0, 0) : tc::idesc_f8(128, kN);
+            const uint32_t id1 = kDtype == IDX_MXFP4 ? tc::idesc_mxf4(128, kN, 2, 2) : id0;
+            int64_t n_units = 0;
+            int s = 0;
+            uint32_t kph = 0, aph = 1, sfa_sel = 0;
+            while (sch.next(a, u)) {
+                if (*abort_flag) break;
+                const int slot = (int)(n_units & 1);
+                if (!tc::mbar_wait(&q_full[slot], (uint32_t)((n_units >> 1) & 1))) {
+                    *abort_flag = 1;
+                    break;
+                }
+                tc::tc_fence_after();
+                const uint64_t db = dB0 + (uint64_t)((slot * C::kQImg) >> 4);
+                const uint32_t sfb = t_sfb + 8 * slot;
+                if (kDtype == IDX_MXFP4) {
+                    // B's two scale atoms: rows 0-127 and 128-255
+                    const uint64_t dsb = dSB0 + (uint64_t)((slot * C::kQSf) >> 4);
+                    tc::cp_32x128b_warpx4(sfb, dsb);
+                    tc::cp_32x128b_warpx4(sfb + 4, dsb + 32);
+                }
+                bool ok = true;
+                for (int64_t j = 0; j < u.tiles; ++j) {
+                    if (!tc::mbar_wait(&k_full[s], kph) || !tc::mbar_wait(acc_empty, aph)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    const uint64_t da = dA0 + (uint64_t)((s * C::kStage) >> 4);
+                    if (kDtype == IDX_MXFP4) {
+                        const uint32_t sfa = t_sfa + 4 * sfa_sel;
+                        tc::cp_32x128b_warpx4(sfa, dSA0 + (uint64_t)((s * C::kStage) >> 4));
+                        tc::mma_mxf4(tbase, da, db, id0, sfa, sfb, 0);
+                        tc::mma_mxf4(tbase, da + 16, db + 16, id1, sfa, sfb, 1);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) tc::mma_f8(tbase, da + 16 * k, db + 16 * k, id0, k);
+                    }
+                    tc::mma_commit(&k_empty[s]);
+                    tc::mma_commit(acc_full);
+                    if (++s == C::kStages) { s = 0; kph ^= 1; }
+                    aph ^= 1;
+                    sfa_sel ^= 1;
+                }
+                if (!ok) {
+                    *abort_flag = 1;
+                    break;
+                }
+                tc::mma_commit(&q_empty[slot]);
+                ++n_units;
+            }
+            if (*abort_flag) report(a.dev_status, IDX_STATUS_TIMEOUT);
+        }
+    } else {
+        // -------------------------------------------------------------- epilogue warps
+        const int ew = warp - 2;          // 0..7
+        const int quad = warp & 3;        // TMEM lane quadrant this warp may access
+        const int half = ew >> 2;         // which half of the block's columns
+        const int m = quad * 32 + lane;
+        const uint32_t lane_addr = tbase + ((uint32_t)(quad * 32) << 16) + half * (kN / 2);
+        const bool split = P == 64 && kDtype == IDX_MXFP4;
+        const int khalf = split ? ((m >> 4) & 1) : (m >> 6);
+        const int koff = split ? (64 * khalf + (m & 15) + 16 * (m >> 5)) : m;
+        constexpr int QH = QB / 2;  // queries per half (two chunks of 64 / HP)
+        const int qh0 = half * QH;
+        int64_t kt = 0;
+        while (sch.next(a, u)) {
+            const int32_t* pt = a.page_table + (int64_t)u.b * a.pt_stride;
+            for (int64_t j = 0; j < u.tiles; ++j, ++kt) {
+                // page lookups are issued before the accumulator wait (their latency hides
+                // behind it) and used after it
+                const int64_t key = j * 128 + koff;
+                const bool in_seq = key < u.len;
+                const int32_t pg = in_seq ? __ldg(pt + key / P) : -1;
+                const bool got = __all_sync(kFull, tc::mbar_wait(acc_full, (uint32_t)(kt & 1)));
+                if (!got) {
+                    *abort_flag = 1;
+                    report(a.dev_status, IDX_STATUS_TIMEOUT);
+                    break;
+                }
+                tc::tc_fence_after();
+                const bool key_ok = in_seq && pg >= 0 && pg < a.num_pages;
+                float kscale = 1.0f;
+                if (kDtype == IDX_FP8 && key_ok)
+                    kscale = __ldg(reinterpret_cast<const float*>(a.pool + (int64_t)pg * a.page_stride + 128 * P + 4 * (key % P)));
+                // this half's 128 columns (queries qh0 .. qh0+QH-1, HP columns each), drained in
+                // two chunks of 64; the accumulator is released after the second load, so the
+                // next tile's MMAs overlap the second chunk's head sums
+#pragma unroll
+                for (int chunk = 0; chunk < 2; ++chunk) {
+                    float v[64];
+#pragma unroll
+                    for (int c = 0; c < 64; c += 32) {
+                        uint32_t r[32];
+                        tc::tmem_ld32(lane_addr + chunk * 64 + c, r);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[c + i] = __uint_as_float(r[i]);
+                    }
+                    tc::tmem_ld_wait();
+                    if (chunk == 1) {
+                        tc::tc_fence_before();
+                        tc::mbar_arrive(acc_empty);
+                    }
+                    constexpr int QC = 64 / HP;  // queries in this chunk
+#pragma unroll
+                    for (int qq = 0; qq < QC; ++qq) {
+                        const int q = qh0 + chunk * QC + qq;
+                        if (q >= u.nq_blk) break;
+                        const int64_t qi = u.q0 + q;  // sequence-local query index
+                        const int64_t t = u.t0 + qi;
+                        float logit = 0.0f;
+                        if ((H & 3) == 0) {
+                            const float4* w4 = reinterpret_cast<const float4*>(a.w + t * H);
+#pragma unroll
+                            for (int h = 0; h < HP; h += 4) {
+                                if (h < H) {
+                                    const float4 ww = __ldg(w4 + h / 4);
+                                    logit = fmaf(ww.x, fmaxf(v[qq * HP + h], 0.0f), logit);
+                                    logit = fmaf(ww.y, fmaxf(v[qq * HP + h + 1], 0.0f), logit);
+                                    logit = fmaf(ww.z, fmaxf(v[qq * HP + h + 2], 0.0f), logit);
+                                    logit = fmaf(ww.w, fmaxf(v[qq * HP + h + 3], 0.0f), logit);
+                                }
+                            }
+                        } else {
+                            const float* wq = a.w + t * H;
+#pragma unroll
+                            for (int h = 0; h < HP; ++h)
+                                if (h < H) logit = fmaf(__ldg(wq + h), fmaxf(v[qq * HP + h], 0.0f), logit);
+                        }
+                        if (key_ok && key < visible_keys(u.len, u.nq, qi, a.causal))
+                            a.logits[t * a.ld + key] = logit * kscale;
+                    }
+                }
+            }
+            if (__any_sync(kFull, *abort_flag != 0)) break;  // warp-uniform exit
+        }
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tbase, C::kCols);
+    }
+}
+
+int sm_count() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 1;
+    }
+    return n;
+}
+
+template <int kDtype, int HP>
+cudaError_t launch_hp(const ScoreArgs& a, cudaStream_t st) {
+    using C = PCfg<kDtype>;
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kDtype, HP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmem);
+    if (e != cudaSuccess) return e;
+    constexpr int QB = kN / HP;
+    const int64_t units = (int64_t)a.B * ((a.max_q_len + QB - 1) / QB);
+    const int grid = (int)(units < sm_count() ? (units > 0 ? units : 1) : sm_count());
+    prefill_kernel<kDtype, HP><<<grid, kThreads, C::kSmem, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <int kDtype>
+cudaError_t launch(const ScoreArgs& a, cudaStream_t st) {
+    if (a.H <= 8) return launch_hp<kDtype, 8>(a, st);
+    if (a.H <= 16) return launch_hp<kDtype, 16>(a, st);
+    if (a.H <= 32) return launch_hp<kDtype, 32>(a, st);
+    return launch_hp<kDtype, 64>(a, st);
+}
+
+}  // namespace
+
+cudaError_t launch_scorer_prefill(const ScoreArgs& a, cudaStream_t st) {
+    if (a.T == 0 || a.max_seq_len_k == 0 || a.B == 0) return cudaSuccess;
+    return a.dtype == IDX_MXFP4 ? launch<IDX_MXFP4>(a, st) : launch<IDX_FP8>(a, st);
+}
+
+}  // namespace idx

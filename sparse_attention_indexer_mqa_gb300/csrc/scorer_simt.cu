@@ -54,15 +54,17 @@ __global__ void __launch_bounds__(kKeys) scorer_simt_kernel(ScoreArgs a) {
     if (s0 >= vis) return;
     const int H = a.H;
 
+    const int Hq = (H + 7) & ~7;
     for (int i = threadIdx.x; i < H * 128; i += kKeys) {
         const int h = i >> 7, d = i & 127;
-        const int64_t row = t * H + h;
         float v;
         if (kDtype == IDX_MXFP4) {
-            uint32_t byte = a.q_codes[row * 64 + (d >> 1)];
-            v = e2m1_value((d & 1) ? byte >> 4 : byte & 15) * e8m0_value(a.q_scales[row * 4 + (d >> 5)]);
+            // canonical Q image (see idx.h): chunk d/32 of head h, byte (d%32)/2
+            const uint32_t byte = a.q_codes[t * Hq * 64 + ((h >> 3) * 4 + (d >> 5)) * 128 + (h & 7) * 16 + ((d & 31) >> 1)];
+            const uint32_t sb = a.q_scales[t * 512 + (h & 31) * 16 + (h >> 5) * 4 + (d >> 5)];
+            v = e2m1_value((d & 1) ? byte >> 4 : byte & 15) * e8m0_value(sb);
         } else {
-            v = e4m3_value(a.q_codes[row * 128 + d]);
+            v = e4m3_value(a.q_codes[t * Hq * 128 + ((h >> 3) * 8 + (d >> 4)) * 128 + (h & 7) * 16 + (d & 15)]);
         }
         qf[i] = v;
     }

@@ -7,10 +7,11 @@
 // indices equal to it, each group in increasing index order, so the result is
 // deterministic.
 //
-// One CTA per query row. Logits are mapped to order-preserving uint32 keys; three
-// histogram passes (11, 11, 10 bits, shared-memory atomics) fix the k-th key exactly; a
-// final ordered compaction (block scans over tiles of 512) writes the indices. The row is
-// read four times, the later passes mostly from L2.
+// One CTA (1024 threads) per query row. The row's logits are read from global memory once,
+// mapped to order-preserving uint32 keys and kept in shared memory (rows longer than the
+// shared-memory capacity are re-read from global memory instead). Three histogram passes
+// (11, 11, 10 bits, shared-memory atomics) fix the k-th key exactly; the final pass gives
+// each thread a contiguous chunk of the row, so one block-wide scan orders the output.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -18,8 +19,9 @@ namespace idx {
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
+constexpr int64_t kSmemKeysMax = 48 * 1024;  // 192 KB of keys
 
 __device__ __forceinline__ uint32_t order_key(float f) {
     uint32_t u = __float_as_uint(f);
@@ -27,35 +29,37 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 // Inclusive sum scan over the CTA; `total` receives the CTA-wide sum.
-__device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* warp_sums, uint32_t& total) {
+template <typename T>
+__device__ __forceinline__ T block_scan(T v, T* warp_sums, T& total) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    uint32_t x = v;
+    T x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        uint32_t y = __shfl_up_sync(kFull, x, o);
+        T y = __shfl_up_sync(kFull, x, o);
         if (lane >= o) x += y;
     }
     if (lane == 31) warp_sums[w] = x;
     __syncthreads();
     if (w == 0) {
-        uint32_t s = lane < kWarps ? warp_sums[lane] : 0;
+        T s = lane < kWarps ? warp_sums[lane] : T(0);
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            uint32_t y = __shfl_up_sync(kFull, s, o);
+            T y = __shfl_up_sync(kFull, s, o);
             if (lane >= o) s += y;
         }
         if (lane < kWarps) warp_sums[lane] = s;
     }
     __syncthreads();
-    const uint32_t add = w > 0 ? warp_sums[w - 1] : 0;
+    const T add = w > 0 ? warp_sums[w - 1] : T(0);
     total = warp_sums[kWarps - 1];
     __syncthreads();
     return x + add;
 }
 
-__global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
+__global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int64_t smem_keys) {
+    extern __shared__ uint32_t skeys[];
     __shared__ uint32_t hist[2048];
-    __shared__ uint32_t warp_sums[kWarps];
+    __shared__ uint64_t warp_sums[kWarps];
     __shared__ uint32_t sel_bin, sel_above;
 
     const int64_t t = blockIdx.x;
@@ -71,6 +75,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
         for (int i = threadIdx.x; i < a.k; i += kThreads) out[i] = i < vis ? i : -1;
         return;
     }
+    const bool cached = vis <= smem_keys;
+    auto key_at = [&](int64_t i) -> uint32_t { return cached ? skeys[i] : order_key(row[i]); };
 
     uint32_t prefix = 0, pmask = 0, remaining = (uint32_t)a.k;
     for (int pass = 0; pass < 3; ++pass) {
@@ -78,9 +84,17 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
         const uint32_t nb = pass == 2 ? 1024u : 2048u;
         for (uint32_t i = threadIdx.x; i < nb; i += kThreads) hist[i] = 0;
         __syncthreads();
-        for (int64_t i = threadIdx.x; i < vis; i += kThreads) {
-            const uint32_t key = order_key(row[i]);
-            if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
+        if (pass == 0) {
+            for (int64_t i = threadIdx.x; i < vis; i += kThreads) {
+                const uint32_t key = order_key(row[i]);
+                if (cached) skeys[i] = key;
+                atomicAdd(&hist[key >> shift], 1u);
+            }
+        } else {
+            for (int64_t i = threadIdx.x; i < vis; i += kThreads) {
+                const uint32_t key = key_at(i);
+                if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
+            }
         }
         __syncthreads();
         // thread r owns the bins [nb - per*(r+1), nb - per*r), highest bins first
@@ -88,8 +102,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
         const int top = (int)nb - per * (int)threadIdx.x;
         uint32_t local = 0;
         for (int j = 1; j <= per; ++j) local += hist[top - j];
-        uint32_t total;
-        const uint32_t incl = block_scan(local, warp_sums, total);
+        uint64_t total;
+        const uint32_t incl = (uint32_t)block_scan<uint64_t>(local, warp_sums, total);
         const uint32_t before = incl - local;
         if (before < remaining && remaining <= incl) {
             uint32_t run = before;
@@ -110,23 +124,31 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
         __syncthreads();
     }
 
-    // prefix is now the k-th largest key; `remaining` keys equal to it are still needed
+    // prefix is the k-th largest key; `remaining` keys equal to it are still needed. Each
+    // thread takes a contiguous chunk, counts, and one scan places every chunk's output.
     const uint32_t n_gt = (uint32_t)a.k - remaining;
-    uint32_t base_gt = 0, base_eq = 0;
-    for (int64_t i0 = 0; i0 < vis; i0 += kThreads) {
-        const int64_t i = i0 + threadIdx.x;
-        const uint32_t key = i < vis ? order_key(row[i]) : 0u;
-        const bool gt = i < vis && key > prefix, eq = i < vis && key == prefix;
-        const uint32_t packed = (gt ? 1u : 0u) | (eq ? 0x10000u : 0u);
-        uint32_t tot;
-        const uint32_t ex = block_scan(packed, warp_sums, tot) - packed;
-        if (gt) out[base_gt + (ex & 0xffffu)] = (int32_t)i;
-        if (eq) {
-            const uint32_t r = base_eq + (ex >> 16);
-            if (r < remaining) out[n_gt + r] = (int32_t)i;
+    const int64_t chunk = (vis + kThreads - 1) / kThreads;
+    const int64_t lo = min(vis, chunk * threadIdx.x), hi = min(vis, lo + chunk);
+    uint32_t c_gt = 0, c_eq = 0;
+    for (int64_t i = lo; i < hi; ++i) {
+        const uint32_t key = key_at(i);
+        c_gt += key > prefix;
+        c_eq += key == prefix;
+    }
+    const uint64_t packed = (uint64_t)c_gt | ((uint64_t)c_eq << 32);
+    uint64_t tot;
+    const uint64_t ex = block_scan<uint64_t>(packed, warp_sums, tot) - packed;
+    uint32_t og = (uint32_t)ex, oe = (uint32_t)(ex >> 32);
+    for (int64_t i = lo; i < hi && (c_gt > 0 || (c_eq > 0 && oe < remaining)); ++i) {
+        const uint32_t key = key_at(i);
+        if (key > prefix) {
+            out[og++] = (int32_t)i;
+            --c_gt;
+        } else if (key == prefix) {
+            if (oe < remaining) out[n_gt + oe] = (int32_t)i;
+            ++oe;
+            --c_eq;
         }
-        base_gt += tot & 0xffffu;
-        base_eq += tot >> 16;
     }
 }
 
@@ -134,7 +156,11 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
     if (a.T == 0) return cudaSuccess;
-    topk_kernel<<<(unsigned)a.T, kThreads, 0, st>>>(a);
+    const int64_t keys = a.ld < kSmemKeysMax ? a.ld : kSmemKeysMax;
+    const size_t smem = (size_t)keys * sizeof(uint32_t);
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    topk_kernel<<<(unsigned)a.T, kThreads, smem, st>>>(a, keys);
     return cudaGetLastError();
 }
 

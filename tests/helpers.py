@@ -67,11 +67,12 @@ class Dev:
         off = wl.base_offset_pages * wl.page_stride
         self.pool = self.pool_buf[off:]
         T, H = wl.T, wl.H
+        Hq = (H + 7) // 8 * 8
         if wl.dtype == W.MXFP4:
-            self.q_codes = torch.zeros((T, H, 64), dtype=torch.uint8, device=device)
-            self.q_scales = torch.zeros((T, H, 4), dtype=torch.uint8, device=device)
+            self.q_codes = torch.full((T, Hq, 64), 0xEE, dtype=torch.uint8, device=device)
+            self.q_scales = torch.full((T, 512), 0xEE, dtype=torch.uint8, device=device)
         else:
-            self.q_codes = torch.zeros((T, H, 128), dtype=torch.uint8, device=device)
+            self.q_codes = torch.full((T, Hq, 128), 0xEE, dtype=torch.uint8, device=device)
             self.q_scales = torch.zeros((T, H), dtype=torch.float32, device=device)
         self.w = torch.zeros((T, H), dtype=torch.float32, device=device)
         self.logits = torch.full((T, wl.ld_logits), float("nan"), dtype=torch.float32,
@@ -125,6 +126,29 @@ class Dev:
         import torch
         torch.cuda.synchronize()
         return getattr(self, name).cpu().numpy()
+
+
+# ------------------------------------------------------------------------------ Q layout
+
+def q_image_to_plain(codes, scales, H, dtype):
+    """The library's Q output (tensor-core image per query, see include/idx.h) mapped to
+    the oracle's plain layout: MXFP4 codes [T][H][64] + scales [T][H][4]; FP8 codes
+    [T][H][128]. Also checks the documented padding (heads H..Hq-1: zero codes, scale
+    bytes 127)."""
+    T = codes.shape[0]
+    Hq = (H + 7) // 8 * 8
+    kc = 4 if dtype == W.MXFP4 else 8          # 16-byte chunks per head row
+    img = codes.reshape(T, Hq // 8, kc, 8, 16)  # [t][group][chunk][head in group][byte]
+    plain = img.transpose(0, 1, 3, 2, 4).reshape(T, Hq, kc * 16)
+    assert not plain[:, H:].any(), "padding heads must be zero"
+    if dtype != W.MXFP4:
+        return plain[:, :H], None
+    h = np.arange(Hq)
+    atom = scales.reshape(T, 512)
+    idx = (h % 32)[:, None] * 16 + (h // 32)[:, None] * 4 + np.arange(4)[None, :]
+    sc = atom[:, idx]                            # [T][Hq][4]
+    assert (sc[:, H:] == 127).all(), "padding heads must have scale byte 127"
+    return plain[:, :H], sc[:, :H]
 
 
 # ------------------------------------------------------------------------------ comparisons

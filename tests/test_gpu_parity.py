@@ -11,7 +11,7 @@ import oracle as O
 from sparse_attention_indexer_mqa_gb300 import workloads as W
 
 from helpers import (Dev, assert_logits_close, assert_topk_valid, oracle_logits, oracle_q,
-                     oracle_store, oracle_topk)
+                     oracle_store, oracle_topk, q_image_to_plain)
 
 pytestmark = pytest.mark.gpu
 
@@ -70,8 +70,12 @@ def _check_store_and_quant(wl, label):
     diff = np.nonzero(pool_gpu != pool_ref)[0]
     assert diff.size == 0, f"{label}: {diff.size} cache bytes differ, first at {diff[:8]}"
     qc, qs, w = oracle_q(wl)
-    np.testing.assert_array_equal(d.host("q_codes"), qc, err_msg=label)
-    np.testing.assert_array_equal(d.host("q_scales").view(np.uint8), qs.view(np.uint8), err_msg=label)
+    gc, gs = q_image_to_plain(d.host("q_codes"), d.host("q_scales"), wl.H, wl.dtype)
+    np.testing.assert_array_equal(gc, qc, err_msg=label)
+    if wl.dtype == W.MXFP4:
+        np.testing.assert_array_equal(gs, qs, err_msg=label)
+    else:
+        np.testing.assert_array_equal(d.host("q_scales").view(np.uint32), qs.view(np.uint32), err_msg=label)
     np.testing.assert_array_equal(d.host("w").view(np.uint32), w.view(np.uint32), err_msg=label)
     return d, pool_ref, (qc, qs, w)
 
@@ -305,3 +309,44 @@ def test_large_pool_addresses(torch):
     qc, qs, w = oracle_q(small)
     exact = oracle_logits(small, pool_ref, qc, qs, w)
     assert_logits_close(d.host("logits"), exact, wl.visible(), label="large pool")
+
+
+def _chunked_prefill(dtype, H, P, causal, lens, nqs, seed):
+    """Several sequences, each scoring its last nq tokens (chunked prefill) against all of
+    its keys, K stored by the full LayerNorm + RoPE path."""
+    rng = np.random.default_rng(seed)
+    lens = np.array(lens, np.int32)
+    nqs = np.array(nqs, np.int32)
+    B = len(lens)
+    need = [(int(L) + P - 1) // P for L in lens]
+    pool = sum(need) + 5
+    perm = rng.permutation(pool).astype(np.int32)
+    pt = np.full((B, max(need)), -1, np.int32)
+    o = 0
+    for b, n in enumerate(need):
+        pt[b, :n] = perm[o:o + n]
+        o += n
+    slots = np.concatenate([pt[b, np.arange(L) // P].astype(np.int64) * P + np.arange(L) % P
+                            for b, L in enumerate(lens)])
+    kpos = np.concatenate([np.arange(L, dtype=np.int32) for L in lens])
+    qpos = np.concatenate([np.arange(L - n, L, dtype=np.int32) for L, n in zip(lens, nqs)])
+    T = int(nqs.sum())
+    rope = W.ROPE_INTERLEAVED if dtype == W.FP8 else W.ROPE_NEOX
+    return W.Workload(
+        name="chunked", dtype=dtype, B=B, H=H, page_size=P, pool_pages=pool, base_offset_pages=1,
+        page_stride=W.page_bytes(dtype, P), seq_lens_k=lens,
+        cu_seqlens_q=np.concatenate([[0], np.cumsum(nqs)]).astype(np.int32), page_table=pt,
+        causal=causal, topk=64, k=W.bf16_bits(rng.standard_normal((int(lens.sum()), 128)).astype(np.float32)),
+        slot_mapping=slots, k_positions=kpos, k_rope=rope, k_norm=1, step_rows=np.arange(1),
+        q=W.bf16_bits(rng.standard_normal((T, H, 128)).astype(np.float32)), q_positions=qpos,
+        q_rope=rope, w_in=(rng.standard_normal((T, H)) / np.sqrt(H)).astype(np.float32),
+        softmax_scale=float(128 ** -0.5), head_scale=1.0, cos_sin=W.rope_table(int(lens.max())),
+        ld_logits=(int(lens.max()) + 3) // 4 * 4)
+
+
+@pytest.mark.parametrize("dtype,H,P,causal", [
+    (W.MXFP4, 4, 64, 1), (W.MXFP4, 24, 128, 0), (W.MXFP4, 64, 64, 1), (W.MXFP4, 32, 64, 0),
+    (W.FP8, 64, 64, 1), (W.FP8, 8, 128, 0), (W.FP8, 32, 128, 1)])
+def test_path_chunked_prefill(torch, dtype, H, P, causal):
+    wl = _chunked_prefill(dtype, H, P, causal, [300, 517, 129, 1], [37, 200, 129, 1], seed=H * 7 + P)
+    _full_path(wl, label=f"chunked prefill dtype={dtype} H={H} P={P} causal={causal}")
