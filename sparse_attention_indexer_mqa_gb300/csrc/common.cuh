@@ -23,21 +23,21 @@ __device__ __forceinline__ void report(int32_t* status, int32_t bit) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// e2m1 code of v (|v| < 8 after block scaling): round to nearest, ties to the even code,
-// saturate at 6; the sign bit follows the sign of v. Midpoints of the grid
-// {0, .5, 1, 1.5, 2, 3, 4, 6} are .25 .75 1.25 1.75 2.5 3.5 5; at a midpoint the even code
-// wins, hence "<=" below even codes and "<" below odd ones.
-__device__ __forceinline__ uint32_t e2m1_code(float v) {
-    float a = fabsf(v);
-    uint32_t c = (a <= 0.25f) ? 0u
-               : (a < 0.75f)  ? 1u
-               : (a <= 1.25f) ? 2u
-               : (a < 1.75f)  ? 3u
-               : (a <= 2.5f)  ? 4u
-               : (a < 3.5f)   ? 5u
-               : (a <= 5.0f)  ? 6u
-                              : 7u;
-    return c | ((__float_as_uint(v) >> 31) << 3);
+// e2m1 codes of eight block-scaled values (|v| < 8), packed two per byte (element 2i in the
+// low nibble): the hardware conversion cvt.rn.satfinite.e2m1x2.f32, i.e. round to nearest,
+// ties to even, saturating at 6, keeping the sign (a negative that rounds to zero is -0).
+// vllm PR 60834 "Purpose" names this instruction for DeepSeek-V4's MXFP4 packing.
+__device__ __forceinline__ uint32_t e2m1x8(const float* v) {
+    uint32_t w;
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+        " mov.b32 %0, {b0, b1, b2, b3};\n}"
+        : "=r"(w)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    return w;
 }
 
 // e4m3 (fn) code of v: the hardware conversion, round to nearest even, saturating at 448.

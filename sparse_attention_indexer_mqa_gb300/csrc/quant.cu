@@ -101,9 +101,10 @@ __device__ __forceinline__ void mx_quant(const float* x, uint32_t& word, uint32_
     amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
     const int e = mx_exponent(amax);
     const float inv = pow2_neg(e);
-    word = 0;
+    float v[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) word |= e2m1_code(__fmul_rn(x[i], inv)) << (4 * i);
+    for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(x[i], inv);
+    word = e2m1x8(v);
     sbyte = (uint32_t)(e + 127);
 }
 
@@ -221,10 +222,15 @@ __global__ void __launch_bounds__(kThreads) q_quant_kernel(QQuantArgs a) {
         uint32_t s1 = __shfl_down_sync(kFull, sbyte, 4);
         uint32_t s2 = __shfl_down_sync(kFull, sbyte, 8);
         uint32_t s3 = __shfl_down_sync(kFull, sbyte, 12);
+        // gather each 16-byte chunk (4 lanes' words) into its first lane
+        const uint32_t w1 = __shfl_down_sync(kFull, word, 1);
+        const uint32_t w2 = __shfl_down_sync(kFull, word, 2);
+        const uint32_t w3 = __shfl_down_sync(kFull, word, 3);
         if (live && (ok || !real)) {
             // canonical image: 8-head groups of [4 chunks][8 heads][16 B]
             uint8_t* img = a.q_codes + t * Hq * 64 + ((h >> 3) * 4 + (l16 >> 2)) * 128 + (h & 7) * 16;
-            reinterpret_cast<uint32_t*>(img)[l16 & 3] = real ? word : 0u;
+            if ((l16 & 3) == 0)
+                *reinterpret_cast<uint4*>(img) = real ? make_uint4(word, w1, w2, w3) : make_uint4(0, 0, 0, 0);
             if (l16 == 0) {
                 uint8_t* atom = reinterpret_cast<uint8_t*>(a.q_scales) + t * 512 + (h & 31) * 16 + (h >> 5) * 4;
                 *reinterpret_cast<uint32_t*>(atom) = real ? (sbyte | (s1 << 8) | (s2 << 16) | (s3 << 24)) : 0x7f7f7f7fu;
@@ -235,9 +241,12 @@ __global__ void __launch_bounds__(kThreads) q_quant_kernel(QQuantArgs a) {
         uint32_t lo, hi;
         float scale;
         f8_quant(x, lo, hi, scale);
+        const uint32_t plo = __shfl_down_sync(kFull, lo, 1);
+        const uint32_t phi = __shfl_down_sync(kFull, hi, 1);
         if (live && (ok || !real)) {
             uint8_t* img = a.q_codes + t * Hq * 128 + ((h >> 3) * 8 + (l16 >> 1)) * 128 + (h & 7) * 16;
-            reinterpret_cast<uint2*>(img)[l16 & 1] = real ? make_uint2(lo, hi) : make_uint2(0, 0);
+            if ((l16 & 1) == 0)
+                *reinterpret_cast<uint4*>(img) = real ? make_uint4(lo, hi, plo, phi) : make_uint4(0, 0, 0, 0);
             if (l16 == 0 && real) {
                 if (a.q_scales) reinterpret_cast<float*>(a.q_scales)[row] = scale;
                 a.w_out[row] = __fmul_rn(__fmul_rn(__ldg(a.w_in + row), a.fold), scale);
@@ -250,7 +259,8 @@ __global__ void debug_encode_kernel(int kind, const float* in, int64_t n, uint8_
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x) {
         float v = in[i];
-        out[i] = (uint8_t)(kind == 0 ? e2m1_code(v) : e4m3_code(v));
+        float v8[8] = {v, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+        out[i] = (uint8_t)(kind == 0 ? (e2m1x8(v8) & 15u) : e4m3_code(v));
     }
 }
 

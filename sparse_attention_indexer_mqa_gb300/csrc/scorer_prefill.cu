@@ -9,19 +9,27 @@
 // K first).
 //
 // Operands: A = a 128-key tile of the sequence's paged cache (as in the decode scorer), B =
-// a block of QB queries x Hq heads = N <= 256 rows of the quantised Q image (consecutive
-// queries' images concatenate into one canonical operand). One block-scaled MMA pair
-// (kind::mxf4, K = 64 each) or four kind::f8f6f4 MMAs (K = 32) give D[key][query, head]
-// in tensor memory. The ReLU-weighted head sum is the epilogue: each thread owns one key
-// and half of the block's queries, so no cross-thread reduction is needed.
+// a block of QB queries: each query's Hq = roundup(H, 8) quantised head rows are placed HP
+// rows apart (HP = power of two >= Hq), N = QB * HP <= 224 rows. One block-scaled MMA pair
+// (kind::mxf4, K = 64 each) or four kind::f8f6f4 MMAs (K = 32) give D[key][query, head] in
+// tensor memory; the ReLU-weighted head sum is the epilogue: each thread owns one key.
 //
-// The work per query block grows with its position (causal), so the persistent CTAs take
-// query blocks heaviest first, in snake order (CTA c gets ranks c, 2G-1-c, 2G+c, ...).
-// Roles: warp 0 = producer (Q block image by bulk copy, its scale atoms assembled by the
-// warp's lanes, K tiles into a ring of stages by bulk copy); warp 1 = tensor-memory owner
-// and MMA issuer; warps 2-9 = epilogue, two warps per 32-lane TMEM quadrant. The single
-// accumulator is drained to registers at once, so the next tile's MMAs run while the
-// epilogue does its (ALU-bound) head sums.
+// Per (query, key) pair the epilogue issues 2H instructions (max, fused multiply-add) while
+// the tensor core does 2*H*128 flops, so the epilogue's issue rate is the bound. Two
+// accumulator buffers (2 x 224 columns), each fed by its own MMA-issuing warp (even / odd
+// tiles) and drained by two epilogue warpgroups (half of the queries each), keep the MMAs of
+// the next tiles and the head sums of the current ones in flight together; four epilogue
+// warps per scheduler hide the latency of their chains. The epilogue is written to issue little
+// beyond its 2H instructions per pair: compile-time trip counts (double-buffered registers
+// rename instead of copying), the causal test only on diagonal tiles, per-block row pointers,
+// and the block's head weights in shared memory read 16 bytes at a time.
+//
+// Work: query blocks, heaviest first (causal), in snake order over persistent CTAs (CTA c
+// takes ranks c, 2G-1-c, 2G+c, ...). Roles: warp 0 = producer (Q image of the block by bulk
+// copy; the block's scale atoms and weights by the warp's lanes; K tiles by bulk copy, one
+// tile per lane); warps 1 and 2 = MMA issuers for even and odd tiles (warp 1 also owns the
+// tensor memory); warps 3-18 = four epilogue warpgroups: two per accumulator, each taking
+// half of the block's queries (one warp per 32-lane TMEM quadrant each).
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -30,44 +38,33 @@ namespace idx {
 
 namespace {
 
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kEpiGroups = 4;
+constexpr int kEpiWarps = 4 * kEpiGroups;
 constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kN = 256;  // B rows (query x head) per block, at most
+constexpr int kThreads = 32 * (3 + kEpiWarps);
+constexpr int kNmax = 224;          // B rows per block, at most
 
 template <int kDtype>
 struct PCfg {
     static constexpr int kTileCode = kDtype == IDX_MXFP4 ? 128 * 64 : 128 * 128;
     static constexpr int kTileSf = kDtype == IDX_MXFP4 ? 512 : 0;
     static constexpr int kStage = kTileCode + kTileSf;
-    static constexpr int kStages = kDtype == IDX_MXFP4 ? 12 : 6;
+    static constexpr int kStages = kDtype == IDX_MXFP4 ? 12 : 5;
     static constexpr int kQRow = kDtype == IDX_MXFP4 ? 64 : 128;
-    static constexpr int kQImg = kN * kQRow;
+    static constexpr int kQImg = 256 * kQRow;                    // Q slot (rows up to 256)
     static constexpr int kQSf = kDtype == IDX_MXFP4 ? 1024 : 0;  // two scale atoms
+    static constexpr int kW = kNmax * 4;                         // head weights of a block
     static constexpr uint32_t kSbo = kDtype == IDX_MXFP4 ? 512 : 1024;
-    static constexpr uint32_t kCols = 512;  // accumulator 256 + scale factors
+    static constexpr uint32_t kCols = 512;  // 2 accumulators of N, A and B scale factors
     static constexpr int oStages = 0;
     static constexpr int oQ = kStages * kStage;   // two Q slots (double-buffered blocks)
     static constexpr int oQSf = oQ + 2 * kQImg;
-    static constexpr int oBars = oQSf + 2 * kQSf;
-    static constexpr int kBars = 2 * kStages + 6;
+    static constexpr int oW = oQSf + 2 * kQSf;
+    static constexpr int oBars = oW + 2 * kW;
+    static constexpr int kBars = 2 * kStages + 8;
     static constexpr int oMisc = oBars + 8 * kBars;
     static constexpr int kSmem = oMisc + 64;
 };
-
-// Query block geometry: each query's Hq = roundup(H, 8) image rows are placed HP rows apart
-// in B (HP = the power of two >= Hq, 8..64), QB = 256 / HP queries per block, N = 256.
-struct Geo {
-    int Hq, QB, N;
-};
-template <int HP>
-__device__ __forceinline__ Geo geo(int H) {
-    Geo g;
-    g.Hq = (H + 7) & ~7;
-    g.QB = kN / HP;
-    g.N = kN;
-    return g;
-}
 
 struct Unit {
     int b;
@@ -79,15 +76,15 @@ struct Unit {
 
 // Unit of virtual rank v: blocks are ranked heaviest first: v -> (jr = v / B, b = v % B),
 // block j = MB - 1 - jr of sequence b (empty if the sequence has fewer blocks).
-__device__ __forceinline__ bool unit_of(const ScoreArgs& a, const Geo& g, int64_t MB, int64_t v, Unit& u) {
+__device__ __forceinline__ bool unit_of(const ScoreArgs& a, int QB, int64_t MB, int64_t v, Unit& u) {
     const int64_t jr = v / a.B;
     u.b = (int)(v - jr * a.B);
     const int64_t j = MB - 1 - jr;
     u.t0 = a.cu_seqlens_q[u.b];
     u.nq = a.cu_seqlens_q[u.b + 1] - u.t0;
-    u.q0 = j * g.QB;
+    u.q0 = j * QB;
     if (u.nq <= 0 || u.q0 >= u.nq) return false;
-    u.nq_blk = min((int64_t)g.QB, u.nq - u.q0);
+    u.nq_blk = min((int64_t)QB, u.nq - u.q0);
     int64_t len = a.seq_lens_k[u.b];
     u.len = len < 0 ? 0 : (len > a.max_seq_len_k ? a.max_seq_len_k : len);
     const int64_t vis_last = visible_keys(u.len, u.nq, u.q0 + u.nq_blk - 1, a.causal);
@@ -98,11 +95,10 @@ __device__ __forceinline__ bool unit_of(const ScoreArgs& a, const Geo& g, int64_
 // Iterates this CTA's units: ranks c, 2G-1-c, 2G+c, 4G-1-c, ... (snake order).
 struct Sched {
     int64_t k, V, MB;
-    int c, G;
-    Geo g;
-    __device__ __forceinline__ void init(const ScoreArgs& a, const Geo& gg) {
-        g = gg;
-        MB = ((int64_t)a.max_q_len + g.QB - 1) / g.QB;
+    int c, G, QB;
+    __device__ __forceinline__ void init(const ScoreArgs& a, int qb) {
+        QB = qb;
+        MB = ((int64_t)a.max_q_len + QB - 1) / QB;
         V = MB * a.B;
         k = 0;
         c = blockIdx.x;
@@ -110,32 +106,59 @@ struct Sched {
     }
     __device__ __forceinline__ bool next(const ScoreArgs& a, Unit& u) {
         for (;;) {
-            const int64_t v = k * G + ((k & 1) ? (G - 1 - c) : c);
             if (k * G >= V) return false;
+            const int64_t v = k * G + ((k & 1) ? (G - 1 - c) : c);
             ++k;
-            if (v < V && unit_of(a, g, MB, v, u)) return true;
+            if (v < V && unit_of(a, QB, MB, v, u)) return true;
         }
     }
 };
 
+// tcgen05.ld of NC consecutive accumulator columns of this warp's lane quadrant
+template <int NC>
+__device__ __forceinline__ void ld_cols(uint32_t taddr, float* v) {
+    if constexpr (NC == 8) {
+        uint32_t r[4];
+        tc::tmem_ld4(taddr, r);
+        uint32_t r2[4];
+        tc::tmem_ld4(taddr + 4, r2);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) { v[i] = __uint_as_float(r[i]); v[4 + i] = __uint_as_float(r2[i]); }
+    } else if constexpr (NC == 16) {
+        uint32_t r[16];
+        tc::tmem_ld16(taddr, r);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+    } else {
+#pragma unroll
+        for (int c = 0; c < NC; c += 32) {
+            uint32_t r[32];
+            tc::tmem_ld32(taddr + c, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[c + i] = __uint_as_float(r[i]);
+        }
+    }
+}
+
 template <int kDtype, int HP>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
     using C = PCfg<kDtype>;
+    constexpr int QB = kNmax / HP;  // queries per block
+    constexpr int N = QB * HP;      // B rows (224 or 192)
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::oBars);
     uint64_t* k_full = bars;
     uint64_t* k_empty = k_full + C::kStages;
     uint64_t* q_full = k_empty + C::kStages;   // 2
     uint64_t* q_empty = q_full + 2;            // 2
-    uint64_t* acc_full = q_empty + 2;
-    uint64_t* acc_empty = acc_full + 1;
+    uint64_t* acc_full = q_empty + 2;          // 2
+    uint64_t* acc_empty = acc_full + 2;        // 2
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::oMisc);
     volatile uint32_t* abort_flag = misc + 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H, P = a.page_size;
-    const Geo g = geo<HP>(H);
-    constexpr int QB = kN / HP;
+    const int Hq = (H + 7) & ~7;
 
     if (tid == 0) {
         misc[1] = 0;
@@ -145,10 +168,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&q_full[i], 1);
-            tc::mbar_init(&q_empty[i], 1);
+            // released by both MMA issuers' commits and by every epilogue thread (they read
+            // the slot's head weights after the MMAs are done)
+            tc::mbar_init(&q_empty[i], 2 + kEpiThreads);
+            tc::mbar_init(&acc_full[i], 1);
+            tc::mbar_init(&acc_empty[i], kEpiThreads / 2);  // two warpgroups per buffer
         }
-        tc::mbar_init(acc_full, 1);
-        tc::mbar_init(acc_empty, kEpiThreads);
         tc::fence_mbar_init();
     }
     if (warp == 1) {
@@ -159,11 +184,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tbase = misc[0];
-    const uint32_t t_sfa = tbase + kN;       // 2 x 4 columns (alternating tiles)
-    const uint32_t t_sfb = t_sfa + 8;        // per Q slot: 2 atoms x 4 columns
+    // tensor memory: accumulators [2][N]; A scale slot per buffer [2][4]; B scale atoms per
+    // buffer (MMA issuer) and Q slot [2][2][8]
+    const uint32_t t_sfa = tbase + 2 * N;
+    const uint32_t t_sfb = t_sfa + 8;
 
     Sched sch;
-    sch.init(a, g);
+    sch.init(a, QB);
     Unit u;
 
     if (warp == 0) {
@@ -171,34 +198,40 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
         int64_t n_units = 0, kt = 0;  // units and tiles issued so far
         while (sch.next(a, u)) {
             if (__any_sync(kFull, *abort_flag != 0)) break;  // warp-uniform exit
-            // Q block into slot n % 2, once the MMAs of block n-2 are done with that slot
+            // Q block into slot n % 2, once the MMAs and epilogues of block n-2 are done with it
             const int slot = (int)(n_units & 1);
             if (!__all_sync(kFull, tc::mbar_wait(&q_empty[slot], (uint32_t)(((n_units >> 1) & 1) ^ 1)))) {
                 if (lane == 0) *abort_flag = 1;
                 break;
             }
-            const uint32_t qrow_bytes = (uint32_t)(g.Hq * C::kQRow);  // one query's image
-            const uint32_t qbytes = (uint32_t)u.nq_blk * qrow_bytes;
+            // head weights of the block (zero past its queries) and, for MXFP4, B's scale
+            // atoms: row n = q*HP + h -> byte (n%32)*16 + ((n/32)%4)*4 of atom n/128, from
+            // query q's own atom (head h at (h%32)*16 + (h/32)*4)
+            float* wsm = reinterpret_cast<float*>(smem + C::oW + slot * C::kW);
+            for (int i = lane; i < QB * H; i += 32) {
+                const int q = i / H;
+                wsm[i] = q < u.nq_blk ? __ldg(a.w + (u.t0 + u.q0) * H + i) : 0.0f;
+            }
             if (kDtype == IDX_MXFP4) {
-                // scale atoms of B: row n = q*Hq + h -> byte (n%32)*16 + ((n/32)%4)*4 of atom n/128,
-                // from query q's own atom (head h at (h%32)*16 + (h/32)*4)
                 uint8_t* sf = smem + C::oQSf + slot * C::kQSf;
-                for (int n = lane; n < kN; n += 32) {
+                for (int n = lane; n < 256; n += 32) {
                     const int q = n / HP, h = n % HP;
                     uint32_t v = 0x7f7f7f7fu;
-                    if (q < u.nq_blk && h < g.Hq)
-                        v = *reinterpret_cast<const uint32_t*>(a.q_scales + (u.t0 + u.q0 + q) * 512 +
-                                                               (h & 31) * 16 + (h >> 5) * 4);
+                    if (q < u.nq_blk && h < Hq)
+                        v = __ldg(reinterpret_cast<const uint32_t*>(a.q_scales + (u.t0 + u.q0 + q) * 512 +
+                                                                    (h & 31) * 16 + (h >> 5) * 4));
                     *reinterpret_cast<uint32_t*>(sf + (n >> 7) * 512 + (n & 31) * 16 + ((n >> 5) & 3) * 4) = v;
                 }
                 tc::fence_proxy_async();
             }
             __syncwarp();
             if (lane == 0) {
-                tc::mbar_arrive_expect_tx(&q_full[slot], qbytes);
-                const uint8_t* qsrc = a.q_codes + (u.t0 + u.q0) * g.Hq * C::kQRow;
+                const uint32_t qrow_bytes = (uint32_t)(Hq * C::kQRow);  // one query's image
+                const uint32_t qbytes = (uint32_t)u.nq_blk * qrow_bytes;
+                tc::mbar_arrive_expect_tx(&q_full[slot], qbytes);  // after the lanes' stores (warp-synchronised)
+                const uint8_t* qsrc = a.q_codes + (u.t0 + u.q0) * Hq * C::kQRow;
                 uint8_t* qdst = smem + C::oQ + slot * C::kQImg;
-                if (g.Hq == HP) {
+                if (Hq == HP) {
                     tc::bulk_g2s(qdst, qsrc, qbytes, &q_full[slot]);
                 } else {  // padded spacing: one copy per query (padding rows are never summed)
                     for (int q = 0; q < u.nq_blk; ++q)
@@ -237,8 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                             if (pg[hh] < 0) continue;
                             const uint8_t* src = a.pool + (int64_t)pg[hh] * a.page_stride;
                             if (P == 128) {
-                                tc::bulk_g2s(dK, src, C::kTileCode, &k_full[s]);
-                                if (kDtype == IDX_MXFP4) tc::bulk_g2s(dS, src + C::kTileCode, 512, &k_full[s]);
+                                // codes and scale atom are contiguous in the page and in the stage
+                                tc::bulk_g2s(dK, src, C::kStage, &k_full[s]);
                             } else if (kDtype == IDX_MXFP4) {
                                 for (int q = 0; q < 4; ++q)
                                     tc::bulk_g2s(dK + q * 2048 + hh * 1024, src + q * 1024, 1024, &k_full[s]);
@@ -256,8 +289,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
             __syncwarp();
         }
         if (lane == 0 && *abort_flag) report(a.dev_status, IDX_STATUS_TIMEOUT);
-    } else if (warp == 1) {
-        // -------------------------------------------------------------- MMA issuer
+    } else if (warp == 1 || warp == 2) {
+        // -------------------------------------------------------------- MMA issuers
+        // warp 1 issues the even tiles into accumulator 0, warp 2 the odd ones into
+        // accumulator 1; each keeps its own A and B scale-factor slots
+        const int buf = warp - 1;
         if (lane == 0) {
             // descriptors of stage 0 / Q slot 0; stages, slots and K steps add (bytes >> 4)
             // to the start-address field (shared-memory addresses stay below 256 KB)
@@ -265,11 +301,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
             const uint64_t dB0 = tc::smem_desc(tc::smem_u32(smem + C::oQ), 128, C::kSbo);
             const uint64_t dSA0 = tc::smem_desc(tc::smem_u32(smem + C::oStages + C::kTileCode), 128, 128);
             const uint64_t dSB0 = tc::smem_desc(tc::smem_u32(smem + C::oQSf), 128, 128);
-            const uint32_t id0 = kDtype == IDX_MXFP4 ? tc::idesc_mxf4(128, kN, 0, 0) : tc::idesc_f8(128, kN);
-            const uint32_t id1 = kDtype == IDX_MXFP4 ? tc::idesc_mxf4(128, kN, 2, 2) : id0;
-            int64_t n_units = 0;
-            int s = 0;
-            uint32_t kph = 0, aph = 1, sfa_sel = 0;
+            const uint32_t id0 = kDtype == IDX_MXFP4 ? tc::idesc_mxf4(128, N, 0, 0) : tc::idesc_f8(128, N);
+            const uint32_t id1 = kDtype == IDX_MXFP4 ? tc::idesc_mxf4(128, N, 2, 2) : id0;
+            const uint32_t d = tbase + buf * N;
+            const uint32_t sfa = t_sfa + 4 * buf;
+            int64_t n_units = 0, kt = 0;
+            uint32_t aph = 1;
             while (sch.next(a, u)) {
                 if (*abort_flag) break;
                 const int slot = (int)(n_units & 1);
@@ -279,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                 }
                 tc::tc_fence_after();
                 const uint64_t db = dB0 + (uint64_t)((slot * C::kQImg) >> 4);
-                const uint32_t sfb = t_sfb + 8 * slot;
+                const uint32_t sfb = t_sfb + 16 * buf + 8 * slot;
                 if (kDtype == IDX_MXFP4) {
                     // B's two scale atoms: rows 0-127 and 128-255
                     const uint64_t dsb = dSB0 + (uint64_t)((slot * C::kQSf) >> 4);
@@ -287,118 +324,159 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                     tc::cp_32x128b_warpx4(sfb + 4, dsb + 32);
                 }
                 bool ok = true;
-                for (int64_t j = 0; j < u.tiles; ++j) {
-                    if (!tc::mbar_wait(&k_full[s], kph) || !tc::mbar_wait(acc_empty, aph)) {
+                for (int64_t j = 0; j < u.tiles; ++j, ++kt) {
+                    if ((kt & 1) != buf) continue;
+                    const int s = (int)(kt % C::kStages);
+                    if (!tc::mbar_wait(&k_full[s], (uint32_t)((kt / C::kStages) & 1)) ||
+                        !tc::mbar_wait(&acc_empty[buf], aph)) {
                         ok = false;
                         break;
                     }
+                    aph ^= 1;
                     tc::tc_fence_after();
                     const uint64_t da = dA0 + (uint64_t)((s * C::kStage) >> 4);
                     if (kDtype == IDX_MXFP4) {
-                        const uint32_t sfa = t_sfa + 4 * sfa_sel;
                         tc::cp_32x128b_warpx4(sfa, dSA0 + (uint64_t)((s * C::kStage) >> 4));
-                        tc::mma_mxf4(tbase, da, db, id0, sfa, sfb, 0);
-                        tc::mma_mxf4(tbase, da + 16, db + 16, id1, sfa, sfb, 1);
+                        tc::mma_mxf4(d, da, db, id0, sfa, sfb, 0);
+                        tc::mma_mxf4(d, da + 16, db + 16, id1, sfa, sfb, 1);
                     } else {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) tc::mma_f8(tbase, da + 16 * k, db + 16 * k, id0, k);
+                        for (int k = 0; k < 4; ++k) tc::mma_f8(d, da + 16 * k, db + 16 * k, id0, k);
                     }
                     tc::mma_commit(&k_empty[s]);
-                    tc::mma_commit(acc_full);
-                    if (++s == C::kStages) { s = 0; kph ^= 1; }
-                    aph ^= 1;
-                    sfa_sel ^= 1;
+                    tc::mma_commit(&acc_full[buf]);
                 }
                 if (!ok) {
                     *abort_flag = 1;
                     break;
                 }
-                tc::mma_commit(&q_empty[slot]);
+                tc::mma_commit(&q_empty[slot]);  // arrives when this warp's MMAs of the block end
                 ++n_units;
             }
             if (*abort_flag) report(a.dev_status, IDX_STATUS_TIMEOUT);
         }
     } else {
-        // -------------------------------------------------------------- epilogue warps
-        const int ew = warp - 2;          // 0..7
+        // -------------------------------------------------------------- epilogue warpgroups
+        // warpgroup g drains accumulator g % 2, i.e. the tiles with (tile count % 2) == g % 2,
+        // for half g / 2 of the block's queries; every thread owns one key
+        const int g = (warp - 3) >> 2;
+        const int gb = g & 1, gh = g >> 1;
         const int quad = warp & 3;        // TMEM lane quadrant this warp may access
-        const int half = ew >> 2;         // which half of the block's columns
         const int m = quad * 32 + lane;
-        const uint32_t lane_addr = tbase + ((uint32_t)(quad * 32) << 16) + half * (kN / 2);
         const bool split = P == 64 && kDtype == IDX_MXFP4;
         const int khalf = split ? ((m >> 4) & 1) : (m >> 6);
         const int koff = split ? (64 * khalf + (m & 15) + 16 * (m >> 5)) : m;
-        constexpr int QH = QB / 2;  // queries per half (two chunks of 64 / HP)
-        const int qh0 = half * QH;
-        int64_t kt = 0;
+        const bool vec_w = (H & 3) == 0;
+        int64_t kt = 0, n_units = 0;
+        uint32_t aph = 0;
+        constexpr int QC = HP <= 32 ? 32 / HP : 1;  // queries per 32-column load (HP = 64: 2 loads)
+        constexpr int CW = QC * HP;                 // columns per chunk
+        constexpr int QH0 = (QB + 1) / 2;           // queries of the first half
+        constexpr int NCH = (QH0 + QC - 1) / QC;    // chunks per tile, at most
+        const int qlo = gh ? QH0 : 0, qhi = gh ? QB : QH0;
+        const int nch = (qhi - qlo + QC - 1) / QC;
+        const uint32_t lane_addr = tbase + ((uint32_t)(quad * 32) << 16) + gb * N + qlo * HP;
         while (sch.next(a, u)) {
+            const int slot = (int)(n_units & 1);
+            // the block's weights: wait for the slot's fill (the same phase the MMA issuers used)
+            if (!__all_sync(kFull, tc::mbar_wait(&q_full[slot], (uint32_t)((n_units >> 1) & 1)))) {
+                *abort_flag = 1;
+                report(a.dev_status, IDX_STATUS_TIMEOUT);
+                break;
+            }
+            const float* wsm = reinterpret_cast<const float*>(smem + C::oW + slot * C::kW);
             const int32_t* pt = a.page_table + (int64_t)u.b * a.pt_stride;
+            const int nqb = (int)u.nq_blk;
+            // query q of the block sees keys < vis0 + q (causal; unclamped, so it also holds when
+            // the block has more queries than keys) or keys < len; key < len is checked apart
+            const int64_t vis0 = a.causal ? u.len - u.nq + u.q0 + 1 : u.len;
+            const int qstep = a.causal ? 1 : 0;
+            float* lrow = a.logits + (u.t0 + u.q0) * a.ld;  // the block's first logits row
+            const int64_t ld = a.ld;
             for (int64_t j = 0; j < u.tiles; ++j, ++kt) {
+                if ((kt & 1) != gb) continue;
                 // page lookups are issued before the accumulator wait (their latency hides
                 // behind it) and used after it
                 const int64_t key = j * 128 + koff;
                 const bool in_seq = key < u.len;
                 const int32_t pg = in_seq ? __ldg(pt + key / P) : -1;
-                const bool got = __all_sync(kFull, tc::mbar_wait(acc_full, (uint32_t)(kt & 1)));
+                const bool got = __all_sync(kFull, tc::mbar_wait(&acc_full[gb], aph));
                 if (!got) {
                     *abort_flag = 1;
                     report(a.dev_status, IDX_STATUS_TIMEOUT);
                     break;
                 }
+                aph ^= 1;
                 tc::tc_fence_after();
                 const bool key_ok = in_seq && pg >= 0 && pg < a.num_pages;
                 float kscale = 1.0f;
                 if (kDtype == IDX_FP8 && key_ok)
                     kscale = __ldg(reinterpret_cast<const float*>(a.pool + (int64_t)pg * a.page_stride + 128 * P + 4 * (key % P)));
-                // this half's 128 columns (queries qh0 .. qh0+QH-1, HP columns each), drained in
-                // two chunks of 64; the accumulator is released after the second load, so the
-                // next tile's MMAs overlap the second chunk's head sums
+                // this key is visible to queries q >= qmin (all of them off the diagonal)
+                const int64_t d = key - vis0 + 1;  // causal: query q sees the key iff q >= d
+                const int qmin = !key_ok ? QB : (qstep == 0 ? (key < vis0 ? 0 : QB) : (d <= 0 ? 0 : (d >= QB ? QB : (int)d)));
+                // software-pipelined drain: chunk c+1 is loaded while chunk c is summed; the
+                // accumulator is released as soon as this half's last chunk is in registers
+                float v[2][CW];
+                ld_cols<CW>(lane_addr, v[0]);
+                tc::tmem_ld_wait();
+                if (nch == 1) {
+                    tc::tc_fence_before();
+                    tc::mbar_arrive(&acc_empty[gb]);
+                }
 #pragma unroll
-                for (int chunk = 0; chunk < 2; ++chunk) {
-                    float v[64];
-#pragma unroll
-                    for (int c = 0; c < 64; c += 32) {
-                        uint32_t r[32];
-                        tc::tmem_ld32(lane_addr + chunk * 64 + c, r);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[c + i] = __uint_as_float(r[i]);
-                    }
-                    tc::tmem_ld_wait();
-                    if (chunk == 1) {
-                        tc::tc_fence_before();
-                        tc::mbar_arrive(acc_empty);
-                    }
-                    constexpr int QC = 64 / HP;  // queries in this chunk
+                for (int c = 0; c < NCH; ++c) {
+                    if (c >= nch) break;
+                    float* va = v[c & 1];
+                    if (c + 1 < nch) ld_cols<CW>(lane_addr + (c + 1) * CW, v[(c + 1) & 1]);
 #pragma unroll
                     for (int qq = 0; qq < QC; ++qq) {
-                        const int q = qh0 + chunk * QC + qq;
-                        if (q >= u.nq_blk) break;
-                        const int64_t qi = u.q0 + q;  // sequence-local query index
-                        const int64_t t = u.t0 + qi;
-                        float logit = 0.0f;
-                        if ((H & 3) == 0) {
-                            const float4* w4 = reinterpret_cast<const float4*>(a.w + t * H);
+                        const int q = qlo + c * QC + qq;
+                        if (q < qhi && q < nqb && q >= qmin) {
+                            const float* wq = wsm + q * H;
+                            float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                            if (H == HP) {  // every column is a head: no per-head guard
+                                float4 w4[HP / 4];
 #pragma unroll
-                            for (int h = 0; h < HP; h += 4) {
-                                if (h < H) {
-                                    const float4 ww = __ldg(w4 + h / 4);
-                                    logit = fmaf(ww.x, fmaxf(v[qq * HP + h], 0.0f), logit);
-                                    logit = fmaf(ww.y, fmaxf(v[qq * HP + h + 1], 0.0f), logit);
-                                    logit = fmaf(ww.z, fmaxf(v[qq * HP + h + 2], 0.0f), logit);
-                                    logit = fmaf(ww.w, fmaxf(v[qq * HP + h + 3], 0.0f), logit);
+                                for (int i = 0; i < HP / 4; ++i) w4[i] = reinterpret_cast<const float4*>(wq)[i];
+#pragma unroll
+                                for (int i = 0; i < HP / 4; ++i) {
+                                    part[0] = fmaf(w4[i].x, fmaxf(va[qq * HP + 4 * i], 0.0f), part[0]);
+                                    part[1] = fmaf(w4[i].y, fmaxf(va[qq * HP + 4 * i + 1], 0.0f), part[1]);
+                                    part[2] = fmaf(w4[i].z, fmaxf(va[qq * HP + 4 * i + 2], 0.0f), part[2]);
+                                    part[3] = fmaf(w4[i].w, fmaxf(va[qq * HP + 4 * i + 3], 0.0f), part[3]);
                                 }
-                            }
-                        } else {
-                            const float* wq = a.w + t * H;
+                            } else if (vec_w) {
 #pragma unroll
-                            for (int h = 0; h < HP; ++h)
-                                if (h < H) logit = fmaf(__ldg(wq + h), fmaxf(v[qq * HP + h], 0.0f), logit);
+                                for (int h = 0; h < HP; h += 4) {
+                                    if (h < H) {
+                                        const float4 w4 = *reinterpret_cast<const float4*>(wq + h);
+                                        part[0] = fmaf(w4.x, fmaxf(va[qq * HP + h], 0.0f), part[0]);
+                                        part[1] = fmaf(w4.y, fmaxf(va[qq * HP + h + 1], 0.0f), part[1]);
+                                        part[2] = fmaf(w4.z, fmaxf(va[qq * HP + h + 2], 0.0f), part[2]);
+                                        part[3] = fmaf(w4.w, fmaxf(va[qq * HP + h + 3], 0.0f), part[3]);
+                                    }
+                                }
+                            } else {
+#pragma unroll
+                                for (int h = 0; h < HP; ++h)
+                                    if (h < H) part[h & 3] = fmaf(wq[h], fmaxf(va[qq * HP + h], 0.0f), part[h & 3]);
+                            }
+                            lrow[q * ld + key] = ((part[0] + part[1]) + (part[2] + part[3])) * kscale;
                         }
-                        if (key_ok && key < visible_keys(u.len, u.nq, qi, a.causal))
-                            a.logits[t * a.ld + key] = logit * kscale;
+                    }
+                    if (c + 1 < nch) {
+                        tc::tmem_ld_wait();
+                        if (c + 2 == nch) {  // the last chunk is in registers
+                            tc::tc_fence_before();
+                            tc::mbar_arrive(&acc_empty[gb]);
+                        }
                     }
                 }
             }
+            // done with the slot's weights
+            tc::mbar_arrive(&q_empty[slot]);
+            ++n_units;
             if (__any_sync(kFull, *abort_flag != 0)) break;  // warp-uniform exit
         }
     }
@@ -428,7 +506,7 @@ cudaError_t launch_hp(const ScoreArgs& a, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kDtype, HP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmem);
     if (e != cudaSuccess) return e;
-    constexpr int QB = kN / HP;
+    constexpr int QB = kNmax / HP;
     const int64_t units = (int64_t)a.B * ((a.max_q_len + QB - 1) / QB);
     const int grid = (int)(units < sm_count() ? (units > 0 ? units : 1) : sm_count());
     prefill_kernel<kDtype, HP><<<grid, kThreads, C::kSmem, st>>>(a);
