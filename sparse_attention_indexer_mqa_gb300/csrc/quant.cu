@@ -123,8 +123,8 @@ __device__ __forceinline__ void f8_quant(const float* x, uint32_t& lo, uint32_t&
     for (int i = 0; i < 4; ++i) hi |= e4m3_code(__fdiv_rn(x[4 + i], scale)) << (8 * i);
 }
 
-__device__ __forceinline__ void load_row8(const uint16_t* src, bool ok, float* x) {
-    uint4 v = ok ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0, 0, 0, 0);
+// eight bf16 (one 16-byte load) -> fp32
+__device__ __forceinline__ void unpack8(const uint4 v, float* x) {
     x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x);
     x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
     x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z);
@@ -135,27 +135,27 @@ template <int kDtype>
 __global__ void __launch_bounds__(kThreads) k_store_kernel(KStoreArgs a) {
     const int l16 = threadIdx.x & 15;
     const int64_t row = (int64_t)blockIdx.x * kRowsPerCta + (threadIdx.x >> 4);
-    bool ok = row < a.n_rows;
-    int64_t slot = ok ? __ldg(a.slot_mapping + row) : -1;
-    ok = ok && slot >= 0;
+    const bool in = row < a.n_rows;
+    // the slot, the position and the K row are independent loads: issue them together
+    const int64_t slot = in ? __ldg(a.slot_mapping + row) : -1;
+    int32_t pos = (in && a.rope != IDX_ROPE_NONE) ? __ldg(a.positions + row) : 0;
+    const uint4 raw = in ? __ldg(reinterpret_cast<const uint4*>(a.k + row * a.k_row_stride + 8 * l16))
+                         : make_uint4(0, 0, 0, 0);
+    bool ok = in && slot >= 0;
     const int64_t page = ok ? slot / a.page_size : 0;
     const int s = ok ? (int)(slot - page * a.page_size) : 0;
     if (ok && page >= a.num_pages) {
         if (l16 == 0) report(a.dev_status, IDX_STATUS_BAD_SLOT);
         ok = false;
     }
-    int32_t pos = 0;
-    if (a.rope != IDX_ROPE_NONE && ok) {
-        pos = __ldg(a.positions + row);
-        if (pos < 0 || pos >= a.max_pos) {
-            if (l16 == 0) report(a.dev_status, IDX_STATUS_BAD_POS);
-            ok = false;
-            pos = 0;
-        }
+    if (a.rope != IDX_ROPE_NONE && ok && (pos < 0 || pos >= a.max_pos)) {
+        if (l16 == 0) report(a.dev_status, IDX_STATUS_BAD_POS);
+        ok = false;
     }
+    if (!ok) pos = 0;
     // every lane keeps going (zeros for skipped rows) so that the shuffles stay converged
     float x[8];
-    load_row8(a.k + (ok ? row : 0) * a.k_row_stride + 8 * l16, ok, x);
+    unpack8(ok ? raw : make_uint4(0, 0, 0, 0), x);
     if (a.apply_norm) layernorm(x, l16, a.gamma, a.beta, a.eps);
     if (a.rope != IDX_ROPE_NONE) rope(x, l16, a.cos_sin + (int64_t)pos * 64, a.rope);
 
@@ -192,64 +192,82 @@ __global__ void __launch_bounds__(kThreads) k_store_kernel(KStoreArgs a) {
 }
 
 // Q rows are walked over T x Hq "virtual" heads, Hq = H rounded up to 8: heads past H
-// write the zero/neutral padding of the tensor-core image (see idx.h for the layout).
+// write the zero/neutral padding of the tensor-core image (see idx.h for the layout). Each
+// 16-lane group takes kQRows rows (kRowsPerCta apart, so every load instruction of the CTA
+// stays coalesced) and issues all their loads before it computes, which keeps several
+// 16-byte loads per thread in flight.
+constexpr int kQRows = 1;
+
 template <int kDtype>
 __global__ void __launch_bounds__(kThreads) q_quant_kernel(QQuantArgs a) {
     const int l16 = threadIdx.x & 15;
-    const int64_t vrow = (int64_t)blockIdx.x * kRowsPerCta + (threadIdx.x >> 4);  // t*Hq + h
     const int Hq = (a.H + 7) & ~7;
-    bool live = vrow < a.n_rows;  // n_rows = T * Hq
-    const int64_t t = live ? vrow / Hq : 0;
-    const int h = live ? (int)(vrow - t * Hq) : 0;
-    const bool real = live && h < a.H;
-    bool ok = real;
-    int32_t pos = 0;
-    if (a.rope != IDX_ROPE_NONE && ok) {
-        pos = __ldg(a.positions + t);
-        if (pos < 0 || pos >= a.max_pos) {
+    const int64_t v0 = (int64_t)blockIdx.x * kRowsPerCta * kQRows + (threadIdx.x >> 4);
+    uint4 raw[kQRows];
+    int32_t pos[kQRows];
+#pragma unroll
+    for (int r = 0; r < kQRows; ++r) {
+        const int64_t vrow = v0 + r * kRowsPerCta;  // t*Hq + h
+        const int64_t t = vrow / Hq;
+        const int h = (int)(vrow - t * Hq);
+        const bool real = vrow < a.n_rows && h < a.H;
+        raw[r] = real ? __ldg(reinterpret_cast<const uint4*>(a.q + (t * a.H + h) * 128 + 8 * l16))
+                      : make_uint4(0, 0, 0, 0);
+        pos[r] = (real && a.rope != IDX_ROPE_NONE) ? __ldg(a.positions + t) : 0;
+    }
+#pragma unroll
+    for (int r = 0; r < kQRows; ++r) {
+        const int64_t vrow = v0 + r * kRowsPerCta;
+        const bool live = vrow < a.n_rows;  // n_rows = T * Hq
+        const int64_t t = live ? vrow / Hq : 0;
+        const int h = live ? (int)(vrow - t * Hq) : 0;
+        const bool real = live && h < a.H;
+        bool ok = real;
+        int32_t p = pos[r];
+        if (a.rope != IDX_ROPE_NONE && ok && (p < 0 || p >= a.max_pos)) {
             if (l16 == 0) report(a.dev_status, IDX_STATUS_BAD_POS);
             ok = false;
-            pos = 0;
         }
-    }
-    const int64_t row = t * a.H + h;  // index of (t, h) in q, w_in, w_out
-    float x[8];
-    load_row8(a.q + (ok ? row : 0) * 128 + 8 * l16, ok, x);
-    if (a.rope != IDX_ROPE_NONE) rope(x, l16, a.cos_sin + (int64_t)pos * 64, a.rope);
-    if (kDtype == IDX_MXFP4) {
-        uint32_t word, sbyte;
-        mx_quant(x, word, sbyte);
-        uint32_t s1 = __shfl_down_sync(kFull, sbyte, 4);
-        uint32_t s2 = __shfl_down_sync(kFull, sbyte, 8);
-        uint32_t s3 = __shfl_down_sync(kFull, sbyte, 12);
-        // gather each 16-byte chunk (4 lanes' words) into its first lane
-        const uint32_t w1 = __shfl_down_sync(kFull, word, 1);
-        const uint32_t w2 = __shfl_down_sync(kFull, word, 2);
-        const uint32_t w3 = __shfl_down_sync(kFull, word, 3);
-        if (live && (ok || !real)) {
-            // canonical image: 8-head groups of [4 chunks][8 heads][16 B]
-            uint8_t* img = a.q_codes + t * Hq * 64 + ((h >> 3) * 4 + (l16 >> 2)) * 128 + (h & 7) * 16;
-            if ((l16 & 3) == 0)
-                *reinterpret_cast<uint4*>(img) = real ? make_uint4(word, w1, w2, w3) : make_uint4(0, 0, 0, 0);
-            if (l16 == 0) {
-                uint8_t* atom = reinterpret_cast<uint8_t*>(a.q_scales) + t * 512 + (h & 31) * 16 + (h >> 5) * 4;
-                *reinterpret_cast<uint32_t*>(atom) = real ? (sbyte | (s1 << 8) | (s2 << 16) | (s3 << 24)) : 0x7f7f7f7fu;
-                if (real) a.w_out[row] = __fmul_rn(__ldg(a.w_in + row), a.fold);
+        if (!ok) p = 0;
+        const int64_t row = t * a.H + h;  // index of (t, h) in q, w_in, w_out
+        float x[8];
+        unpack8(ok ? raw[r] : make_uint4(0, 0, 0, 0), x);
+        if (a.rope != IDX_ROPE_NONE) rope(x, l16, a.cos_sin + (int64_t)p * 64, a.rope);
+        if (kDtype == IDX_MXFP4) {
+            uint32_t word, sbyte;
+            mx_quant(x, word, sbyte);
+            const uint32_t s1 = __shfl_down_sync(kFull, sbyte, 4);
+            const uint32_t s2 = __shfl_down_sync(kFull, sbyte, 8);
+            const uint32_t s3 = __shfl_down_sync(kFull, sbyte, 12);
+            // gather each 16-byte chunk (4 lanes' words) into its first lane
+            const uint32_t w1 = __shfl_down_sync(kFull, word, 1);
+            const uint32_t w2 = __shfl_down_sync(kFull, word, 2);
+            const uint32_t w3 = __shfl_down_sync(kFull, word, 3);
+            if (live && (ok || !real)) {
+                // canonical image: 8-head groups of [4 chunks][8 heads][16 B]
+                uint8_t* img = a.q_codes + t * Hq * 64 + ((h >> 3) * 4 + (l16 >> 2)) * 128 + (h & 7) * 16;
+                if ((l16 & 3) == 0)
+                    *reinterpret_cast<uint4*>(img) = real ? make_uint4(word, w1, w2, w3) : make_uint4(0, 0, 0, 0);
+                if (l16 == 0) {
+                    uint8_t* atom = reinterpret_cast<uint8_t*>(a.q_scales) + t * 512 + (h & 31) * 16 + (h >> 5) * 4;
+                    *reinterpret_cast<uint32_t*>(atom) = real ? (sbyte | (s1 << 8) | (s2 << 16) | (s3 << 24)) : 0x7f7f7f7fu;
+                    if (real) a.w_out[row] = __fmul_rn(__ldg(a.w_in + row), a.fold);
+                }
             }
-        }
-    } else {
-        uint32_t lo, hi;
-        float scale;
-        f8_quant(x, lo, hi, scale);
-        const uint32_t plo = __shfl_down_sync(kFull, lo, 1);
-        const uint32_t phi = __shfl_down_sync(kFull, hi, 1);
-        if (live && (ok || !real)) {
-            uint8_t* img = a.q_codes + t * Hq * 128 + ((h >> 3) * 8 + (l16 >> 1)) * 128 + (h & 7) * 16;
-            if ((l16 & 1) == 0)
-                *reinterpret_cast<uint4*>(img) = real ? make_uint4(lo, hi, plo, phi) : make_uint4(0, 0, 0, 0);
-            if (l16 == 0 && real) {
-                if (a.q_scales) reinterpret_cast<float*>(a.q_scales)[row] = scale;
-                a.w_out[row] = __fmul_rn(__fmul_rn(__ldg(a.w_in + row), a.fold), scale);
+        } else {
+            uint32_t lo, hi;
+            float scale;
+            f8_quant(x, lo, hi, scale);
+            const uint32_t plo = __shfl_down_sync(kFull, lo, 1);
+            const uint32_t phi = __shfl_down_sync(kFull, hi, 1);
+            if (live && (ok || !real)) {
+                uint8_t* img = a.q_codes + t * Hq * 128 + ((h >> 3) * 8 + (l16 >> 1)) * 128 + (h & 7) * 16;
+                if ((l16 & 1) == 0)
+                    *reinterpret_cast<uint4*>(img) = real ? make_uint4(lo, hi, plo, phi) : make_uint4(0, 0, 0, 0);
+                if (l16 == 0 && real) {
+                    if (a.q_scales) reinterpret_cast<float*>(a.q_scales)[row] = scale;
+                    a.w_out[row] = __fmul_rn(__fmul_rn(__ldg(a.w_in + row), a.fold), scale);
+                }
             }
         }
     }
@@ -276,7 +294,7 @@ cudaError_t launch_k_store(const KStoreArgs& a, cudaStream_t st) {
 
 cudaError_t launch_q_quant(const QQuantArgs& a, cudaStream_t st) {
     if (a.n_rows == 0) return cudaSuccess;
-    const int64_t grid = (a.n_rows + kRowsPerCta - 1) / kRowsPerCta;
+    const int64_t grid = (a.n_rows + kRowsPerCta * kQRows - 1) / (kRowsPerCta * kQRows);
     if (a.dtype == IDX_MXFP4) q_quant_kernel<IDX_MXFP4><<<(unsigned)grid, kThreads, 0, st>>>(a);
     else q_quant_kernel<IDX_FP8><<<(unsigned)grid, kThreads, 0, st>>>(a);
     return cudaGetLastError();
