@@ -101,7 +101,8 @@ int idx_cache_layout(int32_t dtype, int32_t page_size, idx_layout* out);
  *   floor(log2 amax) - 2 clamped to [-127, 127] (amax = 0 gives -127), elements x*2^-E
  *   rounded to nearest-even e2m1 with saturation at 6 and the input's sign; FP8 scale
  *   max(amax, 1e-10)/448, elements x/scale rounded to nearest-even e4m3 saturating at 448.
- * cos_sin: fp32 [max_pos][64] = cos of the 32 frequencies, then sin of them.
+ * cos_sin: fp32 [max_pos][64] = cos of the 32 frequencies, then sin of them; 16-byte
+ * aligned (IDX_EINVAL otherwise).
  * gamma, beta: fp32 [128]; both may be NULL (meaning 1 and 0) when apply_norm != 0.
  * slot_mapping: int64 [n_rows]; slot < 0 skips the row ([P3] "Purpose": PAD_SLOT_ID).
  * positions: int32 [n_rows]; may be NULL when rope == IDX_ROPE_NONE.
@@ -178,7 +179,8 @@ int idx_mqa_logits_paged(const uint8_t* q_codes, const void* q_scales, const flo
  * exact for the fp32 logits given; its order is: indices of values above the k-th value in
  * increasing index order, then indices equal to it in increasing index order. If
  * visible(t) < k all visible indices are returned, followed by -1 padding.
- * 1 <= k <= 4096. Any visible length is accepted.
+ * 1 <= k <= 4096; ld_logits <= INT32_MAX (IDX_EUNSUPPORTED otherwise). logits is a
+ * 4-byte aligned device buffer (IDX_EINVAL otherwise); any visible length is accepted.
  */
 int idx_topk(const float* logits, int64_t ld_logits, const int32_t* seq_lens_k,
              const int32_t* cu_seqlens_q, int32_t B, int64_t T, int32_t causal, int32_t k,

@@ -67,7 +67,8 @@ int idx_k_store(const uint16_t* k, int64_t n_rows, int64_t k_row_stride,
     if (n_rows == 0) return IDX_OK;
     if (!k || !slot_mapping || !aligned(k, 16) || k_row_stride < 128 || k_row_stride % 8 != 0)
         return IDX_EINVAL;
-    if (rope != IDX_ROPE_NONE && (!positions || !cos_sin || max_pos <= 0)) return IDX_EINVAL;
+    if (rope != IDX_ROPE_NONE && (!positions || !cos_sin || !aligned(cos_sin, 16) || max_pos <= 0))
+        return IDX_EINVAL;
     if (apply_norm && !(eps >= 0.0f && std::isfinite(eps))) return IDX_EINVAL;
     idx::KStoreArgs a{};
     a.k = k; a.n_rows = n_rows; a.k_row_stride = k_row_stride; a.slot_mapping = slot_mapping;
@@ -89,9 +90,11 @@ int idx_q_quant(const uint16_t* q, int64_t T, int32_t H, const int32_t* position
         return IDX_EINVAL;
     if (dtype == IDX_MXFP4 && (!q_scales || !aligned(q_scales, 16))) return IDX_EINVAL;
     if (q_scales && !aligned(q_scales, 4)) return IDX_EINVAL;
-    if (rope != IDX_ROPE_NONE && (!positions || !cos_sin || max_pos <= 0)) return IDX_EINVAL;
+    if (rope != IDX_ROPE_NONE && (!positions || !cos_sin || !aligned(cos_sin, 16) || max_pos <= 0))
+        return IDX_EINVAL;
+    if (T > INT32_MAX) return IDX_EUNSUPPORTED;  // one grid column per token
     idx::QQuantArgs a{};
-    a.q = q; a.n_rows = T * (int64_t)((H + 7) & ~7); a.H = H; a.positions = positions; a.cos_sin = cos_sin;
+    a.q = q; a.T = T; a.H = H; a.positions = positions; a.cos_sin = cos_sin;
     a.max_pos = max_pos; a.rope = rope; a.dtype = dtype; a.w_in = w_in;
     a.fold = (float)((double)softmax_scale * (double)head_scale);  // one rounding
     a.q_codes = q_codes; a.q_scales = q_scales; a.w_out = w_out; a.dev_status = dev_status;
@@ -133,7 +136,9 @@ int idx_topk(const float* logits, int64_t ld_logits, const int32_t* seq_lens_k,
     if (T < 0 || B < 0 || ld_logits < 0) return IDX_EINVAL;
     if (k < 1 || k > 4096) return IDX_EUNSUPPORTED;
     if (T == 0) return IDX_OK;
-    if (!logits || !seq_lens_k || !cu_seqlens_q || !out_idx || B == 0) return IDX_EINVAL;
+    if (!logits || !seq_lens_k || !cu_seqlens_q || !out_idx || B == 0 || !aligned(logits, 4))
+        return IDX_EINVAL;
+    if (ld_logits > INT32_MAX) return IDX_EUNSUPPORTED;  // key indices are int32
     idx::TopkArgs a{};
     a.logits = logits; a.ld = ld_logits; a.seq_lens_k = seq_lens_k; a.cu_seqlens_q = cu_seqlens_q;
     a.B = B; a.T = T; a.causal = causal != 0; a.k = k; a.out = out_idx;

@@ -26,7 +26,7 @@ struct KStoreArgs {
 
 struct QQuantArgs {
     const uint16_t* q;
-    int64_t n_rows;  // T * Hq (Hq = H rounded up to 8)
+    int64_t T;  // tokens; each has H heads (Hq = H rounded up to 8 in the image)
     int32_t H;
     const int32_t* positions;
     const float* cos_sin;

@@ -62,7 +62,7 @@ __device__ __forceinline__ void layernorm(float* x, int l16, const float* gamma,
 
 // RoPE on dims 0..63 (lanes 0..7 of the row). NeoX pairs dims (i, i+32): lane l < 4 holds
 // the first element of its pairs, lane l+4 the second. Interleaved pairs (2i, 2i+1) lie
-// inside one lane. cs = the table row [cos f0..f31, sin f0..f31].
+// inside one lane. cs = the table row [cos f0..f0+31, sin f0..f0+31] (16-byte aligned).
 __device__ __forceinline__ void rope(float* x, int l16, const float* cs, int mode) {
     if (mode == IDX_ROPE_NEOX) {
         float p[8];
@@ -70,22 +70,28 @@ __device__ __forceinline__ void rope(float* x, int l16, const float* cs, int mod
         for (int i = 0; i < 8; ++i) p[i] = __shfl_xor_sync(kFull, x[i], 4);
         if (l16 < 8) {
             const int f0 = (8 * l16) & 31;
+            const float4 c0 = __ldg(reinterpret_cast<const float4*>(cs + f0));
+            const float4 c1 = __ldg(reinterpret_cast<const float4*>(cs + f0 + 4));
+            const float4 s0 = __ldg(reinterpret_cast<const float4*>(cs + 32 + f0));
+            const float4 s1 = __ldg(reinterpret_cast<const float4*>(cs + 32 + f0 + 4));
+            const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                float c = __ldg(cs + f0 + i), s = __ldg(cs + 32 + f0 + i);
-                if (l16 < 4) x[i] = __fsub_rn(__fmul_rn(x[i], c), __fmul_rn(p[i], s));  // a' = ac - bs
-                else         x[i] = __fadd_rn(__fmul_rn(x[i], c), __fmul_rn(p[i], s));  // b' = bc + as
+                if (l16 < 4) x[i] = __fsub_rn(__fmul_rn(x[i], c[i]), __fmul_rn(p[i], sn[i]));  // a' = ac - bs
+                else         x[i] = __fadd_rn(__fmul_rn(x[i], c[i]), __fmul_rn(p[i], sn[i]));  // b' = bc + as
             }
         }
     } else if (mode == IDX_ROPE_INTERLEAVED) {
         if (l16 < 8) {
+            const float4 c4 = __ldg(reinterpret_cast<const float4*>(cs + 4 * l16));
+            const float4 s4 = __ldg(reinterpret_cast<const float4*>(cs + 32 + 4 * l16));
+            const float c[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const int f = 4 * l16 + q;
-                float c = __ldg(cs + f), s = __ldg(cs + 32 + f);
-                float a = x[2 * q], b = x[2 * q + 1];
-                x[2 * q] = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s));
-                x[2 * q + 1] = __fadd_rn(__fmul_rn(b, c), __fmul_rn(a, s));
+                const float a = x[2 * q], b = x[2 * q + 1];
+                x[2 * q] = __fsub_rn(__fmul_rn(a, c[q]), __fmul_rn(b, sn[q]));
+                x[2 * q + 1] = __fadd_rn(__fmul_rn(b, c[q]), __fmul_rn(a, sn[q]));
             }
         }
     }
@@ -191,83 +197,65 @@ __global__ void __launch_bounds__(kThreads) k_store_kernel(KStoreArgs a) {
     }
 }
 
-// Q rows are walked over T x Hq "virtual" heads, Hq = H rounded up to 8: heads past H
-// write the zero/neutral padding of the tensor-core image (see idx.h for the layout). Each
-// 16-lane group takes kQRows rows (kRowsPerCta apart, so every load instruction of the CTA
-// stays coalesced) and issues all their loads before it computes, which keeps several
-// 16-byte loads per thread in flight.
-constexpr int kQRows = 1;
-
+// Q rows: CTA (t, y) takes token t's heads 16y .. 16y+15 of the Hq = H rounded up to 8
+// heads; heads past H write the zero/neutral padding of the tensor-core image (see idx.h
+// for the layout). Hq is a multiple of 8, so the two rows of a warp are live together.
 template <int kDtype>
 __global__ void __launch_bounds__(kThreads) q_quant_kernel(QQuantArgs a) {
     const int l16 = threadIdx.x & 15;
     const int Hq = (a.H + 7) & ~7;
-    const int64_t v0 = (int64_t)blockIdx.x * kRowsPerCta * kQRows + (threadIdx.x >> 4);
-    uint4 raw[kQRows];
-    int32_t pos[kQRows];
-#pragma unroll
-    for (int r = 0; r < kQRows; ++r) {
-        const int64_t vrow = v0 + r * kRowsPerCta;  // t*Hq + h
-        const int64_t t = vrow / Hq;
-        const int h = (int)(vrow - t * Hq);
-        const bool real = vrow < a.n_rows && h < a.H;
-        raw[r] = real ? __ldg(reinterpret_cast<const uint4*>(a.q + (t * a.H + h) * 128 + 8 * l16))
-                      : make_uint4(0, 0, 0, 0);
-        pos[r] = (real && a.rope != IDX_ROPE_NONE) ? __ldg(a.positions + t) : 0;
+    const int64_t t = blockIdx.x;
+    const int h = blockIdx.y * kRowsPerCta + (threadIdx.x >> 4);
+    if (h >= Hq) return;
+    const bool real = h < a.H;
+    const int64_t row = t * a.H + h;  // index of (t, h) in q, w_in, w_out
+    // the Q row and the position are independent loads: issue them together
+    const uint4 raw = real ? __ldg(reinterpret_cast<const uint4*>(a.q + row * 128 + 8 * l16))
+                           : make_uint4(0, 0, 0, 0);
+    int32_t pos = (real && a.rope != IDX_ROPE_NONE) ? __ldg(a.positions + t) : 0;
+    bool ok = real;
+    if (a.rope != IDX_ROPE_NONE && ok && (pos < 0 || pos >= a.max_pos)) {
+        if (l16 == 0) report(a.dev_status, IDX_STATUS_BAD_POS);
+        ok = false;
     }
-#pragma unroll
-    for (int r = 0; r < kQRows; ++r) {
-        const int64_t vrow = v0 + r * kRowsPerCta;
-        const bool live = vrow < a.n_rows;  // n_rows = T * Hq
-        const int64_t t = live ? vrow / Hq : 0;
-        const int h = live ? (int)(vrow - t * Hq) : 0;
-        const bool real = live && h < a.H;
-        bool ok = real;
-        int32_t p = pos[r];
-        if (a.rope != IDX_ROPE_NONE && ok && (p < 0 || p >= a.max_pos)) {
-            if (l16 == 0) report(a.dev_status, IDX_STATUS_BAD_POS);
-            ok = false;
-        }
-        if (!ok) p = 0;
-        const int64_t row = t * a.H + h;  // index of (t, h) in q, w_in, w_out
-        float x[8];
-        unpack8(ok ? raw[r] : make_uint4(0, 0, 0, 0), x);
-        if (a.rope != IDX_ROPE_NONE) rope(x, l16, a.cos_sin + (int64_t)p * 64, a.rope);
-        if (kDtype == IDX_MXFP4) {
-            uint32_t word, sbyte;
-            mx_quant(x, word, sbyte);
-            const uint32_t s1 = __shfl_down_sync(kFull, sbyte, 4);
-            const uint32_t s2 = __shfl_down_sync(kFull, sbyte, 8);
-            const uint32_t s3 = __shfl_down_sync(kFull, sbyte, 12);
-            // gather each 16-byte chunk (4 lanes' words) into its first lane
-            const uint32_t w1 = __shfl_down_sync(kFull, word, 1);
-            const uint32_t w2 = __shfl_down_sync(kFull, word, 2);
-            const uint32_t w3 = __shfl_down_sync(kFull, word, 3);
-            if (live && (ok || !real)) {
-                // canonical image: 8-head groups of [4 chunks][8 heads][16 B]
-                uint8_t* img = a.q_codes + t * Hq * 64 + ((h >> 3) * 4 + (l16 >> 2)) * 128 + (h & 7) * 16;
-                if ((l16 & 3) == 0)
-                    *reinterpret_cast<uint4*>(img) = real ? make_uint4(word, w1, w2, w3) : make_uint4(0, 0, 0, 0);
-                if (l16 == 0) {
-                    uint8_t* atom = reinterpret_cast<uint8_t*>(a.q_scales) + t * 512 + (h & 31) * 16 + (h >> 5) * 4;
-                    *reinterpret_cast<uint32_t*>(atom) = real ? (sbyte | (s1 << 8) | (s2 << 16) | (s3 << 24)) : 0x7f7f7f7fu;
-                    if (real) a.w_out[row] = __fmul_rn(__ldg(a.w_in + row), a.fold);
-                }
+    if (!ok) pos = 0;
+    float x[8];
+    unpack8(ok ? raw : make_uint4(0, 0, 0, 0), x);
+    if (a.rope != IDX_ROPE_NONE) rope(x, l16, a.cos_sin + (int64_t)pos * 64, a.rope);
+    if (kDtype == IDX_MXFP4) {
+        uint32_t word, sbyte;
+        mx_quant(x, word, sbyte);
+        const uint32_t s1 = __shfl_down_sync(kFull, sbyte, 4);
+        const uint32_t s2 = __shfl_down_sync(kFull, sbyte, 8);
+        const uint32_t s3 = __shfl_down_sync(kFull, sbyte, 12);
+        // gather each 16-byte chunk (4 lanes' words) into its first lane
+        const uint32_t w1 = __shfl_down_sync(kFull, word, 1);
+        const uint32_t w2 = __shfl_down_sync(kFull, word, 2);
+        const uint32_t w3 = __shfl_down_sync(kFull, word, 3);
+        if (ok || !real) {
+            // canonical image: 8-head groups of [4 chunks][8 heads][16 B]
+            uint8_t* img = a.q_codes + t * Hq * 64 + ((h >> 3) * 4 + (l16 >> 2)) * 128 + (h & 7) * 16;
+            if ((l16 & 3) == 0)
+                *reinterpret_cast<uint4*>(img) = real ? make_uint4(word, w1, w2, w3) : make_uint4(0, 0, 0, 0);
+            if (l16 == 0) {
+                uint8_t* atom = reinterpret_cast<uint8_t*>(a.q_scales) + t * 512 + (h & 31) * 16 + (h >> 5) * 4;
+                *reinterpret_cast<uint32_t*>(atom) = real ? (sbyte | (s1 << 8) | (s2 << 16) | (s3 << 24)) : 0x7f7f7f7fu;
+                if (real) a.w_out[row] = __fmul_rn(__ldg(a.w_in + row), a.fold);
             }
-        } else {
-            uint32_t lo, hi;
-            float scale;
-            f8_quant(x, lo, hi, scale);
-            const uint32_t plo = __shfl_down_sync(kFull, lo, 1);
-            const uint32_t phi = __shfl_down_sync(kFull, hi, 1);
-            if (live && (ok || !real)) {
-                uint8_t* img = a.q_codes + t * Hq * 128 + ((h >> 3) * 8 + (l16 >> 1)) * 128 + (h & 7) * 16;
-                if ((l16 & 1) == 0)
-                    *reinterpret_cast<uint4*>(img) = real ? make_uint4(lo, hi, plo, phi) : make_uint4(0, 0, 0, 0);
-                if (l16 == 0 && real) {
-                    if (a.q_scales) reinterpret_cast<float*>(a.q_scales)[row] = scale;
-                    a.w_out[row] = __fmul_rn(__fmul_rn(__ldg(a.w_in + row), a.fold), scale);
-                }
+        }
+    } else {
+        uint32_t lo, hi;
+        float scale;
+        f8_quant(x, lo, hi, scale);
+        const uint32_t plo = __shfl_down_sync(kFull, lo, 1);
+        const uint32_t phi = __shfl_down_sync(kFull, hi, 1);
+        if (ok || !real) {
+            uint8_t* img = a.q_codes + t * Hq * 128 + ((h >> 3) * 8 + (l16 >> 1)) * 128 + (h & 7) * 16;
+            if ((l16 & 1) == 0)
+                *reinterpret_cast<uint4*>(img) = real ? make_uint4(lo, hi, plo, phi) : make_uint4(0, 0, 0, 0);
+            if (l16 == 0 && real) {
+                if (a.q_scales) reinterpret_cast<float*>(a.q_scales)[row] = scale;
+                a.w_out[row] = __fmul_rn(__fmul_rn(__ldg(a.w_in + row), a.fold), scale);
             }
         }
     }
@@ -293,10 +281,11 @@ cudaError_t launch_k_store(const KStoreArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_q_quant(const QQuantArgs& a, cudaStream_t st) {
-    if (a.n_rows == 0) return cudaSuccess;
-    const int64_t grid = (a.n_rows + kRowsPerCta * kQRows - 1) / (kRowsPerCta * kQRows);
-    if (a.dtype == IDX_MXFP4) q_quant_kernel<IDX_MXFP4><<<(unsigned)grid, kThreads, 0, st>>>(a);
-    else q_quant_kernel<IDX_FP8><<<(unsigned)grid, kThreads, 0, st>>>(a);
+    if (a.T == 0) return cudaSuccess;
+    const int Hq = (a.H + 7) & ~7;
+    const dim3 grid((unsigned)a.T, (unsigned)((Hq + kRowsPerCta - 1) / kRowsPerCta));
+    if (a.dtype == IDX_MXFP4) q_quant_kernel<IDX_MXFP4><<<grid, kThreads, 0, st>>>(a);
+    else q_quant_kernel<IDX_FP8><<<grid, kThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
 

@@ -43,6 +43,7 @@ constexpr int kWarps = 6;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kEpiThreads = 128;
 constexpr int kAccG = 2;  // accumulator groups in tensor memory
+constexpr int kSeqWin = 32;  // sequences described by the shared-memory table
 
 template <int kDtype, int NP>
 struct Cfg {
@@ -55,36 +56,47 @@ struct Cfg {
     static constexpr int kTileSf = kDtype == IDX_MXFP4 ? 512 : 0;          // scale atom (MXFP4)
     static constexpr int kTile = kTileCode + kTileSf;
     static constexpr int kGroup = G * kTile;
-    static constexpr int kSG = ((kCps == 1 ? 184 : 200 / kCps) * 1024) / kGroup;  // stage groups
     static constexpr int kQRow = kDtype == IDX_MXFP4 ? 64 : 128;
     static constexpr int kQImg = NP * kQRow;                               // per Q slot
     static constexpr int kQSf = kDtype == IDX_MXFP4 ? 512 : 0;
+    // Q slots (a ring): a producer batch touches at most kQS sequences, so a slot it waits
+    // for is always released by tiles of earlier batches
+    static constexpr int kQS = NP <= 32 ? 4 : 2;
+    // shared memory of one CTA: an SM has 228 KB, of which 1 KB per resident CTA is reserved;
+    // one CTA per SM leaves room for the tile rings of the other kernels' CTAs
+    static constexpr int kBudget = kCps == 1 ? 184 * 1024 : (228 * 1024) / kCps - 1024;
+    static constexpr int kFixed = kQS * (kQImg + kQSf) + 64 + kSeqWin * 16 + 8 * (2 * kQS + 1 + 2 * kAccG);
+    static constexpr int kSG = (kBudget - kFixed) / (kGroup + 16);        // stage groups
     static constexpr uint32_t kSbo = kDtype == IDX_MXFP4 ? 512 : 1024;
-    static constexpr int kColsUsed = kAccG * G * (NP + 4) + 8;             // acc + SFA + SFB
+    static constexpr int kColsUsed = kAccG * G * (NP + 4) + 4 * kQS;       // acc + SFA + SFB
     static constexpr uint32_t kCols = kColsUsed <= 64 ? 64 : kColsUsed <= 128 ? 128 : kColsUsed <= 256 ? 256 : 512;
     static constexpr int kBatch = G * kSG < 32 ? G * kSG : (32 / G) * G;   // tiles per producer batch
     // shared memory map
     static constexpr int oStages = 0;
     static constexpr int oQ = kSG * kGroup;
-    static constexpr int oQSf = oQ + 2 * kQImg;
-    static constexpr int oBars = oQSf + 2 * kQSf;
-    static constexpr int kBars = 2 * kSG + 4 + 2 * kAccG;
+    static constexpr int oQSf = oQ + kQS * kQImg;
+    static constexpr int oBars = oQSf + kQS * kQSf;
+    static constexpr int kBars = 2 * kSG + 2 * kQS + 1 + 2 * kAccG;
     static constexpr int oMisc = oBars + 8 * kBars;
-    static constexpr int kSmem = oMisc + 64;
+    static constexpr int oSeq = oMisc + 64;
+    static constexpr int kSmem = oSeq + kSeqWin * 16;
     static_assert(kBatch % G == 0 && kBatch <= G * kSG, "a batch covers whole, distinct stage groups");
     static_assert(kCols * kCps <= 512, "tensor memory of the CTAs sharing an SM");
+    static_assert(kSmem <= kBudget, "shared memory of the CTAs sharing an SM");
 };
 
-// Tile count and first query row of sequence b (0 tiles if it has no query).
+// Tile count, visible keys and query row of sequence b (0 tiles if it has no query). The
+// three loads are issued together.
 struct SeqInfo {
     int64_t t, vis, tiles;
 };
 
 __device__ __forceinline__ SeqInfo seq_info(const ScoreArgs& a, int b) {
-    SeqInfo r{0, 0, 0};
-    const int64_t q0 = a.cu_seqlens_q[b], nq = a.cu_seqlens_q[b + 1] - q0;
-    if (nq <= 0) return r;
+    const int64_t q0 = a.cu_seqlens_q[b], q1 = a.cu_seqlens_q[b + 1];
     int64_t len = a.seq_lens_k[b];
+    SeqInfo r{0, 0, 0};
+    const int64_t nq = q1 - q0;
+    if (nq <= 0) return r;
     len = len < 0 ? 0 : (len > a.max_seq_len_k ? a.max_seq_len_k : len);
     r.t = q0;
     r.vis = visible_keys(len, nq, nq - 1, a.causal);
@@ -92,22 +104,44 @@ __device__ __forceinline__ SeqInfo seq_info(const ScoreArgs& a, int b) {
     return r;
 }
 
+// The kSeqWin sequences from the slice's first one on are described by a table in shared
+// memory, written once by the prologue, so that walking from one sequence to the next costs
+// no global load (a slice that reaches past the window reads global memory).
+struct SeqEnt {
+    int64_t t;
+    int32_t vis, tiles;
+};
+
+struct Seqs {
+    const ScoreArgs* a;
+    const SeqEnt* tab;
+    int b_tab;  // sequence of tab[0]
+    __device__ __forceinline__ SeqInfo get(int b) const {
+        const unsigned r = (unsigned)(b - b_tab);
+        if (r < (unsigned)kSeqWin) {
+            const SeqEnt e = tab[r];
+            return SeqInfo{e.t, e.vis, e.tiles};
+        }
+        return seq_info(*a, b);
+    }
+};
+
 // Walks (sequence, tile) units in order from a starting unit.
 struct Walker {
     int b;
     int64_t j;
     SeqInfo si;
-    __device__ __forceinline__ void init(const ScoreArgs& a, int b0, int64_t j0) {
+    __device__ __forceinline__ void init(const Seqs& S, int b0, int64_t j0) {
         b = b0;
         j = j0;
-        si = seq_info(a, b);
+        si = b0 < S.a->B ? S.get(b0) : SeqInfo{0, 0, 1};
     }
-    __device__ __forceinline__ void next(const ScoreArgs& a) {
+    __device__ __forceinline__ void next(const Seqs& S) {
         if (++j < si.tiles) return;
         j = 0;
         do {
             ++b;
-            si = b < a.B ? seq_info(a, b) : SeqInfo{0, 0, 1};
+            si = b < S.a->B ? S.get(b) : SeqInfo{0, 0, 1};
         } while (si.tiles == 0);
     }
 };
@@ -141,9 +175,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
     uint64_t* k_full = bars;              // per stage group: G arrivals (+ bytes)
     uint64_t* k_empty = k_full + C::kSG;  // per stage group: one commit
     uint64_t* q_full = k_empty + C::kSG;
-    uint64_t* q_empty = q_full + 2;
-    uint64_t* acc_full = q_empty + 2;
+    uint64_t* q_empty = q_full + C::kQS;
+    uint64_t* acc_full = q_empty + C::kQS;
     uint64_t* acc_empty = acc_full + kAccG;
+    uint64_t* drain = acc_empty + kAccG;  // the MMA issuer's last commit when it gives up
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::oMisc);
     // misc[0] tmem base, misc[1] start sequence, misc[2..3] start tile, misc[4..5] unit count,
     // misc[6] abort flag
@@ -153,12 +188,26 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
     const int H = a.H, P = a.page_size;
     const int Hq = (H + 7) & ~7;
 
+    SeqEnt* seq_tab = reinterpret_cast<SeqEnt*>(smem + C::oSeq);
+
     // ---- this CTA's slice of the units: two warp-wide scans over the sequences ----------
+    // The first reads every sequence (eight per lane, loads issued together; the first 256
+    // sequences' tile counts stay in registers); the second finds the slice's first unit.
     if (warp == 0) {
-        int64_t total = 0;
-        for (int base = 0; base < a.B; base += 32) {
-            const int b = base + lane;
-            int64_t n = b < a.B ? seq_info(a, b).tiles : 0;
+        int64_t total = 0, tl[8];
+        for (int base = 0; base < a.B; base += 256) {
+            SeqInfo si[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int b = base + 32 * k + lane;
+                si[k] = b < a.B ? seq_info(a, b) : SeqInfo{0, 0, 0};
+            }
+            int64_t n = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (base == 0) tl[k] = si[k].tiles;
+                n += si[k].tiles;
+            }
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) n += __shfl_xor_sync(kFull, n, o);
             total += n;
@@ -167,9 +216,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
         int64_t acc = 0;
         int b0 = a.B;
         int64_t j0 = 0;
-        for (int base = 0; base < a.B && b0 == a.B; base += 32) {
-            const int b = base + lane;
-            const int64_t n = b < a.B ? seq_info(a, b).tiles : 0;
+        auto scan32 = [&](int base, int64_t n) {  // one chunk of 32 sequences in order
             int64_t inc = n;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -184,6 +231,18 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
                 j0 = u0 - (acc + __shfl_sync(kFull, inc - n, src));
             }
             acc += __shfl_sync(kFull, inc, 31);
+        };
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (32 * k < a.B && b0 == a.B) scan32(32 * k, 32 * k + lane < a.B ? tl[k] : 0);
+        for (int base = 256; base < a.B && b0 == a.B; base += 32) {
+            const int b = base + lane;
+            scan32(base, b < a.B ? seq_info(a, b).tiles : 0);
+        }
+        {  // the table of the window of sequences from b0 on
+            const int b = b0 + lane;
+            const SeqInfo si = b < a.B ? seq_info(a, b) : SeqInfo{0, 0, 0};
+            seq_tab[lane] = SeqEnt{si.t, (int32_t)si.vis, (int32_t)si.tiles};
         }
         if (lane == 0) {
             const int64_t n = b0 < a.B ? u1 - u0 : 0;
@@ -197,10 +256,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
                 tc::mbar_init(&k_full[i], G);
                 tc::mbar_init(&k_empty[i], 1);
             }
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < C::kQS; ++i) {
                 tc::mbar_init(&q_full[i], 1);
                 tc::mbar_init(&q_empty[i], 1);
             }
+            tc::mbar_init(drain, 1);
             for (int i = 0; i < kAccG; ++i) {
                 tc::mbar_init(&acc_full[i], 1);
                 tc::mbar_init(&acc_empty[i], kEpiThreads);
@@ -217,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
     tc::tc_fence_after();
     const uint32_t tbase = misc[0];
     const int b_start = (int)misc[1];
+    const Seqs S{&a, seq_tab, b_start};
     const int64_t j_start = (int64_t)misc[2] | ((int64_t)misc[3] << 32);
     const int64_t n_units = (int64_t)misc[4] | ((int64_t)misc[5] << 32);
     const int64_t n_groups = (n_units + G - 1) / G;
@@ -224,24 +285,33 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
 
     if (warp == 0 && n_units > 0) {
         // ---------------------------------------------------------------- producer warp
-        // Tiles go out in batches of kBatch (whole stage groups, each group once): lane L
-        // owns tile slot i0+L and issues its page lookups, its stage-group wait and its bulk
-        // copies, so the warp issues the batch at once. Every wait of a lane depends only on
-        // earlier batches or on lower lanes, which never wait on it (no warp barrier inside
-        // a batch). Empty slots of the last group arrive without bytes.
+        // Tiles go out in batches of up to kBatch: lane L owns tile slot i0+L and issues its
+        // page lookups, its stage-group wait and its bulk copies, so the warp issues the
+        // batch at once. A batch touches at most kQS sequences: then every wait of a lane
+        // (a stage group or a Q slot being released) depends only on tiles of earlier
+        // batches, never on a lane of the same batch. Empty slots of the last group arrive
+        // without bytes.
         Walker w;  // position of the batch's first unit (same in every lane)
-        w.init(a, b_start, j_start);
+        w.init(S, b_start, j_start);
         int prev_b = -1;     // sequence of the unit before the batch
         int64_t q_base = 0;  // sequences started before the batch
-        for (int64_t i0 = 0; i0 < n_slots && !__any_sync(kFull, *abort_flag != 0); i0 += C::kBatch) {
-            const int nb = (int)min((int64_t)C::kBatch, n_units - i0);  // real tiles (may be <= 0)
-            const int ns = (int)min((int64_t)C::kBatch, n_slots - i0);  // slots
-            const bool real = lane < nb;
+        int64_t armed_g = -1, armed_q = -1;  // last stage group / Q fill armed (warp-wide)
+        for (int64_t i0 = 0; i0 < n_slots && !__any_sync(kFull, *abort_flag != 0);) {
+            int nb = (int)min((int64_t)C::kBatch, n_units - i0);  // real tiles (may be <= 0)
             Walker my = w;
-            for (int k = 0; k < lane && k + 1 < nb; ++k) my.next(a);
+            for (int k = 0; k < lane && k + 1 < nb; ++k) my.next(S);
             const int b_before = __shfl_up_sync(kFull, my.b, 1);
-            const bool newseq = real && my.b != (lane == 0 ? prev_b : b_before);
-            const unsigned starts = __ballot_sync(kFull, newseq);
+            unsigned starts = __ballot_sync(kFull, lane < nb && my.b != (lane == 0 ? prev_b : b_before));
+            const int allowed = C::kQS - (nb > 0 && w.b == prev_b ? 1 : 0);
+            if (__popc(starts) > allowed) {
+                unsigned m = starts;  // cut the batch at the (allowed+1)-th sequence start
+                for (int r = 0; r < allowed; ++r) m &= m - 1;
+                nb = __ffs(m) - 1;
+                starts &= (1u << nb) - 1u;
+            }
+            const bool real = lane < nb;
+            const bool newseq = real && ((starts >> lane) & 1u);
+            const int ns = i0 + nb >= n_units ? (int)min((int64_t)C::kBatch, n_slots - i0) : nb;  // slots
             if (lane < ns) {
                 const int64_t i = i0 + lane;
                 const int64_t gi = i / G;
@@ -251,8 +321,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
                 if (real) {
                     if (newseq) {
                         const int64_t qk = q_base + __popc(starts & ((2u << lane) - 1)) - 1;
-                        const int slot = (int)(qk & 1);
-                        if (!tc::mbar_wait(&q_empty[slot], (uint32_t)(((qk >> 1) & 1) ^ 1))) {
+                        const int slot = (int)(qk % C::kQS);
+                        if (!tc::mbar_wait(&q_empty[slot], (uint32_t)(((qk / C::kQS) & 1) ^ 1))) {
                             *abort_flag = 1;
                         } else {
                             const uint32_t qbytes = (uint32_t)(Hq * C::kQRow);
@@ -303,26 +373,41 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
                 }
             }
             __syncwarp();
+            armed_g = (i0 + ns - 1) / G;
+            armed_q = q_base + __popc(starts) - 1;
             if (nb <= 0) break;
             // next batch: one unit after this batch's last real unit
-            const int src = (nb < C::kBatch ? nb : C::kBatch) - 1;
             Walker last = my;
-            last.b = __shfl_sync(kFull, my.b, src);
-            last.j = __shfl_sync(kFull, my.j, src);
-            last.si.t = __shfl_sync(kFull, my.si.t, src);
-            last.si.vis = __shfl_sync(kFull, my.si.vis, src);
-            last.si.tiles = __shfl_sync(kFull, my.si.tiles, src);
+            last.b = __shfl_sync(kFull, my.b, nb - 1);
+            last.j = __shfl_sync(kFull, my.j, nb - 1);
+            last.si.t = __shfl_sync(kFull, my.si.t, nb - 1);
+            last.si.vis = __shfl_sync(kFull, my.si.vis, nb - 1);
+            last.si.tiles = __shfl_sync(kFull, my.si.tiles, nb - 1);
             prev_b = last.b;
             q_base += __popc(starts);
             w = last;
-            if (i0 + C::kBatch < n_units) w.next(a);
+            if (i0 + nb < n_units) w.next(S);
+            i0 += ns;
+        }
+        if (*abort_flag) {
+            // do not leave while copies are in flight: wait (bounded) for the last fill armed
+            // in each stage group and each Q slot
+            const uint64_t deadline = tc::global_ns() + tc::kWaitLimitNs;
+            if (lane < C::kSG && armed_g >= lane) {
+                const int64_t g = armed_g - ((armed_g - lane) % C::kSG);
+                tc::mbar_wait_until(&k_full[lane], (uint32_t)((g / C::kSG) & 1), deadline);
+            }
+            if (lane < C::kQS && armed_q >= lane) {
+                const int64_t q = armed_q - ((armed_q - lane) % C::kQS);
+                tc::mbar_wait_until(&q_full[lane], (uint32_t)((q / C::kQS) & 1), deadline);
+            }
         }
         if (lane == 0 && *abort_flag) report(a.dev_status, IDX_STATUS_TIMEOUT);
     } else if (warp == 1 && lane == 0 && n_units > 0) {
         // ---------------------------------------------------------------- MMA issuer
         // tensor memory: accumulators [kAccG][G][NP], then A scale slots [kAccG][G][4] (a slot
         // is rewritten only after the epilogue released its accumulator group, i.e. after the
-        // MMAs that read it ended), then the B scale slot of each Q slot [2][4]
+        // MMAs that read it ended), then the B scale slot of each Q slot [kQS][4]
         const uint32_t t_sfa = tbase + kAccG * G * NP;
         const uint32_t t_sfb = t_sfa + kAccG * G * 4;
         // descriptors of stage 0 / Q slot 0; other tiles, slots and K steps add (bytes >> 4)
@@ -334,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
         const uint32_t id0 = kDtype == IDX_MXFP4 ? tc::idesc_mxf4(128, NP, 0, 0) : tc::idesc_f8(128, NP);
         const uint32_t id1 = kDtype == IDX_MXFP4 ? tc::idesc_mxf4(128, NP, 2, 2) : id0;
         Walker w;
-        w.init(a, b_start, j_start);
+        w.init(S, b_start, j_start);
         int prev_b = -1;
         int64_t qk = -1;
         int slot = 0;
@@ -352,8 +437,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
                 if (i >= n_units) break;
                 if (w.b != prev_b) {
                     ++qk;
-                    slot = (int)(qk & 1);
-                    if (!tc::mbar_wait(&q_full[slot], (uint32_t)((qk >> 1) & 1))) {
+                    slot = (int)(qk % C::kQS);
+                    if (!tc::mbar_wait(&q_full[slot], (uint32_t)((qk / C::kQS) & 1))) {
                         *abort_flag = 1;
                         break;
                     }
@@ -377,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
                     for (int k = 0; k < 4; ++k) tc::mma_f8(d, da + 16 * k, db + 16 * k, id0, k);
                 }
                 const int cur_b = w.b;
-                w.next(a);
+                w.next(S);
                 if (i + 1 == n_units || w.b != cur_b) tc::mma_commit(&q_empty[slot]);
             }
             if (*abort_flag) break;
@@ -386,7 +471,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
             if (++grp == C::kSG) { grp = 0; kph ^= 1; }
             if (++ag == kAccG) { ag = 0; aph ^= 1; }
         }
-        if (*abort_flag) report(a.dev_status, IDX_STATUS_TIMEOUT);
+        if (*abort_flag) {
+            // do not free tensor memory under MMAs still running: one more commit tracks
+            // every tcgen05 operation issued so far; wait (bounded) for it
+            report(a.dev_status, IDX_STATUS_TIMEOUT);
+            tc::mma_commit(drain);
+            tc::mbar_wait(drain, 0);
+        }
     } else if (warp >= 2 && n_units > 0) {
         // ---------------------------------------------------------------- epilogue
         const int quad = warp & 3;
@@ -398,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
         const int half = split ? ((m >> 4) & 1) : (m >> 6);
         const int koff = split ? (64 * half + (m & 15) + 16 * (m >> 5)) : m;
         Walker w;
-        w.init(a, b_start, j_start);
+        w.init(S, b_start, j_start);
         int prev_b = -1;
         float wr[NP];
         int ag = 0;
@@ -413,7 +504,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
                 const int64_t i = gi * G + t;
                 const int64_t key = wk.j * 128 + koff;
                 pg[t] = (i < n_units && key < wk.si.vis) ? __ldg(a.page_table + (int64_t)wk.b * a.pt_stride + key / P) : -1;
-                if (i + 1 < n_units) wk.next(a);
+                if (i + 1 < n_units) wk.next(S);
+            }
+            // so are the head weights when the group's first tile starts a sequence
+            if (w.b != prev_b) {
+#pragma unroll
+                for (int h = 0; h < NP; ++h) wr[h] = h < H ? __ldg(a.w + w.si.t * H + h) : 0.0f;
+                prev_b = w.b;
             }
             const bool got = __all_sync(kFull, tc::mbar_wait(&acc_full[ag], aph));
             if (!got) {
@@ -446,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
                     if (h < H) part[h & 3] = fmaf(wr[h], fmaxf(v[h], 0.0f), part[h & 3]);
                 const float logit = (part[0] + part[1]) + (part[2] + part[3]);
                 if (key_ok) a.logits[w.si.t * a.ld + key] = logit * kscale;
-                w.next(a);
+                w.next(S);
             }
             tc::tc_fence_before();
             tc::mbar_arrive(&acc_empty[ag]);

@@ -8,10 +8,20 @@
 // deterministic.
 //
 // One CTA per query row: 1024 threads, or 256 when there are more rows than SMs and the
-// rows are short (several rows then share an SM). The row's logits are read from global memory once, mapped to order-preserving uint32 keys and kept in shared memory (rows longer than the
-// shared-memory capacity are re-read from global memory instead). Three histogram passes
-// (11, 11, 10 bits, shared-memory atomics) fix the k-th key exactly; the final pass gives
-// each warp a contiguous chunk of the row, so one scan over the warps orders the output.
+// rows are short (several rows then share an SM). Warp w owns the contiguous slice
+// [w*chunk, (w+1)*chunk) of the row and its lanes read consecutive keys, so global loads are
+// coalesced, shared-memory reads are conflict-free and ballots keep the index order.
+//
+//   1. The row's logits are read once, mapped to order-preserving uint32 keys, kept in
+//      shared memory (rows longer than that capacity are re-read from global memory), and
+//      histogrammed on their top 11 bits: the bin b0 holding the k-th key is found.
+//   2. One pass over the keys counts, per warp, the keys above bin b0 and gathers the
+//      indices of the keys inside b0 (the candidates) into a shared list.
+//   3. Two more histogram passes (11 and 10 bits) over the candidates only fix the k-th key
+//      exactly (over all keys of bin b0 when the list overflowed).
+//   4. Per-warp counts of candidates above / equal to the k-th key complete the warps'
+//      counts; one scan over the warps places each warp's output, and a last pass writes
+//      the indices with ballots.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -19,57 +29,82 @@ namespace idx {
 
 namespace {
 
-constexpr int64_t kSmemKeysMax = 48 * 1024;    // 192 KB of keys
-constexpr int64_t kNarrowKeysMax = 12 * 1024;  // 48 KB of keys: four 256-thread CTAs per SM
+constexpr int kSmemKeysMax = 48 * 1024;    // 192 KB of keys
+constexpr int kNarrowKeysMax = 12 * 1024;  // 48 KB of keys: several 256-thread CTAs per SM
 
+// Order-preserving map of fp32 to uint32 (-0.0 and +0.0 share a key: they compare equal).
 __device__ __forceinline__ uint32_t order_key(float f) {
     uint32_t u = __float_as_uint(f);
+    if (u == 0x80000000u) u = 0;
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Inclusive sum scan over the CTA; `total` receives the CTA-wide sum.
-template <int kThreads, typename T>
-__device__ __forceinline__ T block_scan(T v, T* warp_sums, T& total) {
+// Find the bin of the `remaining`-th largest key in hist[0..nb): every thread returns the bin
+// and the number of keys in higher bins. Thread r owns the bins [nb - per*(r+1), nb - per*r),
+// highest bins first; one scan over the CTA orders the owners.
+template <int kThreads>
+__device__ __forceinline__ void select_bin(const uint32_t* hist, int nb, uint32_t remaining,
+                                           uint32_t* warp_sums, uint32_t* sel, uint32_t& bin,
+                                           uint32_t& above) {
     constexpr int kWarps = kThreads / 32;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    T x = v;
+    const int per = nb / kThreads;
+    const int top = nb - per * (int)threadIdx.x;
+    uint32_t local = 0;
+    for (int j = 1; j <= per; ++j) local += hist[top - j];
+    uint32_t x = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        T y = __shfl_up_sync(kFull, x, o);
+        const uint32_t y = __shfl_up_sync(kFull, x, o);
         if (lane >= o) x += y;
     }
     if (lane == 31) warp_sums[w] = x;
     __syncthreads();
     if (w == 0) {
-        T s = lane < kWarps ? warp_sums[lane] : T(0);
+        uint32_t s = lane < kWarps ? warp_sums[lane] : 0u;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            T y = __shfl_up_sync(kFull, s, o);
+            const uint32_t y = __shfl_up_sync(kFull, s, o);
             if (lane >= o) s += y;
         }
         if (lane < kWarps) warp_sums[lane] = s;
     }
     __syncthreads();
-    const T add = w > 0 ? warp_sums[w - 1] : T(0);
-    total = warp_sums[kWarps - 1];
+    const uint32_t incl = x + (w > 0 ? warp_sums[w - 1] : 0u);
+    const uint32_t before = incl - local;
+    if (before < remaining && remaining <= incl) {
+        uint32_t run = before;
+        for (int j = 1; j <= per; ++j) {
+            const uint32_t c = hist[top - j];
+            if (run + c >= remaining) {
+                sel[0] = (uint32_t)(top - j);
+                sel[1] = run;
+                break;
+            }
+            run += c;
+        }
+    }
     __syncthreads();
-    return x + add;
+    bin = sel[0];
+    above = sel[1];
 }
 
-template <int kThreads>
-__global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int64_t smem_keys) {
+template <int kThreads, int kCand>
+__global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_keys) {
     constexpr int kWarps = kThreads / 32;
     extern __shared__ uint32_t skeys[];
     __shared__ uint32_t hist[2048];
-    __shared__ uint64_t warp_sums[kWarps];
-    __shared__ uint32_t sel_bin, sel_above;
+    __shared__ int32_t cand[kCand];
+    __shared__ uint32_t warp_sums[kWarps], warp_gt[kWarps], warp_eq[kWarps];
+    __shared__ uint32_t sel[2], n_cand;
 
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t t = blockIdx.x;
     const int b = seq_of_query(a.cu_seqlens_q, a.B, t);
-    int64_t vis = 0;
+    int vis = 0;
     if (b >= 0) {
         const int64_t q0 = a.cu_seqlens_q[b], nq = a.cu_seqlens_q[b + 1] - q0;
-        vis = visible_keys(a.seq_lens_k[b], nq, t - q0, a.causal);
+        vis = (int)visible_keys(a.seq_lens_k[b], nq, t - q0, a.causal);
     }
     int32_t* out = a.out + t * a.k;
     const float* row = a.logits + t * a.ld;
@@ -78,126 +113,136 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int64_t smem
         return;
     }
     const bool cached = vis <= smem_keys;
-    auto key_at = [&](int64_t i) -> uint32_t { return cached ? skeys[i] : order_key(row[i]); };
+    auto key_at = [&](int i) -> uint32_t { return cached ? skeys[i] : order_key(row[i]); };
 
-    uint32_t prefix = 0, pmask = 0, remaining = (uint32_t)a.k;
-    for (int pass = 0; pass < 3; ++pass) {
-        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-        const uint32_t nb = pass == 2 ? 1024u : 2048u;
-        for (uint32_t i = threadIdx.x; i < nb; i += kThreads) hist[i] = 0;
-        __syncthreads();
-        if (pass == 0) {
-            // rows start 16-byte aligned (ld is a multiple of 4): float4 loads, two in flight
-            const int64_t n4 = vis >> 2;
-            const float4* row4 = reinterpret_cast<const float4*>(row);
-            int64_t j = threadIdx.x;
-            for (; j + kThreads < n4; j += 2 * kThreads) {
-                const float4 v0 = row4[j], v1 = row4[j + kThreads];
-                const uint4 k0 = make_uint4(order_key(v0.x), order_key(v0.y), order_key(v0.z), order_key(v0.w));
-                const uint4 k1 = make_uint4(order_key(v1.x), order_key(v1.y), order_key(v1.z), order_key(v1.w));
-                if (cached) {
-                    reinterpret_cast<uint4*>(skeys)[j] = k0;
-                    reinterpret_cast<uint4*>(skeys)[j + kThreads] = k1;
-                }
-                atomicAdd(&hist[k0.x >> shift], 1u);
-                atomicAdd(&hist[k0.y >> shift], 1u);
-                atomicAdd(&hist[k0.z >> shift], 1u);
-                atomicAdd(&hist[k0.w >> shift], 1u);
-                atomicAdd(&hist[k1.x >> shift], 1u);
-                atomicAdd(&hist[k1.y >> shift], 1u);
-                atomicAdd(&hist[k1.z >> shift], 1u);
-                atomicAdd(&hist[k1.w >> shift], 1u);
-            }
-            for (; j < n4; j += kThreads) {
-                const float4 v0 = row4[j];
-                const uint4 k0 = make_uint4(order_key(v0.x), order_key(v0.y), order_key(v0.z), order_key(v0.w));
-                if (cached) reinterpret_cast<uint4*>(skeys)[j] = k0;
-                atomicAdd(&hist[k0.x >> shift], 1u);
-                atomicAdd(&hist[k0.y >> shift], 1u);
-                atomicAdd(&hist[k0.z >> shift], 1u);
-                atomicAdd(&hist[k0.w >> shift], 1u);
-            }
-            for (int64_t i = 4 * n4 + threadIdx.x; i < vis; i += kThreads) {
-                const uint32_t key = order_key(row[i]);
-                if (cached) skeys[i] = key;
-                atomicAdd(&hist[key >> shift], 1u);
+    for (int i = threadIdx.x; i < 2048; i += kThreads) hist[i] = 0;
+    if (threadIdx.x == 0) n_cand = 0;
+    __syncthreads();
+
+    // 1. read, stage, histogram the top 11 bits (thread-strided, float4 where aligned)
+    {
+        const int head = min(vis, (int)(((16u - ((uint32_t)(uintptr_t)row & 15u)) & 15u) >> 2));
+        const int n4 = (vis - head) >> 2;
+        const float4* row4 = reinterpret_cast<const float4*>(row + head);
+        auto put = [&](int i, uint32_t key) {
+            if (cached) skeys[i] = key;
+            atomicAdd(&hist[key >> 21], 1u);
+        };
+        if ((int)threadIdx.x < head) put(threadIdx.x, order_key(row[threadIdx.x]));
+        int j = threadIdx.x;
+        for (; j + kThreads < n4; j += 2 * kThreads) {
+            const float4 v0 = row4[j], v1 = row4[j + kThreads];
+            const int i0 = head + 4 * j, i1 = head + 4 * (j + kThreads);
+            put(i0, order_key(v0.x)); put(i0 + 1, order_key(v0.y));
+            put(i0 + 2, order_key(v0.z)); put(i0 + 3, order_key(v0.w));
+            put(i1, order_key(v1.x)); put(i1 + 1, order_key(v1.y));
+            put(i1 + 2, order_key(v1.z)); put(i1 + 3, order_key(v1.w));
+        }
+        for (; j < n4; j += kThreads) {
+            const float4 v0 = row4[j];
+            const int i0 = head + 4 * j;
+            put(i0, order_key(v0.x)); put(i0 + 1, order_key(v0.y));
+            put(i0 + 2, order_key(v0.z)); put(i0 + 3, order_key(v0.w));
+        }
+        for (int i = head + 4 * n4 + threadIdx.x; i < vis; i += kThreads) put(i, order_key(row[i]));
+    }
+    __syncthreads();
+    uint32_t b0, above;
+    select_bin<kThreads>(hist, 2048, (uint32_t)a.k, warp_sums, sel, b0, above);
+    uint32_t remaining = (uint32_t)a.k - above;
+
+    // 2. per-warp count of keys above bin b0; gather bin b0's indices
+    const int chunk = ((vis + kWarps - 1) / kWarps + 31) & ~31;
+    const int lo = min(vis, chunk * warp), hi = min(vis, lo + chunk);
+    uint32_t c_hi = 0;
+    for (int i = lo + lane; i < hi; i += 32) {
+        const uint32_t bin = key_at(i) >> 21;
+        c_hi += bin > b0;
+        if (bin == b0) {
+            const uint32_t p = atomicAdd(&n_cand, 1u);
+            if (p < (uint32_t)kCand) cand[p] = i;
+        }
+    }
+    c_hi = __reduce_add_sync(kFull, c_hi);
+    if (lane == 0) {
+        warp_gt[warp] = c_hi;
+        warp_eq[warp] = 0;
+    }
+    __syncthreads();
+    const uint32_t nc = n_cand;
+    const bool listed = nc <= (uint32_t)kCand;
+    // visit every candidate (key in bin b0): from the list, or by rescanning the row
+    auto for_each_cand = [&](auto&& f) {
+        if (listed) {
+            for (uint32_t j = threadIdx.x; j < nc; j += kThreads) {
+                const int i = cand[j];
+                f(i, key_at(i));
             }
         } else {
-            for (int64_t i = threadIdx.x; i < vis; i += kThreads) {
+            for (int i = threadIdx.x; i < vis; i += kThreads) {
                 const uint32_t key = key_at(i);
-                if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
+                if ((key >> 21) == b0) f(i, key);
             }
         }
+    };
+
+    // 3. fix the low 21 bits of the k-th key over the candidates
+    uint32_t prefix = b0 << 21;
+    for (int pass = 1; pass < 3; ++pass) {
+        const int shift = pass == 1 ? 10 : 0;
+        const int nb = pass == 1 ? 2048 : 1024;
+        const uint32_t pmask = pass == 1 ? 0xffe00000u : 0xfffffc00u;
+        for (int i = threadIdx.x; i < nb; i += kThreads) hist[i] = 0;
         __syncthreads();
-        // thread r owns the bins [nb - per*(r+1), nb - per*r), highest bins first
-        const int per = (int)nb / kThreads;
-        const int top = (int)nb - per * (int)threadIdx.x;
-        uint32_t local = 0;
-        for (int j = 1; j <= per; ++j) local += hist[top - j];
-        uint64_t total;
-        const uint32_t incl = (uint32_t)block_scan<kThreads, uint64_t>(local, warp_sums, total);
-        const uint32_t before = incl - local;
-        if (before < remaining && remaining <= incl) {
-            uint32_t run = before;
-            for (int j = 1; j <= per; ++j) {
-                const int bin = top - j;
-                if (run + hist[bin] >= remaining) {
-                    sel_bin = (uint32_t)bin;
-                    sel_above = run;
-                    break;
-                }
-                run += hist[bin];
-            }
-        }
+        for_each_cand([&](int, uint32_t key) {
+            if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & (uint32_t)(nb - 1)], 1u);
+        });
         __syncthreads();
-        prefix |= sel_bin << shift;
-        pmask |= (nb - 1) << shift;
-        remaining -= sel_above;
-        __syncthreads();
+        uint32_t bin, ab;
+        select_bin<kThreads>(hist, nb, remaining, warp_sums, sel, bin, ab);
+        prefix |= bin << shift;
+        remaining -= ab;
     }
 
-    // prefix is the k-th largest key; `remaining` keys equal to it are still needed. Each
-    // warp takes a contiguous chunk of the row (lanes read consecutive keys, so shared-memory
-    // reads are conflict-free), counts, and one scan over the warps' counts places each
-    // warp's output; inside a warp, ballots keep the index order.
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t n_gt = (uint32_t)a.k - remaining;
-    const int64_t chunk = ((vis + kWarps - 1) / kWarps + 31) & ~int64_t(31);
-    const int64_t lo = min(vis, chunk * warp), hi = min(vis, lo + chunk);
-    uint32_t c_gt = 0, c_eq = 0;
-    for (int64_t i = lo + lane; i < hi; i += 32) {
-        const uint32_t key = key_at(i);
-        c_gt += key > prefix;
-        c_eq += key == prefix;
-    }
-    c_gt = __reduce_add_sync(kFull, c_gt);
-    c_eq = __reduce_add_sync(kFull, c_eq);
-    __shared__ uint64_t warp_base[kWarps];
-    if (lane == 0) warp_base[warp] = (uint64_t)c_gt | ((uint64_t)c_eq << 32);
+    // 4. prefix is the k-th largest key; `remaining` keys equal to it are taken, lowest
+    //    indices first. Candidates above / equal to it complete the per-warp counts.
+    const uint32_t kth = prefix;
+    for_each_cand([&](int i, uint32_t key) {
+        if (key > kth) atomicAdd(&warp_gt[i / chunk], 1u);
+        else if (key == kth) atomicAdd(&warp_eq[i / chunk], 1u);
+    });
     __syncthreads();
-    if (warp == 0) {  // exclusive scan of the warps' packed (gt, eq) counts
-        const uint64_t v = lane < kWarps ? warp_base[lane] : 0;
-        uint64_t inc = v;
+    uint32_t c_gt = warp_gt[warp], c_eq = warp_eq[warp];
+    __syncthreads();
+    if (warp == 0) {  // exclusive scans of the warps' counts (kWarps <= 32)
+        const uint32_t g = lane < kWarps ? warp_gt[lane] : 0u, e = lane < kWarps ? warp_eq[lane] : 0u;
+        uint32_t ig = g, ie = e;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const uint64_t y = __shfl_up_sync(kFull, inc, o);
-            if (lane >= o) inc += y;
+            const uint32_t yg = __shfl_up_sync(kFull, ig, o), ye = __shfl_up_sync(kFull, ie, o);
+            if (lane >= o) {
+                ig += yg;
+                ie += ye;
+            }
         }
-        if (lane < kWarps) warp_base[lane] = inc - v;
+        if (lane < kWarps) {
+            warp_gt[lane] = ig - g;
+            warp_eq[lane] = ie - e;
+        }
     }
     __syncthreads();
-    const uint64_t ex = warp_base[warp];
-    uint32_t og = (uint32_t)ex, oe = (uint32_t)(ex >> 32);
+    const uint32_t n_gt = (uint32_t)a.k - remaining;
+    uint32_t og = warp_gt[warp], oe = warp_eq[warp];
     const uint32_t below = (1u << lane) - 1u;
-    for (int64_t base = lo; base < hi && (c_gt > 0 || (c_eq > 0 && oe < remaining)); base += 32) {
-        const int64_t i = base + lane;
+    for (int base = lo; base < hi && (c_gt > 0 || (c_eq > 0 && oe < remaining)); base += 32) {
+        const int i = base + lane;
         const uint32_t key = i < hi ? key_at(i) : 0u;
-        const bool gt = i < hi && key > prefix, eq = i < hi && key == prefix;
+        const bool gt = i < hi && key > kth, eq = i < hi && key == kth;
         const uint32_t mg = __ballot_sync(kFull, gt), me = __ballot_sync(kFull, eq);
-        if (gt) out[og + __popc(mg & below)] = (int32_t)i;
+        if (gt) out[og + __popc(mg & below)] = i;
         if (eq) {
             const uint32_t r = oe + __popc(me & below);
-            if (r < remaining) out[n_gt + r] = (int32_t)i;
+            if (r < remaining) out[n_gt + r] = i;
         }
         og += __popc(mg);
         oe += __popc(me);
@@ -206,13 +251,14 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int64_t smem
     }
 }
 
-template <int kThreads>
+template <int kThreads, int kCand>
 cudaError_t launch_threads(const TopkArgs& a, cudaStream_t st) {
-    const int64_t keys = a.ld < kSmemKeysMax ? a.ld : kSmemKeysMax;
+    const int keys = (int)(a.ld < kSmemKeysMax ? a.ld : kSmemKeysMax);
     const size_t smem = (size_t)keys * sizeof(uint32_t);
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel<kThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel<kThreads, kCand>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    topk_kernel<kThreads><<<(unsigned)a.T, kThreads, smem, st>>>(a, keys);
+    topk_kernel<kThreads, kCand><<<(unsigned)a.T, kThreads, smem, st>>>(a, keys);
     return cudaGetLastError();
 }
 
@@ -226,7 +272,8 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    return (a.T > sms && a.ld <= kNarrowKeysMax) ? launch_threads<256>(a, st) : launch_threads<1024>(a, st);
+    return (a.T > sms && a.ld <= kNarrowKeysMax) ? launch_threads<256, 2048>(a, st)
+                                                 : launch_threads<1024, 4096>(a, st);
 }
 
 }  // namespace idx

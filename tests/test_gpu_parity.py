@@ -350,3 +350,15 @@ def _chunked_prefill(dtype, H, P, causal, lens, nqs, seed):
 def test_path_chunked_prefill(torch, dtype, H, P, causal):
     wl = _chunked_prefill(dtype, H, P, causal, [300, 517, 129, 1], [37, 200, 129, 1], seed=H * 7 + P)
     _full_path(wl, label=f"chunked prefill dtype={dtype} H={H} P={P} causal={causal}")
+
+
+@pytest.mark.parametrize("dtype,H,P,B", [(W.MXFP4, 32, 64, 20000), (W.FP8, 16, 128, 3000)])
+def test_path_decode_many_short_sequences(torch, dtype, H, P, B):
+    """Thousands of short decode sequences (1..300 keys, some empty of queries' keys): a
+    scorer CTA's slice then spans more sequences than its shared-memory window describes,
+    and the prologue scans past its first 256 sequences."""
+    rng = np.random.default_rng(B)
+    lens = rng.integers(1, 301, B)
+    wl = _chunked_prefill(dtype, H, P, 0, lens.tolist(), [1] * B, seed=B + H)
+    _full_path(wl, rows=np.sort(rng.choice(B, 400, replace=False)),
+               label=f"many short decode dtype={dtype} B={B}")

@@ -1,0 +1,141 @@
+"""GPU top-k against the oracle on the same fp32 logits, index for index.
+
+Both sides decide on the same fp32 values, so the selected set must be identical (ties at
+the k-th value resolved towards the lowest indices on both sides). The library's documented
+order is also checked: indices above the k-th value in increasing order, then the indices
+equal to it in increasing order. The cases reach every branch of the kernel: rows shorter
+than k, rows staged in shared memory and rows too long for it, the narrow (many short rows)
+and wide CTA shapes, candidate lists that fit and ones that overflow (heavy ties), unaligned
+row starts, signed zeros, and causal prefill rows of growing length.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+from sparse_attention_indexer_mqa_gb300 import binding as Bn
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch as T
+    Bn.load()
+    return T
+
+
+def expected_order(logits32, vis, k):
+    """The documented order, built from the oracle's selection."""
+    if vis <= k:
+        return np.concatenate([np.arange(vis), np.full(k - vis, -1)]).astype(np.int32)
+    sel = O.topk(logits32.astype(np.float64)[None, :], np.array([vis], np.int32),
+                 np.array([0, 1], np.int32), 0, k)[0]
+    chosen = sel[:k]
+    kth = logits32[chosen].min()
+    above = np.sort(chosen[logits32[chosen] > kth])
+    equal = np.sort(chosen[logits32[chosen] == kth])
+    return np.concatenate([above, equal]).astype(np.int32)
+
+
+def run_rows(torch, rows, k, ld=None, causal=0, cu=None, seq_lens=None):
+    """rows: list of fp32 arrays (one query row each, decode layout) or an explicit
+    (T, ld) matrix with cu/seq_lens for causal prefill."""
+    if isinstance(rows, np.ndarray) and rows.ndim == 2:
+        mat = rows
+    else:
+        L = max(len(r) for r in rows)
+        ld = ld or L
+        mat = np.full((len(rows), ld), np.nan, np.float32)
+        for i, r in enumerate(rows):
+            mat[i, :len(r)] = r
+        seq_lens = np.array([len(r) for r in rows], np.int32)
+        cu = np.arange(len(rows) + 1, dtype=np.int32)
+    T = mat.shape[0]
+    dl = torch.from_numpy(mat).cuda()
+    dsl = torch.from_numpy(seq_lens).cuda()
+    dcu = torch.from_numpy(cu).cuda()
+    out = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+    Bn.idx_topk(dl, dsl, dcu, causal, k, out)
+    torch.cuda.synchronize()
+    return mat, out.cpu().numpy()
+
+
+def check(mat, got, seq_lens, cu, causal, k):
+    B = len(seq_lens)
+    for b in range(B):
+        q0, q1 = int(cu[b]), int(cu[b + 1])
+        for t in range(q0, q1):
+            L = int(seq_lens[b])
+            vis = L - (q1 - q0) + (t - q0) + 1 if causal else L
+            vis = max(0, min(L, vis))
+            exp = expected_order(mat[t, :vis], vis, k)
+            np.testing.assert_array_equal(got[t], exp, err_msg=f"row {t} (visible {vis})")
+
+
+def _decode(torch, rows, k, ld=None):
+    mat, got = run_rows(torch, rows, k, ld=ld)
+    seq = np.array([len(r) for r in rows], np.int32)
+    check(mat, got, seq, np.arange(len(rows) + 1), 0, k)
+
+
+def test_topk_lengths_around_k(torch):
+    rng = np.random.default_rng(1)
+    k = 1024
+    rows = [rng.standard_normal(n).astype(np.float32) for n in
+            (0, 1, 5, 1023, 1024, 1025, 1100, 2047, 4096, 8192, 8191, 12289)]
+    _decode(torch, rows, k)
+
+
+def test_topk_wide_uncached_rows(torch):
+    """Rows longer than the shared-memory staging capacity (48K keys) are re-read."""
+    rng = np.random.default_rng(2)
+    rows = [rng.standard_normal(n).astype(np.float32) * 3 for n in (49153, 65536, 70001)]
+    _decode(torch, rows, 2048)
+
+
+def test_topk_narrow_ctas_many_rows(torch):
+    """More rows than SMs with short rows: the narrow CTA shape."""
+    rng = np.random.default_rng(3)
+    rows = [rng.standard_normal(int(n)).astype(np.float32) for n in rng.integers(1, 9000, 400)]
+    _decode(torch, rows, 512)
+
+
+@pytest.mark.parametrize("n_rows", [8, 400])
+def test_topk_heavy_ties_overflow_candidates(torch, n_rows):
+    """Few distinct values: the candidate list overflows and the k-th value is tied."""
+    rng = np.random.default_rng(4)
+    rows = [rng.integers(0, 3, 9000).astype(np.float32) for _ in range(n_rows)]
+    rows[0][:] = 1.5  # one all-equal row
+    _decode(torch, rows, 1024)
+
+
+def test_topk_unaligned_rows_and_signed_zero(torch):
+    """Odd leading dimension (row starts off 16-byte boundaries); -0.0 equals +0.0."""
+    rng = np.random.default_rng(5)
+    rows = []
+    for n in (3001, 3000, 2999, 5003):
+        r = rng.standard_normal(n).astype(np.float32)
+        z = rng.random(n) < 0.3
+        r[z] = np.where(rng.random(z.sum()) < 0.5, np.float32(0.0), np.float32(-0.0))
+        r[r < 0] = np.abs(r[r < 0]) * 0  # many zeros of both signs at the boundary
+        rows.append(r)
+    _decode(torch, rows, 1500, ld=5007)
+
+
+@pytest.mark.parametrize("k", [1, 7, 4096])
+def test_topk_extreme_k(torch, k):
+    rng = np.random.default_rng(6)
+    rows = [rng.standard_normal(n).astype(np.float32) for n in (10000, 4097, 300)]
+    _decode(torch, rows, k)
+
+
+def test_topk_causal_prefill_rows(torch):
+    """Causal chunked prefill: each query sees a longer prefix; two sequences."""
+    rng = np.random.default_rng(7)
+    lens = np.array([3000, 2200], np.int32)
+    nq = np.array([700, 300], np.int32)
+    cu = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    ld = 3004
+    mat = rng.standard_normal((int(nq.sum()), ld)).astype(np.float32)
+    _, got = run_rows(torch, mat, 512, causal=1, cu=cu, seq_lens=lens)
+    check(mat, got, lens, cu, 1, 512)
