@@ -261,6 +261,24 @@ def time_graph(torch, g, stream):
     return s.elapsed_time(e)
 
 
+def rank_max(x, world, device):
+    """Maximum of a per-rank float over all ranks (the slowest rank sets the job's time);
+    the value itself when there is one rank. `device` is where the collective's tensor
+    lives: the rank's GPU under NCCL, the CPU under gloo."""
+    if world <= 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(pairs_per_rank, ms_per_step, world):
+    """Whole-job throughput in K-tokens/s: every rank scores its own replica's pairs each
+    step (weak scaling), in the slowest rank's time."""
+    return world * pairs_per_rank / (ms_per_step / 1e3) / 1e3
+
+
 def run_gpu(args, rank, world):
     import torch
     from sparse_attention_indexer_mqa_gb300 import binding as Bn
@@ -300,10 +318,7 @@ def run_gpu(args, rank, world):
         g_step.replay()
         torch.cuda.synchronize()
     clk = clocks.stop()
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = rank_max(ms, world, dev)
 
     # per-kernel device time: each kernel captured K times (same rotation) and timed alone
     per_kernel_ms = {}
@@ -315,10 +330,10 @@ def run_gpu(args, rank, world):
 
     # end to end through the C ABI with host buffers: H2D of the step's inputs (new K rows,
     # slots, positions, Q, weights) from pinned memory, the four calls, D2H of the top-k
-    e2e = run_e2e(rep, args, torch, stream)
+    e2e = run_e2e(rep, args, torch, stream, world, dev)
 
     pairs = wl.pairs()
-    value = world * pairs / (ms / args.steps / 1e3) / 1e3
+    value = job_rate(pairs, ms / args.steps, world)
     ab = algorithmic_bytes(wl)
     peaks, peak_kind = measured_peaks()
     sc_s = per_kernel_ms["scorer"] / 1e3
@@ -356,9 +371,7 @@ def run_gpu(args, rank, world):
         "dtype": "mxfp4" if wl.dtype == W.MXFP4 else "fp8e4m3",
         "data": "synthetic (seeded numpy PCG64: bf16 N(0,1) q/k, N(0,1/H) head weights, "
                 "permuted physical pages)",
-        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "D": 128,
-                   "seq_len_k": int(wl.seq_lens_k.max()), "page_size": wl.page_size,
-                   "topk": wl.topk, "queries": wl.T, "pairs": pairs, "causal": wl.causal,
+        "config": {**config_of(wl),
                    "l2": f"inputs rotate over {copies} copies of cache+Q "
                          f"({copies * ws / 2**20:.0f} MiB)" if copies > 1 else
                          f"working set {ws / 2**20:.0f} MiB > 16x L2",
@@ -376,7 +389,14 @@ def run_gpu(args, rank, world):
     return line
 
 
-def run_e2e(rep, args, torch, stream):
+def config_of(wl):
+    return {"workload": wl.name, "B": wl.B, "H": wl.H, "D": 128,
+            "seq_len_k": int(wl.seq_lens_k.max()), "page_size": wl.page_size,
+            "topk": wl.topk, "queries": wl.T, "pairs": wl.pairs(), "causal": wl.causal,
+            "parallelism": "one independent replica per rank (weak scaling)"}
+
+
+def run_e2e(rep, args, torch, stream, world, dev):
     """The same step through the C ABI with host buffers: the step's inputs (new K rows,
     slots, positions, Q, positions, weights) are packed in one pinned host buffer and copied
     to the device in one H2D copy; the top-k indices come back in one D2H copy."""
@@ -409,8 +429,10 @@ def run_e2e(rep, args, torch, stream):
     g = capture(torch, lambda i: one(args.warmup + i), args.steps)
     g.replay()
     torch.cuda.synchronize()
-    ms = time_graph(torch, g, stream) / args.steps
-    return {"value": round(wl.pairs() / (ms / 1e3) / 1e3, 1), "unit": "K-tokens/s",
+    if world > 1:
+        torch.distributed.barrier()
+    ms = rank_max(time_graph(torch, g, stream) / args.steps, world, dev)
+    return {"value": round(job_rate(wl.pairs(), ms, world), 1), "unit": "K-tokens/s",
             "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h),
             "how": "K steps of (one packed H2D from pinned host, 4 library calls, one D2H of "
@@ -499,8 +521,7 @@ def run_reference(args, rank, world):
         "value": v, "unit": "K-tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": wl.name, "B": wl.B, "H": wl.H,
-                                        "seq_len_k": int(wl.seq_lens_k.max())},
+        "data": "synthetic (same seeded workload as the GPU arm)", "config": config_of(wl),
         "cpu_baseline": {"value": v, "unit": "K-tokens/s", "cores": n_threads, "kind": "oracle",
                          "sample": f"each step: K store of {len(wl.step_rows)} new keys, Q quant, "
                                    f"scoring + top-k of {len(rows)} of {wl.T} queries spread evenly"},

@@ -61,7 +61,7 @@ struct PCfg {
     static constexpr int oQSf = oQ + 2 * kQImg;
     static constexpr int oW = oQSf + 2 * kQSf;
     static constexpr int oBars = oW + 2 * kW;
-    static constexpr int kBars = 2 * kStages + 8;
+    static constexpr int kBars = 2 * kStages + 10;
     static constexpr int oMisc = oBars + 8 * kBars;
     static constexpr int kSmem = oMisc + 64;
 };
@@ -153,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
     uint64_t* q_empty = q_full + 2;            // 2
     uint64_t* acc_full = q_empty + 2;          // 2
     uint64_t* acc_empty = acc_full + 2;        // 2
+    uint64_t* drain = acc_empty + 2;           // 2: an MMA issuer's last commit when it gives up
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::oMisc);
     volatile uint32_t* abort_flag = misc + 1;
 
@@ -173,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
             tc::mbar_init(&q_empty[i], 2 + kEpiThreads);
             tc::mbar_init(&acc_full[i], 1);
             tc::mbar_init(&acc_empty[i], kEpiThreads / 2);  // two warpgroups per buffer
+            tc::mbar_init(&drain[i], 1);
         }
         tc::fence_mbar_init();
     }
@@ -196,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
     if (warp == 0) {
         // -------------------------------------------------------------- producer warp
         int64_t n_units = 0, kt = 0;  // units and tiles issued so far
+        int64_t q_armed = -1;         // last unit whose Q fill was armed
         while (sch.next(a, u)) {
             if (__any_sync(kFull, *abort_flag != 0)) break;  // warp-uniform exit
             // Q block into slot n % 2, once the MMAs and epilogues of block n-2 are done with it
@@ -229,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                 const uint32_t qrow_bytes = (uint32_t)(Hq * C::kQRow);  // one query's image
                 const uint32_t qbytes = (uint32_t)u.nq_blk * qrow_bytes;
                 tc::mbar_arrive_expect_tx(&q_full[slot], qbytes);  // after the lanes' stores (warp-synchronised)
+                q_armed = n_units;
                 const uint8_t* qsrc = a.q_codes + (u.t0 + u.q0) * Hq * C::kQRow;
                 uint8_t* qdst = smem + C::oQ + slot * C::kQImg;
                 if (Hq == HP) {
@@ -288,7 +292,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
             ++n_units;
             __syncwarp();
         }
-        if (lane == 0 && *abort_flag) report(a.dev_status, IDX_STATUS_TIMEOUT);
+        if (*abort_flag) {
+            if (lane == 0) report(a.dev_status, IDX_STATUS_TIMEOUT);
+            // do not leave while copies are in flight: wait (bounded) for the last fill armed
+            // in each stage and Q slot
+            const uint64_t deadline = tc::global_ns() + tc::kWaitLimitNs;
+            if (lane < C::kStages && kt - 1 >= lane) {
+                const int64_t k = (kt - 1) - ((kt - 1 - lane) % C::kStages);
+                tc::mbar_wait_until(&k_full[lane], (uint32_t)((k / C::kStages) & 1), deadline);
+            }
+            q_armed = __shfl_sync(kFull, q_armed, 0);
+            if (lane < 2 && q_armed >= lane) {
+                const int64_t n = q_armed - ((q_armed - lane) & 1);
+                tc::mbar_wait_until(&q_full[lane], (uint32_t)((n >> 1) & 1), deadline);
+            }
+        }
     } else if (warp == 1 || warp == 2) {
         // -------------------------------------------------------------- MMA issuers
         // warp 1 issues the even tiles into accumulator 0, warp 2 the odd ones into
@@ -353,7 +371,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                 tc::mma_commit(&q_empty[slot]);  // arrives when this warp's MMAs of the block end
                 ++n_units;
             }
-            if (*abort_flag) report(a.dev_status, IDX_STATUS_TIMEOUT);
+            if (*abort_flag) {
+                // do not free tensor memory under MMAs still running: one more commit tracks
+                // every tcgen05 operation of this thread; wait (bounded) for it
+                report(a.dev_status, IDX_STATUS_TIMEOUT);
+                tc::mma_commit(&drain[buf]);
+                tc::mbar_wait(&drain[buf], 0);
+            }
         }
     } else {
         // -------------------------------------------------------------- epilogue warpgroups
