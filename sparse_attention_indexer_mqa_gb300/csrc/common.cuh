@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/idx.h"
 
 namespace idx {
@@ -17,6 +19,36 @@ constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ void report(int32_t* status, int32_t bit) {
     if (status) atomicOr(status, bit);
+}
+
+// ---- programmatic dependent launch --------------------------------------------------------
+// Every kernel of the library is launched so that it may start while the previous kernel in
+// the stream finishes. Before pdl_wait() a kernel only reads caller inputs that no kernel of
+// the path writes (lengths, page table, positions, RoPE table, bf16 q / k, head weights) and
+// sets up shared and tensor memory; it writes nothing. pdl_wait() returns once the previous
+// grid has completed and its memory is visible (at once when there is no such grid);
+// pdl_launch_dependents(), issued only after pdl_wait(), lets the next kernel start early, so
+// at most two consecutive kernels overlap and the earlier one has finished all its waiting.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch with programmatic stream serialization (the kernel calls pdl_wait()).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args&&... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // bf16 pair in a 32-bit word -> two fp32 (exact)

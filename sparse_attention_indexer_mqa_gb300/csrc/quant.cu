@@ -169,6 +169,8 @@ __global__ void __launch_bounds__(kThreads) k_store_kernel(KStoreArgs a) {
     if (kDtype == IDX_MXFP4) {
         uint32_t word, sbyte;
         mx_quant(x, word, sbyte);
+        pdl_wait();  // the cache may still be read by the previous kernel
+        pdl_launch_dependents();
         // gather the 4 words of a 16-byte chunk (= one scale block) into its first lane
         uint32_t w1 = __shfl_down_sync(kFull, word, 1);
         uint32_t w2 = __shfl_down_sync(kFull, word, 2);
@@ -188,6 +190,8 @@ __global__ void __launch_bounds__(kThreads) k_store_kernel(KStoreArgs a) {
         uint32_t lo, hi;
         float scale;
         f8_quant(x, lo, hi, scale);
+        pdl_wait();
+        pdl_launch_dependents();
         uint32_t plo = __shfl_down_sync(kFull, lo, 1);
         uint32_t phi = __shfl_down_sync(kFull, hi, 1);
         if (ok && (l16 & 1) == 0) {
@@ -225,6 +229,8 @@ __global__ void __launch_bounds__(kThreads) q_quant_kernel(QQuantArgs a) {
     if (kDtype == IDX_MXFP4) {
         uint32_t word, sbyte;
         mx_quant(x, word, sbyte);
+        pdl_wait();  // the Q image and weights may still be read by the previous kernel
+        pdl_launch_dependents();
         const uint32_t s1 = __shfl_down_sync(kFull, sbyte, 4);
         const uint32_t s2 = __shfl_down_sync(kFull, sbyte, 8);
         const uint32_t s3 = __shfl_down_sync(kFull, sbyte, 12);
@@ -247,6 +253,8 @@ __global__ void __launch_bounds__(kThreads) q_quant_kernel(QQuantArgs a) {
         uint32_t lo, hi;
         float scale;
         f8_quant(x, lo, hi, scale);
+        pdl_wait();
+        pdl_launch_dependents();
         const uint32_t plo = __shfl_down_sync(kFull, lo, 1);
         const uint32_t phi = __shfl_down_sync(kFull, hi, 1);
         if (ok || !real) {
@@ -275,18 +283,16 @@ __global__ void debug_encode_kernel(int kind, const float* in, int64_t n, uint8_
 cudaError_t launch_k_store(const KStoreArgs& a, cudaStream_t st) {
     if (a.n_rows == 0) return cudaSuccess;
     const int64_t grid = (a.n_rows + kRowsPerCta - 1) / kRowsPerCta;
-    if (a.dtype == IDX_MXFP4) k_store_kernel<IDX_MXFP4><<<(unsigned)grid, kThreads, 0, st>>>(a);
-    else k_store_kernel<IDX_FP8><<<(unsigned)grid, kThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    return a.dtype == IDX_MXFP4 ? launch_pdl(k_store_kernel<IDX_MXFP4>, dim3((unsigned)grid), dim3(kThreads), 0, st, a)
+                                : launch_pdl(k_store_kernel<IDX_FP8>, dim3((unsigned)grid), dim3(kThreads), 0, st, a);
 }
 
 cudaError_t launch_q_quant(const QQuantArgs& a, cudaStream_t st) {
     if (a.T == 0) return cudaSuccess;
     const int Hq = (a.H + 7) & ~7;
     const dim3 grid((unsigned)a.T, (unsigned)((Hq + kRowsPerCta - 1) / kRowsPerCta));
-    if (a.dtype == IDX_MXFP4) q_quant_kernel<IDX_MXFP4><<<grid, kThreads, 0, st>>>(a);
-    else q_quant_kernel<IDX_FP8><<<grid, kThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    return a.dtype == IDX_MXFP4 ? launch_pdl(q_quant_kernel<IDX_MXFP4>, grid, dim3(kThreads), 0, st, a)
+                                : launch_pdl(q_quant_kernel<IDX_FP8>, grid, dim3(kThreads), 0, st, a);
 }
 
 cudaError_t launch_debug_encode(int kind, const float* in, int64_t n, uint8_t* out, cudaStream_t st) {

@@ -275,6 +275,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
+    // the prologue read only the caller's lengths; Q, weights and the cache come from the
+    // previous kernels
+    pdl_wait();
+    pdl_launch_dependents();
     const uint32_t tbase = misc[0];
     const int b_start = (int)misc[1];
     const Seqs S{&a, seq_tab, b_start};
@@ -580,8 +584,7 @@ cudaError_t launch_np(const ScoreArgs& a, cudaStream_t st) {
     const int64_t units_max = (int64_t)a.B * ((a.max_seq_len_k + 127) / 128);
     const int ctas = C::kCps * sm_count();
     const int grid = (int)(units_max < ctas ? (units_max > 0 ? units_max : 1) : ctas);
-    decode_kernel<kDtype, NP><<<grid, kThreads, C::kSmem, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(decode_kernel<kDtype, NP>, dim3(grid), dim3(kThreads), C::kSmem, st, a);
 }
 
 template <int kDtype>

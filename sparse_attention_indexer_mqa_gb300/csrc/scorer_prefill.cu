@@ -185,6 +185,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
+    // the prologue read only the caller's lengths; Q, weights and the cache come from the
+    // previous kernels
+    pdl_wait();
+    pdl_launch_dependents();
     const uint32_t tbase = misc[0];
     // tensor memory: accumulators [2][N]; A scale slot per buffer [2][4]; B scale atoms per
     // buffer (MMA issuer) and Q slot [2][2][8]
@@ -533,8 +537,7 @@ cudaError_t launch_hp(const ScoreArgs& a, cudaStream_t st) {
     constexpr int QB = kNmax / HP;
     const int64_t units = (int64_t)a.B * ((a.max_q_len + QB - 1) / QB);
     const int grid = (int)(units < sm_count() ? (units > 0 ? units : 1) : sm_count());
-    prefill_kernel<kDtype, HP><<<grid, kThreads, C::kSmem, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(prefill_kernel<kDtype, HP>, dim3(grid), dim3(kThreads), C::kSmem, st, a);
 }
 
 template <int kDtype>

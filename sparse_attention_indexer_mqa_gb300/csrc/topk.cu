@@ -101,6 +101,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t t = blockIdx.x;
     const int b = seq_of_query(a.cu_seqlens_q, a.B, t);
+    pdl_wait();  // the logits come from the previous kernel
+    pdl_launch_dependents();
     int vis = 0;
     if (b >= 0) {
         const int64_t q0 = a.cu_seqlens_q[b], nq = a.cu_seqlens_q[b + 1] - q0;
@@ -258,8 +260,7 @@ cudaError_t launch_threads(const TopkArgs& a, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(topk_kernel<kThreads, kCand>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    topk_kernel<kThreads, kCand><<<(unsigned)a.T, kThreads, smem, st>>>(a, keys);
-    return cudaGetLastError();
+    return launch_pdl(topk_kernel<kThreads, kCand>, dim3((unsigned)a.T), dim3(kThreads), smem, st, a, keys);
 }
 
 }  // namespace
