@@ -87,19 +87,19 @@ struct Cfg {
 
 // Tile count, visible keys and query row of sequence b (0 tiles if it has no query). The
 // three loads are issued together.
-struct SeqInfo {
-    int64_t t, vis, tiles;
+struct SeqInfo {  // 32-bit: T <= INT32_MAX and lengths are int32 (checked by the API)
+    int32_t t, vis, tiles;
 };
 
 __device__ __forceinline__ SeqInfo seq_info(const ScoreArgs& a, int b) {
-    const int64_t q0 = a.cu_seqlens_q[b], q1 = a.cu_seqlens_q[b + 1];
-    int64_t len = a.seq_lens_k[b];
+    const int32_t q0 = a.cu_seqlens_q[b], q1 = a.cu_seqlens_q[b + 1];
+    int32_t len = a.seq_lens_k[b];
     SeqInfo r{0, 0, 0};
-    const int64_t nq = q1 - q0;
+    const int32_t nq = q1 - q0;
     if (nq <= 0) return r;
     len = len < 0 ? 0 : (len > a.max_seq_len_k ? a.max_seq_len_k : len);
     r.t = q0;
-    r.vis = visible_keys(len, nq, nq - 1, a.causal);
+    r.vis = (int32_t)visible_keys(len, nq, nq - 1, a.causal);
     r.tiles = (r.vis + 127) / 128;
     return r;
 }
@@ -108,8 +108,7 @@ __device__ __forceinline__ SeqInfo seq_info(const ScoreArgs& a, int b) {
 // memory, written once by the prologue, so that walking from one sequence to the next costs
 // no global load (a slice that reaches past the window reads global memory).
 struct SeqEnt {
-    int64_t t;
-    int32_t vis, tiles;
+    int32_t t, vis, tiles, pad;
 };
 
 struct Seqs {
@@ -129,9 +128,9 @@ struct Seqs {
 // Walks (sequence, tile) units in order from a starting unit.
 struct Walker {
     int b;
-    int64_t j;
+    int32_t j;
     SeqInfo si;
-    __device__ __forceinline__ void init(const Seqs& S, int b0, int64_t j0) {
+    __device__ __forceinline__ void init(const Seqs& S, int b0, int32_t j0) {
         b = b0;
         j = j0;
         si = b0 < S.a->B ? S.get(b0) : SeqInfo{0, 0, 1};
@@ -194,7 +193,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
     // The first reads every sequence (eight per lane, loads issued together; the first 256
     // sequences' tile counts stay in registers); the second finds the slice's first unit.
     if (warp == 0) {
-        int64_t total = 0, tl[8];
+        int64_t total = 0;
+        SeqInfo s0[8];  // the first 256 sequences: sequence 32k + lane in s0[k]
         for (int base = 0; base < a.B; base += 256) {
             SeqInfo si[8];
 #pragma unroll
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
             int64_t n = 0;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                if (base == 0) tl[k] = si[k].tiles;
+                if (base == 0) s0[k] = si[k];
                 n += si[k].tiles;
             }
 #pragma unroll
@@ -234,15 +234,26 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
         };
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-            if (32 * k < a.B && b0 == a.B) scan32(32 * k, 32 * k + lane < a.B ? tl[k] : 0);
+            if (32 * k < a.B && b0 == a.B) scan32(32 * k, 32 * k + lane < a.B ? s0[k].tiles : 0);
         for (int base = 256; base < a.B && b0 == a.B; base += 32) {
             const int b = base + lane;
             scan32(base, b < a.B ? seq_info(a, b).tiles : 0);
         }
-        {  // the table of the window of sequences from b0 on
+        {  // the table of the window of sequences from b0 on (from registers when b0 + 31 < 256)
             const int b = b0 + lane;
-            const SeqInfo si = b < a.B ? seq_info(a, b) : SeqInfo{0, 0, 0};
-            seq_tab[lane] = SeqEnt{si.t, (int32_t)si.vis, (int32_t)si.tiles};
+            SeqInfo si{0, 0, 0};
+            if (b0 + 31 < 256) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int32_t t = __shfl_sync(kFull, s0[k].t, b & 31);
+                    const int32_t v = __shfl_sync(kFull, s0[k].vis, b & 31);
+                    const int32_t n = __shfl_sync(kFull, s0[k].tiles, b & 31);
+                    if ((b >> 5) == k && b < a.B) si = SeqInfo{t, v, n};
+                }
+            } else if (b < a.B) {
+                si = seq_info(a, b);
+            }
+            seq_tab[lane] = SeqEnt{si.t, si.vis, si.tiles, 0};
         }
         if (lane == 0) {
             const int64_t n = b0 < a.B ? u1 - u0 : 0;
@@ -276,13 +287,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
     __syncthreads();
     tc::tc_fence_after();
     // the prologue read only the caller's lengths; Q, weights and the cache come from the
-    // previous kernels
-    pdl_wait();
-    pdl_launch_dependents();
+    // previous kernels (the producer issues its first page lookups before it waits)
+    if (warp != 0) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
     const uint32_t tbase = misc[0];
     const int b_start = (int)misc[1];
     const Seqs S{&a, seq_tab, b_start};
-    const int64_t j_start = (int64_t)misc[2] | ((int64_t)misc[3] << 32);
+    const int32_t j_start = (int32_t)misc[2];
     const int64_t n_units = (int64_t)misc[4] | ((int64_t)misc[5] << 32);
     const int64_t n_groups = (n_units + G - 1) / G;
     const int64_t n_slots = n_groups * G;  // tile slots incl. the last group's empty ones
@@ -300,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
         int prev_b = -1;     // sequence of the unit before the batch
         int64_t q_base = 0;  // sequences started before the batch
         int64_t armed_g = -1, armed_q = -1;  // last stage group / Q fill armed (warp-wide)
+        bool dep_done = false;               // the first batch's page lookups precede pdl_wait
         for (int64_t i0 = 0; i0 < n_slots && !__any_sync(kFull, *abort_flag != 0);) {
             int nb = (int)min((int64_t)C::kBatch, n_units - i0);  // real tiles (may be <= 0)
             Walker my = w;
@@ -323,6 +337,18 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
                 int32_t pg[2] = {-1, -1};
                 int halves = 0;
                 if (real) {
+                    const int64_t key0 = my.j * 128;
+                    halves = P == 128 ? 1 : (key0 + 64 < my.si.vis ? 2 : 1);
+                    const int32_t* pt = a.page_table + (int64_t)my.b * a.pt_stride;
+                    pg[0] = __ldg(pt + key0 / P);
+                    if (halves == 2) pg[1] = __ldg(pt + (key0 + 64) / P);
+                }
+                if (!dep_done) {  // Q and the cache come from the previous kernels
+                    pdl_wait();
+                    pdl_launch_dependents();
+                    dep_done = true;
+                }
+                if (real) {
                     if (newseq) {
                         const int64_t qk = q_base + __popc(starts & ((2u << lane) - 1)) - 1;
                         const int slot = (int)(qk % C::kQS);
@@ -331,18 +357,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
                         } else {
                             const uint32_t qbytes = (uint32_t)(Hq * C::kQRow);
                             tc::mbar_arrive_expect_tx(&q_full[slot], qbytes + C::kQSf);
-                            tc::bulk_g2s(smem + C::oQ + slot * C::kQImg, a.q_codes + my.si.t * Hq * C::kQRow,
+                            tc::bulk_g2s(smem + C::oQ + slot * C::kQImg, a.q_codes + (int64_t)my.si.t * Hq * C::kQRow,
                                          qbytes, &q_full[slot]);
                             if (kDtype == IDX_MXFP4)
-                                tc::bulk_g2s(smem + C::oQSf + slot * C::kQSf, a.q_scales + my.si.t * 512, 512,
+                                tc::bulk_g2s(smem + C::oQSf + slot * C::kQSf, a.q_scales + (int64_t)my.si.t * 512, 512,
                                              &q_full[slot]);
                         }
                     }
-                    const int64_t key0 = my.j * 128;
-                    halves = P == 128 ? 1 : (key0 + 64 < my.si.vis ? 2 : 1);
-                    const int32_t* pt = a.page_table + (int64_t)my.b * a.pt_stride;
-                    pg[0] = __ldg(pt + key0 / P);
-                    if (halves == 2) pg[1] = __ldg(pt + (key0 + 64) / P);
                 }
                 if (*abort_flag || !tc::mbar_wait(&k_empty[grp], (uint32_t)(((gi / C::kSG) & 1) ^ 1))) {
                     *abort_flag = 1;
@@ -513,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
             // so are the head weights when the group's first tile starts a sequence
             if (w.b != prev_b) {
 #pragma unroll
-                for (int h = 0; h < NP; ++h) wr[h] = h < H ? __ldg(a.w + w.si.t * H + h) : 0.0f;
+                for (int h = 0; h < NP; ++h) wr[h] = h < H ? __ldg(a.w + (int64_t)w.si.t * H + h) : 0.0f;
                 prev_b = w.b;
             }
             const bool got = __all_sync(kFull, tc::mbar_wait(&acc_full[ag], aph));
@@ -529,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
                 if (i >= n_units) break;
                 if (w.b != prev_b) {
 #pragma unroll
-                    for (int h = 0; h < NP; ++h) wr[h] = h < H ? __ldg(a.w + w.si.t * H + h) : 0.0f;
+                    for (int h = 0; h < NP; ++h) wr[h] = h < H ? __ldg(a.w + (int64_t)w.si.t * H + h) : 0.0f;
                     prev_b = w.b;
                 }
                 const int64_t key = w.j * 128 + koff;
@@ -546,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
                 for (int h = 0; h < NP; ++h)
                     if (h < H) part[h & 3] = fmaf(wr[h], fmaxf(v[h], 0.0f), part[h & 3]);
                 const float logit = (part[0] + part[1]) + (part[2] + part[3]);
-                if (key_ok) a.logits[w.si.t * a.ld + key] = logit * kscale;
+                if (key_ok) a.logits[(int64_t)w.si.t * a.ld + key] = logit * kscale;
                 w.next(S);
             }
             tc::tc_fence_before();

@@ -7,7 +7,7 @@
 // indices equal to it, each group in increasing index order, so the result is
 // deterministic.
 //
-// One CTA per query row: 1024 threads, or 256 when there are more rows than SMs and the
+// One CTA per query row: 1024 threads, or 512 when there are more rows than SMs and the
 // rows are short (several rows then share an SM). Warp w owns the contiguous slice
 // [w*chunk, (w+1)*chunk) of the row and its lanes read consecutive keys, so global loads are
 // coalesced, shared-memory reads are conflict-free and ballots keep the index order.
@@ -15,10 +15,10 @@
 //   1. The row's logits are read once, mapped to order-preserving uint32 keys, kept in
 //      shared memory (rows longer than that capacity are re-read from global memory), and
 //      histogrammed on their top 11 bits: the bin b0 holding the k-th key is found.
-//   2. One pass over the keys counts, per warp, the keys above bin b0 and gathers the
-//      indices of the keys inside b0 (the candidates) into a shared list.
-//   3. Two more histogram passes (11 and 10 bits) over the candidates only fix the k-th key
-//      exactly (over all keys of bin b0 when the list overflowed).
+//   2. One pass over the keys counts, per warp, the keys above bin b0 and gathers the keys
+//      inside b0 (the candidates: index and key) into a shared list.
+//   3. Two more histogram passes (11 and 10 bits) over the listed candidates fix the k-th
+//      key exactly (over every key of bin b0 when the list overflowed).
 //   4. Per-warp counts of candidates above / equal to the k-th key complete the warps'
 //      counts; one scan over the warps places each warp's output, and a last pass writes
 //      the indices with ballots.
@@ -30,7 +30,7 @@ namespace idx {
 namespace {
 
 constexpr int kSmemKeysMax = 48 * 1024;    // 192 KB of keys
-constexpr int kNarrowKeysMax = 12 * 1024;  // 48 KB of keys: several 256-thread CTAs per SM
+constexpr int kNarrowKeysMax = 12 * 1024;  // 48 KB of keys: several 512-thread CTAs per SM
 
 // Order-preserving map of fp32 to uint32 (-0.0 and +0.0 share a key: they compare equal).
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -89,12 +89,16 @@ __device__ __forceinline__ void select_bin(const uint32_t* hist, int nb, uint32_
     above = sel[1];
 }
 
-template <int kThreads, int kCand>
+// kVec: every row fits in shared memory and starts on a 16-byte boundary (ld % 4 == 0), so
+// the key passes move four keys per access; otherwise the generic form (rows re-read from
+// global memory when longer than shared memory, any alignment).
+template <int kThreads, int kCand, bool kVec>
 __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_keys) {
     constexpr int kWarps = kThreads / 32;
     extern __shared__ uint32_t skeys[];
     __shared__ uint32_t hist[2048];
     __shared__ int32_t cand[kCand];
+    __shared__ uint32_t ckey[kCand];  // the candidates' keys, in list order
     __shared__ uint32_t warp_sums[kWarps], warp_gt[kWarps], warp_eq[kWarps];
     __shared__ uint32_t sel[2], n_cand;
 
@@ -122,7 +126,32 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
     __syncthreads();
 
     // 1. read, stage, histogram the top 11 bits (thread-strided, float4 where aligned)
-    {
+    if constexpr (kVec) {
+        const int n4 = vis >> 2;
+        const float4* row4 = reinterpret_cast<const float4*>(row);
+        uint4* sk4 = reinterpret_cast<uint4*>(skeys);
+        auto put4 = [&](int j, const float4 v) {
+            const uint4 k = make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
+            sk4[j] = k;
+            atomicAdd(&hist[k.x >> 21], 1u);
+            atomicAdd(&hist[k.y >> 21], 1u);
+            atomicAdd(&hist[k.z >> 21], 1u);
+            atomicAdd(&hist[k.w >> 21], 1u);
+        };
+        int j = threadIdx.x;
+        for (; j + kThreads < n4; j += 2 * kThreads) {
+            const float4 v0 = row4[j], v1 = row4[j + kThreads];
+            put4(j, v0);
+            put4(j + kThreads, v1);
+        }
+        if (j < n4) put4(j, row4[j]);
+        if ((int)threadIdx.x < (vis & 3)) {
+            const int i = 4 * n4 + threadIdx.x;
+            const uint32_t key = order_key(row[i]);
+            skeys[i] = key;
+            atomicAdd(&hist[key >> 21], 1u);
+        }
+    } else {
         const int head = min(vis, (int)(((16u - ((uint32_t)(uintptr_t)row & 15u)) & 15u) >> 2));
         const int n4 = (vis - head) >> 2;
         const float4* row4 = reinterpret_cast<const float4*>(row + head);
@@ -154,15 +183,43 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
     uint32_t remaining = (uint32_t)a.k - above;
 
     // 2. per-warp count of keys above bin b0; gather bin b0's indices
-    const int chunk = ((vis + kWarps - 1) / kWarps + 31) & ~31;
+    constexpr int kStep = kVec ? 128 : 32;  // keys per warp iteration
+    const int chunk = ((vis + kWarps - 1) / kWarps + kStep - 1) & ~(kStep - 1);
     const int lo = min(vis, chunk * warp), hi = min(vis, lo + chunk);
     uint32_t c_hi = 0;
-    for (int i = lo + lane; i < hi; i += 32) {
-        const uint32_t bin = key_at(i) >> 21;
-        c_hi += bin > b0;
-        if (bin == b0) {
-            const uint32_t p = atomicAdd(&n_cand, 1u);
-            if (p < (uint32_t)kCand) cand[p] = i;
+    if constexpr (kVec) {
+        const uint4* sk4 = reinterpret_cast<const uint4*>(skeys);
+        // lo is a multiple of 128 whenever lo < hi; the trip count is warp-uniform
+        for (int base = lo; base < hi; base += 128) {
+            const int i0 = base + 4 * lane;
+            const uint4 k4 = i0 < hi ? sk4[i0 >> 2] : make_uint4(0, 0, 0, 0);
+            const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const bool valid = i0 + e < hi;
+                const uint32_t bin = kk[e] >> 21;
+                c_hi += valid && bin > b0;
+                if (valid && bin == b0) {
+                    const uint32_t p = atomicAdd(&n_cand, 1u);
+                    if (p < (uint32_t)kCand) {
+                        cand[p] = i0 + e;
+                        ckey[p] = kk[e];
+                    }
+                }
+            }
+        }
+    } else {
+        for (int i = lo + lane; i < hi; i += 32) {
+            const uint32_t key = key_at(i);
+            const uint32_t bin = key >> 21;
+            c_hi += bin > b0;
+            if (bin == b0) {
+                const uint32_t p = atomicAdd(&n_cand, 1u);
+                if (p < (uint32_t)kCand) {
+                    cand[p] = i;
+                    ckey[p] = key;
+                }
+            }
         }
     }
     c_hi = __reduce_add_sync(kFull, c_hi);
@@ -176,10 +233,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
     // visit every candidate (key in bin b0): from the list, or by rescanning the row
     auto for_each_cand = [&](auto&& f) {
         if (listed) {
-            for (uint32_t j = threadIdx.x; j < nc; j += kThreads) {
-                const int i = cand[j];
-                f(i, key_at(i));
-            }
+            for (uint32_t j = threadIdx.x; j < nc; j += kThreads) f(cand[j], ckey[j]);
         } else {
             for (int i = threadIdx.x; i < vis; i += kThreads) {
                 const uint32_t key = key_at(i);
@@ -188,7 +242,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
         }
     };
 
-    // 3. fix the low 21 bits of the k-th key over the candidates
+    // 3. fix the low 21 bits of the k-th key over the candidates (listed, or every key of
+    //    bin b0 when the list overflowed)
     uint32_t prefix = b0 << 21;
     for (int pass = 1; pass < 3; ++pass) {
         const int shift = pass == 1 ? 10 : 0;
@@ -235,6 +290,46 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
     __syncthreads();
     const uint32_t n_gt = (uint32_t)a.k - remaining;
     uint32_t og = warp_gt[warp], oe = warp_eq[warp];
+    if constexpr (kVec) {
+        // lane L of an iteration holds keys 4L..4L+3 of the warp's next 128: per-lane counts
+        // and one warp scan place them in index order
+        const uint4* sk4 = reinterpret_cast<const uint4*>(skeys);
+        for (int base = lo; base < hi && (c_gt > 0 || (c_eq > 0 && oe < remaining)); base += 128) {
+            const int i0 = base + 4 * lane;
+            const uint4 k4 = i0 < hi ? sk4[i0 >> 2] : make_uint4(0, 0, 0, 0);
+            const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+            uint32_t fg = 0, fe = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const bool valid = i0 + e < hi;
+                fg |= (uint32_t)(valid && kk[e] > kth) << e;
+                fe |= (uint32_t)(valid && kk[e] == kth) << e;
+            }
+            const uint32_t cnt = (uint32_t)__popc(fg) | ((uint32_t)__popc(fe) << 16);
+            uint32_t inc = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(kFull, inc, o);
+                if (lane >= o) inc += y;
+            }
+            const uint32_t tot = __shfl_sync(kFull, inc, 31);
+            const uint32_t ex = inc - cnt;
+            uint32_t pg = og + (ex & 0xffffu), pe = oe + (ex >> 16);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if ((fg >> e) & 1u) out[pg++] = i0 + e;
+                if ((fe >> e) & 1u) {
+                    if (pe < remaining) out[n_gt + pe] = i0 + e;
+                    ++pe;
+                }
+            }
+            og += tot & 0xffffu;
+            oe += tot >> 16;
+            c_gt -= tot & 0xffffu;
+            c_eq -= tot >> 16;
+        }
+        return;
+    }
     const uint32_t below = (1u << lane) - 1u;
     for (int base = lo; base < hi && (c_gt > 0 || (c_eq > 0 && oe < remaining)); base += 32) {
         const int i = base + lane;
@@ -253,14 +348,21 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
     }
 }
 
-template <int kThreads, int kCand>
-cudaError_t launch_threads(const TopkArgs& a, cudaStream_t st) {
+template <int kThreads, int kCand, bool kVec>
+cudaError_t launch_form(const TopkArgs& a, cudaStream_t st) {
     const int keys = (int)(a.ld < kSmemKeysMax ? a.ld : kSmemKeysMax);
     const size_t smem = (size_t)keys * sizeof(uint32_t);
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel<kThreads, kCand>,
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel<kThreads, kCand, kVec>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(topk_kernel<kThreads, kCand>, dim3((unsigned)a.T), dim3(kThreads), smem, st, a, keys);
+    return launch_pdl(topk_kernel<kThreads, kCand, kVec>, dim3((unsigned)a.T), dim3(kThreads), smem, st, a,
+                      keys);
+}
+
+template <int kThreads, int kCand>
+cudaError_t launch_threads(const TopkArgs& a, cudaStream_t st) {
+    const bool vec = a.ld % 4 == 0 && a.ld <= kSmemKeysMax && ((uintptr_t)a.logits & 15) == 0;
+    return vec ? launch_form<kThreads, kCand, true>(a, st) : launch_form<kThreads, kCand, false>(a, st);
 }
 
 }  // namespace
@@ -273,8 +375,8 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    return (a.T > sms && a.ld <= kNarrowKeysMax) ? launch_threads<256, 2048>(a, st)
-                                                 : launch_threads<1024, 4096>(a, st);
+    return (a.T > sms && a.ld <= kNarrowKeysMax) ? launch_threads<512, 1024>(a, st)
+                                                 : launch_threads<1024, 2048>(a, st);
 }
 
 }  // namespace idx

@@ -73,9 +73,14 @@ def check(mat, got, seq_lens, cu, causal, k):
 
 
 def _decode(torch, rows, k, ld=None):
-    mat, got = run_rows(torch, rows, k, ld=ld)
+    """Each case runs in both kernel forms: a 16-byte aligned leading dimension (four keys
+    per shared-memory access) and an odd one (the generic form)."""
+    L = max(len(r) for r in rows)
+    lds = [ld] if ld is not None else [(L + 3) // 4 * 4, (L + 3) // 4 * 4 + 1]
     seq = np.array([len(r) for r in rows], np.int32)
-    check(mat, got, seq, np.arange(len(rows) + 1), 0, k)
+    for d in lds:
+        mat, got = run_rows(torch, rows, k, ld=d)
+        check(mat, got, seq, np.arange(len(rows) + 1), 0, k)
 
 
 def test_topk_lengths_around_k(torch):
@@ -120,6 +125,7 @@ def test_topk_unaligned_rows_and_signed_zero(torch):
         r[r < 0] = np.abs(r[r < 0]) * 0  # many zeros of both signs at the boundary
         rows.append(r)
     _decode(torch, rows, 1500, ld=5007)
+    _decode(torch, rows, 1500, ld=5008)
 
 
 @pytest.mark.parametrize("k", [1, 7, 4096])
@@ -135,7 +141,7 @@ def test_topk_causal_prefill_rows(torch):
     lens = np.array([3000, 2200], np.int32)
     nq = np.array([700, 300], np.int32)
     cu = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
-    ld = 3004
-    mat = rng.standard_normal((int(nq.sum()), ld)).astype(np.float32)
-    _, got = run_rows(torch, mat, 512, causal=1, cu=cu, seq_lens=lens)
-    check(mat, got, lens, cu, 1, 512)
+    for ld in (3004, 3005):
+        mat = rng.standard_normal((int(nq.sum()), ld)).astype(np.float32)
+        _, got = run_rows(torch, mat, 512, causal=1, cu=cu, seq_lens=lens)
+        check(mat, got, lens, cu, 1, 512)
