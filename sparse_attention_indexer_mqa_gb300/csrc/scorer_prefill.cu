@@ -140,7 +140,8 @@ __device__ __forceinline__ void ld_cols(uint32_t taddr, float* v) {
     }
 }
 
-template <int kDtype, int HP>
+// kFull: H == HP, every accumulator column is a head (no per-head guard in the epilogue).
+template <int kDtype, int HP, bool kFull>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
     using C = PCfg<kDtype>;
     constexpr int QB = kNmax / HP;  // queries per block
@@ -443,61 +444,131 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                 // this key is visible to queries q >= qmin (all of them off the diagonal)
                 const int64_t d = key - vis0 + 1;  // causal: query q sees the key iff q >= d
                 const int qmin = !key_ok ? QB : (qstep == 0 ? (key < vis0 ? 0 : QB) : (d <= 0 ? 0 : (d >= QB ? QB : (int)d)));
-                // software-pipelined drain: chunk c+1 is loaded while chunk c is summed; the
-                // accumulator is released as soon as this half's last chunk is in registers
-                float v[2][CW];
-                ld_cols<CW>(lane_addr, v[0]);
-                tc::tmem_ld_wait();
-                if (nch == 1) {
-                    tc::tc_fence_before();
-                    tc::mbar_arrive(&acc_empty[gb]);
-                }
+                if constexpr (kFull) {
+                    // software-pipelined drain in 16-column chunks (chunk c+1 is loaded while
+                    // chunk c is summed): chunk c holds head columns h0 .. h0+15 of query
+                    // qlo + 16c / HP (two queries when HP = 8); the accumulator is released as
+                    // soon as this half's last chunk is in registers
+                    constexpr int QPC = HP >= 16 ? 1 : 16 / HP;    // queries per chunk
+                    constexpr int NCH16 = (QH0 * HP + 15) / 16;    // chunks per half, at most
+                    const int qend = min(qhi, nqb);
+                    const int nch16 = qend > qlo ? ((qend - qlo) * HP + 15) / 16 : 0;
+                    float v[2][16];
+                    if (nch16 > 0) {
+                        tc::tmem_ld16(lane_addr, *reinterpret_cast<uint32_t(*)[16]>(v[0]));
+                        tc::tmem_ld_wait();
+                    }
+                    if (nch16 <= 1) {
+                        tc::tc_fence_before();
+                        tc::mbar_arrive(&acc_empty[gb]);
+                    }
+                    float2 acc[QPC][2] = {};
 #pragma unroll
-                for (int c = 0; c < NCH; ++c) {
-                    if (c >= nch) break;
-                    float* va = v[c & 1];
-                    if (c + 1 < nch) ld_cols<CW>(lane_addr + (c + 1) * CW, v[(c + 1) & 1]);
+                    for (int c = 0; c < NCH16; ++c) {
+                        if (c >= nch16) break;
+                        const float* va = v[c & 1];
+                        if (c + 1 < nch16)
+                            tc::tmem_ld16(lane_addr + (c + 1) * 16, *reinterpret_cast<uint32_t(*)[16]>(v[(c + 1) & 1]));
 #pragma unroll
-                    for (int qq = 0; qq < QC; ++qq) {
-                        const int q = qlo + c * QC + qq;
-                        if (q < qhi && q < nqb && q >= qmin) {
-                            const float* wq = wsm + q * H;
-                            float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                            if (H == HP) {  // every column is a head: no per-head guard
-                                float4 w4[HP / 4];
+                        for (int qq = 0; qq < QPC; ++qq) {
+                            constexpr int kColsQ = HP >= 16 ? 16 : HP;  // this query's columns here
+                            const int q = qlo + (16 * c) / HP + qq;
+                            const int h0 = (16 * c) % HP;
+                            if (h0 == 0) acc[qq][0] = acc[qq][1] = make_float2(0.0f, 0.0f);
+                            if (q >= qmin && q < qend) {
+                                const float4* w4p = reinterpret_cast<const float4*>(wsm + q * H + h0);
 #pragma unroll
-                                for (int i = 0; i < HP / 4; ++i) w4[i] = reinterpret_cast<const float4*>(wq)[i];
-#pragma unroll
-                                for (int i = 0; i < HP / 4; ++i) {
-                                    part[0] = fmaf(w4[i].x, fmaxf(va[qq * HP + 4 * i], 0.0f), part[0]);
-                                    part[1] = fmaf(w4[i].y, fmaxf(va[qq * HP + 4 * i + 1], 0.0f), part[1]);
-                                    part[2] = fmaf(w4[i].z, fmaxf(va[qq * HP + 4 * i + 2], 0.0f), part[2]);
-                                    part[3] = fmaf(w4[i].w, fmaxf(va[qq * HP + 4 * i + 3], 0.0f), part[3]);
+                                for (int i = 0; i < kColsQ / 4; ++i) {
+                                    const float4 w4 = w4p[i];
+                                    const float* x = va + qq * kColsQ + 4 * i;
+                                    acc[qq][0] = __ffma2_rn(make_float2(w4.x, w4.y),
+                                                            make_float2(fmaxf(x[0], 0.0f), fmaxf(x[1], 0.0f)), acc[qq][0]);
+                                    acc[qq][1] = __ffma2_rn(make_float2(w4.z, w4.w),
+                                                            make_float2(fmaxf(x[2], 0.0f), fmaxf(x[3], 0.0f)), acc[qq][1]);
                                 }
-                            } else if (vec_w) {
-#pragma unroll
-                                for (int h = 0; h < HP; h += 4) {
-                                    if (h < H) {
-                                        const float4 w4 = *reinterpret_cast<const float4*>(wq + h);
-                                        part[0] = fmaf(w4.x, fmaxf(va[qq * HP + h], 0.0f), part[0]);
-                                        part[1] = fmaf(w4.y, fmaxf(va[qq * HP + h + 1], 0.0f), part[1]);
-                                        part[2] = fmaf(w4.z, fmaxf(va[qq * HP + h + 2], 0.0f), part[2]);
-                                        part[3] = fmaf(w4.w, fmaxf(va[qq * HP + h + 3], 0.0f), part[3]);
-                                    }
+                                if (h0 + kColsQ == HP) {
+                                    const float2 s2 = __fadd2_rn(acc[qq][0], acc[qq][1]);
+                                    lrow[q * ld + key] = (s2.x + s2.y) * kscale;
                                 }
-                            } else {
-#pragma unroll
-                                for (int h = 0; h < HP; ++h)
-                                    if (h < H) part[h & 3] = fmaf(wq[h], fmaxf(va[qq * HP + h], 0.0f), part[h & 3]);
                             }
-                            lrow[q * ld + key] = ((part[0] + part[1]) + (part[2] + part[3])) * kscale;
+                        }
+                        if (c + 1 < nch16) {
+                            tc::tmem_ld_wait();
+                            if (c + 2 == nch16) {  // the last chunk is in registers
+                                tc::tc_fence_before();
+                                tc::mbar_arrive(&acc_empty[gb]);
+                            }
                         }
                     }
-                    if (c + 1 < nch) {
-                        tc::tmem_ld_wait();
-                        if (c + 2 == nch) {  // the last chunk is in registers
-                            tc::tc_fence_before();
-                            tc::mbar_arrive(&acc_empty[gb]);
+                } else {
+                    // software-pipelined drain: chunk c+1 is loaded while chunk c is summed; the
+                    // accumulator is released as soon as this half's last chunk is in registers
+                    float v[2][CW];
+                    ld_cols<CW>(lane_addr, v[0]);
+                    tc::tmem_ld_wait();
+                    if (nch == 1) {
+                        tc::tc_fence_before();
+                        tc::mbar_arrive(&acc_empty[gb]);
+                    }
+    #pragma unroll
+                    for (int c = 0; c < NCH; ++c) {
+                        if (c >= nch) break;
+                        float* va = v[c & 1];
+                        if (c + 1 < nch) ld_cols<CW>(lane_addr + (c + 1) * CW, v[(c + 1) & 1]);
+    #pragma unroll
+                        for (int qq = 0; qq < QC; ++qq) {
+                            const int q = qlo + c * QC + qq;
+                            if (q < qhi && q < nqb && q >= qmin) {
+                                const float* wq = wsm + q * H;
+                                float logit;
+                                if constexpr (kFull) {
+                                    // eight independent chains as four packed pairs (fma.rn.f32x2:
+                                    // each lane an ordinary fp32 fused multiply-add)
+                                    float2 acc[4] = {{0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}};
+                                    const float4* w4p = reinterpret_cast<const float4*>(wq);
+    #pragma unroll
+                                    for (int i = 0; i < HP / 4; ++i) {
+                                        const float4 w4 = w4p[i];
+                                        const float* x = va + qq * HP + 4 * i;
+                                        acc[(2 * i) & 3] = __ffma2_rn(make_float2(w4.x, w4.y),
+                                                                      make_float2(fmaxf(x[0], 0.0f), fmaxf(x[1], 0.0f)),
+                                                                      acc[(2 * i) & 3]);
+                                        acc[(2 * i + 1) & 3] = __ffma2_rn(make_float2(w4.z, w4.w),
+                                                                          make_float2(fmaxf(x[2], 0.0f), fmaxf(x[3], 0.0f)),
+                                                                          acc[(2 * i + 1) & 3]);
+                                    }
+                                    const float2 s01 = __fadd2_rn(acc[0], acc[1]), s23 = __fadd2_rn(acc[2], acc[3]);
+                                    const float2 s = __fadd2_rn(s01, s23);
+                                    logit = s.x + s.y;
+                                } else {
+                                    float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                                    if (vec_w) {
+    #pragma unroll
+                                        for (int h = 0; h < HP; h += 4) {
+                                            if (h < H) {
+                                                const float4 w4 = *reinterpret_cast<const float4*>(wq + h);
+                                                part[0] = fmaf(w4.x, fmaxf(va[qq * HP + h], 0.0f), part[0]);
+                                                part[1] = fmaf(w4.y, fmaxf(va[qq * HP + h + 1], 0.0f), part[1]);
+                                                part[2] = fmaf(w4.z, fmaxf(va[qq * HP + h + 2], 0.0f), part[2]);
+                                                part[3] = fmaf(w4.w, fmaxf(va[qq * HP + h + 3], 0.0f), part[3]);
+                                            }
+                                        }
+                                    } else {
+    #pragma unroll
+                                        for (int h = 0; h < HP; ++h)
+                                            if (h < H) part[h & 3] = fmaf(wq[h], fmaxf(va[qq * HP + h], 0.0f), part[h & 3]);
+                                    }
+                                    logit = (part[0] + part[1]) + (part[2] + part[3]);
+                                }
+                                lrow[q * ld + key] = logit * kscale;
+                            }
+                        }
+                        if (c + 1 < nch) {
+                            tc::tmem_ld_wait();
+                            if (c + 2 == nch) {  // the last chunk is in registers
+                                tc::tc_fence_before();
+                                tc::mbar_arrive(&acc_empty[gb]);
+                            }
                         }
                     }
                 }
@@ -528,24 +599,31 @@ int sm_count() {
     return n;
 }
 
-template <int kDtype, int HP>
+template <int kDtype, int HP, bool kFull>
 cudaError_t launch_hp(const ScoreArgs& a, cudaStream_t st) {
     using C = PCfg<kDtype>;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kDtype, HP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kDtype, HP, kFull>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     constexpr int QB = kNmax / HP;
     const int64_t units = (int64_t)a.B * ((a.max_q_len + QB - 1) / QB);
     const int grid = (int)(units < sm_count() ? (units > 0 ? units : 1) : sm_count());
-    return launch_pdl(prefill_kernel<kDtype, HP>, dim3(grid), dim3(kThreads), C::kSmem, st, a);
+    return launch_pdl(prefill_kernel<kDtype, HP, kFull>, dim3(grid), dim3(kThreads), C::kSmem, st, a);
 }
 
 template <int kDtype>
 cudaError_t launch(const ScoreArgs& a, cudaStream_t st) {
-    if (a.H <= 8) return launch_hp<kDtype, 8>(a, st);
-    if (a.H <= 16) return launch_hp<kDtype, 16>(a, st);
-    if (a.H <= 32) return launch_hp<kDtype, 32>(a, st);
-    return launch_hp<kDtype, 64>(a, st);
+    switch (a.H) {
+        case 8: return launch_hp<kDtype, 8, true>(a, st);
+        case 16: return launch_hp<kDtype, 16, true>(a, st);
+        case 32: return launch_hp<kDtype, 32, true>(a, st);
+        case 64: return launch_hp<kDtype, 64, true>(a, st);
+        default: break;
+    }
+    if (a.H < 8) return launch_hp<kDtype, 8, false>(a, st);
+    if (a.H < 16) return launch_hp<kDtype, 16, false>(a, st);
+    if (a.H < 32) return launch_hp<kDtype, 32, false>(a, st);
+    return launch_hp<kDtype, 64, false>(a, st);
 }
 
 }  // namespace
