@@ -148,8 +148,9 @@ __global__ void __launch_bounds__(kThreads) k_store_kernel(KStoreArgs a) {
     const uint4 raw = in ? __ldg(reinterpret_cast<const uint4*>(a.k + row * a.k_row_stride + 8 * l16))
                          : make_uint4(0, 0, 0, 0);
     bool ok = in && slot >= 0;
-    const int64_t page = ok ? slot / a.page_size : 0;
-    const int s = ok ? (int)(slot - page * a.page_size) : 0;
+    const int lp = a.page_size == 128 ? 7 : 6;  // page sizes are 64 or 128
+    const int64_t page = ok ? slot >> lp : 0;
+    const int s = ok ? (int)(slot & (a.page_size - 1)) : 0;
     if (ok && page >= a.num_pages) {
         if (l16 == 0) report(a.dev_status, IDX_STATUS_BAD_SLOT);
         ok = false;

@@ -185,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H, P = a.page_size;
+    const int lp = P == 128 ? 7 : 6;  // log2 of the page size (64 or 128)
     const int Hq = (H + 7) & ~7;
 
     SeqEnt* seq_tab = reinterpret_cast<SeqEnt*>(smem + C::oSeq);
@@ -340,8 +341,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
                     const int64_t key0 = my.j * 128;
                     halves = P == 128 ? 1 : (key0 + 64 < my.si.vis ? 2 : 1);
                     const int32_t* pt = a.page_table + (int64_t)my.b * a.pt_stride;
-                    pg[0] = __ldg(pt + key0 / P);
-                    if (halves == 2) pg[1] = __ldg(pt + (key0 + 64) / P);
+                    pg[0] = __ldg(pt + (key0 >> lp));
+                    if (halves == 2) pg[1] = __ldg(pt + ((key0 + 64) >> lp));
                 }
                 if (!dep_done) {  // Q and the cache come from the previous kernels
                     pdl_wait();
@@ -528,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
             for (int t = 0; t < G; ++t) {
                 const int64_t i = gi * G + t;
                 const int64_t key = wk.j * 128 + koff;
-                pg[t] = (i < n_units && key < wk.si.vis) ? __ldg(a.page_table + (int64_t)wk.b * a.pt_stride + key / P) : -1;
+                pg[t] = (i < n_units && key < wk.si.vis) ? __ldg(a.page_table + (int64_t)wk.b * a.pt_stride + (key >> lp)) : -1;
                 if (i + 1 < n_units) wk.next(S);
             }
             // so are the head weights when the group's first tile starts a sequence
@@ -558,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
                 float kscale = 1.0f;
                 if (kDtype == IDX_FP8 && key_ok)
                     kscale = __ldg(reinterpret_cast<const float*>(a.pool + (int64_t)pg[t] * a.page_stride + 128 * P +
-                                                                  4 * (key % P)));
+                                                                  4 * ((key & (P - 1)))));
                 float v[NP];
                 load_acc<NP>(lane_addr + (ag * G + t) * NP, v);
                 // four independent accumulation chains over the heads

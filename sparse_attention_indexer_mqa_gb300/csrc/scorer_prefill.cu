@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H, P = a.page_size;
+    const int lp = P == 128 ? 7 : 6;  // log2 of the page size (64 or 128)
     const int Hq = (H + 7) & ~7;
 
     if (tid == 0) {
@@ -258,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                     const int64_t j = j0 + lane, k = kt + lane;
                     const int64_t key0 = j * 128;
                     const int halves = P == 128 ? 1 : (key0 + 64 < u.len ? 2 : 1);
-                    int32_t pg[2] = {__ldg(pt + key0 / P), halves == 2 ? __ldg(pt + (key0 + 64) / P) : -1};
+                    int32_t pg[2] = {__ldg(pt + (key0 >> lp)), halves == 2 ? __ldg(pt + ((key0 + 64) >> lp)) : -1};
                     const int s = (int)(k % C::kStages);
                     if (!tc::mbar_wait(&k_empty[s], (uint32_t)(((k / C::kStages) & 1) ^ 1))) {
                         *abort_flag = 1;
@@ -428,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                 // behind it) and used after it
                 const int64_t key = j * 128 + koff;
                 const bool in_seq = key < u.len;
-                const int32_t pg = in_seq ? __ldg(pt + key / P) : -1;
+                const int32_t pg = in_seq ? __ldg(pt + (key >> lp)) : -1;
                 const bool got = __all_sync(kFull, tc::mbar_wait(&acc_full[gb], aph));
                 if (!got) {
                     *abort_flag = 1;
@@ -440,63 +441,66 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                 const bool key_ok = in_seq && pg >= 0 && pg < a.num_pages;
                 float kscale = 1.0f;
                 if (kDtype == IDX_FP8 && key_ok)
-                    kscale = __ldg(reinterpret_cast<const float*>(a.pool + (int64_t)pg * a.page_stride + 128 * P + 4 * (key % P)));
+                    kscale = __ldg(reinterpret_cast<const float*>(a.pool + (int64_t)pg * a.page_stride + 128 * P + 4 * ((key & (P - 1)))));
                 // this key is visible to queries q >= qmin (all of them off the diagonal)
                 const int64_t d = key - vis0 + 1;  // causal: query q sees the key iff q >= d
                 const int qmin = !key_ok ? QB : (qstep == 0 ? (key < vis0 ? 0 : QB) : (d <= 0 ? 0 : (d >= QB ? QB : (int)d)));
                 if constexpr (kFull) {
-                    // software-pipelined drain in 16-column chunks (chunk c+1 is loaded while
-                    // chunk c is summed): chunk c holds head columns h0 .. h0+15 of query
-                    // qlo + 16c / HP (two queries when HP = 8); the accumulator is released as
-                    // soon as this half's last chunk is in registers
-                    constexpr int QPC = HP >= 16 ? 1 : 16 / HP;    // queries per chunk
-                    constexpr int NCH16 = (QH0 * HP + 15) / 16;    // chunks per half, at most
+                    // drain in 64-column chunks, one tcgen05.wait::ld each (a wait covers every
+                    // load in flight, so fewer, larger loads pay the tensor-memory latency less
+                    // often); the accumulator is released as soon as this half's last chunk
+                    // is in registers. Sub-chunk s of chunk c holds head columns h0 .. h0+15
+                    // of query qlo + (64c + 16s) / HP (two queries when HP = 8).
+                    constexpr int CH = 64;
+                    constexpr int QPS = HP >= 16 ? 1 : 16 / HP;    // queries per 16 columns
+                    constexpr int kColsQ = HP >= 16 ? 16 : HP;     // a query's columns per 16
+                    constexpr int NCHK = (QH0 * HP + CH - 1) / CH; // chunks per half, at most
                     const int qend = min(qhi, nqb);
-                    const int nch16 = qend > qlo ? ((qend - qlo) * HP + 15) / 16 : 0;
-                    float v[2][16];
-                    if (nch16 > 0) {
-                        tc::tmem_ld16(lane_addr, *reinterpret_cast<uint32_t(*)[16]>(v[0]));
-                        tc::tmem_ld_wait();
-                    }
-                    if (nch16 <= 1) {
+                    const int nchk = qend > qlo ? ((qend - qlo) * HP + CH - 1) / CH : 0;
+                    if (nchk == 0) {
                         tc::tc_fence_before();
                         tc::mbar_arrive(&acc_empty[gb]);
                     }
-                    float2 acc[QPC][2] = {};
+                    float2 acc[QPS][2] = {};
 #pragma unroll
-                    for (int c = 0; c < NCH16; ++c) {
-                        if (c >= nch16) break;
-                        const float* va = v[c & 1];
-                        if (c + 1 < nch16)
-                            tc::tmem_ld16(lane_addr + (c + 1) * 16, *reinterpret_cast<uint32_t(*)[16]>(v[(c + 1) & 1]));
-#pragma unroll
-                        for (int qq = 0; qq < QPC; ++qq) {
-                            constexpr int kColsQ = HP >= 16 ? 16 : HP;  // this query's columns here
-                            const int q = qlo + (16 * c) / HP + qq;
-                            const int h0 = (16 * c) % HP;
-                            if (h0 == 0) acc[qq][0] = acc[qq][1] = make_float2(0.0f, 0.0f);
-                            if (q >= qmin && q < qend) {
-                                const float4* w4p = reinterpret_cast<const float4*>(wsm + q * H + h0);
-#pragma unroll
-                                for (int i = 0; i < kColsQ / 4; ++i) {
-                                    const float4 w4 = w4p[i];
-                                    const float* x = va + qq * kColsQ + 4 * i;
-                                    acc[qq][0] = __ffma2_rn(make_float2(w4.x, w4.y),
-                                                            make_float2(fmaxf(x[0], 0.0f), fmaxf(x[1], 0.0f)), acc[qq][0]);
-                                    acc[qq][1] = __ffma2_rn(make_float2(w4.z, w4.w),
-                                                            make_float2(fmaxf(x[2], 0.0f), fmaxf(x[3], 0.0f)), acc[qq][1]);
-                                }
-                                if (h0 + kColsQ == HP) {
-                                    const float2 s2 = __fadd2_rn(acc[qq][0], acc[qq][1]);
-                                    lrow[q * ld + key] = (s2.x + s2.y) * kscale;
-                                }
-                            }
+                    for (int c = 0; c < NCHK; ++c) {
+                        if (c >= nchk) break;
+                        uint32_t r[CH];
+                        tc::tmem_ld32(lane_addr + c * CH, *reinterpret_cast<uint32_t(*)[32]>(r));
+                        tc::tmem_ld32(lane_addr + c * CH + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+                        tc::tmem_ld_wait();
+                        if (c + 1 == nchk) {  // the last chunk is in registers
+                            tc::tc_fence_before();
+                            tc::mbar_arrive(&acc_empty[gb]);
                         }
-                        if (c + 1 < nch16) {
-                            tc::tmem_ld_wait();
-                            if (c + 2 == nch16) {  // the last chunk is in registers
-                                tc::tc_fence_before();
-                                tc::mbar_arrive(&acc_empty[gb]);
+#pragma unroll
+                        for (int sc = 0; sc < CH / 16; ++sc) {
+#pragma unroll
+                            for (int qq = 0; qq < QPS; ++qq) {
+                                const int col = c * CH + 16 * sc;     // compile-time
+                                const int q = qlo + col / HP + qq;
+                                const int h0 = col % HP;
+                                if (h0 == 0) acc[qq][0] = acc[qq][1] = make_float2(0.0f, 0.0f);
+                                if (q >= qmin && q < qend) {
+                                    const float4* w4p = reinterpret_cast<const float4*>(wsm + q * H + h0);
+#pragma unroll
+                                    for (int i = 0; i < kColsQ / 4; ++i) {
+                                        const float4 w4 = w4p[i];
+                                        const uint32_t* x = r + 16 * sc + qq * kColsQ + 4 * i;
+                                        acc[qq][0] = __ffma2_rn(make_float2(w4.x, w4.y),
+                                                                make_float2(fmaxf(__uint_as_float(x[0]), 0.0f),
+                                                                            fmaxf(__uint_as_float(x[1]), 0.0f)),
+                                                                acc[qq][0]);
+                                        acc[qq][1] = __ffma2_rn(make_float2(w4.z, w4.w),
+                                                                make_float2(fmaxf(__uint_as_float(x[2]), 0.0f),
+                                                                            fmaxf(__uint_as_float(x[3]), 0.0f)),
+                                                                acc[qq][1]);
+                                    }
+                                    if (h0 + kColsQ == HP) {
+                                        const float2 s2 = __fadd2_rn(acc[qq][0], acc[qq][1]);
+                                        lrow[q * ld + key] = (s2.x + s2.y) * kscale;
+                                    }
+                                }
                             }
                         }
                     }
