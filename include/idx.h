@@ -158,7 +158,8 @@ int idx_q_quant(const uint16_t* q, int64_t T, int32_t H, const int32_t* position
  * max_q_len: an upper bound of the queries per sequence (1 selects the decode kernel);
  * max_seq_len_k: an upper bound of seq_lens_k (sizes the grid).
  * q_codes / q_scales / w as produced by idx_q_quant (w = its w_out).
- * H: 1..64 for MXFP4 and FP8. ld_logits >= max visible; logits fp32, 16-byte aligned.
+ * H: 1..64 for MXFP4 and FP8. ld_logits >= max visible, a multiple of 4 and at most
+ * INT32_MAX / 32 (IDX_EUNSUPPORTED otherwise); logits fp32, 16-byte aligned.
  * Products are exact in the tensor core; sums are fp32. Accuracy against the exact
  * (fp64) scores: |error| <= 1e-4 * max_s |logit[t,s]| per row.
  */

@@ -120,6 +120,7 @@ int idx_mqa_logits_paged(const uint8_t* q_codes, const void* q_scales, const flo
         ld_logits % 4 != 0)
         return IDX_EINVAL;
     if (pt_stride < (max_seq_len_k + page_size - 1) / page_size) return IDX_EINVAL;
+    if (ld_logits > INT32_MAX / 32) return IDX_EUNSUPPORTED;  // 32-bit offsets inside a query block
     idx::ScoreArgs a{};
     a.q_codes = q_codes; a.q_scales = static_cast<const uint8_t*>(q_scales); a.w = w; a.T = T;
     a.H = H; a.dtype = dtype; a.pool = static_cast<const uint8_t*>(pool); a.num_pages = num_pages;

@@ -419,15 +419,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
             const int nqb = (int)u.nq_blk;
             // query q of the block sees keys < vis0 + q (causal; unclamped, so it also holds when
             // the block has more queries than keys) or keys < len; key < len is checked apart
-            const int64_t vis0 = a.causal ? u.len - u.nq + u.q0 + 1 : u.len;
+            // (32-bit key arithmetic: lengths are int32 and the host checks QB * ld < 2^31)
+            const int32_t vis0 = (int32_t)(a.causal ? u.len - u.nq + u.q0 + 1 : u.len);
             const int qstep = a.causal ? 1 : 0;
             float* lrow = a.logits + (u.t0 + u.q0) * a.ld;  // the block's first logits row
-            const int64_t ld = a.ld;
-            for (int64_t j = 0; j < u.tiles; ++j, ++kt) {
-                if ((kt & 1) != gb) continue;
+            const int32_t ld = (int32_t)a.ld;
+            const int tiles = (int)u.tiles;
+            // this warpgroup's tiles of the block: every other one, from the parity of the
+            // tiles scored before the block
+            for (int j = (int)((gb - kt) & 1); j < tiles; j += 2) {
                 // page lookups are issued before the accumulator wait (their latency hides
                 // behind it) and used after it
-                const int64_t key = j * 128 + koff;
+                const int32_t key = j * 128 + koff;
                 const bool in_seq = key < u.len;
                 const int32_t pg = in_seq ? __ldg(pt + (key >> lp)) : -1;
                 const bool got = __all_sync(kFull, tc::mbar_wait(&acc_full[gb], aph));
@@ -443,15 +446,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                 if (kDtype == IDX_FP8 && key_ok)
                     kscale = __ldg(reinterpret_cast<const float*>(a.pool + (int64_t)pg * a.page_stride + 128 * P + 4 * ((key & (P - 1)))));
                 // this key is visible to queries q >= qmin (all of them off the diagonal)
-                const int64_t d = key - vis0 + 1;  // causal: query q sees the key iff q >= d
+                const int32_t d = key - vis0 + 1;  // causal: query q sees the key iff q >= d
                 const int qmin = !key_ok ? QB : (qstep == 0 ? (key < vis0 ? 0 : QB) : (d <= 0 ? 0 : (d >= QB ? QB : (int)d)));
                 if constexpr (kFull) {
-                    // drain in 64-column chunks, one tcgen05.wait::ld each (a wait covers every
+                    // drain in 32-column chunks, one tcgen05.wait::ld each (a wait covers every
                     // load in flight, so fewer, larger loads pay the tensor-memory latency less
                     // often); the accumulator is released as soon as this half's last chunk
                     // is in registers. Sub-chunk s of chunk c holds head columns h0 .. h0+15
-                    // of query qlo + (64c + 16s) / HP (two queries when HP = 8).
-                    constexpr int CH = 64;
+                    // of query qlo + (32c + 16s) / HP (two queries when HP = 8).
+                    constexpr int CH = 32;
                     constexpr int QPS = HP >= 16 ? 1 : 16 / HP;    // queries per 16 columns
                     constexpr int kColsQ = HP >= 16 ? 16 : HP;     // a query's columns per 16
                     constexpr int NCHK = (QH0 * HP + CH - 1) / CH; // chunks per half, at most
@@ -466,8 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                     for (int c = 0; c < NCHK; ++c) {
                         if (c >= nchk) break;
                         uint32_t r[CH];
-                        tc::tmem_ld32(lane_addr + c * CH, *reinterpret_cast<uint32_t(*)[32]>(r));
-                        tc::tmem_ld32(lane_addr + c * CH + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+                        tc::tmem_ld32(lane_addr + c * CH, r);
                         tc::tmem_ld_wait();
                         if (c + 1 == nchk) {  // the last chunk is in registers
                             tc::tc_fence_before();
@@ -577,6 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                     }
                 }
             }
+            kt += tiles;
             // done with the slot's weights
             tc::mbar_arrive(&q_empty[slot]);
             ++n_units;
