@@ -14,15 +14,18 @@
 // (kind::mxf4, K = 64 each) or four kind::f8f6f4 MMAs (K = 32) give D[key][query, head] in
 // tensor memory; the ReLU-weighted head sum is the epilogue: each thread owns one key.
 //
-// Per (query, key) pair the epilogue issues 2H instructions (max, fused multiply-add) while
-// the tensor core does 2*H*128 flops, so the epilogue's issue rate is the bound. Two
+// Per (query, key) pair the epilogue issues about 1.5H instructions (H maxes for the ReLU,
+// H/2 packed fp32x2 fused multiply-adds) while the tensor core does 2*H*128 flops, so the
+// epilogue, not the tensor core, is the bound (the maxes run on the half-rate ALU pipe). Two
 // accumulator buffers (2 x 224 columns), each fed by its own MMA-issuing warp (even / odd
 // tiles) and drained by two epilogue warpgroups (half of the queries each), keep the MMAs of
 // the next tiles and the head sums of the current ones in flight together; four epilogue
-// warps per scheduler hide the latency of their chains. The epilogue is written to issue little
-// beyond its 2H instructions per pair: compile-time trip counts (double-buffered registers
-// rename instead of copying), the causal test only on diagonal tiles, per-block row pointers,
-// and the block's head weights in shared memory read 16 bytes at a time.
+// warps per scheduler hide the tensor-memory load latency, and each warp loads 64 columns per
+// tcgen05.wait::ld (a wait covers every load in flight, so a warp cannot overlap its own loads
+// with its sums; fewer, larger loads pay the latency less often). The epilogue is written to
+// issue little beyond its sums: compile-time trip counts and head offsets, 32-bit key
+// arithmetic, the causal test only on diagonal tiles, per-block row pointers, and the block's
+// head weights in shared memory read 16 bytes at a time.
 //
 // Work: query blocks, heaviest first (causal), in snake order over persistent CTAs (CTA c
 // takes ranks c, 2G-1-c, 2G+c, ...). Roles: warp 0 = producer (Q image of the block by bulk
@@ -449,12 +452,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                 const int32_t d = key - vis0 + 1;  // causal: query q sees the key iff q >= d
                 const int qmin = !key_ok ? QB : (qstep == 0 ? (key < vis0 ? 0 : QB) : (d <= 0 ? 0 : (d >= QB ? QB : (int)d)));
                 if constexpr (kFull) {
-                    // drain in 32-column chunks, one tcgen05.wait::ld each (a wait covers every
+                    // drain in 64-column chunks, one tcgen05.wait::ld each (a wait covers every
                     // load in flight, so fewer, larger loads pay the tensor-memory latency less
                     // often); the accumulator is released as soon as this half's last chunk
                     // is in registers. Sub-chunk s of chunk c holds head columns h0 .. h0+15
-                    // of query qlo + (32c + 16s) / HP (two queries when HP = 8).
-                    constexpr int CH = 32;
+                    // of query qlo + (64c + 16s) / HP (two queries when HP = 8).
+                    constexpr int CH = 64;
                     constexpr int QPS = HP >= 16 ? 1 : 16 / HP;    // queries per 16 columns
                     constexpr int kColsQ = HP >= 16 ? 16 : HP;     // a query's columns per 16
                     constexpr int NCHK = (QH0 * HP + CH - 1) / CH; // chunks per half, at most
@@ -469,7 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                     for (int c = 0; c < NCHK; ++c) {
                         if (c >= nchk) break;
                         uint32_t r[CH];
-                        tc::tmem_ld32(lane_addr + c * CH, r);
+                        tc::tmem_ld32(lane_addr + c * CH, *reinterpret_cast<uint32_t(*)[32]>(r));
+                        tc::tmem_ld32(lane_addr + c * CH + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
                         tc::tmem_ld_wait();
                         if (c + 1 == nchk) {  // the last chunk is in registers
                             tc::tc_fence_before();
