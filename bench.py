@@ -49,8 +49,7 @@ def algorithmic_bytes(wl):
     return {
         "scorer": keys * per_tok + wl.T * wl.H * (per_q + 4) + pt + 4 * wl.B + 4 * (wl.B + 1)
         + 4 * wl.pairs(),
-        "k_store": len(wl.step_rows) * (256 + per_tok + 8 + 4),
-        "q_quant": wl.T * wl.H * (256 + per_q + 4 + 4),
+        "qk_prep": len(wl.step_rows) * (256 + per_tok + 8 + 4) + wl.T * wl.H * (256 + per_q + 4 + 4),
         "topk": 4 * wl.pairs() + 4 * wl.T * wl.topk,
     }
 
@@ -168,6 +167,9 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------------------
 
+STEP_CALLS = ("qk_prep", "scorer", "topk")  # one library call (one kernel launch) each
+
+
 class Replica:
     """Device state of one workload: R rotating copies of the K cache and Q inputs."""
 
@@ -215,16 +217,14 @@ class Replica:
         r = i % len(self.pools)
         pool = self.pools[r]
         inp = inputs or {}
-        if name == "k_store":
-            Bn.idx_k_store(inp.get("k", self.k_new), inp.get("slot", self.slot_new),
-                           inp.get("pos", self.pos_new) if wl.k_rope else None,
-                           self.cos_sin if wl.k_rope else None, wl.k_rope, wl.k_norm, wl.dtype,
-                           pool, wl.pool_pages, wl.page_size, wl.page_stride)
-        elif name == "q_quant":
-            Bn.idx_q_quant(inp.get("q", self.q[r]), inp.get("qpos", self.qpos) if wl.q_rope else None,
-                           self.cos_sin if wl.q_rope else None, wl.q_rope, inp.get("w", self.w_in),
-                           wl.softmax_scale, wl.head_scale, wl.dtype, self.q_codes, self.q_scales,
-                           self.w)
+        if name == "qk_prep":  # K store of the step's keys + Q quant, one launch
+            Bn.idx_qk_prep(inp.get("k", self.k_new), inp.get("slot", self.slot_new),
+                           inp.get("pos", self.pos_new) if wl.k_rope else None, wl.k_rope, wl.k_norm,
+                           pool, wl.pool_pages, wl.page_size, wl.page_stride, inp.get("q", self.q[r]),
+                           inp.get("qpos", self.qpos) if wl.q_rope else None, wl.q_rope,
+                           inp.get("w", self.w_in), wl.softmax_scale, wl.head_scale, self.q_codes,
+                           self.q_scales, self.w, self.cos_sin if (wl.k_rope or wl.q_rope) else None,
+                           wl.dtype)
         elif name == "scorer":
             Bn.idx_mqa_logits_paged(self.q_codes, self.q_scales, self.w, wl.dtype, pool,
                                     wl.pool_pages, wl.page_size, wl.page_stride, self.page_table,
@@ -234,7 +234,7 @@ class Replica:
             Bn.idx_topk(self.logits, self.seq_lens_k, self.cu, wl.causal, wl.topk, self.topk)
 
     def step(self, i, inputs=None):
-        for n in ("k_store", "q_quant", "scorer", "topk"):
+        for n in STEP_CALLS:
             self.call(n, i, inputs)
 
 
@@ -322,7 +322,7 @@ def run_gpu(args, rank, world):
 
     # per-kernel device time: each kernel captured K times (same rotation) and timed alone
     per_kernel_ms = {}
-    for name in ("k_store", "q_quant", "scorer", "topk"):
+    for name in STEP_CALLS:
         g = capture(torch, lambda i, n=name: rep.call(n, args.warmup + i), args.steps)
         g.replay()
         torch.cuda.synchronize()
@@ -375,11 +375,11 @@ def run_gpu(args, rank, world):
                    "l2": f"inputs rotate over {copies} copies of cache+Q "
                          f"({copies * ws / 2**20:.0f} MiB)" if copies > 1 else
                          f"working set {ws / 2**20:.0f} MiB > 16x L2",
-                   "step": "k_store(step keys) + q_quant + mqa_logits_paged + topk",
+                   "step": "qk_prep (K store of the step's keys + Q quant, one launch) + mqa_logits_paged + topk",
                    "launch": "K steps captured in one CUDA graph, replayed once"},
         "kernel_us": {n: round(v * 1e3, 3) for n, v in per_kernel_ms.items()},
         "roofline": roof,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": len(STEP_CALLS) * args.steps,
         "clocks": clk,
         "e2e": e2e,
     }
@@ -435,7 +435,7 @@ def run_e2e(rep, args, torch, stream, world, dev):
     return {"value": round(job_rate(wl.pairs(), ms, world), 1), "unit": "K-tokens/s",
             "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h),
-            "how": "K steps of (one packed H2D from pinned host, 4 library calls, one D2H of "
+            "how": "K steps of (one packed H2D from pinned host, 3 library calls, one D2H of "
                    "the top-k) in one CUDA graph"}
 
 

@@ -145,6 +145,24 @@ int idx_q_quant(const uint16_t* q, int64_t T, int32_t H, const int32_t* position
                 void* q_scales, float* w_out, int32_t* dev_status, cudaStream_t stream);
 
 /*
+ * K store and Q quant in one launch ([P3] "Purpose": the indexer's QK pre-processing as a
+ * single fused kernel instead of separate launches). Computes exactly what idx_k_store(k,
+ * n_rows, k_row_stride, slot_mapping, k_positions, cos_sin, max_pos, k_rope, apply_norm,
+ * gamma, beta, eps, dtype, pool, ...) followed by idx_q_quant(q, T, H, q_positions, cos_sin,
+ * max_pos, q_rope, w_in, softmax_scale, head_scale, dtype, q_codes, q_scales, w_out) would,
+ * with the same arguments, layouts, rounding, checks and status bits; the cache and the Q
+ * image share one dtype and one RoPE table. Either half may be empty (n_rows = 0 or T = 0).
+ */
+int idx_qk_prep(const uint16_t* k, int64_t n_rows, int64_t k_row_stride, const int64_t* slot_mapping,
+                const int32_t* k_positions, int32_t k_rope, int32_t apply_norm, const float* gamma,
+                const float* beta, float eps, void* pool, int64_t num_pages, int32_t page_size,
+                int64_t page_stride, const uint16_t* q, int64_t T, int32_t H,
+                const int32_t* q_positions, int32_t q_rope, const float* w_in, float softmax_scale,
+                float head_scale, uint8_t* q_codes, void* q_scales, float* w_out,
+                const float* cos_sin, int32_t max_pos, int32_t dtype, int32_t* dev_status,
+                cudaStream_t stream);
+
+/*
  * Paged MQA logits ([P1] "Purpose", "Performance and accuracy"; [P2] "Purpose": the
  * scorer reads the cache in place, without gathering K first):
  *   logits[t * ld_logits + s] = sum_h w[t,h] * ReLU(q[t,h] . k[s])     (MXFP4)

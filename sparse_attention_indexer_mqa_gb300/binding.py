@@ -73,11 +73,13 @@ def _declare(L):
                               i32, i64, vp, vp]
     L.idx_q_quant.argtypes = [vp, i64, i32, vp, vp, i32, i32, vp, f32, f32, i32, vp, vp, vp, vp,
                               vp]
+    L.idx_qk_prep.argtypes = [vp, i64, i64, vp, vp, i32, i32, vp, vp, f32, vp, i64, i32, i64,
+                              vp, i64, i32, vp, i32, vp, f32, f32, vp, vp, vp, vp, i32, i32, vp, vp]
     L.idx_mqa_logits_paged.argtypes = [vp, vp, vp, i64, i32, i32, vp, i64, i32, i64, vp, i32, vp,
                                        vp, i32, i32, i32, i32, vp, i64, vp, vp]
     L.idx_topk.argtypes = [vp, i64, vp, vp, i32, i64, i32, i32, vp, vp]
     L.idx_debug_encode.argtypes = [i32, vp, i64, vp, vp]
-    for n in ("idx_cache_layout", "idx_k_store", "idx_q_quant", "idx_mqa_logits_paged",
+    for n in ("idx_cache_layout", "idx_k_store", "idx_q_quant", "idx_qk_prep", "idx_mqa_logits_paged",
               "idx_topk", "idx_debug_encode"):
         getattr(L, n).restype = C.c_int
 
@@ -136,6 +138,22 @@ def idx_q_quant(q, positions, cos_sin, rope, w_in, softmax_scale, head_scale, dt
     _check("idx_q_quant", load().idx_q_quant(
         _ptr(q), T, H, _ptr(positions), _ptr(cos_sin), max_pos, rope, _ptr(w_in), softmax_scale,
         head_scale, dtype, _ptr(q_codes), _ptr(q_scales), _ptr(w_out), _ptr(dev_status),
+        _stream(stream)))
+
+
+def idx_qk_prep(k, slot_mapping, k_positions, k_rope, apply_norm, pool, num_pages, page_size,
+                page_stride, q, q_positions, q_rope, w_in, softmax_scale, head_scale, q_codes,
+                q_scales, w_out, cos_sin, dtype, gamma=None, beta=None, eps=1e-6, dev_status=None,
+                stream=None):
+    n = k.shape[0] if k is not None else 0
+    stride = k.stride(0) if k is not None else 128
+    T, H = q.shape[0], q.shape[1]
+    max_pos = cos_sin.shape[0] if cos_sin is not None else 0
+    _check("idx_qk_prep", load().idx_qk_prep(
+        _ptr(k), n, stride, _ptr(slot_mapping), _ptr(k_positions), k_rope, int(apply_norm),
+        _ptr(gamma), _ptr(beta), eps, _ptr(pool), num_pages, page_size, page_stride, _ptr(q), T, H,
+        _ptr(q_positions), q_rope, _ptr(w_in), softmax_scale, head_scale, _ptr(q_codes),
+        _ptr(q_scales), _ptr(w_out), _ptr(cos_sin), max_pos, dtype, _ptr(dev_status),
         _stream(stream)))
 
 

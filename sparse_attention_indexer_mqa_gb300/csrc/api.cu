@@ -55,36 +55,44 @@ int idx_cache_layout(int32_t dtype, int32_t page_size, idx_layout* out) {
     return IDX_OK;
 }
 
-int idx_k_store(const uint16_t* k, int64_t n_rows, int64_t k_row_stride,
-                const int64_t* slot_mapping, const int32_t* positions, const float* cos_sin,
-                int32_t max_pos, int32_t rope, int32_t apply_norm, const float* gamma,
-                const float* beta, float eps, int32_t dtype, void* pool, int64_t num_pages,
-                int32_t page_size, int64_t page_stride, int32_t* dev_status,
-                cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Host-side checks and argument packing shared by idx_k_store and idx_qk_prep.
+int k_store_args(const uint16_t* k, int64_t n_rows, int64_t k_row_stride, const int64_t* slot_mapping,
+                 const int32_t* positions, const float* cos_sin, int32_t max_pos, int32_t rope,
+                 int32_t apply_norm, const float* gamma, const float* beta, float eps, int32_t dtype,
+                 void* pool, int64_t num_pages, int32_t page_size, int64_t page_stride,
+                 int32_t* dev_status, idx::KStoreArgs& a) {
     if (n_rows < 0 || !valid_rope(rope)) return IDX_EINVAL;
     int st = check_pool(dtype, pool, num_pages, page_size, page_stride);
     if (st != IDX_OK) return st;
+    a = idx::KStoreArgs{};
+    a.dtype = dtype;
     if (n_rows == 0) return IDX_OK;
     if (!k || !slot_mapping || !aligned(k, 16) || k_row_stride < 128 || k_row_stride % 8 != 0)
         return IDX_EINVAL;
     if (rope != IDX_ROPE_NONE && (!positions || !cos_sin || !aligned(cos_sin, 16) || max_pos <= 0))
         return IDX_EINVAL;
     if (apply_norm && !(eps >= 0.0f && std::isfinite(eps))) return IDX_EINVAL;
-    idx::KStoreArgs a{};
     a.k = k; a.n_rows = n_rows; a.k_row_stride = k_row_stride; a.slot_mapping = slot_mapping;
     a.positions = positions; a.cos_sin = cos_sin; a.max_pos = max_pos; a.rope = rope;
-    a.apply_norm = apply_norm != 0; a.dtype = dtype; a.gamma = gamma; a.beta = beta; a.eps = eps;
+    a.apply_norm = apply_norm != 0; a.gamma = gamma; a.beta = beta; a.eps = eps;
     a.pool = static_cast<uint8_t*>(pool); a.num_pages = num_pages; a.page_size = page_size;
     a.page_stride = page_stride; a.dev_status = dev_status;
-    return cuda_status(idx::launch_k_store(a, stream));
+    return IDX_OK;
 }
 
-int idx_q_quant(const uint16_t* q, int64_t T, int32_t H, const int32_t* positions,
-                const float* cos_sin, int32_t max_pos, int32_t rope, const float* w_in,
-                float softmax_scale, float head_scale, int32_t dtype, uint8_t* q_codes,
-                void* q_scales, float* w_out, int32_t* dev_status, cudaStream_t stream) {
+// Host-side checks and argument packing shared by idx_q_quant and idx_qk_prep.
+int q_quant_args(const uint16_t* q, int64_t T, int32_t H, const int32_t* positions, const float* cos_sin,
+                 int32_t max_pos, int32_t rope, const float* w_in, float softmax_scale,
+                 float head_scale, int32_t dtype, uint8_t* q_codes, void* q_scales, float* w_out,
+                 int32_t* dev_status, idx::QQuantArgs& a) {
     if (T < 0 || !valid_rope(rope) || !valid_dtype(dtype)) return IDX_EINVAL;
     if (H < 1 || H > 64) return IDX_EUNSUPPORTED;
+    a = idx::QQuantArgs{};
+    a.dtype = dtype; a.H = H;
     if (T == 0) return IDX_OK;
     if (!q || !w_in || !q_codes || !w_out || !aligned(q, 16) || !aligned(q_codes, 16))
         return IDX_EINVAL;
@@ -93,12 +101,61 @@ int idx_q_quant(const uint16_t* q, int64_t T, int32_t H, const int32_t* position
     if (rope != IDX_ROPE_NONE && (!positions || !cos_sin || !aligned(cos_sin, 16) || max_pos <= 0))
         return IDX_EINVAL;
     if (T > INT32_MAX) return IDX_EUNSUPPORTED;  // one grid column per token
-    idx::QQuantArgs a{};
-    a.q = q; a.T = T; a.H = H; a.positions = positions; a.cos_sin = cos_sin;
-    a.max_pos = max_pos; a.rope = rope; a.dtype = dtype; a.w_in = w_in;
+    a.q = q; a.T = T; a.positions = positions; a.cos_sin = cos_sin;
+    a.max_pos = max_pos; a.rope = rope; a.w_in = w_in;
     a.fold = (float)((double)softmax_scale * (double)head_scale);  // one rounding
     a.q_codes = q_codes; a.q_scales = q_scales; a.w_out = w_out; a.dev_status = dev_status;
+    return IDX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int idx_k_store(const uint16_t* k, int64_t n_rows, int64_t k_row_stride,
+                const int64_t* slot_mapping, const int32_t* positions, const float* cos_sin,
+                int32_t max_pos, int32_t rope, int32_t apply_norm, const float* gamma,
+                const float* beta, float eps, int32_t dtype, void* pool, int64_t num_pages,
+                int32_t page_size, int64_t page_stride, int32_t* dev_status,
+                cudaStream_t stream) {
+    idx::KStoreArgs a;
+    const int st = k_store_args(k, n_rows, k_row_stride, slot_mapping, positions, cos_sin, max_pos, rope,
+                                apply_norm, gamma, beta, eps, dtype, pool, num_pages, page_size,
+                                page_stride, dev_status, a);
+    if (st != IDX_OK || n_rows == 0) return st;
+    return cuda_status(idx::launch_k_store(a, stream));
+}
+
+int idx_q_quant(const uint16_t* q, int64_t T, int32_t H, const int32_t* positions,
+                const float* cos_sin, int32_t max_pos, int32_t rope, const float* w_in,
+                float softmax_scale, float head_scale, int32_t dtype, uint8_t* q_codes,
+                void* q_scales, float* w_out, int32_t* dev_status, cudaStream_t stream) {
+    idx::QQuantArgs a;
+    const int st = q_quant_args(q, T, H, positions, cos_sin, max_pos, rope, w_in, softmax_scale,
+                                head_scale, dtype, q_codes, q_scales, w_out, dev_status, a);
+    if (st != IDX_OK || T == 0) return st;
     return cuda_status(idx::launch_q_quant(a, stream));
+}
+
+int idx_qk_prep(const uint16_t* k, int64_t n_rows, int64_t k_row_stride, const int64_t* slot_mapping,
+                const int32_t* k_positions, int32_t k_rope, int32_t apply_norm, const float* gamma,
+                const float* beta, float eps, void* pool, int64_t num_pages, int32_t page_size,
+                int64_t page_stride, const uint16_t* q, int64_t T, int32_t H,
+                const int32_t* q_positions, int32_t q_rope, const float* w_in, float softmax_scale,
+                float head_scale, uint8_t* q_codes, void* q_scales, float* w_out,
+                const float* cos_sin, int32_t max_pos, int32_t dtype, int32_t* dev_status,
+                cudaStream_t stream) {
+    idx::KStoreArgs ka;
+    idx::QQuantArgs qa;
+    int st = k_store_args(k, n_rows, k_row_stride, slot_mapping, k_positions, cos_sin, max_pos, k_rope,
+                          apply_norm, gamma, beta, eps, dtype, pool, num_pages, page_size, page_stride,
+                          dev_status, ka);
+    if (st != IDX_OK) return st;
+    st = q_quant_args(q, T, H, q_positions, cos_sin, max_pos, q_rope, w_in, softmax_scale, head_scale,
+                      dtype, q_codes, q_scales, w_out, dev_status, qa);
+    if (st != IDX_OK) return st;
+    if (n_rows == 0 && T == 0) return IDX_OK;
+    return cuda_status(idx::launch_qk_prep(ka, qa, stream));
 }
 
 int idx_mqa_logits_paged(const uint8_t* q_codes, const void* q_scales, const float* w,

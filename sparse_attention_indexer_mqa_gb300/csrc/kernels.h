@@ -72,6 +72,7 @@ struct TopkArgs {
 
 cudaError_t launch_k_store(const KStoreArgs& a, cudaStream_t st);
 cudaError_t launch_q_quant(const QQuantArgs& a, cudaStream_t st);
+cudaError_t launch_qk_prep(const KStoreArgs& ka, const QQuantArgs& qa, cudaStream_t st);
 cudaError_t launch_debug_encode(int kind, const float* in, int64_t n, uint8_t* out, cudaStream_t st);
 cudaError_t launch_scorer(const ScoreArgs& a, cudaStream_t st);
 cudaError_t launch_scorer_decode(const ScoreArgs& a, cudaStream_t st);

@@ -1,12 +1,13 @@
 // quant.cu -- the fused K store (LayerNorm -> RoPE -> MXFP4/FP8 -> paged store) and the
-// Q quant (RoPE -> MXFP4/FP8, weight fold) kernels.
+// Q quant (RoPE -> MXFP4/FP8, weight fold) kernels, alone or together in one launch.
 //
 // vllm PR 53094 "Purpose" lists the pre-processing of one indexer layer as five launches
 // (LayerNorm on k; RoPE on q and k; per-token-group FP8 quantisation of q; fold of the
 // q scale into the weights; FP8 quantisation of k plus the paged cache write) and replaces
 // them with one fused kernel; vllm PR 60834 "Changes / K write" and "Q quant" do the same
 // for MXFP4 (norm -> RoPE -> MXFP4 -> preshuffled pages; RoPE -> MXFP4 with the softmax
-// and head scales folded into fp32 weights). Here each of the two steps is one launch.
+// and head scales folded into fp32 weights). Each of the two steps is one kernel, and
+// qk_prep_kernel runs both in a single launch (one block range each).
 //
 // Mapping: 16 threads per 128-element row, 8 consecutive elements (one 16-byte load of
 // bf16) per thread; a 256-thread CTA handles 16 rows. Reductions use a fixed tree (group
@@ -137,10 +138,11 @@ __device__ __forceinline__ void unpack8(const uint4 v, float* x) {
     x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
 }
 
+// K store of the 16 rows of block `blk` (one row per 16 lanes).
 template <int kDtype>
-__global__ void __launch_bounds__(kThreads) k_store_kernel(KStoreArgs a) {
+__device__ __forceinline__ void k_store_rows(const KStoreArgs& a, int64_t blk) {
     const int l16 = threadIdx.x & 15;
-    const int64_t row = (int64_t)blockIdx.x * kRowsPerCta + (threadIdx.x >> 4);
+    const int64_t row = blk * kRowsPerCta + (threadIdx.x >> 4);
     const bool in = row < a.n_rows;
     // the slot, the position and the K row are independent loads: issue them together
     const int64_t slot = in ? __ldg(a.slot_mapping + row) : -1;
@@ -205,12 +207,12 @@ __global__ void __launch_bounds__(kThreads) k_store_kernel(KStoreArgs a) {
 // Q rows: CTA (t, y) takes token t's heads 16y .. 16y+15 of the Hq = H rounded up to 8
 // heads; heads past H write the zero/neutral padding of the tensor-core image (see idx.h
 // for the layout). Hq is a multiple of 8, so the two rows of a warp are live together.
+// Q quant of token t's heads 16y .. 16y+15.
 template <int kDtype>
-__global__ void __launch_bounds__(kThreads) q_quant_kernel(QQuantArgs a) {
+__device__ __forceinline__ void q_quant_rows(const QQuantArgs& a, int64_t t, int y) {
     const int l16 = threadIdx.x & 15;
     const int Hq = (a.H + 7) & ~7;
-    const int64_t t = blockIdx.x;
-    const int h = blockIdx.y * kRowsPerCta + (threadIdx.x >> 4);
+    const int h = y * kRowsPerCta + (threadIdx.x >> 4);
     if (h >= Hq) return;
     const bool real = h < a.H;
     const int64_t row = t * a.H + h;  // index of (t, h) in q, w_in, w_out
@@ -270,6 +272,31 @@ __global__ void __launch_bounds__(kThreads) q_quant_kernel(QQuantArgs a) {
     }
 }
 
+template <int kDtype>
+__global__ void __launch_bounds__(kThreads) k_store_kernel(KStoreArgs a) {
+    k_store_rows<kDtype>(a, blockIdx.x);
+}
+
+template <int kDtype>
+__global__ void __launch_bounds__(kThreads) q_quant_kernel(QQuantArgs a) {
+    q_quant_rows<kDtype>(a, blockIdx.x, blockIdx.y);
+}
+
+// K store and Q quant in one launch: blocks [0, nk) store K rows, the rest quantise Q (block
+// nk + t*ny + y takes token t's head block y). The two halves touch disjoint buffers.
+template <int kDtype>
+__global__ void __launch_bounds__(kThreads) qk_prep_kernel(KStoreArgs ka, QQuantArgs qa, int64_t nk, int ny) {
+    const int64_t b = blockIdx.x;
+    if (b < nk) {
+        k_store_rows<kDtype>(ka, b);
+    } else {
+        // ny = 1..4 and the grid is below 2^31: a 32-bit divide by a constant
+        const uint32_t i = (uint32_t)(b - nk);
+        const uint32_t t = ny == 1 ? i : (ny == 2 ? i >> 1 : (ny == 4 ? i >> 2 : i / 3u));
+        q_quant_rows<kDtype>(qa, t, (int)(i - t * (uint32_t)ny));
+    }
+}
+
 __global__ void debug_encode_kernel(int kind, const float* in, int64_t n, uint8_t* out) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -294,6 +321,18 @@ cudaError_t launch_q_quant(const QQuantArgs& a, cudaStream_t st) {
     const dim3 grid((unsigned)a.T, (unsigned)((Hq + kRowsPerCta - 1) / kRowsPerCta));
     return a.dtype == IDX_MXFP4 ? launch_pdl(q_quant_kernel<IDX_MXFP4>, grid, dim3(kThreads), 0, st, a)
                                 : launch_pdl(q_quant_kernel<IDX_FP8>, grid, dim3(kThreads), 0, st, a);
+}
+
+cudaError_t launch_qk_prep(const KStoreArgs& ka, const QQuantArgs& qa, cudaStream_t st) {
+    const int64_t nk = (ka.n_rows + kRowsPerCta - 1) / kRowsPerCta;
+    const int Hq = (qa.H + 7) & ~7;
+    const int ny = (Hq + kRowsPerCta - 1) / kRowsPerCta;
+    const int64_t grid = nk + qa.T * ny;
+    if (grid == 0) return cudaSuccess;
+    if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
+    return ka.dtype == IDX_MXFP4
+               ? launch_pdl(qk_prep_kernel<IDX_MXFP4>, dim3((unsigned)grid), dim3(kThreads), 0, st, ka, qa, nk, ny)
+               : launch_pdl(qk_prep_kernel<IDX_FP8>, dim3((unsigned)grid), dim3(kThreads), 0, st, ka, qa, nk, ny);
 }
 
 cudaError_t launch_debug_encode(int kind, const float* in, int64_t n, uint8_t* out, cudaStream_t st) {

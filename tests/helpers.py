@@ -93,6 +93,17 @@ class Dev:
                        wl.k_rope, wl.k_norm, wl.dtype, self.pool, wl.pool_pages, wl.page_size,
                        wl.page_stride, dev_status=self.status)
 
+    def prep(self):
+        """K store and Q quant in one launch (idx_qk_prep)."""
+        from sparse_attention_indexer_mqa_gb300 import binding as Bn
+        wl = self.wl
+        Bn.idx_qk_prep(self.k, self.slot, self.kpos if wl.k_rope else None, wl.k_rope, wl.k_norm,
+                       self.pool, wl.pool_pages, wl.page_size, wl.page_stride, self.q,
+                       self.qpos if wl.q_rope else None, wl.q_rope, self.w_in, wl.softmax_scale,
+                       wl.head_scale, self.q_codes, self.q_scales, self.w,
+                       self.cos_sin if (wl.k_rope or wl.q_rope) else None, wl.dtype,
+                       dev_status=self.status)
+
     def quant(self):
         from sparse_attention_indexer_mqa_gb300 import binding as Bn
         wl = self.wl

@@ -15,8 +15,8 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = Bn.exported_names()
-    assert {"idx_cache_layout", "idx_k_store", "idx_q_quant", "idx_mqa_logits_paged",
-            "idx_topk"} <= set(names)
+    assert {"idx_cache_layout", "idx_k_store", "idx_q_quant", "idx_qk_prep",
+            "idx_mqa_logits_paged", "idx_topk"} <= set(names)
     for n in names:
         assert hasattr(lib, n), n
 
@@ -69,5 +69,12 @@ def test_host_validation(lib):
                                     100, 16, 64, None, None) == -1
     assert lib.idx_mqa_logits_paged(16, 16, 16, 1, 4, 0, 16, 1, 64, 4352, 16, 1, 16, 16, 1, 0, 1,
                                     100, 16, 128, None, None) == -1
+    # fused K store + Q quant: bad dtype, H out of range, unsupported page size
+    qk = lambda dtype, H, P: lib.idx_qk_prep(16, 1, 128, 16, None, 0, 0, None, None, 1e-6, 16, 1, P,
+                                             4352, 16, 1, H, None, 0, 16, 1.0, 1.0, 16, 16, 16,
+                                             None, 0, dtype, None, None)
+    assert qk(2, 4, 64) == -1
+    assert qk(0, 65, 64) == -2
+    assert qk(0, 4, 96) == -2
     assert lib.idx_debug_encode(3, 16, 1, 16, None) == -1
     assert Bn.load().idx_status_string(-3) == b"CUDA launch error"

@@ -60,10 +60,13 @@ def test_e4m3_encoder_matches_oracle(torch):
 
 # ------------------------------------------------------------------ K store / Q quant
 
-def _check_store_and_quant(wl, label):
+def _check_store_and_quant(wl, label, fused=False):
     d = Dev(wl)
-    d.store()
-    d.quant()
+    if fused:  # one launch (idx_qk_prep) must give the same bytes as the two entry points
+        d.prep()
+    else:
+        d.store()
+        d.quant()
     pool_gpu = d.host("pool_buf")
     pool_ref = oracle_store(wl)
     assert d.host("status")[0] == 0
@@ -87,11 +90,12 @@ def test_store_quant_tiny_decode(torch):
     assert not d.host("pool_buf")[:wl.page_stride].any()
 
 
+@pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("n", [1, 7, 32, 257, 1023])
 @pytest.mark.parametrize("P", [64, 128])
 @pytest.mark.parametrize("rope", [W.ROPE_NEOX, W.ROPE_INTERLEAVED])
 @pytest.mark.parametrize("dtype", [W.MXFP4, W.FP8])
-def test_store_quant_grid(torch, n, P, rope, dtype):
+def test_store_quant_grid(torch, n, P, rope, dtype, fused):
     """Token-count x page-size x RoPE-layout grid of the fused pre-processing op test
     (vllm PR 53094 "Test Plan / Op test"), here bit-exact against the oracle."""
     rng = np.random.default_rng(1000 + n)
@@ -111,7 +115,7 @@ def test_store_quant_grid(torch, n, P, rope, dtype):
         q_positions=rng.integers(0, 4000, n).astype(np.int32), q_rope=rope,
         w_in=rng.standard_normal((n, H)).astype(np.float32), softmax_scale=0.088388,
         head_scale=0.5, cos_sin=W.rope_table(4000), ld_logits=n)
-    _check_store_and_quant(wl, f"grid n={n} P={P} rope={rope} dtype={dtype}")
+    _check_store_and_quant(wl, f"grid n={n} P={P} rope={rope} dtype={dtype} fused={fused}", fused)
 
 
 def test_store_quant_only_mode_outliers(torch):
@@ -119,12 +123,37 @@ def test_store_quant_only_mode_outliers(torch):
     _check_store_and_quant(wl, "quant-only")
 
 
-def test_store_quant_compressed_full(torch):
-    _check_store_and_quant(W.make("decode_compressed"), "compressed decode, full size")
+@pytest.mark.parametrize("fused", [False, True])
+def test_store_quant_compressed_full(torch, fused):
+    _check_store_and_quant(W.make("decode_compressed"), "compressed decode, full size", fused)
 
 
-def test_store_quant_fp8_full(torch):
-    _check_store_and_quant(W.make("prefill_fp8"), "fp8 prefill, full size")
+@pytest.mark.parametrize("fused", [False, True])
+def test_store_quant_fp8_full(torch, fused):
+    _check_store_and_quant(W.make("prefill_fp8"), "fp8 prefill, full size", fused)
+
+
+def test_qk_prep_one_side_empty(torch):
+    """idx_qk_prep with no K rows only quantises Q; with no queries only stores K."""
+    import torch as T
+    from sparse_attention_indexer_mqa_gb300 import binding as Bn
+    wl = W.make("tiny_decode")
+    d = Dev(wl)
+    Bn.idx_qk_prep(None, None, None, wl.k_rope, wl.k_norm, d.pool, wl.pool_pages, wl.page_size,
+                   wl.page_stride, d.q, d.qpos, wl.q_rope, d.w_in, wl.softmax_scale, wl.head_scale,
+                   d.q_codes, d.q_scales, d.w, d.cos_sin, wl.dtype, dev_status=d.status)
+    assert not d.host("pool_buf").any()
+    qc, qs, w = oracle_q(wl)
+    gc, _ = q_image_to_plain(d.host("q_codes"), d.host("q_scales"), wl.H, wl.dtype)
+    np.testing.assert_array_equal(gc, qc)
+    d2 = Dev(wl)
+    empty_q = d2.q[:0]
+    Bn.idx_qk_prep(d2.k, d2.slot, d2.kpos, wl.k_rope, wl.k_norm, d2.pool, wl.pool_pages,
+                   wl.page_size, wl.page_stride, empty_q, d2.qpos, wl.q_rope, d2.w_in,
+                   wl.softmax_scale, wl.head_scale, d2.q_codes, d2.q_scales, d2.w, d2.cos_sin,
+                   wl.dtype, dev_status=d2.status)
+    np.testing.assert_array_equal(d2.host("pool_buf"), oracle_store(wl))
+    assert (d2.host("q_codes") == 0xEE).all()  # untouched
 
 
 def test_store_bad_rows_set_status(torch):
