@@ -47,11 +47,11 @@ constexpr int kSeqWin = 32;  // sequences described by the shared-memory table
 
 template <int kDtype, int NP>
 struct Cfg {
-    // CTAs per SM: for H <= 32, four independent pipelines share an SM (tensor memory <= 128
-    // columns each) so that one CTA's issue, MMA and epilogue latencies overlap the others';
-    // one CTA per SM for 64 heads. Tiles per group G: 1 with four CTAs per SM, else 2-4.
-    static constexpr int kCps = NP <= 32 ? 4 : 1;
-    static constexpr int G = kCps == 4 ? 1 : ((kDtype == IDX_MXFP4 && NP <= 32) ? 4 : 2);
+    // CTAs per SM: independent pipelines that share an SM so that one CTA's issue, MMA and
+    // epilogue latencies overlap the others' (tensor memory <= 128 columns each for H <= 32,
+    // four CTAs; <= 256 for 64 heads, two CTAs). One tile per stage group and mbarrier phase.
+    static constexpr int kCps = NP <= 32 ? 4 : 2;
+    static constexpr int G = 1;
     static constexpr int kTileCode = kDtype == IDX_MXFP4 ? 128 * 64 : 128 * 128;
     static constexpr int kTileSf = kDtype == IDX_MXFP4 ? 512 : 0;          // scale atom (MXFP4)
     static constexpr int kTile = kTileCode + kTileSf;
@@ -62,9 +62,8 @@ struct Cfg {
     // Q slots (a ring): a producer batch touches at most kQS sequences, so a slot it waits
     // for is always released by tiles of earlier batches
     static constexpr int kQS = NP <= 32 ? 4 : 2;
-    // shared memory of one CTA: an SM has 228 KB, of which 1 KB per resident CTA is reserved;
-    // one CTA per SM leaves room for the tile rings of the other kernels' CTAs
-    static constexpr int kBudget = kCps == 1 ? 184 * 1024 : (228 * 1024) / kCps - 1024;
+    // shared memory of one CTA: an SM has 228 KB, of which 1 KB per resident CTA is reserved
+    static constexpr int kBudget = (228 * 1024) / kCps - 1024;
     static constexpr int kFixed = kQS * (kQImg + kQSf) + 64 + kSeqWin * 16 + 8 * (2 * kQS + 1 + 2 * kAccG);
     static constexpr int kSG = (kBudget - kFixed) / (kGroup + 16);        // stage groups
     static constexpr uint32_t kSbo = kDtype == IDX_MXFP4 ? 512 : 1024;
