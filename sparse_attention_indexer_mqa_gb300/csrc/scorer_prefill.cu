@@ -354,8 +354,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                 for (int64_t j = 0; j < u.tiles; ++j, ++kt) {
                     if ((kt & 1) != buf) continue;
                     const int s = (int)(kt % C::kStages);
-                    if (!tc::mbar_wait(&k_full[s], (uint32_t)((kt / C::kStages) & 1)) ||
-                        !tc::mbar_wait(&acc_empty[buf], aph)) {
+                    if (!tc::mbar_wait(&k_full[s], (uint32_t)((kt / C::kStages) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    // the tile's A scale atom goes to tensor memory before the accumulator
+                    // wait: it overwrites only this issuer's scale slot, which the previous
+                    // (earlier-issued, in-order) MMA of this issuer has read
+                    if (kDtype == IDX_MXFP4) tc::cp_32x128b_warpx4(sfa, dSA0 + (uint64_t)((s * C::kStage) >> 4));
+                    if (!tc::mbar_wait(&acc_empty[buf], aph)) {
                         ok = false;
                         break;
                     }
@@ -363,7 +371,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                     tc::tc_fence_after();
                     const uint64_t da = dA0 + (uint64_t)((s * C::kStage) >> 4);
                     if (kDtype == IDX_MXFP4) {
-                        tc::cp_32x128b_warpx4(sfa, dSA0 + (uint64_t)((s * C::kStage) >> 4));
                         tc::mma_mxf4(d, da, db, id0, sfa, sfb, 0);
                         tc::mma_mxf4(d, da + 16, db + 16, id1, sfa, sfb, 1);
                     } else {
