@@ -92,9 +92,9 @@ def test_topk_lengths_around_k(torch):
 
 
 def test_topk_wide_uncached_rows(torch):
-    """Rows longer than the shared-memory staging capacity (48K keys) are re-read."""
+    """Rows longer than the shared-memory staging capacity (48K keys) are re-read; a row just below it stays staged."""
     rng = np.random.default_rng(2)
-    rows = [rng.standard_normal(n).astype(np.float32) * 3 for n in (49153, 65536, 70001)]
+    rows = [rng.standard_normal(n).astype(np.float32) * 3 for n in (48 * 1024 - 3, 49153, 65536, 70001)]
     _decode(torch, rows, 2048)
 
 
