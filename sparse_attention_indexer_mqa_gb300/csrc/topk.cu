@@ -18,7 +18,9 @@
 //   2. One pass over the keys counts, per warp, the keys above bin b0 and gathers the keys
 //      inside b0 (the candidates: index and key) into a shared list.
 //   3. Two more histogram passes (11 and 10 bits) over the listed candidates fix the k-th
-//      key exactly (over every key of bin b0 when the list overflowed).
+//      key exactly (over every key of bin b0 when the list overflowed); when every key of
+//      the 22-bit bin found by the first of them is taken (the common case: one key), the
+//      k-th key is their minimum and the second pass is skipped.
 //   4. Per-warp counts of candidates above / equal to the k-th key complete the warps'
 //      counts; one scan over the warps places each warp's output, and a last pass writes
 //      the indices with ballots.
@@ -100,7 +102,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
     __shared__ int32_t cand[kCand];
     __shared__ uint32_t ckey[kCand];  // the candidates' keys, in list order
     __shared__ uint32_t warp_sums[kWarps], warp_gt[kWarps], warp_eq[kWarps];
-    __shared__ uint32_t sel[2], n_cand;
+    __shared__ uint32_t sel[2], n_cand, bin_min, bin_eq;
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t t = blockIdx.x;
@@ -122,7 +124,11 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
     auto key_at = [&](int i) -> uint32_t { return cached ? skeys[i] : order_key(row[i]); };
 
     for (int i = threadIdx.x; i < 2048; i += kThreads) hist[i] = 0;
-    if (threadIdx.x == 0) n_cand = 0;
+    if (threadIdx.x == 0) {
+        n_cand = 0;
+        bin_min = 0xffffffffu;
+        bin_eq = 0;
+    }
     __syncthreads();
 
     // 1. read, stage, histogram the top 11 bits (thread-strided, float4 where aligned)
@@ -257,8 +263,25 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
         __syncthreads();
         uint32_t bin, ab;
         select_bin<kThreads>(hist, nb, remaining, warp_sums, sel, bin, ab);
+        const uint32_t cnt = hist[bin];  // read before the next pass clears it
         prefix |= bin << shift;
         remaining -= ab;
+        if (pass == 1 && cnt == remaining) {
+            // every key with this 22-bit prefix is taken (usually there is one): the k-th key
+            // is their minimum, and all copies of it are taken
+            for_each_cand([&](int, uint32_t key) {
+                if ((key & 0xfffffc00u) == prefix) atomicMin(&bin_min, key);
+            });
+            __syncthreads();
+            const uint32_t mn = bin_min;
+            for_each_cand([&](int, uint32_t key) {
+                if (key == mn) atomicAdd(&bin_eq, 1u);
+            });
+            __syncthreads();
+            prefix = mn;
+            remaining = bin_eq;
+            break;
+        }
     }
 
     // 4. prefix is the k-th largest key; `remaining` keys equal to it are taken, lowest
