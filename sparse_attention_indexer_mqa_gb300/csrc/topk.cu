@@ -251,6 +251,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
     // 3. fix the low 21 bits of the k-th key over the candidates (listed, or every key of
     //    bin b0 when the list overflowed)
     uint32_t prefix = b0 << 21;
+    bool counted = false;  // per-warp counts of step 4 already complete
     for (int pass = 1; pass < 3; ++pass) {
         const int shift = pass == 1 ? 10 : 0;
         const int nb = pass == 1 ? 2048 : 1024;
@@ -274,12 +275,19 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
             });
             __syncthreads();
             const uint32_t mn = bin_min;
-            for_each_cand([&](int, uint32_t key) {
-                if (key == mn) atomicAdd(&bin_eq, 1u);
+            // this pass also completes the per-warp counts of step 4
+            for_each_cand([&](int i, uint32_t key) {
+                if (key > mn) {
+                    atomicAdd(&warp_gt[i / chunk], 1u);
+                } else if (key == mn) {
+                    atomicAdd(&bin_eq, 1u);
+                    atomicAdd(&warp_eq[i / chunk], 1u);
+                }
             });
             __syncthreads();
             prefix = mn;
             remaining = bin_eq;
+            counted = true;
             break;
         }
     }
@@ -287,11 +295,13 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
     // 4. prefix is the k-th largest key; `remaining` keys equal to it are taken, lowest
     //    indices first. Candidates above / equal to it complete the per-warp counts.
     const uint32_t kth = prefix;
-    for_each_cand([&](int i, uint32_t key) {
-        if (key > kth) atomicAdd(&warp_gt[i / chunk], 1u);
-        else if (key == kth) atomicAdd(&warp_eq[i / chunk], 1u);
-    });
-    __syncthreads();
+    if (!counted) {
+        for_each_cand([&](int i, uint32_t key) {
+            if (key > kth) atomicAdd(&warp_gt[i / chunk], 1u);
+            else if (key == kth) atomicAdd(&warp_eq[i / chunk], 1u);
+        });
+        __syncthreads();
+    }
     uint32_t c_gt = warp_gt[warp], c_eq = warp_eq[warp];
     __syncthreads();
     if (warp == 0) {  // exclusive scans of the warps' counts (kWarps <= 32)
@@ -339,11 +349,15 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
             const uint32_t ex = inc - cnt;
             uint32_t pg = og + (ex & 0xffffu), pe = oe + (ex >> 16);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+            for (int e = 0; e < 4; ++e)
                 if ((fg >> e) & 1u) out[pg++] = i0 + e;
-                if ((fe >> e) & 1u) {
-                    if (pe < remaining) out[n_gt + pe] = i0 + e;
-                    ++pe;
+            if (fe) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if ((fe >> e) & 1u) {
+                        if (pe < remaining) out[n_gt + pe] = i0 + e;
+                        ++pe;
+                    }
                 }
             }
             og += tot & 0xffffu;
