@@ -17,19 +17,25 @@
 // kind::mxf4 block-scaled MMAs (two of K = 64); FP8 runs kind::f8f6f4 (four of K = 32) and
 // applies the per-key scale in the epilogue.
 //
-// Persistent, warp-specialised: one CTA per SM takes a contiguous, balanced slice of all
-// (sequence, 128-key tile) units. Tiles move through the pipeline in groups of G (a
-// shared-memory stage holds G tiles and one mbarrier phase covers them), because each
-// mbarrier wait and tcgen05.commit costs hundreds of cycles of the issuing thread: with one
-// tile per phase the MMA thread, not HBM, set the pace.
-//   warp 0   producer: bulk copies of the query images and of the tiles into a ring of
-//            stage groups; each lane of the warp issues one tile, so a batch of tiles goes
-//            out at once (HBM bound: many tiles stay in flight);
-//   warp 1   tensor-memory owner and MMA issuer: scale atoms -> TMEM, G tiles' MMAs into
-//            one of two accumulator groups, one commit to free the stage group, one to
-//            publish the accumulators;
+// Persistent, warp-specialised: four CTAs per SM (two for 64 heads) each take a contiguous,
+// balanced slice of all (sequence, 128-key tile) units, so that one CTA's issue, MMA and
+// epilogue latencies overlap the others'. The stage ring is sized from the SM's shared memory
+// (about five 8.7 KB tiles per CTA for H <= 32); the code allows G tiles per stage group and
+// mbarrier phase, and G = 1 is what every configuration uses.
+//   warp 0   producer: bulk copies of the query images (a ring of Q slots; a batch never
+//            touches more sequences than there are slots) and of the tiles; each lane of the
+//            warp issues one tile, so a batch of tiles goes out at once;
+//   warp 1   tensor-memory owner and MMA issuer: scale atoms -> TMEM, a tile's MMAs into one
+//            of two accumulators, one commit to free the stage, one to publish the
+//            accumulator;
 //   warps 2-5 epilogue (one 32-lane TMEM quadrant each): tcgen05.ld, ReLU-weighted head
 //            sum in fp32, coalesced logits stores.
+// The prologue scans the sequences once (eight per lane, loads issued together) and keeps the
+// 32 sequences from the slice's start in a shared table; it overlaps the previous kernel
+// (programmatic dependent launch), and the producer's first page lookups precede its wait.
+// Every bounded wait that gives up sets IDX_STATUS_TIMEOUT; the producer then waits (bounded)
+// for the copies it armed and the MMA thread for its last tensor-core operations before the
+// CTA frees tensor memory.
 // Every role walks the same unit sequence, so no metadata is passed between roles.
 #include "common.cuh"
 #include "kernels.h"
