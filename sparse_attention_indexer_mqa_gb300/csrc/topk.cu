@@ -195,21 +195,30 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
     uint32_t c_hi = 0;
     if constexpr (kVec) {
         const uint4* sk4 = reinterpret_cast<const uint4*>(skeys);
-        // lo is a multiple of 128 whenever lo < hi; the trip count is warp-uniform
+        // bin b0 holds the keys [lo_t, lo_t + 2^21); lo is a multiple of 128 whenever lo < hi
+        const uint32_t lo_t = b0 << 21, hi_t = lo_t + ((1u << 21) - 1u);
         for (int base = lo; base < hi; base += 128) {
             const int i0 = base + 4 * lane;
-            const uint4 k4 = i0 < hi ? sk4[i0 >> 2] : make_uint4(0, 0, 0, 0);
+            if (i0 >= hi) continue;
+            const uint4 k4 = sk4[i0 >> 2];
             const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+            const int nv = min(4, hi - i0);  // valid keys of this quad (4 but at the chunk's end)
+            uint32_t m = 0;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const bool valid = i0 + e < hi;
-                const uint32_t bin = kk[e] >> 21;
-                c_hi += valid && bin > b0;
-                if (valid && bin == b0) {
-                    const uint32_t p = atomicAdd(&n_cand, 1u);
-                    if (p < (uint32_t)kCand) {
-                        cand[p] = i0 + e;
-                        ckey[p] = kk[e];
+                const bool valid = e < nv;
+                c_hi += valid && kk[e] > hi_t;
+                m |= (uint32_t)(valid && kk[e] - lo_t < (1u << 21)) << e;
+            }
+            if (m) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if ((m >> e) & 1u) {
+                        const uint32_t p = atomicAdd(&n_cand, 1u);
+                        if (p < (uint32_t)kCand) {
+                            cand[p] = i0 + e;
+                            ckey[p] = kk[e];
+                        }
                     }
                 }
             }
@@ -329,14 +338,16 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
         const uint4* sk4 = reinterpret_cast<const uint4*>(skeys);
         for (int base = lo; base < hi && (c_gt > 0 || (c_eq > 0 && oe < remaining)); base += 128) {
             const int i0 = base + 4 * lane;
-            const uint4 k4 = i0 < hi ? sk4[i0 >> 2] : make_uint4(0, 0, 0, 0);
-            const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
             uint32_t fg = 0, fe = 0;
+            if (i0 < hi) {
+                const uint4 k4 = sk4[i0 >> 2];
+                const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+                const int nv = min(4, hi - i0);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const bool valid = i0 + e < hi;
-                fg |= (uint32_t)(valid && kk[e] > kth) << e;
-                fe |= (uint32_t)(valid && kk[e] == kth) << e;
+                for (int e = 0; e < 4; ++e) {
+                    fg |= (uint32_t)(e < nv && kk[e] > kth) << e;
+                    fe |= (uint32_t)(e < nv && kk[e] == kth) << e;
+                }
             }
             const uint32_t cnt = (uint32_t)__popc(fg) | ((uint32_t)__popc(fe) << 16);
             uint32_t inc = cnt;
