@@ -441,3 +441,195 @@ def test_topk_against_argsort():
     sl2 = np.array([20], np.int32)
     got = O.topk(lg[:1], sl2, np.array([0, 1], np.int32), 0, k)
     assert sorted(got[0][:20].tolist()) == list(range(20)) and (got[0][20:] == -1).all()
+
+
+# --------------------------------------------------------------------------------------
+# composition pins: the weight fold, the RoPE position of every head, and the order
+# LayerNorm -> RoPE -> quantisation of the K store, each against an independent numpy
+# restatement (fp32 numpy arithmetic is one correctly rounded operation per ufunc, so the
+# restatement reproduces the stated rounding order without sharing any code with oracle.c)
+# --------------------------------------------------------------------------------------
+
+F32 = np.float32
+
+
+def _np_rope(x, cs_row, mode):
+    """RoPE of one fp32 row (dims 0..63; NeoX pairs (i, i+32), interleaved (2i, 2i+1)):
+    a' = a*c - b*s, b' = b*c + a*s, every product and sum rounded to fp32."""
+    y = x.astype(F32).copy()
+    c, s = cs_row[:32].astype(F32), cs_row[32:].astype(F32)
+    ia = np.arange(32) if mode == O.ROPE_NEOX else 2 * np.arange(32)
+    ib = ia + 32 if mode == O.ROPE_NEOX else ia + 1
+    a, b = y[ia].copy(), y[ib].copy()
+    y[ia] = (a * c) - (b * s)
+    y[ib] = (b * c) + (a * s)
+    return y
+
+
+def _np_mx_quant(x):
+    """OCP MX quantisation of a 128-value fp32 row: per 32-block E = floor(log2 amax) - 2
+    (frexp), clamped to [-127, 127] (amax 0 -> -127), elements x * 2^-E in fp32, then
+    round-half-even onto the e2m1 grid with saturation (`_e2m1_by_rounding`). Returns the
+    64 packed code bytes and the 4 scale bytes."""
+    codes = np.empty(128, np.uint8)
+    scales = np.empty(4, np.uint8)
+    for b in range(4):
+        blk = x[32 * b:32 * b + 32].astype(F32)
+        amax = float(np.abs(blk).max())
+        if amax == 0.0:
+            E = -127
+        else:
+            _, e = math.frexp(amax)
+            E = max(-127, min(127, e - 1 - 2))
+        scales[b] = E + 127
+        v = blk * F32(2.0 ** -E)
+        codes[32 * b:32 * b + 32] = _e2m1_by_rounding(v)
+    return (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8), scales
+
+
+def _fold_case(dtype, seed):
+    rng = np.random.default_rng(seed)
+    T, H = 7, 4
+    q = W.bf16_bits((rng.standard_normal((T, H, 128)) * 2).astype(F32))
+    pos = rng.permutation(np.arange(40, 40 + T)).astype(np.int32)   # distinct, not t
+    cs = W.rope_table(64)
+    w_in = rng.standard_normal((T, H)).astype(F32)
+    return q, pos, cs, w_in
+
+
+@pytest.mark.parametrize("dtype", [O.MXFP4, O.FP8])
+def test_q_weight_fold_against_restatement(dtype):
+    """w_out = fp32(w_in * fp32(softmax_scale * head_scale)) for MXFP4, and
+    fp32(fp32(w_in * c) * q_scale) with q_scale = fp32(max(amax, 1e-10) / 448) of the RoPE'd
+    row for FP8 (vllm PR 60834 "Changes / Q quant": fp32 weights with the softmax and head
+    scales folded in; vllm PR 53094 "Purpose" step 4: the q scale folded into the weights).
+    Scales away from 1 so that a dropped factor, or the q scale left out, is visible."""
+    q, pos, cs, w_in = _fold_case(dtype, 40 + dtype)
+    ss, hs = 0.08838834764831845, 0.125
+    _, qs, w_out = O.q_quant(q, pos, cs, O.ROPE_NEOX, w_in, ss, hs, dtype)
+    c = F32(np.float64(F32(ss)) * np.float64(F32(hs)))
+    wc = w_in * c
+    if dtype == O.MXFP4:
+        expect = wc
+    else:
+        T, H = w_in.shape
+        expect = np.empty_like(w_in)
+        for t in range(T):
+            for h in range(H):
+                y = _np_rope(W.bf16_to_f32(q[t, h]), cs[pos[t]], O.ROPE_NEOX)
+                scale = F32(max(F32(np.abs(y).max()), F32(1e-10))) / F32(448.0)
+                assert qs[t, h].view(np.uint32) == F32(scale).view(np.uint32)
+                expect[t, h] = wc[t, h] * F32(scale)
+    np.testing.assert_array_equal(w_out.view(np.uint32), expect.astype(F32).view(np.uint32))
+    # the pin separates the plausible slips
+    assert not np.array_equal(w_out, w_in * F32(hs))        # softmax scale dropped
+    assert not np.array_equal(w_out, w_in * F32(ss))        # head scale dropped
+    if dtype == O.FP8:
+        assert not np.array_equal(w_out, wc)                 # q scale not folded
+
+
+@pytest.mark.parametrize("mode", [O.ROPE_NEOX, O.ROPE_INTERLEAVED])
+def test_q_quant_rope_position_of_every_head(mode):
+    """Every head of query t is rotated at positions[t] (vllm PR 53094 "Purpose" step 2:
+    RoPE on the leading rope dims of q): the oracle's MXFP4 codes and scales equal an
+    independent numpy RoPE + MX quantisation at positions[t], and differ from the same at
+    the plausible wrong positions (t itself, or a per-row index t*H + h)."""
+    q, pos, cs, w_in = _fold_case(O.MXFP4, 50 + mode)
+    T, H = w_in.shape
+    qc, qs, _ = O.q_quant(q, pos, cs, mode, w_in, 1.0, 1.0, O.MXFP4)
+    wrong_t = wrong_row = 0
+    for t in range(T):
+        for h in range(H):
+            x = W.bf16_to_f32(q[t, h])
+            c, s = _np_mx_quant(_np_rope(x, cs[pos[t]], mode))
+            np.testing.assert_array_equal(qc[t, h], c)
+            np.testing.assert_array_equal(qs[t, h], s)
+            c1, _ = _np_mx_quant(_np_rope(x, cs[t], mode))
+            c2, _ = _np_mx_quant(_np_rope(x, cs[(t * H + h) % cs.shape[0]], mode))
+            wrong_t += not np.array_equal(c1, c)
+            wrong_row += not np.array_equal(c2, c)
+    assert wrong_t > 0 and wrong_row > 0
+
+
+def _deq_stored_row(pool, dtype, P, stride, slot):
+    """Dequantised 128 values of the token at `slot`, read through the layout functions."""
+    page, r = slot // P, slot % P
+    off = page * stride
+    if dtype == O.MXFP4:
+        cb = np.array([pool[off + O.code_offset(dtype, P, r, j)] for j in range(64)])
+        sc = np.array([pool[off + O.scale_offset(dtype, P, r, b)] for b in range(4)])
+        e2 = np.array([O.e2m1_decode(c) for c in range(16)])
+        v = np.empty(128)
+        v[0::2], v[1::2] = e2[cb & 15], e2[cb >> 4]
+        return v * np.repeat(2.0 ** (sc.astype(np.int64) - 127), 32), sc.astype(np.int64) - 127
+    cb = np.array([pool[off + O.code_offset(dtype, P, r, j)] for j in range(128)])
+    ks = np.frombuffer(bytes(pool[off + O.scale_offset(dtype, P, r):][:4]), np.float32)[0]
+    return np.array([O.e4m3_decode(int(c)) for c in cb]) * float(ks), float(ks)
+
+
+def _np64_layernorm(x, eps=1e-6):
+    xd = x.astype(np.float64)
+    mu = xd.mean()
+    return (xd - mu) / np.sqrt(((xd - mu) ** 2).mean() + eps)
+
+
+def _np64_rope(x, pos, mode):
+    y = x.copy()
+    ang = pos * 10000.0 ** (-np.arange(32) / 32.0)
+    c, s = np.cos(ang), np.sin(ang)
+    ia = np.arange(32) if mode == O.ROPE_NEOX else 2 * np.arange(32)
+    ib = ia + 32 if mode == O.ROPE_NEOX else ia + 1
+    a, b = x[ia], x[ib]
+    y[ia], y[ib] = a * c - b * s, b * c + a * s
+    return y
+
+
+def _within_quant_bound(deq, ref, dtype, E_or_scale):
+    """|dequantised - ref| within half a quantisation step (plus fp32 slack)."""
+    if dtype == O.MXFP4:
+        scale = np.repeat(2.0 ** E_or_scale, 32)
+        v = ref / scale
+        a = np.abs(v)
+        half = np.where(a < 2, 0.25, np.where(a < 4, 0.5, 1.0))
+        err = np.abs(deq / scale - v)
+        sat = a > 6
+        ok = np.where(sat, np.abs(deq / scale) == 6, err <= half + 1e-4 * np.maximum(a, 1))
+        return bool(ok.all())
+    s = E_or_scale
+    err = np.abs(deq - ref)
+    bound = np.maximum(np.abs(ref) * 2.0 ** -4, 2.0 ** -10 * s) * 1.0001 + 1e-6 * np.abs(ref)
+    return bool((err <= bound).all())
+
+
+@pytest.mark.parametrize("dtype", [O.MXFP4, O.FP8])
+@pytest.mark.parametrize("mode", [O.ROPE_NEOX, O.ROPE_INTERLEAVED])
+def test_k_store_norm_then_rope_then_quant(dtype, mode):
+    """The K store applies LayerNorm, then RoPE at positions[row], then quantisation
+    (vllm PR 53094 "Purpose" steps 1, 2, 5; vllm PR 60834 "Changes / K write": norm ->
+    RoPE -> MXFP4 -> store). Each stored row, dequantised, lies within half a quantisation
+    step of an fp64 RoPE(LayerNorm(x)) at positions[row]; rows with a large common offset
+    make the other orders (RoPE before the norm, no norm) and a wrong position (the row
+    index) fall far outside that bound."""
+    rng = np.random.default_rng(60 + 2 * dtype + mode)
+    P, n = 64, 24
+    stride = O.page_bytes(dtype, P)
+    x = (rng.standard_normal((n, 128)) * rng.uniform(0.5, 3, (n, 1))
+         + rng.uniform(4, 12, (n, 1)) * rng.choice([-1, 1], (n, 1))).astype(F32)
+    k = W.bf16_bits(x)
+    xf = W.bf16_to_f32(k)
+    slots = rng.permutation(2 * P)[:n].astype(np.int64)
+    pos = rng.integers(100, 3000, n).astype(np.int32)
+    pool = np.zeros(2 * stride, np.uint8)
+    assert O.k_store(pool, k, slots, pos, W.rope_table(3000), mode, 1, dtype, 2, P, stride) == 0
+    slips = {"rope before norm": 0, "no norm": 0, "position = row": 0}
+    for r in range(n):
+        deq, es = _deq_stored_row(pool, dtype, P, stride, int(slots[r]))
+        ref = _np64_rope(_np64_layernorm(xf[r]), float(pos[r]), mode)
+        assert _within_quant_bound(deq, ref, dtype, es), f"row {r}"
+        slips["rope before norm"] += not _within_quant_bound(
+            deq, _np64_layernorm(_np64_rope(xf[r].astype(np.float64), float(pos[r]), mode)), dtype, es)
+        slips["no norm"] += not _within_quant_bound(
+            deq, _np64_rope(xf[r].astype(np.float64), float(pos[r]), mode), dtype, es)
+        slips["position = row"] += not _within_quant_bound(
+            deq, _np64_rope(_np64_layernorm(xf[r]), float(r), mode), dtype, es)
+    assert all(v >= n // 2 for v in slips.values()), slips
