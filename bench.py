@@ -231,7 +231,7 @@ class Replica:
                                     self.seq_lens_k, self.cu, wl.causal, self.max_q, self.max_k,
                                     self.logits)
         else:
-            Bn.idx_topk(self.logits, self.seq_lens_k, self.cu, wl.causal, wl.topk,
+            Bn.idx_topk(self.logits, self.seq_lens_k, self.cu, wl.causal, self.max_k, wl.topk,
                         inp.get("topk_out", self.topk))
 
     def step(self, i, inputs=None):

@@ -49,7 +49,7 @@ typedef enum { IDX_ROPE_NONE = 0, IDX_ROPE_NEOX = 1, IDX_ROPE_INTERLEAVED = 2 } 
 #define IDX_STATUS_BAD_POS 0x2      /* position outside [0, max_pos): row skipped */
 #define IDX_STATUS_BAD_PAGE 0x4     /* page-table entry outside [0, num_pages): tile skipped */
 #define IDX_STATUS_TIMEOUT 0x8      /* a bounded wait ran out: the CTA stopped early */
-#define IDX_STATUS_BAD_LEN 0x10     /* a sequence/query length was inconsistent: skipped */
+#define IDX_STATUS_BAD_LEN 0x10     /* a sequence's key or query count broke its bound: skipped */
 
 /*
  * Page layout of the paged indexer K cache. This library owns it: callers learn it only
@@ -173,8 +173,11 @@ int idx_qk_prep(const uint16_t* k, int64_t n_rows, int64_t k_row_stride, const i
  *   (int32 [B]); key s of sequence b lives in page page_table[b*pt_stride + s/P], row s%P.
  *   causal = 0: visible(t) = seq_lens_k[b]; causal = 1: the n_q queries are the last n_q
  *   tokens of the sequence and query i sees keys 0 .. seq_lens_k[b] - n_q + i.
- * max_q_len: an upper bound of the queries per sequence (1 selects the decode kernel);
+ * max_q_len: an upper bound of the queries per sequence (<= 1 selects the decode kernel);
  * max_seq_len_k: an upper bound of seq_lens_k (sizes the grid).
+ * A sequence whose key count is negative or above max_seq_len_k, or whose query count
+ * (cu_seqlens_q[b+1] - cu_seqlens_q[b]) is negative or above max_q_len, is skipped (none
+ * of its logits are written) and sets IDX_STATUS_BAD_LEN.
  * q_codes / q_scales / w as produced by idx_q_quant (w = its w_out).
  * H: 1..64 for MXFP4 and FP8. ld_logits >= max visible, a multiple of 4 and at most
  * INT32_MAX / 32 (IDX_EUNSUPPORTED otherwise); logits fp32, 16-byte aligned.
@@ -199,11 +202,16 @@ int idx_mqa_logits_paged(const uint8_t* q_codes, const void* q_scales, const flo
  * increasing index order, then indices equal to it in increasing index order. If
  * visible(t) < k all visible indices are returned, followed by -1 padding.
  * 1 <= k <= 4096; ld_logits <= INT32_MAX (IDX_EUNSUPPORTED otherwise). logits is a
- * 4-byte aligned device buffer (IDX_EINVAL otherwise); any visible length is accepted.
+ * 4-byte aligned device buffer and 0 <= max_seq_len_k <= ld_logits (IDX_EINVAL otherwise).
+ * max_seq_len_k is the scorer's bound: a row whose sequence has a negative key count or one
+ * above max_seq_len_k gets -1 in all k slots and sets IDX_STATUS_BAD_LEN in *dev_status
+ * (when non-NULL), so no row is ever read past max_seq_len_k <= ld_logits. A row that
+ * belongs to no sequence gets -1 in all k slots.
  */
 int idx_topk(const float* logits, int64_t ld_logits, const int32_t* seq_lens_k,
-             const int32_t* cu_seqlens_q, int32_t B, int64_t T, int32_t causal, int32_t k,
-             int32_t* out_idx, cudaStream_t stream);
+             const int32_t* cu_seqlens_q, int32_t B, int64_t T, int32_t causal,
+             int32_t max_seq_len_k, int32_t k, int32_t* out_idx, int32_t* dev_status,
+             cudaStream_t stream);
 
 /*
  * Verification hook: applies the device element encoders used by the store and quant

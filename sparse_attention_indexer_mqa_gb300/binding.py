@@ -77,7 +77,7 @@ def _declare(L):
                               vp, i64, i32, vp, i32, vp, f32, f32, vp, vp, vp, vp, i32, i32, vp, vp]
     L.idx_mqa_logits_paged.argtypes = [vp, vp, vp, i64, i32, i32, vp, i64, i32, i64, vp, i32, vp,
                                        vp, i32, i32, i32, i32, vp, i64, vp, vp]
-    L.idx_topk.argtypes = [vp, i64, vp, vp, i32, i64, i32, i32, vp, vp]
+    L.idx_topk.argtypes = [vp, i64, vp, vp, i32, i64, i32, i32, i32, vp, vp, vp]
     L.idx_debug_encode.argtypes = [i32, vp, i64, vp, vp]
     for n in ("idx_cache_layout", "idx_k_store", "idx_q_quant", "idx_qk_prep", "idx_mqa_logits_paged",
               "idx_topk", "idx_debug_encode"):
@@ -168,11 +168,13 @@ def idx_mqa_logits_paged(q_codes, q_scales, w, dtype, pool, num_pages, page_size
         logits.stride(0), _ptr(dev_status), _stream(stream)))
 
 
-def idx_topk(logits, seq_lens_k, cu_seqlens_q, causal, k, out_idx, stream=None, T=None):
+def idx_topk(logits, seq_lens_k, cu_seqlens_q, causal, max_seq_len_k, k, out_idx,
+             dev_status=None, stream=None, T=None):
     T = logits.shape[0] if T is None else T
     _check("idx_topk", load().idx_topk(
         _ptr(logits), logits.stride(0), _ptr(seq_lens_k), _ptr(cu_seqlens_q),
-        seq_lens_k.shape[0], T, int(causal), k, _ptr(out_idx), _stream(stream)))
+        seq_lens_k.shape[0], T, int(causal), int(max_seq_len_k), k, _ptr(out_idx),
+        _ptr(dev_status), _stream(stream)))
 
 
 def idx_debug_encode(kind, x, out, stream=None):

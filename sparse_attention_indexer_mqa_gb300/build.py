@@ -69,7 +69,7 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
     tmp = LIB + f".tmp{os.getpid()}"
-    r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcuda"], capture_output=True,
+    r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcuda", "-ldl"], capture_output=True,
                        text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -2,10 +2,20 @@
 // the caller's stream. Nothing here allocates, frees or synchronises.
 #include <cmath>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/idx.h"
 #include "kernels.h"
 
 namespace {
+
+// One NVTX range per entry point call (visible in Nsight timelines; near free otherwise).
+struct Range {
+    explicit Range(const char* name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+    Range(const Range&) = delete;
+    Range& operator=(const Range&) = delete;
+};
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 inline bool valid_dtype(int32_t d) { return d == IDX_MXFP4 || d == IDX_FP8; }
@@ -118,6 +128,7 @@ int idx_k_store(const uint16_t* k, int64_t n_rows, int64_t k_row_stride,
                 const float* beta, float eps, int32_t dtype, void* pool, int64_t num_pages,
                 int32_t page_size, int64_t page_stride, int32_t* dev_status,
                 cudaStream_t stream) {
+    Range r("idx_k_store");
     idx::KStoreArgs a;
     const int st = k_store_args(k, n_rows, k_row_stride, slot_mapping, positions, cos_sin, max_pos, rope,
                                 apply_norm, gamma, beta, eps, dtype, pool, num_pages, page_size,
@@ -130,6 +141,7 @@ int idx_q_quant(const uint16_t* q, int64_t T, int32_t H, const int32_t* position
                 const float* cos_sin, int32_t max_pos, int32_t rope, const float* w_in,
                 float softmax_scale, float head_scale, int32_t dtype, uint8_t* q_codes,
                 void* q_scales, float* w_out, int32_t* dev_status, cudaStream_t stream) {
+    Range r("idx_q_quant");
     idx::QQuantArgs a;
     const int st = q_quant_args(q, T, H, positions, cos_sin, max_pos, rope, w_in, softmax_scale,
                                 head_scale, dtype, q_codes, q_scales, w_out, dev_status, a);
@@ -145,6 +157,7 @@ int idx_qk_prep(const uint16_t* k, int64_t n_rows, int64_t k_row_stride, const i
                 float head_scale, uint8_t* q_codes, void* q_scales, float* w_out,
                 const float* cos_sin, int32_t max_pos, int32_t dtype, int32_t* dev_status,
                 cudaStream_t stream) {
+    Range r("idx_qk_prep");
     idx::KStoreArgs ka;
     idx::QQuantArgs qa;
     int st = k_store_args(k, n_rows, k_row_stride, slot_mapping, k_positions, cos_sin, max_pos, k_rope,
@@ -166,6 +179,7 @@ int idx_mqa_logits_paged(const uint8_t* q_codes, const void* q_scales, const flo
                          int32_t causal, int32_t max_q_len, int32_t max_seq_len_k,
                          float* logits, int64_t ld_logits, int32_t* dev_status,
                          cudaStream_t stream) {
+    Range r("idx_mqa_logits_paged");
     int st = check_pool(dtype, pool, num_pages, page_size, page_stride);
     if (st != IDX_OK) return st;
     if (T < 0 || B < 0 || max_q_len < 0 || max_seq_len_k < 0 || pt_stride < 0) return IDX_EINVAL;
@@ -189,17 +203,21 @@ int idx_mqa_logits_paged(const uint8_t* q_codes, const void* q_scales, const flo
 }
 
 int idx_topk(const float* logits, int64_t ld_logits, const int32_t* seq_lens_k,
-             const int32_t* cu_seqlens_q, int32_t B, int64_t T, int32_t causal, int32_t k,
-             int32_t* out_idx, cudaStream_t stream) {
-    if (T < 0 || B < 0 || ld_logits < 0) return IDX_EINVAL;
+             const int32_t* cu_seqlens_q, int32_t B, int64_t T, int32_t causal,
+             int32_t max_seq_len_k, int32_t k, int32_t* out_idx, int32_t* dev_status,
+             cudaStream_t stream) {
+    Range r("idx_topk");
+    if (T < 0 || B < 0 || ld_logits < 0 || max_seq_len_k < 0) return IDX_EINVAL;
     if (k < 1 || k > 4096) return IDX_EUNSUPPORTED;
     if (T == 0) return IDX_OK;
     if (!logits || !seq_lens_k || !cu_seqlens_q || !out_idx || B == 0 || !aligned(logits, 4))
         return IDX_EINVAL;
     if (ld_logits > INT32_MAX) return IDX_EUNSUPPORTED;  // key indices are int32
+    if (max_seq_len_k > ld_logits) return IDX_EINVAL;
     idx::TopkArgs a{};
     a.logits = logits; a.ld = ld_logits; a.seq_lens_k = seq_lens_k; a.cu_seqlens_q = cu_seqlens_q;
-    a.B = B; a.T = T; a.causal = causal != 0; a.k = k; a.out = out_idx;
+    a.B = B; a.T = T; a.causal = causal != 0; a.max_len = max_seq_len_k; a.k = k; a.out = out_idx;
+    a.dev_status = dev_status;
     return cuda_status(idx::launch_topk(a, stream));
 }
 

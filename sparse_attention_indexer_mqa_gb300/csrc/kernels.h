@@ -66,8 +66,9 @@ struct TopkArgs {
     const int32_t* cu_seqlens_q;
     int32_t B;
     int64_t T;
-    int32_t causal, k;
+    int32_t causal, max_len, k;  // max_len: the scorer's max_seq_len_k (<= ld)
     int32_t* out;
+    int32_t* dev_status;
 };
 
 cudaError_t launch_k_store(const KStoreArgs& a, cudaStream_t st);

@@ -91,18 +91,23 @@ struct Cfg {
 };
 
 // Tile count, visible keys and query row of sequence b (0 tiles if it has no query). The
-// three loads are issued together.
+// three loads are issued together. A sequence whose lengths break their bounds (key count
+// negative or above max_seq_len_k, query count negative or above max_q_len <= 1) gets 0
+// tiles and sets *bad.
 struct SeqInfo {  // 32-bit: T <= INT32_MAX and lengths are int32 (checked by the API)
     int32_t t, vis, tiles;
 };
 
-__device__ __forceinline__ SeqInfo seq_info(const ScoreArgs& a, int b) {
+__device__ __forceinline__ SeqInfo seq_info(const ScoreArgs& a, int b, bool* bad = nullptr) {
     const int32_t q0 = a.cu_seqlens_q[b], q1 = a.cu_seqlens_q[b + 1];
-    int32_t len = a.seq_lens_k[b];
+    const int32_t len = a.seq_lens_k[b];
     SeqInfo r{0, 0, 0};
     const int32_t nq = q1 - q0;
-    if (nq <= 0) return r;
-    len = len < 0 ? 0 : (len > a.max_seq_len_k ? a.max_seq_len_k : len);
+    if (nq == 0) return r;
+    if (nq < 0 || nq > a.max_q_len || len < 0 || len > a.max_seq_len_k) {
+        if (bad) *bad = true;
+        return r;
+    }
     r.t = q0;
     r.vis = (int32_t)visible_keys(len, nq, nq - 1, a.causal);
     r.tiles = (r.vis + 127) / 128;
@@ -200,13 +205,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
     // sequences' tile counts stay in registers); the second finds the slice's first unit.
     if (warp == 0) {
         int64_t total = 0;
+        bool bad = false;  // a sequence broke its length bounds (reported by CTA 0)
         SeqInfo s0[8];  // the first 256 sequences: sequence 32k + lane in s0[k]
         for (int base = 0; base < a.B; base += 256) {
             SeqInfo si[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int b = base + 32 * k + lane;
-                si[k] = b < a.B ? seq_info(a, b) : SeqInfo{0, 0, 0};
+                si[k] = b < a.B ? seq_info(a, b, &bad) : SeqInfo{0, 0, 0};
             }
             int64_t n = 0;
 #pragma unroll
@@ -218,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
             for (int o = 16; o >= 1; o >>= 1) n += __shfl_xor_sync(kFull, n, o);
             total += n;
         }
+        if (__any_sync(kFull, bad) && blockIdx.x == 0 && lane == 0) report(a.dev_status, IDX_STATUS_BAD_LEN);
         const int64_t u0 = total * blockIdx.x / gridDim.x, u1 = total * (blockIdx.x + 1) / gridDim.x;
         int64_t acc = 0;
         int b0 = a.B;

@@ -78,18 +78,26 @@ struct Unit {
 };
 
 // Unit of virtual rank v: blocks are ranked heaviest first: v -> (jr = v / B, b = v % B),
-// block j = MB - 1 - jr of sequence b (empty if the sequence has fewer blocks).
-__device__ __forceinline__ bool unit_of(const ScoreArgs& a, int QB, int64_t MB, int64_t v, Unit& u) {
+// block j = MB - 1 - jr of sequence b (empty if the sequence has fewer blocks). A sequence
+// whose lengths break their bounds (key count negative or above max_seq_len_k, query count
+// negative or above max_q_len) has no units; `report` (one thread of the CTA) sets
+// IDX_STATUS_BAD_LEN for it.
+__device__ __forceinline__ bool unit_of(const ScoreArgs& a, int QB, int64_t MB, int64_t v, Unit& u,
+                                        bool report_bad) {
     const int64_t jr = v / a.B;
     u.b = (int)(v - jr * a.B);
     const int64_t j = MB - 1 - jr;
     u.t0 = a.cu_seqlens_q[u.b];
     u.nq = a.cu_seqlens_q[u.b + 1] - u.t0;
     u.q0 = j * QB;
-    if (u.nq <= 0 || u.q0 >= u.nq) return false;
+    const int64_t len = a.seq_lens_k[u.b];
+    if (u.nq < 0 || u.nq > a.max_q_len || len < 0 || len > a.max_seq_len_k) {
+        if (report_bad) report(a.dev_status, IDX_STATUS_BAD_LEN);
+        return false;
+    }
+    if (u.nq == 0 || u.q0 >= u.nq) return false;
     u.nq_blk = min((int64_t)QB, u.nq - u.q0);
-    int64_t len = a.seq_lens_k[u.b];
-    u.len = len < 0 ? 0 : (len > a.max_seq_len_k ? a.max_seq_len_k : len);
+    u.len = len;
     const int64_t vis_last = visible_keys(u.len, u.nq, u.q0 + u.nq_blk - 1, a.causal);
     u.tiles = (vis_last + 127) / 128;
     return u.tiles > 0;
@@ -112,7 +120,7 @@ struct Sched {
             if (k * G >= V) return false;
             const int64_t v = k * G + ((k & 1) ? (G - 1 - c) : c);
             ++k;
-            if (v < V && unit_of(a, QB, MB, v, u)) return true;
+            if (v < V && unit_of(a, QB, MB, v, u, threadIdx.x == 0)) return true;
         }
     }
 };

@@ -112,7 +112,13 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
     int vis = 0;
     if (b >= 0) {
         const int64_t q0 = a.cu_seqlens_q[b], nq = a.cu_seqlens_q[b + 1] - q0;
-        vis = (int)visible_keys(a.seq_lens_k[b], nq, t - q0, a.causal);
+        const int32_t len = a.seq_lens_k[b];
+        if (len < 0 || len > a.max_len) {
+            // the scorer skipped this sequence: no logits to rank (and none past max_len <= ld)
+            if (threadIdx.x == 0) report(a.dev_status, IDX_STATUS_BAD_LEN);
+        } else {
+            vis = (int)visible_keys(len, nq, t - q0, a.causal);  // <= len <= max_len <= ld
+        }
     }
     int32_t* out = a.out + t * a.k;
     const float* row = a.logits + t * a.ld;

@@ -125,7 +125,8 @@ class Dev:
     def select(self):
         from sparse_attention_indexer_mqa_gb300 import binding as Bn
         wl = self.wl
-        Bn.idx_topk(self.logits, self.seq_lens_k, self.cu, wl.causal, wl.topk, self.topk)
+        Bn.idx_topk(self.logits, self.seq_lens_k, self.cu, wl.causal, int(wl.seq_lens_k.max()),
+                    wl.topk, self.topk, dev_status=self.status)
 
     def run_all(self):
         self.store()

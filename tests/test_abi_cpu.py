@@ -62,8 +62,10 @@ def test_host_validation(lib):
     assert lib.idx_q_quant(16, 1, 4, None, None, 0, 0, 16, 1.0, 1.0, 0, 16, None, 16, None,
                            None) == -1
     # top-k: k too large / zero
-    assert lib.idx_topk(16, 8, 16, 16, 1, 1, 0, 5000, 16, None) == -2
-    assert lib.idx_topk(16, 8, 16, 16, 1, 1, 0, 0, 16, None) == -2
+    assert lib.idx_topk(16, 8, 16, 16, 1, 1, 0, 8, 5000, 16, None, None) == -2
+    assert lib.idx_topk(16, 8, 16, 16, 1, 1, 0, 8, 0, 16, None, None) == -2
+    # top-k: the scorer's bound may not exceed the row stride
+    assert lib.idx_topk(16, 8, 16, 16, 1, 1, 0, 9, 32, 16, None, None) == -1
     # scorer: ld below max_seq_len_k, page table stride too small
     assert lib.idx_mqa_logits_paged(16, 16, 16, 1, 4, 0, 16, 1, 64, 4352, 16, 1, 16, 16, 1, 0, 1,
                                     100, 16, 64, None, None) == -1

@@ -391,3 +391,109 @@ def test_path_decode_many_short_sequences(torch, dtype, H, P, B):
     wl = _chunked_prefill(dtype, H, P, 0, lens.tolist(), [1] * B, seed=B + H)
     _full_path(wl, rows=np.sort(rng.choice(B, 400, replace=False)),
                label=f"many short decode dtype={dtype} B={B}")
+
+
+# ------------------------------------------------------------------ injected length faults
+
+def _status_bad_len(d):
+    from sparse_attention_indexer_mqa_gb300 import binding as Bn
+    return bool(int(d.host("status")[0]) & Bn.IDX_STATUS_BAD_LEN)
+
+
+@pytest.mark.parametrize("fault", ["over_max", "negative"])
+def test_decode_bad_key_length_is_skipped_and_reported(torch, fault):
+    """A decode sequence whose key count is above max_seq_len_k (or negative) is skipped:
+    its logits row stays untouched, the status word gets IDX_STATUS_BAD_LEN, and the other
+    sequences are scored exactly as before."""
+    from sparse_attention_indexer_mqa_gb300 import binding as Bn
+    wl = W.make("tiny_decode")
+    d = Dev(wl)
+    d.store(); d.quant()
+    sl = d.seq_lens_k.clone()
+    sl[1] = int(wl.seq_lens_k.max()) + 64 if fault == "over_max" else -5
+    Bn.idx_mqa_logits_paged(d.q_codes, d.q_scales, d.w, wl.dtype, d.pool, wl.pool_pages,
+                            wl.page_size, wl.page_stride, d.page_table, sl, d.cu, wl.causal, 1,
+                            int(wl.seq_lens_k.max()), d.logits, dev_status=d.status)
+    assert _status_bad_len(d)
+    got = d.host("logits")
+    assert np.isnan(got[1]).all()
+    pool_ref = oracle_store(wl)
+    qc, qs, w = oracle_q(wl)
+    exact = oracle_logits(wl, pool_ref, qc, qs, w, rows=np.array([0]))
+    assert_logits_close(got[:1], exact, wl.visible()[:1], label="good sequence")
+
+
+def test_decode_kernel_rejects_multi_query_sequence(torch):
+    """max_q_len = 1 selects the decode scorer; a sequence that nevertheless owns two
+    queries is skipped and reported instead of being scored with the wrong window."""
+    from sparse_attention_indexer_mqa_gb300 import binding as Bn
+    wl = _chunked_prefill(W.MXFP4, 8, 64, 1, [300, 200], [2, 1], seed=3)
+    d = Dev(wl)
+    d.store(); d.quant()
+    Bn.idx_mqa_logits_paged(d.q_codes, d.q_scales, d.w, wl.dtype, d.pool, wl.pool_pages,
+                            wl.page_size, wl.page_stride, d.page_table, d.seq_lens_k, d.cu,
+                            wl.causal, 1, int(wl.seq_lens_k.max()), d.logits, dev_status=d.status)
+    assert _status_bad_len(d)
+    got = d.host("logits")
+    assert np.isnan(got[:2]).all()          # both queries of sequence 0 untouched
+    pool_ref = oracle_store(wl)
+    qc, qs, w = oracle_q(wl)
+    exact = oracle_logits(wl, pool_ref, qc, qs, w, rows=np.array([2]))
+    assert_logits_close(got[2:3], exact, wl.visible()[2:3], label="single-query sequence")
+
+
+@pytest.mark.parametrize("fault", ["too_many_queries", "over_max", "negative"])
+def test_prefill_bad_lengths_are_skipped_and_reported(torch, fault):
+    """Prefill scorer: a sequence with more queries than max_q_len, or a key count above
+    max_seq_len_k or negative, is skipped and reported; the other sequences are exact."""
+    from sparse_attention_indexer_mqa_gb300 import binding as Bn
+    wl = _chunked_prefill(W.MXFP4, 32, 128, 1, [400, 300], [150, 40], seed=4)
+    d = Dev(wl)
+    d.store(); d.quant()
+    sl = d.seq_lens_k.clone()
+    max_q, max_k = 150, int(wl.seq_lens_k.max())
+    if fault == "too_many_queries":
+        max_q = 100
+    elif fault == "over_max":
+        sl[0] = max_k + 1
+    else:
+        sl[0] = -1
+    Bn.idx_mqa_logits_paged(d.q_codes, d.q_scales, d.w, wl.dtype, d.pool, wl.pool_pages,
+                            wl.page_size, wl.page_stride, d.page_table, sl, d.cu, wl.causal,
+                            max_q, max_k, d.logits, dev_status=d.status)
+    assert _status_bad_len(d)
+    got = d.host("logits")
+    assert np.isnan(got[:150]).all()        # sequence 0 untouched
+    rows = np.arange(150, 190)
+    pool_ref = oracle_store(wl)
+    qc, qs, w = oracle_q(wl)
+    exact = oracle_logits(wl, pool_ref, qc, qs, w, rows=rows)
+    assert_logits_close(got[rows], exact, wl.visible()[rows], label="good sequence")
+
+
+def test_topk_bad_lengths_give_padding_and_status(torch):
+    """Top-k rows of a sequence whose key count is above max_seq_len_k (here also above the
+    row stride) or negative are all -1 and set IDX_STATUS_BAD_LEN; the rows of consistent
+    sequences are unaffected."""
+    from sparse_attention_indexer_mqa_gb300 import binding as Bn
+    rng = np.random.default_rng(9)
+    ld, k = 3000, 256
+    logits = torch.from_numpy(rng.standard_normal((3, ld)).astype(np.float32)).cuda()
+    sl = torch.tensor([ld + 500, -3, 2500], dtype=torch.int32, device="cuda")
+    cu = torch.arange(4, dtype=torch.int32, device="cuda")
+    out = torch.full((3, k), -7, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Bn.idx_topk(logits, sl, cu, 0, ld, k, out, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & Bn.IDX_STATUS_BAD_LEN
+    o = out.cpu().numpy()
+    assert (o[0] == -1).all() and (o[1] == -1).all()
+    row = logits[2, :2500].cpu().numpy()
+    assert set(o[2].tolist()) == set(np.argsort(-row, kind="stable")[:k].tolist())
+    # a bound below the true length: the row is reported, not ranked past the bound
+    status.zero_()
+    sl2 = torch.tensor([2000, 2000, 2500], dtype=torch.int32, device="cuda")
+    Bn.idx_topk(logits, sl2, cu, 0, 2400, k, out, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & Bn.IDX_STATUS_BAD_LEN
+    assert (out[2].cpu().numpy() == -1).all()

@@ -55,7 +55,7 @@ def run_rows(torch, rows, k, ld=None, causal=0, cu=None, seq_lens=None):
     dsl = torch.from_numpy(seq_lens).cuda()
     dcu = torch.from_numpy(cu).cuda()
     out = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
-    Bn.idx_topk(dl, dsl, dcu, causal, k, out)
+    Bn.idx_topk(dl, dsl, dcu, causal, int(seq_lens.max()), k, out)
     torch.cuda.synchronize()
     return mat, out.cpu().numpy()
 
