@@ -30,6 +30,8 @@
 //            accumulator;
 //   warps 2-5 epilogue (one 32-lane TMEM quadrant each): tcgen05.ld, ReLU-weighted head
 //            sum in fp32, coalesced logits stores.
+// The cache stream is read with an evict-first L2 policy and the lengths and page table with
+// evict-last, so that the metadata every launch reads stays in L2 under the stream.
 // The prologue scans the sequences once (eight per lane, loads issued together) and keeps the
 // 32 sequences from the slice's start in a shared table; it overlaps the previous kernel
 // (programmatic dependent launch), and the producer's first page lookups precede its wait.
@@ -98,9 +100,9 @@ struct SeqInfo {  // 32-bit: T <= INT32_MAX and lengths are int32 (checked by th
     int32_t t, vis, tiles;
 };
 
-__device__ __forceinline__ SeqInfo seq_info(const ScoreArgs& a, int b, bool* bad = nullptr) {
-    const int32_t q0 = a.cu_seqlens_q[b], q1 = a.cu_seqlens_q[b + 1];
-    const int32_t len = a.seq_lens_k[b];
+__device__ __forceinline__ SeqInfo seq_info(const ScoreArgs& a, int b, uint64_t keep, bool* bad = nullptr) {
+    const int32_t q0 = tc::ld_hint(a.cu_seqlens_q + b, keep), q1 = tc::ld_hint(a.cu_seqlens_q + b + 1, keep);
+    const int32_t len = tc::ld_hint(a.seq_lens_k + b, keep);
     SeqInfo r{0, 0, 0};
     const int32_t nq = q1 - q0;
     if (nq == 0) return r;
@@ -124,14 +126,15 @@ struct SeqEnt {
 struct Seqs {
     const ScoreArgs* a;
     const SeqEnt* tab;
-    int b_tab;  // sequence of tab[0]
+    int b_tab;      // sequence of tab[0]
+    uint64_t keep;  // L2 policy of the metadata loads
     __device__ __forceinline__ SeqInfo get(int b) const {
         const unsigned r = (unsigned)(b - b_tab);
         if (r < (unsigned)kSeqWin) {
             const SeqEnt e = tab[r];
             return SeqInfo{e.t, e.vis, e.tiles};
         }
-        return seq_info(*a, b);
+        return seq_info(*a, b, keep);
     }
 };
 
@@ -199,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
     const int Hq = (H + 7) & ~7;
 
     SeqEnt* seq_tab = reinterpret_cast<SeqEnt*>(smem + C::oSeq);
+    const uint64_t keep = tc::policy_evict_last();  // lengths and page table: read every launch
 
     // ---- this CTA's slice of the units: two warp-wide scans over the sequences ----------
     // The first reads every sequence (eight per lane, loads issued together; the first 256
@@ -212,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int b = base + 32 * k + lane;
-                si[k] = b < a.B ? seq_info(a, b, &bad) : SeqInfo{0, 0, 0};
+                si[k] = b < a.B ? seq_info(a, b, keep, &bad) : SeqInfo{0, 0, 0};
             }
             int64_t n = 0;
 #pragma unroll
@@ -250,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
             if (32 * k < a.B && b0 == a.B) scan32(32 * k, 32 * k + lane < a.B ? s0[k].tiles : 0);
         for (int base = 256; base < a.B && b0 == a.B; base += 32) {
             const int b = base + lane;
-            scan32(base, b < a.B ? seq_info(a, b).tiles : 0);
+            scan32(base, b < a.B ? seq_info(a, b, keep).tiles : 0);
         }
         {  // the table of the window of sequences from b0 on (from registers when b0 + 31 < 256)
             const int b = b0 + lane;
@@ -264,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
                     if ((b >> 5) == k && b < a.B) si = SeqInfo{t, v, n};
                 }
             } else if (b < a.B) {
-                si = seq_info(a, b);
+                si = seq_info(a, b, keep);
             }
             seq_tab[lane] = SeqEnt{si.t, si.vis, si.tiles, 0};
         }
@@ -276,21 +280,22 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
             misc[4] = (uint32_t)n;
             misc[5] = (uint32_t)(n >> 32);
             misc[6] = 0;
-            for (int i = 0; i < C::kSG; ++i) {
-                tc::mbar_init(&k_full[i], G);
-                tc::mbar_init(&k_empty[i], 1);
-            }
-            for (int i = 0; i < C::kQS; ++i) {
-                tc::mbar_init(&q_full[i], 1);
-                tc::mbar_init(&q_empty[i], 1);
-            }
-            tc::mbar_init(drain, 1);
-            for (int i = 0; i < kAccG; ++i) {
-                tc::mbar_init(&acc_full[i], 1);
-                tc::mbar_init(&acc_empty[i], kEpiThreads);
-            }
-            tc::fence_mbar_init();
         }
+        // the barriers, spread over the warp's lanes
+        for (int i = lane; i < C::kSG; i += 32) {
+            tc::mbar_init(&k_full[i], G);
+            tc::mbar_init(&k_empty[i], 1);
+        }
+        if (lane < C::kQS) {
+            tc::mbar_init(&q_full[lane], 1);
+            tc::mbar_init(&q_empty[lane], 1);
+        }
+        if (lane == 0) tc::mbar_init(drain, 1);
+        if (lane < kAccG) {
+            tc::mbar_init(&acc_full[lane], 1);
+            tc::mbar_init(&acc_empty[lane], kEpiThreads);
+        }
+        tc::fence_mbar_init();
     }
     if (warp == 1) {
         tc::tmem_alloc(&misc[0], C::kCols);
@@ -307,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
     }
     const uint32_t tbase = misc[0];
     const int b_start = (int)misc[1];
-    const Seqs S{&a, seq_tab, b_start};
+    const Seqs S{&a, seq_tab, b_start, keep};
     const int32_t j_start = (int32_t)misc[2];
     const int64_t n_units = (int64_t)misc[4] | ((int64_t)misc[5] << 32);
     const int64_t n_groups = (n_units + G - 1) / G;
@@ -321,6 +326,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
         // (a stage group or a Q slot being released) depends only on tiles of earlier
         // batches, never on a lane of the same batch. Empty slots of the last group arrive
         // without bytes.
+        const uint64_t stream = tc::policy_evict_first();  // the cache is read once
         Walker w;  // position of the batch's first unit (same in every lane)
         w.init(S, b_start, j_start);
         int prev_b = -1;     // sequence of the unit before the batch
@@ -353,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
                     const int64_t key0 = my.j * 128;
                     halves = P == 128 ? 1 : (key0 + 64 < my.si.vis ? 2 : 1);
                     const int32_t* pt = a.page_table + (int64_t)my.b * a.pt_stride;
-                    pg[0] = __ldg(pt + (key0 >> lp));
-                    if (halves == 2) pg[1] = __ldg(pt + ((key0 + 64) >> lp));
+                    pg[0] = tc::ld_hint(pt + (key0 >> lp), keep);
+                    if (halves == 2) pg[1] = tc::ld_hint(pt + ((key0 + 64) >> lp), keep);
                 }
                 if (!dep_done) {  // Q and the cache come from the previous kernels
                     pdl_wait();
@@ -398,14 +404,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
                         const uint8_t* src = a.pool + (int64_t)pg[h] * a.page_stride;
                         if (P == 128) {
                             // codes and scale atom are contiguous in the page and in the stage
-                            tc::bulk_g2s(dK, src, C::kTile, &k_full[grp]);
+                            tc::bulk_g2s_hint(dK, src, C::kTile, &k_full[grp], stream);
                         } else if (kDtype == IDX_MXFP4) {
                             // four 1 KB chunks of 16 keys interleave with the other page's chunks
                             for (int q = 0; q < 4; ++q)
-                                tc::bulk_g2s(dK + q * 2048 + h * 1024, src + q * 1024, 1024, &k_full[grp]);
-                            tc::bulk_g2s(dS + h * 256, src + 4096, 256, &k_full[grp]);
+                                tc::bulk_g2s_hint(dK + q * 2048 + h * 1024, src + q * 1024, 1024, &k_full[grp], stream);
+                            tc::bulk_g2s_hint(dS + h * 256, src + 4096, 256, &k_full[grp], stream);
                         } else {
-                            tc::bulk_g2s(dK + h * 8192, src, 8192, &k_full[grp]);
+                            tc::bulk_g2s_hint(dK + h * 8192, src, 8192, &k_full[grp], stream);
                         }
                     }
                 }
@@ -541,7 +547,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
             for (int t = 0; t < G; ++t) {
                 const int64_t i = gi * G + t;
                 const int64_t key = wk.j * 128 + koff;
-                pg[t] = (i < n_units && key < wk.si.vis) ? __ldg(a.page_table + (int64_t)wk.b * a.pt_stride + (key >> lp)) : -1;
+                pg[t] = (i < n_units && key < wk.si.vis)
+                            ? tc::ld_hint(a.page_table + (int64_t)wk.b * a.pt_stride + (key >> lp), keep)
+                            : -1;
                 if (i + 1 < n_units) wk.next(S);
             }
             // so are the head weights when the group's first tile starts a sequence
@@ -572,13 +580,18 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
                 if (kDtype == IDX_FP8 && key_ok)
                     kscale = __ldg(reinterpret_cast<const float*>(a.pool + (int64_t)pg[t] * a.page_stride + 128 * P +
                                                                   4 * ((key & (P - 1)))));
-                float v[NP];
-                load_acc<NP>(lane_addr + (ag * G + t) * NP, v);
-                // four independent accumulation chains over the heads
+                // four independent accumulation chains over the heads, drained 32 columns at a
+                // time (head h always in chain h % 4)
+                constexpr int CH = NP < 32 ? NP : 32;
                 float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                for (int h = 0; h < NP; ++h)
-                    if (h < H) part[h & 3] = fmaf(wr[h], fmaxf(v[h], 0.0f), part[h & 3]);
+                for (int c = 0; c < NP; c += CH) {
+                    float v[CH];
+                    load_acc<CH>(lane_addr + (ag * G + t) * NP + c, v);
+#pragma unroll
+                    for (int h = 0; h < CH; ++h)
+                        if (c + h < H) part[h & 3] = fmaf(wr[c + h], fmaxf(v[h], 0.0f), part[h & 3]);
+                }
                 const float logit = (part[0] + part[1]) + (part[2] + part[3]);
                 if (key_ok) a.logits[(int64_t)w.si.t * a.ld + key] = logit * kscale;
                 w.next(S);

@@ -174,8 +174,9 @@ def tiny_decode(seed=0, **over) -> Workload:
 
 def decode_b64(seed=0, B=64, ctx=8192, H=32, **over) -> Workload:
     """MXFP4 decode: B sequences x 1 query, H=32, 8192 keys each, page 128 from a
-    permuted pool of 4608 pages; 1% of the K rows scaled x20 (outlier blocks); K stored by
-    the quantise-only path (no norm, no RoPE), Q likewise without RoPE; top-k 1024."""
+    permuted pool of 4608 pages; 1% of the K rows scaled x20 (outlier blocks); K stored
+    with NeoX RoPE at position s but without LayerNorm (the norm would undo the x20 rows
+    that exercise the E8M0 scales); Q RoPE'd at the last position; top-k 1024."""
     rk, rq, rw, rp, ro = _streams(seed, 5)
     P = 128
     pool = max(4608, B * ((ctx + P - 1) // P))
@@ -192,17 +193,19 @@ def decode_b64(seed=0, B=64, ctx=8192, H=32, **over) -> Workload:
         pool_pages=pool, base_offset_pages=0, page_stride=page_bytes(MXFP4, P),
         seq_lens_k=lens, cu_seqlens_q=np.arange(B + 1, dtype=np.int32), page_table=pt,
         causal=0, topk=1024, k=bf16_bits(kf), slot_mapping=slots,
-        k_positions=np.zeros(N, np.int32), k_rope=ROPE_NONE, k_norm=0,
-        step_rows=np.cumsum(lens).astype(np.int64) - 1,
-        q=_normal_bf16(rq, (B, H, 128)), q_positions=np.zeros(B, np.int32), q_rope=ROPE_NONE,
+        k_positions=np.concatenate([np.arange(L, dtype=np.int32) for L in lens]),
+        k_rope=ROPE_NEOX, k_norm=0, step_rows=np.cumsum(lens).astype(np.int64) - 1,
+        q=_normal_bf16(rq, (B, H, 128)), q_positions=(lens - 1).astype(np.int32),
+        q_rope=ROPE_NEOX,
         w_in=(rw.standard_normal((B, H), dtype=np.float32) / np.float32(math.sqrt(H))),
-        softmax_scale=1.0, head_scale=1.0, cos_sin=rope_table(1), ld_logits=_ld(ctx),
+        softmax_scale=1.0, head_scale=1.0, cos_sin=rope_table(ctx), ld_logits=_ld(ctx),
     )
 
 
 def prefill_8k(seed=0, T=8192, H=32, **over) -> Workload:
     """MXFP4 causal prefill: one sequence of T queries against its own T paged keys
-    (page 128, shuffled), H=32; quantise-only K and Q; top-k 1024."""
+    (page 128, shuffled), H=32; K through the full store (LayerNorm + NeoX RoPE at
+    position s), query i RoPE'd at position i; top-k 1024."""
     rk, rq, rw, rp = _streams(seed, 4)
     P = 128
     lens = np.array([T], np.int32)
@@ -213,11 +216,13 @@ def prefill_8k(seed=0, T=8192, H=32, **over) -> Workload:
         name=f"prefill_mxfp4_{T}q_h{H}", dtype=MXFP4, B=1, H=H, page_size=P, pool_pages=pool,
         base_offset_pages=0, page_stride=page_bytes(MXFP4, P), seq_lens_k=lens,
         cu_seqlens_q=np.array([0, T], np.int32), page_table=pt, causal=1, topk=1024,
-        k=_normal_bf16(rk, (T, 128)), slot_mapping=slots, k_positions=np.zeros(T, np.int32),
-        k_rope=ROPE_NONE, k_norm=0, step_rows=np.arange(T, dtype=np.int64),
-        q=_normal_bf16(rq, (T, H, 128)), q_positions=np.zeros(T, np.int32), q_rope=ROPE_NONE,
+        k=_normal_bf16(rk, (T, 128)), slot_mapping=slots,
+        k_positions=np.arange(T, dtype=np.int32), k_rope=ROPE_NEOX, k_norm=1,
+        step_rows=np.arange(T, dtype=np.int64),
+        q=_normal_bf16(rq, (T, H, 128)), q_positions=np.arange(T, dtype=np.int32),
+        q_rope=ROPE_NEOX,
         w_in=(rw.standard_normal((T, H), dtype=np.float32) / np.float32(math.sqrt(H))),
-        softmax_scale=1.0, head_scale=1.0, cos_sin=rope_table(1), ld_logits=_ld(T),
+        softmax_scale=1.0, head_scale=1.0, cos_sin=rope_table(T), ld_logits=_ld(T),
     )
 
 
