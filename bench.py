@@ -167,7 +167,9 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------------------
 
-STEP_CALLS = ("qk_prep", "scorer", "topk")  # one library call (one kernel launch) each
+# one library call (one kernel launch) each: the separate calls, and the fused scorer -> top-k
+STEP_CALLS = ("qk_prep", "scorer", "topk")
+FUSED_STEP_CALLS = ("qk_prep", "scorer_topk")
 
 
 class Replica:
@@ -201,6 +203,9 @@ class Replica:
         self.w = torch.zeros((T, H), dtype=torch.float32, device=device)
         self.logits = torch.empty((T, wl.ld_logits), dtype=torch.float32, device=device)
         self.topk = torch.empty((T, wl.topk), dtype=torch.int32, device=device)
+        # workspace of the fused scorer -> top-k (zeroed once: its counters start at zero)
+        n_ws = Bn.idx_mqa_topk_workspace_bytes(T, H, wl.B, self.max_q, self.max_k)
+        self.workspace = torch.zeros(max(n_ws, 256), dtype=torch.uint8, device=device)
         # set-up (untimed): store every key once, then clone the pool R-1 times
         pool0 = torch.zeros(wl.pool_pages * wl.page_stride, dtype=torch.uint8, device=device)
         kall = t(wl.k.view(np.int16))
@@ -230,6 +235,11 @@ class Replica:
                                     wl.pool_pages, wl.page_size, wl.page_stride, self.page_table,
                                     self.seq_lens_k, self.cu, wl.causal, self.max_q, self.max_k,
                                     self.logits)
+        elif name == "scorer_topk":
+            Bn.idx_mqa_topk_paged(self.q_codes, self.q_scales, self.w, wl.dtype, pool, wl.pool_pages,
+                                  wl.page_size, wl.page_stride, self.page_table, self.seq_lens_k,
+                                  self.cu, wl.causal, self.max_q, self.max_k, wl.topk,
+                                  inp.get("topk_out", self.topk), self.workspace)
         else:
             Bn.idx_topk(self.logits, self.seq_lens_k, self.cu, wl.causal, self.max_k, wl.topk,
                         inp.get("topk_out", self.topk))

@@ -214,6 +214,36 @@ int idx_topk(const float* logits, int64_t ld_logits, const int32_t* seq_lens_k,
              cudaStream_t stream);
 
 /*
+ * Paged MQA logits and per-query top-k in one launch ([P2] "Purpose": the cache is scored in
+ * place; [P3] "Purpose": topk_indices_buffer). out_idx[t*k .. t*k+k-1] is what
+ * idx_mqa_logits_paged followed by idx_topk (same arguments, k, max_seq_len_k) would give:
+ * the same set in the same order, since both select on the same fp32 logits. The logits
+ * matrix is never written to caller memory: decode (max_q_len <= 1) scores into a per-query
+ * scratch row of the workspace, and the CTA that finishes a sequence's last tiles selects its
+ * top-k; prefill keeps one block of scratch rows per SM, and the CTA that owns a block of
+ * queries selects their top-k at the end of the block.
+ * Arguments as idx_mqa_logits_paged, plus 1 <= k <= 4096 and out_idx: int32 [T][k].
+ * workspace: device memory of at least the size idx_mqa_topk_workspace_bytes gives for the
+ *   same T, H, B, max_q_len and max_seq_len_k, 256-byte aligned, zero-filled by the caller
+ *   before its first use (decode keeps per-sequence arrival counters there, and every call
+ *   that completes leaves them at zero again; zero it again after a call that reported
+ *   IDX_STATUS_TIMEOUT). One workspace serves one call at a time.
+ * Rows of no sequence, rows with no visible key and rows of sequences that break the length
+ * bounds (IDX_STATUS_BAD_LEN) get -1 in all k slots.
+ */
+int idx_mqa_topk_workspace_bytes(int64_t T, int32_t H, int32_t B, int32_t max_q_len,
+                                 int32_t max_seq_len_k, size_t* bytes);
+
+int idx_mqa_topk_paged(const uint8_t* q_codes, const void* q_scales, const float* w,
+                       int64_t T, int32_t H, int32_t dtype, const void* pool, int64_t num_pages,
+                       int32_t page_size, int64_t page_stride, const int32_t* page_table,
+                       int32_t pt_stride, const int32_t* seq_lens_k,
+                       const int32_t* cu_seqlens_q, int32_t B, int32_t causal,
+                       int32_t max_q_len, int32_t max_seq_len_k, int32_t k, int32_t* out_idx,
+                       void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                       cudaStream_t stream);
+
+/*
  * Verification hook: applies the device element encoders used by the store and quant
  * kernels to n fp32 values. kind 0: e2m1 of v (code in the low nibble, sign in bit 3),
  * kind 1: e4m3 of v (saturating). in and out are device buffers.

@@ -79,8 +79,11 @@ def _declare(L):
                                        vp, i32, i32, i32, i32, vp, i64, vp, vp]
     L.idx_topk.argtypes = [vp, i64, vp, vp, i32, i64, i32, i32, i32, vp, vp, vp]
     L.idx_debug_encode.argtypes = [i32, vp, i64, vp, vp]
+    L.idx_mqa_topk_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, C.POINTER(C.c_size_t)]
+    L.idx_mqa_topk_paged.argtypes = [vp, vp, vp, i64, i32, i32, vp, i64, i32, i64, vp, i32, vp, vp,
+                                     i32, i32, i32, i32, i32, vp, vp, C.c_size_t, vp, vp]
     for n in ("idx_cache_layout", "idx_k_store", "idx_q_quant", "idx_qk_prep", "idx_mqa_logits_paged",
-              "idx_topk", "idx_debug_encode"):
+              "idx_topk", "idx_debug_encode", "idx_mqa_topk_workspace_bytes", "idx_mqa_topk_paged"):
         getattr(L, n).restype = C.c_int
 
 
@@ -175,6 +178,25 @@ def idx_topk(logits, seq_lens_k, cu_seqlens_q, causal, max_seq_len_k, k, out_idx
         _ptr(logits), logits.stride(0), _ptr(seq_lens_k), _ptr(cu_seqlens_q),
         seq_lens_k.shape[0], T, int(causal), int(max_seq_len_k), k, _ptr(out_idx),
         _ptr(dev_status), _stream(stream)))
+
+
+def idx_mqa_topk_workspace_bytes(T, H, B, max_q_len, max_seq_len_k) -> int:
+    n = C.c_size_t(0)
+    _check("idx_mqa_topk_workspace_bytes",
+           load().idx_mqa_topk_workspace_bytes(T, H, B, max_q_len, max_seq_len_k, C.byref(n)))
+    return int(n.value)
+
+
+def idx_mqa_topk_paged(q_codes, q_scales, w, dtype, pool, num_pages, page_size, page_stride,
+                       page_table, seq_lens_k, cu_seqlens_q, causal, max_q_len, max_seq_len_k, k,
+                       out_idx, workspace, dev_status=None, stream=None):
+    T, H = w.shape
+    _check("idx_mqa_topk_paged", load().idx_mqa_topk_paged(
+        _ptr(q_codes), _ptr(q_scales), _ptr(w), T, H, dtype, _ptr(pool), num_pages, page_size,
+        page_stride, _ptr(page_table), page_table.shape[1], _ptr(seq_lens_k), _ptr(cu_seqlens_q),
+        seq_lens_k.shape[0], int(causal), max_q_len, max_seq_len_k, k, _ptr(out_idx),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status),
+        _stream(stream)))
 
 
 def idx_debug_encode(kind, x, out, stream=None):

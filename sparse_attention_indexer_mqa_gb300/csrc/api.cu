@@ -221,6 +221,48 @@ int idx_topk(const float* logits, int64_t ld_logits, const int32_t* seq_lens_k,
     return cuda_status(idx::launch_topk(a, stream));
 }
 
+int idx_mqa_topk_workspace_bytes(int64_t T, int32_t H, int32_t B, int32_t max_q_len, int32_t max_seq_len_k,
+                                 size_t* bytes) {
+    if (!bytes || T < 0 || B < 0 || max_q_len < 0 || max_seq_len_k < 0) return IDX_EINVAL;
+    if (H < 1 || H > 64) return IDX_EUNSUPPORTED;
+    if (max_seq_len_k > INT32_MAX / 32) return IDX_EUNSUPPORTED;
+    const int64_t n = idx::scorer_topk_workspace_bytes(T, H, B, max_q_len, max_seq_len_k);
+    if (n < 0) return IDX_ECUDA;
+    *bytes = (size_t)n;
+    return IDX_OK;
+}
+
+int idx_mqa_topk_paged(const uint8_t* q_codes, const void* q_scales, const float* w, int64_t T, int32_t H,
+                       int32_t dtype, const void* pool, int64_t num_pages, int32_t page_size,
+                       int64_t page_stride, const int32_t* page_table, int32_t pt_stride,
+                       const int32_t* seq_lens_k, const int32_t* cu_seqlens_q, int32_t B, int32_t causal,
+                       int32_t max_q_len, int32_t max_seq_len_k, int32_t k, int32_t* out_idx,
+                       void* workspace, size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream) {
+    Range r("idx_mqa_topk_paged");
+    int st = check_pool(dtype, pool, num_pages, page_size, page_stride);
+    if (st != IDX_OK) return st;
+    if (T < 0 || B < 0 || max_q_len < 0 || max_seq_len_k < 0 || pt_stride < 0) return IDX_EINVAL;
+    if (H < 1 || H > 64 || k < 1 || k > 4096) return IDX_EUNSUPPORTED;
+    if (max_seq_len_k > INT32_MAX / 32) return IDX_EUNSUPPORTED;
+    if (T == 0) return IDX_OK;
+    if (!out_idx || !seq_lens_k || !cu_seqlens_q || B == 0) return IDX_EINVAL;
+    if (max_seq_len_k > 0 && (!q_codes || !w || !page_table)) return IDX_EINVAL;
+    if (dtype == IDX_MXFP4 && max_seq_len_k > 0 && (!q_scales || !aligned(q_scales, 16))) return IDX_EINVAL;
+    if ((q_codes && !aligned(q_codes, 16)) || !aligned(workspace, 256)) return IDX_EINVAL;
+    if (pt_stride < (max_seq_len_k + page_size - 1) / page_size) return IDX_EINVAL;
+    const int64_t need = idx::scorer_topk_workspace_bytes(T, H, B, max_q_len, max_seq_len_k);
+    if (need < 0) return IDX_ECUDA;
+    if (!workspace || (int64_t)workspace_bytes < need) return IDX_EINVAL;
+    idx::ScoreArgs a{};
+    a.q_codes = q_codes; a.q_scales = static_cast<const uint8_t*>(q_scales); a.w = w; a.T = T;
+    a.H = H; a.dtype = dtype; a.pool = static_cast<const uint8_t*>(pool); a.num_pages = num_pages;
+    a.page_size = page_size; a.page_stride = page_stride; a.page_table = page_table;
+    a.pt_stride = pt_stride; a.seq_lens_k = seq_lens_k; a.cu_seqlens_q = cu_seqlens_q; a.B = B;
+    a.causal = causal != 0; a.max_q_len = max_q_len; a.max_seq_len_k = max_seq_len_k;
+    a.topk_k = k; a.out_idx = out_idx; a.dev_status = dev_status;
+    return cuda_status(idx::launch_scorer_topk(a, workspace, stream));
+}
+
 int idx_debug_encode(int32_t kind, const float* in, int64_t n, uint8_t* out, cudaStream_t stream) {
     if ((kind != 0 && kind != 1) || n < 0) return IDX_EINVAL;
     if (n == 0) return IDX_OK;
@@ -235,5 +277,35 @@ namespace idx {
 cudaError_t launch_scorer(const ScoreArgs& a, cudaStream_t st) {
     if (a.max_q_len <= 1) return launch_scorer_decode(a, st);
     return launch_scorer_prefill(a, st);
+}
+
+namespace {
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+int64_t scratch_ld(int32_t max_seq_len_k) { return round_up(max_seq_len_k > 0 ? max_seq_len_k : 1, 4); }
+}  // namespace
+
+// Workspace of the fused scorer -> top-k. Decode (max_q_len <= 1): per-sequence arrival
+// counters [B] int32 (256-byte padded), then a logits scratch row per query [T][ld]. Prefill:
+// one block of scratch rows per CTA [SMs][QB][ld], QB = queries per block for H heads.
+int64_t scorer_topk_workspace_bytes(int64_t T, int32_t H, int32_t B, int32_t max_q_len, int32_t max_seq_len_k) {
+    const int64_t ld = scratch_ld(max_seq_len_k);
+    if (max_q_len <= 1) return round_up(4 * (int64_t)B, 256) + 4 * T * ld;
+    const int sms = device_sm_count();
+    if (sms <= 0) return -1;
+    return 4 * (int64_t)sms * prefill_queries_per_block(H) * ld;
+}
+
+cudaError_t launch_scorer_topk(const ScoreArgs& a0, void* workspace, cudaStream_t st) {
+    ScoreArgs a = a0;
+    a.ld = scratch_ld(a.max_seq_len_k);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (a.max_q_len <= 1) {
+        a.counters = reinterpret_cast<int32_t*>(ws);
+        a.logits = reinterpret_cast<float*>(ws + round_up(4 * (int64_t)a.B, 256));
+        return launch_scorer_decode_select(a, st);
+    }
+    a.counters = nullptr;
+    a.logits = reinterpret_cast<float*>(ws);
+    return launch_scorer_prefill_select(a, st);
 }
 }  // namespace idx

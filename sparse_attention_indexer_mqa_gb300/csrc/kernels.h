@@ -54,9 +54,14 @@ struct ScoreArgs {
     const int32_t* seq_lens_k;
     const int32_t* cu_seqlens_q;
     int32_t B, causal, max_q_len, max_seq_len_k;
-    float* logits;
+    float* logits;  // select mode: the workspace's logits scratch (see launch_scorer_topk)
     int64_t ld;
     int32_t* dev_status;
+    // select mode only (idx_mqa_topk_paged): top-k size, output [T][topk_k], per-sequence
+    // arrival counters of the decode kernel (zero before and after a call)
+    int32_t topk_k;
+    int32_t* out_idx;
+    int32_t* counters;
 };
 
 struct TopkArgs {
@@ -79,5 +84,13 @@ cudaError_t launch_scorer(const ScoreArgs& a, cudaStream_t st);
 cudaError_t launch_scorer_decode(const ScoreArgs& a, cudaStream_t st);
 cudaError_t launch_scorer_prefill(const ScoreArgs& a, cudaStream_t st);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st);
+
+// Fused scorer -> top-k (idx_mqa_topk_paged): bytes of workspace it needs, and the launch.
+int64_t scorer_topk_workspace_bytes(int64_t T, int32_t H, int32_t B, int32_t max_q_len, int32_t max_seq_len_k);
+cudaError_t launch_scorer_topk(const ScoreArgs& a, void* workspace, cudaStream_t st);
+cudaError_t launch_scorer_decode_select(const ScoreArgs& a, cudaStream_t st);
+cudaError_t launch_scorer_prefill_select(const ScoreArgs& a, cudaStream_t st);
+int prefill_queries_per_block(int32_t H);
+int device_sm_count();
 
 }  // namespace idx

@@ -41,6 +41,7 @@
 // Every role walks the same unit sequence, so no metadata is passed between roles.
 #include "common.cuh"
 #include "kernels.h"
+#include "select.cuh"
 #include "tc.cuh"
 
 namespace idx {
@@ -52,6 +53,7 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kEpiThreads = 128;
 constexpr int kAccG = 2;  // accumulator groups in tensor memory
 constexpr int kSeqWin = 32;  // sequences described by the shared-memory table
+constexpr int kSelCand = 256;  // select mode: candidate list of the epilogue warps
 
 template <int kDtype, int NP>
 struct Cfg {
@@ -178,7 +180,23 @@ __device__ __forceinline__ void load_acc(uint32_t taddr, float* v) {
     }
 }
 
-template <int kDtype, int NP>
+// bar.red.or over the CTA's four epilogue warps (named barrier 1): the OR of the predicates
+__device__ __forceinline__ bool epi_barrier_or(bool pred) {
+    uint32_t r;
+    asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+                 : "=r"(r)
+                 : "r"((uint32_t)pred), "r"(kEpiThreads)
+                 : "memory");
+    return r != 0;
+}
+
+// kSel: select mode (idx_mqa_topk_paged). The logits go to the workspace's scratch rows; a
+// sequence's top-k is selected by the CTA that completes its last tiles: a CTA owns the
+// sequences wholly inside its slice, and for the (at most two) sequences it shares with
+// other CTAs it adds its tile count to the sequence's arrival counter, the CTA that brings
+// the counter to the sequence's tile count selecting (and resetting the counter). The four
+// epilogue warps select with the freed stage ring as their work area.
+template <int kDtype, int NP, bool kSel>
 __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel(ScoreArgs a) {
     using C = Cfg<kDtype, NP>;
     constexpr int G = C::G;
@@ -317,6 +335,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
     const int64_t n_units = (int64_t)misc[4] | ((int64_t)misc[5] << 32);
     const int64_t n_groups = (n_units + G - 1) / G;
     const int64_t n_slots = n_groups * G;  // tile slots incl. the last group's empty ones
+    if constexpr (kSel) {
+        if (warp >= 2) pad_orphan_rows(a, tid - 64, kEpiThreads);
+    }
 
     if (warp == 0 && n_units > 0) {
         // ---------------------------------------------------------------- producer warp
@@ -600,6 +621,63 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
             tc::mbar_arrive(&acc_empty[ag]);
             if (++ag == kAccG) { ag = 0; aph ^= 1; }
         }
+        if constexpr (kSel) {
+            // the four epilogue warps' logits stores are done (or given up on); each sequence
+            // of the slice, in order: thread 0 settles whether this CTA selects it, and the
+            // group selects the sequences it owns. Every warp runs the same barriers.
+            __threadfence();
+            const bool stop = epi_barrier_or(*abort_flag != 0);
+            const int etid = tid - 64;
+            volatile int32_t* own = reinterpret_cast<volatile int32_t*>(misc + 8);  // [0] t, [1] vis, [2] more
+            SelectSmem sm;
+            sm.hist = reinterpret_cast<uint32_t*>(smem + C::oStages);
+            sm.cand = reinterpret_cast<int32_t*>(smem + C::oStages + 8192);
+            sm.ckey = reinterpret_cast<uint32_t*>(smem + C::oStages + 8192 + 4 * kSelCand);
+            sm.warp_sums = reinterpret_cast<uint32_t*>(smem + C::oStages + 8192 + 8 * kSelCand);
+            sm.warp_gt = sm.warp_sums + 4;
+            sm.warp_eq = sm.warp_gt + 4;
+            sm.scal = sm.warp_eq + 4;
+            // the rest of the stage ring stages the row's keys (8K keys for MXFP4, 32 heads)
+            sm.keys = reinterpret_cast<uint32_t*>(smem + C::oStages + 8192 + 8 * kSelCand + 128);
+            sm.key_cap = (int)((C::kSG * C::kGroup - (8192 + 8 * kSelCand + 128)) / 4);
+            Walker ws;  // thread 0's walk over the slice's sequences
+            ws.init(S, b_start, j_start);
+            int64_t left = stop ? 0 : n_units;  // tiles of the slice not yet attributed
+            for (;;) {
+                if (etid == 0) {
+                    int32_t t_sel = -1, vis_sel = 0;
+                    while (left > 0 && t_sel < 0) {
+                        const int64_t n_b = min((int64_t)(ws.si.tiles - ws.j), left);
+                        bool mine = ws.j == 0 && n_b == ws.si.tiles;  // the whole sequence
+                        if (!mine) {
+                            int32_t old;
+                            asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;"
+                                         : "=r"(old)
+                                         : "l"(a.counters + ws.b), "r"((int32_t)n_b)
+                                         : "memory");
+                            mine = old + n_b == ws.si.tiles;
+                            if (mine) a.counters[ws.b] = 0;  // for the next call
+                        }
+                        if (mine) {
+                            t_sel = ws.si.t;
+                            vis_sel = ws.si.vis;
+                        }
+                        left -= n_b;
+                        ws.j = ws.si.tiles - 1;  // step to the next sequence with tiles
+                        if (left > 0) ws.next(S);
+                    }
+                    own[0] = t_sel;
+                    own[1] = vis_sel;
+                }
+                NamedBarrier{1, kEpiThreads}();
+                const int32_t t_sel = own[0], vis_sel = own[1];
+                NamedBarrier{1, kEpiThreads}();
+                if (t_sel < 0) break;
+                select_topk_row<kEpiThreads, kSelCand>(a.logits + (int64_t)t_sel * a.ld, vis_sel, a.topk_k,
+                                                        a.out_idx + (int64_t)t_sel * a.topk_k, sm, etid,
+                                                        NamedBarrier{1, kEpiThreads});
+            }
+        }
     }
 
     tc::tc_fence_before();
@@ -621,31 +699,38 @@ int sm_count() {
     return n;
 }
 
-template <int kDtype, int NP>
+template <int kDtype, int NP, bool kSel>
 cudaError_t launch_np(const ScoreArgs& a, cudaStream_t st) {
     using C = Cfg<kDtype, NP>;
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<kDtype, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmem);
+    static_assert(C::kSG * C::kGroup >= 8192 + 8 * kSelCand + 128, "select mode's work area fits the stage ring");
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<kDtype, NP, kSel>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     // an upper bound of the unit count sizes the grid (a CTA with no units exits)
     const int64_t units_max = (int64_t)a.B * ((a.max_seq_len_k + 127) / 128);
     const int ctas = C::kCps * sm_count();
     const int grid = (int)(units_max < ctas ? (units_max > 0 ? units_max : 1) : ctas);
-    return launch_pdl(decode_kernel<kDtype, NP>, dim3(grid), dim3(kThreads), C::kSmem, st, a);
+    return launch_pdl(decode_kernel<kDtype, NP, kSel>, dim3(grid), dim3(kThreads), C::kSmem, st, a);
 }
 
-template <int kDtype>
+template <int kDtype, bool kSel>
 cudaError_t launch_dt(const ScoreArgs& a, cudaStream_t st) {
-    if (a.H <= 16) return launch_np<kDtype, 16>(a, st);
-    if (a.H <= 32) return launch_np<kDtype, 32>(a, st);
-    return launch_np<kDtype, 64>(a, st);
+    if (a.H <= 16) return launch_np<kDtype, 16, kSel>(a, st);
+    if (a.H <= 32) return launch_np<kDtype, 32, kSel>(a, st);
+    return launch_np<kDtype, 64, kSel>(a, st);
 }
 
 }  // namespace
 
 cudaError_t launch_scorer_decode(const ScoreArgs& a, cudaStream_t st) {
     if (a.T == 0 || a.max_seq_len_k == 0 || a.B == 0) return cudaSuccess;
-    return a.dtype == IDX_MXFP4 ? launch_dt<IDX_MXFP4>(a, st) : launch_dt<IDX_FP8>(a, st);
+    return a.dtype == IDX_MXFP4 ? launch_dt<IDX_MXFP4, false>(a, st) : launch_dt<IDX_FP8, false>(a, st);
+}
+
+// Select mode: launched whenever there are rows (rows with no key still get their padding).
+cudaError_t launch_scorer_decode_select(const ScoreArgs& a, cudaStream_t st) {
+    if (a.T == 0 || a.B == 0) return cudaSuccess;
+    return a.dtype == IDX_MXFP4 ? launch_dt<IDX_MXFP4, true>(a, st) : launch_dt<IDX_FP8, true>(a, st);
 }
 
 }  // namespace idx

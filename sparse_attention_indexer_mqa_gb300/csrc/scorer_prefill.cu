@@ -35,6 +35,7 @@
 // half of the block's queries (one warp per 32-lane TMEM quadrant each).
 #include "common.cuh"
 #include "kernels.h"
+#include "select.cuh"
 #include "tc.cuh"
 
 namespace idx {
@@ -66,7 +67,13 @@ struct PCfg {
     static constexpr int oBars = oW + 2 * kW;
     static constexpr int kBars = 2 * kStages + 10;
     static constexpr int oMisc = oBars + 8 * kBars;
-    static constexpr int kSmem = oMisc + 64;
+    // select mode: one top-k work area per epilogue warpgroup (histogram, candidate list,
+    // per-warp counters)
+    static constexpr int kCandS = 512;
+    static constexpr int kSelArea = 2048 * 4 + 2 * kCandS * 4 + 3 * 4 * 4 + 8 * 4;
+    static constexpr int oSel = oMisc + 64;
+    static constexpr int kSmem = oSel;
+    static constexpr int kSmemSel = oSel + kEpiGroups * kSelArea;
 };
 
 struct Unit {
@@ -151,8 +158,38 @@ __device__ __forceinline__ void ld_cols(uint32_t taddr, float* v) {
     }
 }
 
+// The work area of selecting warpgroup g (select mode).
+template <typename C>
+__device__ __forceinline__ SelectSmem sel_smem(uint8_t* smem, int g) {
+    uint8_t* p = smem + C::oSel + g * C::kSelArea;
+    SelectSmem m;
+    m.hist = reinterpret_cast<uint32_t*>(p);
+    m.cand = reinterpret_cast<int32_t*>(p + 2048 * 4);
+    m.ckey = reinterpret_cast<uint32_t*>(p + 2048 * 4 + C::kCandS * 4);
+    m.warp_sums = reinterpret_cast<uint32_t*>(p + 2048 * 4 + 2 * C::kCandS * 4);
+    m.warp_gt = m.warp_sums + 4;
+    m.warp_eq = m.warp_gt + 4;
+    m.scal = m.warp_eq + 4;
+    m.keys = nullptr;
+    m.key_cap = 0;
+    return m;
+}
+
+// bar.red.or over the epilogue warpgroups: every participant gets the OR of the predicates
+__device__ __forceinline__ bool epi_barrier_or(bool pred) {
+    uint32_t r;
+    asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+                 : "=r"(r)
+                 : "r"((uint32_t)pred), "r"(kEpiThreads)
+                 : "memory");
+    return r != 0;
+}
+
 // kFull: H == HP, every accumulator column is a head (no per-head guard in the epilogue).
-template <int kDtype, int HP, bool kFull>
+// kSel: select mode (idx_mqa_topk_paged): a block's logits go to this CTA's rows of the
+// scratch, and at the end of the block the four epilogue warpgroups select the top-k of its
+// rows (one row per warpgroup at a time) and write the indices.
+template <int kDtype, int HP, bool kFull, bool kSel>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
     using C = PCfg<kDtype>;
     constexpr int QB = kNmax / HP;  // queries per block
@@ -423,14 +460,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
         constexpr int NCH = (QH0 + QC - 1) / QC;    // chunks per tile, at most
         const int qlo = gh ? QH0 : 0, qhi = gh ? QB : QH0;
         const int nch = (qhi - qlo + QC - 1) / QC;
+        if constexpr (kSel) pad_orphan_rows(a, (int)threadIdx.x - 96, kEpiThreads);
         const uint32_t lane_addr = tbase + ((uint32_t)(quad * 32) << 16) + gb * N + qlo * HP;
         while (sch.next(a, u)) {
             const int slot = (int)(n_units & 1);
             // the block's weights: wait for the slot's fill (the same phase the MMA issuers used)
+            bool have_q = true;
             if (!__all_sync(kFull, tc::mbar_wait(&q_full[slot], (uint32_t)((n_units >> 1) & 1)))) {
                 *abort_flag = 1;
                 report(a.dev_status, IDX_STATUS_TIMEOUT);
-                break;
+                if constexpr (!kSel) break;
+                have_q = false;  // select mode: no tiles, but the block-end barriers still run
             }
             const float* wsm = reinterpret_cast<const float*>(smem + C::oW + slot * C::kW);
             const int32_t* pt = a.page_table + (int64_t)u.b * a.pt_stride;
@@ -440,12 +480,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
             // (32-bit key arithmetic: lengths are int32 and the host checks QB * ld < 2^31)
             const int32_t vis0 = (int32_t)(a.causal ? u.len - u.nq + u.q0 + 1 : u.len);
             const int qstep = a.causal ? 1 : 0;
-            float* lrow = a.logits + (u.t0 + u.q0) * a.ld;  // the block's first logits row
+            // the block's first logits row (select mode: this CTA's scratch rows)
+            float* lrow = kSel ? a.logits + (int64_t)blockIdx.x * QB * a.ld : a.logits + (u.t0 + u.q0) * a.ld;
             const int32_t ld = (int32_t)a.ld;
             const int tiles = (int)u.tiles;
             // this warpgroup's tiles of the block: every other one, from the parity of the
             // tiles scored before the block
-            for (int j = (int)((gb - kt) & 1); j < tiles; j += 2) {
+            for (int j = (int)((gb - kt) & 1); j < (have_q ? tiles : 0); j += 2) {
                 // page lookups are issued before the accumulator wait (their latency hides
                 // behind it) and used after it
                 const int32_t key = j * 128 + koff;
@@ -602,7 +643,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
             // done with the slot's weights
             tc::mbar_arrive(&q_empty[slot]);
             ++n_units;
-            if (__any_sync(kFull, *abort_flag != 0)) break;  // warp-uniform exit
+            if constexpr (kSel) {
+                // every epilogue warpgroup has written (or given up on) its part of the block's
+                // logits: select each row's top-k, warpgroup g taking rows g, g + 4, ...; every
+                // warpgroup reaches both barriers once per block, also on the give-up path
+                __threadfence();
+                NamedBarrier{1, kEpiThreads}();
+                const int sg = g;
+                const int stid = (int)threadIdx.x - (3 + 4 * sg) * 32;
+                const SelectSmem sm = sel_smem<C>(smem, sg);
+                for (int q = sg; q < nqb; q += kEpiGroups) {
+                    const int vis = (int)visible_keys(u.len, u.nq, u.q0 + q, a.causal);
+                    select_topk_row<128, C::kCandS>(lrow + (int64_t)q * a.ld, vis, a.topk_k,
+                                                    a.out_idx + (u.t0 + u.q0 + q) * a.topk_k, sm, stid,
+                                                    NamedBarrier{(uint32_t)(2 + sg), 128});
+                }
+                if (epi_barrier_or(*abort_flag != 0)) break;  // uniform over the warpgroups
+            } else {
+                if (__any_sync(kFull, *abort_flag != 0)) break;  // warp-uniform exit
+            }
         }
     }
 
@@ -625,38 +684,53 @@ int sm_count() {
     return n;
 }
 
-template <int kDtype, int HP, bool kFull>
+template <int kDtype, int HP, bool kFull, bool kSel>
 cudaError_t launch_hp(const ScoreArgs& a, cudaStream_t st) {
     using C = PCfg<kDtype>;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kDtype, HP, kFull>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    constexpr int smem = kSel ? C::kSmemSel : C::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kDtype, HP, kFull, kSel>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     constexpr int QB = kNmax / HP;
     const int64_t units = (int64_t)a.B * ((a.max_q_len + QB - 1) / QB);
-    const int grid = (int)(units < sm_count() ? (units > 0 ? units : 1) : sm_count());
-    return launch_pdl(prefill_kernel<kDtype, HP, kFull>, dim3(grid), dim3(kThreads), C::kSmem, st, a);
+    // select mode: every CTA runs (the orphan-row pass is strided over the whole grid)
+    const int grid = kSel ? sm_count() : (int)(units < sm_count() ? (units > 0 ? units : 1) : sm_count());
+    return launch_pdl(prefill_kernel<kDtype, HP, kFull, kSel>, dim3(grid), dim3(kThreads), smem, st, a);
 }
 
-template <int kDtype>
+template <int kDtype, bool kSel>
 cudaError_t launch(const ScoreArgs& a, cudaStream_t st) {
     switch (a.H) {
-        case 8: return launch_hp<kDtype, 8, true>(a, st);
-        case 16: return launch_hp<kDtype, 16, true>(a, st);
-        case 32: return launch_hp<kDtype, 32, true>(a, st);
-        case 64: return launch_hp<kDtype, 64, true>(a, st);
+        case 8: return launch_hp<kDtype, 8, true, kSel>(a, st);
+        case 16: return launch_hp<kDtype, 16, true, kSel>(a, st);
+        case 32: return launch_hp<kDtype, 32, true, kSel>(a, st);
+        case 64: return launch_hp<kDtype, 64, true, kSel>(a, st);
         default: break;
     }
-    if (a.H < 8) return launch_hp<kDtype, 8, false>(a, st);
-    if (a.H < 16) return launch_hp<kDtype, 16, false>(a, st);
-    if (a.H < 32) return launch_hp<kDtype, 32, false>(a, st);
-    return launch_hp<kDtype, 64, false>(a, st);
+    if (a.H < 8) return launch_hp<kDtype, 8, false, kSel>(a, st);
+    if (a.H < 16) return launch_hp<kDtype, 16, false, kSel>(a, st);
+    if (a.H < 32) return launch_hp<kDtype, 32, false, kSel>(a, st);
+    return launch_hp<kDtype, 64, false, kSel>(a, st);
 }
 
 }  // namespace
 
 cudaError_t launch_scorer_prefill(const ScoreArgs& a, cudaStream_t st) {
     if (a.T == 0 || a.max_seq_len_k == 0 || a.B == 0) return cudaSuccess;
-    return a.dtype == IDX_MXFP4 ? launch<IDX_MXFP4>(a, st) : launch<IDX_FP8>(a, st);
+    return a.dtype == IDX_MXFP4 ? launch<IDX_MXFP4, false>(a, st) : launch<IDX_FP8, false>(a, st);
 }
+
+cudaError_t launch_scorer_prefill_select(const ScoreArgs& a, cudaStream_t st) {
+    if (a.T == 0 || a.B == 0) return cudaSuccess;
+    return a.dtype == IDX_MXFP4 ? launch<IDX_MXFP4, true>(a, st) : launch<IDX_FP8, true>(a, st);
+}
+
+// Queries per prefill block for H heads (HP = H rounded up to a power of two >= 8).
+int prefill_queries_per_block(int32_t H) {
+    const int hp = H <= 8 ? 8 : H <= 16 ? 16 : H <= 32 ? 32 : 64;
+    return kNmax / hp;
+}
+
+int device_sm_count() { return sm_count(); }
 
 }  // namespace idx

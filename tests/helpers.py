@@ -128,6 +128,24 @@ class Dev:
         Bn.idx_topk(self.logits, self.seq_lens_k, self.cu, wl.causal, int(wl.seq_lens_k.max()),
                     wl.topk, self.topk, dev_status=self.status)
 
+    def select_fused(self, out=None, workspace=None):
+        """Scorer and top-k in one launch (idx_mqa_topk_paged) into `out` (default: a fresh
+        buffer); returns (out, workspace)."""
+        from sparse_attention_indexer_mqa_gb300 import binding as Bn
+        import torch
+        wl = self.wl
+        nq = np.diff(wl.cu_seqlens_q)
+        max_q, max_k = int(nq.max()), int(wl.seq_lens_k.max())
+        if workspace is None:
+            n = Bn.idx_mqa_topk_workspace_bytes(wl.T, wl.H, wl.B, max_q, max_k)
+            workspace = torch.zeros(max(n, 256), dtype=torch.uint8, device=self.k.device)
+        if out is None:
+            out = torch.full((wl.T, wl.topk), -7, dtype=torch.int32, device=self.k.device)
+        Bn.idx_mqa_topk_paged(self.q_codes, self.q_scales, self.w, wl.dtype, self.pool, wl.pool_pages,
+                              wl.page_size, wl.page_stride, self.page_table, self.seq_lens_k, self.cu,
+                              wl.causal, max_q, max_k, wl.topk, out, workspace, dev_status=self.status)
+        return out, workspace
+
     def run_all(self):
         self.store()
         self.quant()

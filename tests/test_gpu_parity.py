@@ -358,7 +358,7 @@ def _chunked_prefill(dtype, H, P, causal, lens, nqs, seed):
     slots = np.concatenate([pt[b, np.arange(L) // P].astype(np.int64) * P + np.arange(L) % P
                             for b, L in enumerate(lens)])
     kpos = np.concatenate([np.arange(L, dtype=np.int32) for L in lens])
-    qpos = np.concatenate([np.arange(L - n, L, dtype=np.int32) for L, n in zip(lens, nqs)])
+    qpos = np.concatenate([np.arange(L - n, L, dtype=np.int32).clip(0) for L, n in zip(lens, nqs)])
     T = int(nqs.sum())
     rope = W.ROPE_INTERLEAVED if dtype == W.FP8 else W.ROPE_NEOX
     return W.Workload(
