@@ -331,13 +331,11 @@ def run_gpu(args, rank, world):
     clk = clocks.stop()
     ms = rank_max(ms, world, dev)
 
-    # per-kernel device time: each kernel captured K times (same rotation) and timed alone
-    per_kernel_ms = {}
-    for name in STEP_CALLS:
-        g = capture(torch, lambda i, n=name: rep.call(n, args.warmup + i), args.steps)
-        g.replay()
-        torch.cuda.synchronize()
-        per_kernel_ms[name] = time_graph(torch, g, stream) / args.steps
+    # per-kernel device time: each kernel captured K times (same rotation) and timed alone;
+    # also the fused scorer -> top-k and the step made with it
+    per_kernel_ms = {name: time_calls(torch, rep, (name,), args.warmup, args.steps, stream)
+                     for name in STEP_CALLS + ("scorer_topk",)}
+    step_fused_ms = time_calls(torch, rep, FUSED_STEP_CALLS, args.warmup, args.steps, stream)
 
     # end to end through the C ABI with host buffers: H2D of the step's inputs (new K rows,
     # slots, positions, Q, weights) from pinned memory, the four calls, D2H of the top-k
@@ -355,19 +353,7 @@ def run_gpu(args, rank, world):
                 "traffic": profile_traffic(f"scorer:{args.config}", SCORER_SOURCES),
                 "algorithmic_bytes": ab["scorer"], "peak_source": f"{peak_kind} (hbm_gbs)"}
     else:
-        alu = scorer_alu_ops(wl) / sc_s
-        tpeak = peaks["bf16_tflops"] * TENSOR_RATIO[wl.dtype]
-        roof = {"kernel": "scorer", "bound": "alu", "achieved": round(alu / 1e12, 2),
-                "peak": round(alu_peak_ops(peaks) / 1e12, 2), "unit": "T instr/s",
-                "frac": round(alu / alu_peak_ops(peaks), 4),
-                "traffic": profile_traffic(f"scorer:{args.config}", SCORER_SOURCES),
-                "algorithmic_ops": scorer_alu_ops(wl),
-                "peak_source": "issue rate 4x32 lanes x 152 SMs x measured max SM clock",
-                "tensor": {"achieved_tflops": round(scorer_flops(wl) / sc_s / 1e12, 1),
-                           "peak_tflops": round(tpeak, 1),
-                           "frac": round(scorer_flops(wl) / sc_s / 1e12 / tpeak, 4),
-                           "peak_source": f"{peak_kind} bf16 x nominal ratio {TENSOR_RATIO[wl.dtype]:g}"},
-                "hbm_gbs": round(ab["scorer"] / sc_s / 1e9, 1)}
+        roof = prefill_roofline(wl, per_kernel_ms["scorer"], peaks, peak_kind)
     line = {
         "metric": metric_name(wl),
         "value": round(value, 1),
@@ -393,11 +379,110 @@ def run_gpu(args, rank, world):
         "gpu_launches": len(STEP_CALLS) * args.steps,
         "clocks": clk,
         "e2e": e2e,
+        "fused": {"step_us": round(step_fused_ms * 1e3, 3),
+                  "value": round(job_rate(pairs, step_fused_ms, world), 1),
+                  "step": "qk_prep + mqa_topk_paged (scorer and top-k in one launch)",
+                  "note": "not the headline step: measured slower than the separate calls"},
     }
+    if is_decode(wl) and args.config == "decode_b64" and not args.no_prefill:
+        line["prefill"] = prefill_block(args, dev, peaks, peak_kind)
+    if not args.no_probe:
+        line["tensor_probe"] = tensor_probe(torch, stream)
+        if "prefill" in line:
+            t = line["prefill"]["roofline"]["tensor"]
+            p = line["tensor_probe"]["mxf4_tflops"]
+            t["probe_tflops"] = p
+            t["frac_of_probe"] = round(t["achieved_tflops"] / p, 4)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget,
                                             rows_per_step=None if is_decode(wl) else args.ref_rows)
     return line
+
+
+def time_calls(torch, rep, calls, first, k, stream):
+    """Device ms per step of `calls` (library calls of the replica), K steps in one graph."""
+    g = capture(torch, lambda i: [rep.call(n, first + i) for n in calls], k)
+    g.replay()
+    torch.cuda.synchronize()
+    return time_graph(torch, g, stream) / k
+
+
+def prefill_roofline(wl, scorer_ms, peaks, peak_kind):
+    """Prefill scorer against the dense tensor rate of its dtype (the measured bf16 rate times
+    the nominal ratio) and against the issue rate of its epilogue."""
+    sc_s = scorer_ms / 1e3
+    alu = scorer_alu_ops(wl) / sc_s
+    tpeak = peaks["bf16_tflops"] * TENSOR_RATIO[wl.dtype]
+    return {"kernel": "scorer", "bound": "alu", "achieved": round(alu / 1e12, 2),
+            "peak": round(alu_peak_ops(peaks) / 1e12, 2), "unit": "T instr/s",
+            "frac": round(alu / alu_peak_ops(peaks), 4),
+            "traffic": profile_traffic(f"scorer:{wl_key(wl)}", SCORER_SOURCES),
+            "algorithmic_ops": scorer_alu_ops(wl),
+            "peak_source": "issue rate 4x32 lanes x 152 SMs x measured max SM clock",
+            "tensor": {"achieved_tflops": round(scorer_flops(wl) / sc_s / 1e12, 1),
+                       "peak_tflops": round(tpeak, 1),
+                       "frac": round(scorer_flops(wl) / sc_s / 1e12 / tpeak, 4),
+                       "peak_source": f"{peak_kind} bf16 x nominal ratio {TENSOR_RATIO[wl.dtype]:g}"},
+            "hbm_gbs": round(algorithmic_bytes(wl)["scorer"] / sc_s / 1e9, 1)}
+
+
+def wl_key(wl):
+    return {"decode_mxfp4_b64_h32_8192": "decode_b64", "prefill_mxfp4_8192q_h32": "prefill_8k"}.get(wl.name, wl.name)
+
+
+def prefill_block(args, dev, peaks, peak_kind):
+    """The prefill half of the metric, measured in the default run: causal MXFP4 prefill, 8192
+    queries x 8192 keys, H=32 (the pages' isolated prefill scorer shape)."""
+    import torch
+    wl = W.make("prefill_8k", seed=args.seed)
+    ws = working_set_bytes(wl)
+    copies = 1 if ws > 16 * L2_BYTES else (2 if ws > 4 * L2_BYTES else max(2, -(-4 * L2_BYTES // ws)))
+    rep = Replica(wl, copies, dev)
+    stream = torch.cuda.current_stream()
+    k = max(3, min(args.steps, 10))
+    for i in range(3):
+        rep.step(i)
+    torch.cuda.synchronize()
+    kernel_ms = {n: time_calls(torch, rep, (n,), 3, k, stream) for n in STEP_CALLS + ("scorer_topk",)}
+    step_ms = time_calls(torch, rep, STEP_CALLS, 3, k, stream)
+    step_fused_ms = time_calls(torch, rep, FUSED_STEP_CALLS, 3, k, stream)
+    pairs = wl.pairs()
+    out = {"workload": wl.name, "queries": wl.T, "pairs": pairs, "steps": k,
+           "step_us": round(step_ms * 1e3, 2), "step_fused_us": round(step_fused_ms * 1e3, 2),
+           "value": round(pairs / (step_ms / 1e3) / 1e3, 1), "unit": "K-tokens/s",
+           "scorer_k_tokens_per_s": round(pairs / (kernel_ms["scorer"] / 1e3) / 1e3, 1),
+           "kernel_us": {n: round(v * 1e3, 2) for n, v in kernel_ms.items()},
+           "roofline": prefill_roofline(wl, kernel_ms["scorer"], peaks, peak_kind),
+           "l2": f"inputs rotate over {copies} copies of cache+Q"}
+    del rep
+    torch.cuda.empty_cache()
+    return out
+
+
+def tensor_probe(torch, stream, iters=2000):
+    """Dense tensor-core rate of tcgen05 kind::mxf4 and kind::f8f6f4 MMAs (M=128, N=256), one
+    CTA per SM, timed with CUDA events."""
+    from sparse_attention_indexer_mqa_gb300 import binding as Bn
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = {}
+    for name, dt in (("mxf4", W.MXFP4), ("f8f6f4", W.FP8)):
+        Bn.idx_debug_mma_rate(dt, 50, status)
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(3):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            f = Bn.idx_debug_mma_rate(dt, iters, status)
+            e.record(stream)
+            torch.cuda.synchronize()
+            t = s.elapsed_time(e) / 1e3
+            best = t if best is None else min(best, t)
+        out[f"{name}_tflops"] = round(f * sms / best / 1e12, 1)
+    out["status"] = int(status.item())
+    out["how"] = (f"{iters} x 8 back-to-back MMAs (M=128, N=256, K=64 mxf4 / K=32 e4m3) per SM on zero "
+                  "operands into one TMEM accumulator, best of 3 launches")
+    return out
 
 
 def config_of(wl):
@@ -609,7 +694,9 @@ def run_reference(args, rank, world):
 SCORER_SOURCES = ["sparse_attention_indexer_mqa_gb300/csrc/scorer_decode.cu",
                   "sparse_attention_indexer_mqa_gb300/csrc/scorer_prefill.cu",
                   "sparse_attention_indexer_mqa_gb300/csrc/tc.cuh",
-                  "sparse_attention_indexer_mqa_gb300/csrc/common.cuh"]
+                  "sparse_attention_indexer_mqa_gb300/csrc/common.cuh",
+                  "sparse_attention_indexer_mqa_gb300/csrc/select.cuh",
+                  "sparse_attention_indexer_mqa_gb300/csrc/kernels.h"]
 
 
 def main():
@@ -623,6 +710,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-rows", type=int, default=8)
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill block of the default run")
+    ap.add_argument("--no-probe", action="store_true", help="skip the tensor-core rate probe")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

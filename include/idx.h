@@ -251,6 +251,16 @@ int idx_mqa_topk_paged(const uint8_t* q_codes, const void* q_scales, const float
 int idx_debug_encode(int32_t kind, const float* in, int64_t n, uint8_t* out,
                      cudaStream_t stream);
 
+/*
+ * Measurement hook: the dense tensor-core rate of the scorers' MMA kinds. Launches one CTA
+ * per SM, each issuing iters x 8 MMAs (M = 128, N = 256, K = 64 block-scaled MXFP4 for
+ * IDX_MXFP4, K = 32 e4m3 for IDX_FP8) on zero operands into one tensor-memory accumulator.
+ * *flops_per_cta (host, may be NULL) receives the flops one CTA performs; the caller times
+ * the launch on `stream` and divides by the SM count times that. dev_status as elsewhere.
+ */
+int idx_debug_mma_rate(int32_t dtype, int32_t iters, int32_t* dev_status, double* flops_per_cta,
+                       cudaStream_t stream);
+
 /* Human-readable name of an idx_status value (static string). */
 const char* idx_status_string(int status);
 

@@ -82,8 +82,10 @@ def _declare(L):
     L.idx_mqa_topk_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, C.POINTER(C.c_size_t)]
     L.idx_mqa_topk_paged.argtypes = [vp, vp, vp, i64, i32, i32, vp, i64, i32, i64, vp, i32, vp, vp,
                                      i32, i32, i32, i32, i32, vp, vp, C.c_size_t, vp, vp]
+    L.idx_debug_mma_rate.argtypes = [i32, i32, vp, C.POINTER(C.c_double), vp]
     for n in ("idx_cache_layout", "idx_k_store", "idx_q_quant", "idx_qk_prep", "idx_mqa_logits_paged",
-              "idx_topk", "idx_debug_encode", "idx_mqa_topk_workspace_bytes", "idx_mqa_topk_paged"):
+              "idx_topk", "idx_debug_encode", "idx_mqa_topk_workspace_bytes", "idx_mqa_topk_paged",
+              "idx_debug_mma_rate"):
         getattr(L, n).restype = C.c_int
 
 
@@ -202,3 +204,11 @@ def idx_mqa_topk_paged(q_codes, q_scales, w, dtype, pool, num_pages, page_size, 
 def idx_debug_encode(kind, x, out, stream=None):
     _check("idx_debug_encode", load().idx_debug_encode(kind, _ptr(x), x.numel(), _ptr(out),
                                                        _stream(stream)))
+
+
+def idx_debug_mma_rate(dtype, iters, dev_status=None, stream=None) -> float:
+    """Launch the tensor-core rate probe; returns the flops one CTA (SM) performs."""
+    f = C.c_double(0.0)
+    _check("idx_debug_mma_rate", load().idx_debug_mma_rate(dtype, iters, _ptr(dev_status), C.byref(f),
+                                                           _stream(stream)))
+    return float(f.value)

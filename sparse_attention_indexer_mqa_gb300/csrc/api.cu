@@ -41,6 +41,13 @@ int check_pool(int32_t dtype, const void* pool, int64_t num_pages, int32_t page_
 
 extern "C" {
 
+int idx_debug_mma_rate(int32_t dtype, int32_t iters, int32_t* dev_status, double* flops_per_cta,
+                       cudaStream_t stream) {
+    if (!valid_dtype(dtype) || iters < 1) return IDX_EINVAL;
+    if (flops_per_cta) *flops_per_cta = (double)idx::mma_rate_flops_per_iter(dtype) * iters;
+    return cuda_status(idx::launch_mma_rate(dtype, iters, dev_status, stream));
+}
+
 const char* idx_status_string(int status) {
     switch (status) {
         case IDX_OK: return "ok";
