@@ -252,6 +252,33 @@ int idx_debug_encode(int32_t kind, const float* in, int64_t n, uint8_t* out,
                      cudaStream_t stream);
 
 /*
+ * idx_mqa_topk_paged without a workspace, for callers that cannot allocate device memory
+ * (code that must not allocate once it runs, or that only holds pointers to its own inputs
+ * and outputs). The web pages have no counterpart of this entry point; it serves deployment.
+ * Decode only (max_q_len <= 1); otherwise arguments, results and status bits as
+ * idx_mqa_topk_paged, whose decode kernel it launches.
+ * Working memory: an 8 MiB array in device memory that the library owns (a per-sequence
+ *   counter for up to 16384 sequences, then T rows of roundup(max_seq_len_k, 4) fp32
+ *   scratch logits in the remaining 8 MiB - 64 KiB). Every GPU that loads the library holds
+ *   the array until the process exits. Larger B or T x row length: IDX_EUNSUPPORTED, before
+ *   anything is enqueued. The call allocates nothing.
+ * Set-up: the first call on a device, with that device current, resolves the array's device
+ *   address (cudaGetSymbolAddress) and keeps it; make that first call before any stream
+ *   capture.
+ * Every call clears the counters (an asynchronous memset on `stream`) and then reuses the
+ *   same array: calls that can overlap on the GPU (other streams, other threads) race on it
+ *   and must be ordered by the caller.
+ */
+int idx_mqa_topk_paged_noalloc(const uint8_t* q_codes, const void* q_scales, const float* w,
+                               int64_t T, int32_t H, int32_t dtype, const void* pool,
+                               int64_t num_pages, int32_t page_size, int64_t page_stride,
+                               const int32_t* page_table, int32_t pt_stride,
+                               const int32_t* seq_lens_k, const int32_t* cu_seqlens_q,
+                               int32_t B, int32_t causal, int32_t max_q_len,
+                               int32_t max_seq_len_k, int32_t k, int32_t* out_idx,
+                               int32_t* dev_status, cudaStream_t stream);
+
+/*
  * Measurement hook: the dense tensor-core rate of the scorers' MMA kinds. Launches one CTA
  * per SM, each issuing iters x 8 MMAs (M = 128, N = 256, K = 64 block-scaled MXFP4 for
  * IDX_MXFP4, K = 32 e4m3 for IDX_FP8) on zero operands into one tensor-memory accumulator.

@@ -83,9 +83,11 @@ def _declare(L):
     L.idx_mqa_topk_paged.argtypes = [vp, vp, vp, i64, i32, i32, vp, i64, i32, i64, vp, i32, vp, vp,
                                      i32, i32, i32, i32, i32, vp, vp, C.c_size_t, vp, vp]
     L.idx_debug_mma_rate.argtypes = [i32, i32, vp, C.POINTER(C.c_double), vp]
+    L.idx_mqa_topk_paged_noalloc.argtypes = [vp, vp, vp, i64, i32, i32, vp, i64, i32, i64, vp, i32,
+                                             vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
     for n in ("idx_cache_layout", "idx_k_store", "idx_q_quant", "idx_qk_prep", "idx_mqa_logits_paged",
               "idx_topk", "idx_debug_encode", "idx_mqa_topk_workspace_bytes", "idx_mqa_topk_paged",
-              "idx_debug_mma_rate"):
+              "idx_debug_mma_rate", "idx_mqa_topk_paged_noalloc"):
         getattr(L, n).restype = C.c_int
 
 
@@ -212,3 +214,14 @@ def idx_debug_mma_rate(dtype, iters, dev_status=None, stream=None) -> float:
     _check("idx_debug_mma_rate", load().idx_debug_mma_rate(dtype, iters, _ptr(dev_status), C.byref(f),
                                                            _stream(stream)))
     return float(f.value)
+
+
+def idx_mqa_topk_paged_noalloc(q_codes, q_scales, w, dtype, pool, num_pages, page_size, page_stride,
+                               page_table, seq_lens_k, cu_seqlens_q, causal, max_q_len, max_seq_len_k,
+                               k, out_idx, dev_status=None, stream=None):
+    T, H = w.shape
+    _check("idx_mqa_topk_paged_noalloc", load().idx_mqa_topk_paged_noalloc(
+        _ptr(q_codes), _ptr(q_scales), _ptr(w), T, H, dtype, _ptr(pool), num_pages, page_size,
+        page_stride, _ptr(page_table), page_table.shape[1], _ptr(seq_lens_k), _ptr(cu_seqlens_q),
+        seq_lens_k.shape[0], int(causal), max_q_len, max_seq_len_k, k, _ptr(out_idx),
+        _ptr(dev_status), _stream(stream)))
