@@ -386,6 +386,7 @@ def run_gpu(args, rank, world):
     }
     if is_decode(wl) and args.config == "decode_b64" and not args.no_prefill:
         line["prefill"] = prefill_block(args, dev, peaks, peak_kind)
+        line["qk_prep_sweep"] = qk_prep_sweep(args, dev, peaks)
     if not args.no_probe:
         line["tensor_probe"] = tensor_probe(torch, stream)
         if "prefill" in line:
@@ -457,6 +458,29 @@ def prefill_block(args, dev, peaks, peak_kind):
     del rep
     torch.cuda.empty_cache()
     return out
+
+
+def qk_prep_sweep(args, dev, peaks):
+    """The fused QK pre-processing alone (idx_qk_prep: K LayerNorm + RoPE + FP8 store of T new
+    keys, Q RoPE + per-(t,h) FP8 quant with the scale fold for T tokens), FP8, block 64, H=32,
+    interleaved RoPE, at the token counts of the pages' fused-preprocessing table."""
+    import torch
+    stream = torch.cuda.current_stream()
+    rows = []
+    for T in (1, 8, 32, 64, 256, 1024):
+        wl = W.make("prefill_fp8", seed=args.seed, B=1, cached=4096, new=T)
+        rep = Replica(wl, 2, dev)
+        for i in range(3):
+            rep.call("qk_prep", i)
+        k = 50
+        ms = time_calls(torch, rep, ("qk_prep",), 3, k, stream)
+        ab = algorithmic_bytes(wl)["qk_prep"]
+        rows.append({"tokens": T, "us": round(ms * 1e3, 2), "bytes": ab,
+                     "gbs": round(ab / (ms / 1e3) / 1e9, 1)})
+        del rep
+    return {"dtype": "fp8e4m3", "block_size": 64, "H": 32, "rope": "interleaved",
+            "graph_of": 50, "rows": rows,
+            "hbm_frac_at_1024": round(rows[-1]["gbs"] / peaks["hbm_gbs"], 4)}
 
 
 def tensor_probe(torch, stream, iters=2000):

@@ -229,9 +229,13 @@ def test_path_prefill_small_ragged(torch):
 
 
 def test_path_prefill_8k_sampled(torch):
+    """At least 512 rows: 8 from every 128-row band of queries (the band's first rows, which sit
+    on the diagonal key tile, its middle and its last row), plus the k-boundary rows."""
     wl = W.make("prefill_8k")
-    rows = np.unique(np.concatenate([np.arange(0, 8), [1022, 1023, 1024, 1025],
-                                     np.linspace(0, 8191, 40).astype(int), np.arange(8184, 8192)]))
+    bands = np.arange(0, 8192, 128)
+    rows = np.unique(np.concatenate([bands[:, None] + np.array([0, 1, 2, 31, 63, 64, 100, 127])[None, :],
+                                     [[1022, 1023, 1024, 1025]]], axis=None))
+    assert rows.size >= 512
     _full_path(wl, rows=rows, label="prefill 8192 (sampled rows)")
 
 
@@ -240,8 +244,13 @@ def test_path_fp8_small(torch):
 
 
 def test_path_fp8_full_sampled(torch):
+    """256 rows per sequence: its first and last 16 queries, the first and last rows of 64-query
+    bands (block edges of the scorer's query blocks and of the 64-key pages), spread middles."""
     wl = W.make("prefill_fp8")
-    rows = np.concatenate([b * 4096 + np.array([0, 1, 2047, 4094, 4095]) for b in range(8)])
+    per = np.unique(np.concatenate([np.arange(16), np.arange(4080, 4096), np.arange(0, 4096, 64),
+                                    np.arange(63, 4096, 64), np.linspace(0, 4095, 120).astype(int)]))
+    assert per.size >= 256
+    rows = np.concatenate([b * 4096 + per for b in range(8)])
     _full_path(wl, rows=rows, label="fp8 32K (sampled rows)")
 
 
