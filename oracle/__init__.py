@@ -80,6 +80,13 @@ def _declare(L):
                               vp, vp]
     L.orc_q_quant.restype = C.c_int
     L.orc_visible.argtypes = [i64, vp, vp, i32, C.c_int]; L.orc_visible.restype = i64
+    L.orc_exp_neg.argtypes = [f32]; L.orc_exp_neg.restype = f32
+    L.orc_rmsnorm128.argtypes = [vp, vp, f32, vp]; L.orc_rmsnorm128.restype = None
+    L.orc_compress_pool128.argtypes = [vp, vp, i64, i64, i64, vp]
+    L.orc_compress_pool128.restype = None
+    L.orc_compress_k_store.argtypes = [vp, vp, i64, vp, vp, i64, i32, vp, vp, vp, i32, C.c_int,
+                                       C.c_int, vp, vp, f32, C.c_int, vp, i64, i32, i64]
+    L.orc_compress_k_store.restype = C.c_int
     L.orc_mqa_logits.argtypes = [vp, vp, vp, i64, i32, C.c_int, vp, i64, i32, i64, vp, i32,
                                  vp, vp, i32, C.c_int, vp, i64, vp, i64, C.c_int]
     L.orc_mqa_logits.restype = C.c_int
@@ -253,3 +260,47 @@ def topk(logits, seq_lens_k, cu_seqlens_q, causal, k, rows=None, n_threads=None)
     lib().orc_topk(_p(lg), lg.shape[1], _p(sl), _p(cu), sl.shape[0], int(causal), _p(rr), n,
                    int(k), _p(out), int(nt))
     return out
+
+
+# --- compressor front end --------------------------------------------------------------
+
+def exp_neg(a: float) -> float:
+    return float(lib().orc_exp_neg(float(a)))
+
+
+def rmsnorm128(x, gamma=None, eps=1e-6):
+    x = _c(x, np.float32)
+    g = _c(np.ones(128) if gamma is None else gamma, np.float32)
+    y = np.empty(128, np.float32)
+    lib().orc_rmsnorm128(_p(x), _p(g), C.c_float(eps), _p(y))
+    return y
+
+
+def compress_pool128(k_raw, gate, lo, hi):
+    """Pooled fp32 row of raw rows lo..hi (inclusive) of k_raw / gate (uint16 [N, 128])."""
+    k_raw = _c(k_raw, np.uint16)
+    gate = _c(gate, np.uint16)
+    out = np.empty(128, np.float32)
+    lib().orc_compress_pool128(_p(k_raw), _p(gate), k_raw.shape[1], int(lo), int(hi), _p(out))
+    return out
+
+
+def compress_k_store(pool, k_raw, gate, boundary, first, ratio, slot_mapping, positions, cos_sin,
+                     rope, norm, dtype, num_pages, page_size, page_stride, gamma=None, beta=None,
+                     eps=1e-6):
+    """Writes the compressed entries into ``pool`` (uint8, in place); returns the rejected count."""
+    assert pool.dtype == np.uint8 and pool.flags.c_contiguous
+    k_raw = _c(k_raw, np.uint16)
+    gate = _c(gate, np.uint16)
+    bnd = _c(boundary, np.int64)
+    fst = _c(first, np.int64)
+    n = bnd.shape[0]
+    slot = _c(slot_mapping, np.int64)
+    pos = _c(positions if positions is not None else np.zeros(n), np.int32)
+    cs = _c(cos_sin if cos_sin is not None else np.zeros((1, 64)), np.float32)
+    g = _c(np.ones(128) if gamma is None else gamma, np.float32)
+    b = _c(np.zeros(128) if beta is None else beta, np.float32)
+    return lib().orc_compress_k_store(_p(k_raw), _p(gate), k_raw.shape[1], _p(bnd), _p(fst), n,
+                                      int(ratio), _p(slot), _p(pos), _p(cs), cs.shape[0], int(rope),
+                                      int(norm), _p(g), _p(b), C.c_float(eps), int(dtype), _p(pool),
+                                      int(num_pages), int(page_size), int(page_stride))

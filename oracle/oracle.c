@@ -20,6 +20,10 @@
  *                operands, K read through the page table. [P1] "Purpose" and
  *                "Performance and accuracy" (scores compared with the exact FP4-dequant
  *                reference); [P2] "Purpose" (in-place paged scoring, no gather).
+ *   Compressor -- softmax-gated overlap pooling of raw K rows -> RMSNorm -> RoPE ->
+ *                quantise -> paged store, one entry per compress-ratio boundary token.
+ *                [P2] "Changes / K write" (the V4 compressor's fused pool/norm/RoPE/MXFP4
+ *                store); readings R13-R16 at orc_compress_k_store.
  *   Top-k     -- per query, indices of the k largest logits among its visible keys.
  *                [P2] "Test Result / GPQA Diamond" (sparse selection of top-k 1024 once
  *                the context passes top-k x compress ratio).
@@ -306,6 +310,144 @@ int orc_k_store(const uint16_t* k, int64_t n_rows, int64_t k_row_stride,
         }
         if (rope != ORC_ROPE_NONE) {
             int32_t pos = positions[r];
+            if (pos < 0 || pos >= max_pos) { ++bad; continue; }
+            orc_rope128(x, cos_sin + (int64_t)pos * 64, rope);
+        }
+        uint8_t* base = pool + page * page_stride;
+        if (dtype == ORC_MXFP4) {
+            uint8_t codes[64], sc[4];
+            orc_mxfp4_quant128(x, codes, sc);
+            for (int j = 0; j < 64; ++j) base[orc_code_offset(dtype, page_size, s, j)] = codes[j];
+            for (int b = 0; b < 4; ++b) base[orc_scale_offset(dtype, page_size, s, b)] = sc[b];
+        } else {
+            uint8_t codes[128];
+            float sc;
+            orc_fp8_quant128(x, codes, &sc);
+            for (int j = 0; j < 128; ++j) base[orc_code_offset(dtype, page_size, s, j)] = codes[j];
+            memcpy(base + orc_scale_offset(dtype, page_size, s, 0), &sc, 4);
+        }
+    }
+    return bad;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Compressor front end: softmax-gated overlap pooling -> norm -> RoPE -> quant -> store  */
+/* ------------------------------------------------------------------------------------ */
+/*
+ * [P2] "Changes / K write": in DeepSeek-V4 the indexer K comes from the indexer's own
+ * compressor; one fused kernel pools (softmax-gated overlap pooling), applies RMSNorm, RoPE
+ * and MXFP4, and stores, one row per boundary token, at compress ratio 4 ([P2] "Purpose").
+ * The pages name the steps, not their formulas; readings taken here:
+ *   R13 entry e pools the raw rows [max(first[e], boundary[e] - 2r + 1), boundary[e]] (its
+ *       own r tokens and the previous r: width 2r, overlap r; clipped at the sequence's
+ *       first token);
+ *   R14 per dimension d the gates of the window go through a softmax: w_i = e_i / S with
+ *       e_i = exp(g_i[d] - max_window g[d]) and S = sum of e_i in token order; the pooled
+ *       value is sum_i w_i * x_i[d] in token order; fp32, every operation rounded once, no
+ *       bf16 rounding of the pooled row (the fused kernel keeps it on chip);
+ *   R15 exp is orc_exp_neg below (both sides use the same method, so the bytes agree);
+ *   R16 RMSNorm: y = (p * (1 / sqrt(S(p*p) / 128 + eps))) * gamma, S the fixed tree of R2.
+ */
+
+/* exp(a) for a <= 0 in fp32 by Cody and Waite's argument reduction and a Taylor polynomial:
+ * n = rint(a * log2(e)); f = (a - n * ln2_hi) - n * ln2_lo, with ln2 split so that n * ln2_hi
+ * is exact; e^f = 1 + f + f^2/2! + ... + f^7/7! by Horner's rule; the result is e^f * 2^n.
+ * Every product and sum is one rounded fp32 operation. Below -87 (where e^a nears the smallest
+ * normal fp32) the result is 0. */
+float orc_exp_neg(float a) {
+    if (!(a > -87.0f)) return 0.0f;
+    if (a > 0.0f) a = 0.0f;
+    const float log2e = 1.44269504f;
+    const float ln2_hi = 0.693145752f; /* 0x3f317200: 16 significant bits */
+    const float ln2_lo = 1.42860677e-06f;
+    float t = a * log2e;
+    float n = rintf(t);
+    float f = a - n * ln2_hi;
+    float nl = n * ln2_lo;
+    f = f - nl;
+    const float c[8] = {1.0f, 1.0f, 0.5f, 1.0f / 6.0f, 1.0f / 24.0f, 1.0f / 120.0f, 1.0f / 720.0f,
+                        1.0f / 5040.0f};
+    float p = c[7];
+    for (int i = 6; i >= 0; --i) {
+        float pf = p * f;
+        p = pf + c[i];
+    }
+    int ni = (int)n;
+    float two_n = bits_to_f32((uint32_t)(ni + 127) << 23); /* n >= -126 here */
+    return p * two_n;
+}
+
+/* RMSNorm over D = 128 (reading R16). */
+void orc_rmsnorm128(const float* x, const float* gamma, float eps, float* y) {
+    const float inv_d = 0.0078125f;
+    float sq[128];
+    for (int i = 0; i < 128; ++i) sq[i] = x[i] * x[i];
+    float ms = tree_sum128(sq) * inv_d;
+    float t = ms + eps;
+    float s = sqrtf(t);
+    float rstd = 1.0f / s;
+    for (int i = 0; i < 128; ++i) {
+        float a = x[i] * rstd;
+        y[i] = a * gamma[i];
+    }
+}
+
+/* Softmax-gated pooling of raw rows lo..hi (inclusive) of k_raw / gate (readings R14, R15). */
+void orc_compress_pool128(const uint16_t* k_raw, const uint16_t* gate, int64_t row_stride,
+                          int64_t lo, int64_t hi, float* out) {
+    for (int d = 0; d < 128; ++d) {
+        float m = bf16_to_f32(gate[lo * row_stride + d]);
+        for (int64_t i = lo + 1; i <= hi; ++i) {
+            float g = bf16_to_f32(gate[i * row_stride + d]);
+            if (g > m) m = g;
+        }
+        float sum = 0.0f;
+        for (int64_t i = lo; i <= hi; ++i) {
+            float g = bf16_to_f32(gate[i * row_stride + d]);
+            sum = sum + orc_exp_neg(g - m);
+        }
+        float p = 0.0f;
+        for (int64_t i = lo; i <= hi; ++i) {
+            float g = bf16_to_f32(gate[i * row_stride + d]);
+            float w = orc_exp_neg(g - m) / sum;
+            float wx = w * bf16_to_f32(k_raw[i * row_stride + d]);
+            p = p + wx;
+        }
+        out[d] = p;
+    }
+}
+
+/* The compressed K store: for entry e, pool the window of reading R13, normalise (norm 0
+ * none, 1 LayerNorm (R2), 2 RMSNorm (R16)), RoPE at positions[e], quantise and write at
+ * slot_mapping[e] as orc_k_store does. Returns the number of rejected entries. */
+int orc_compress_k_store(const uint16_t* k_raw, const uint16_t* gate, int64_t row_stride,
+                         const int64_t* boundary, const int64_t* first, int64_t n_entries,
+                         int32_t ratio, const int64_t* slot_mapping, const int32_t* positions,
+                         const float* cos_sin, int32_t max_pos, int rope, int norm,
+                         const float* gamma, const float* beta, float eps, int dtype,
+                         uint8_t* pool, int64_t num_pages, int32_t page_size,
+                         int64_t page_stride) {
+    int bad = 0;
+    for (int64_t e = 0; e < n_entries; ++e) {
+        int64_t slot = slot_mapping[e];
+        if (slot < 0) continue;
+        int64_t page = slot / page_size;
+        int s = (int)(slot % page_size);
+        if (page >= num_pages) { ++bad; continue; }
+        int64_t hi = boundary[e];
+        int64_t lo = hi - 2 * (int64_t)ratio + 1;
+        if (lo < first[e]) lo = first[e];
+        float x[128], y[128];
+        orc_compress_pool128(k_raw, gate, row_stride, lo, hi, x);
+        if (norm == 1) {
+            orc_layernorm128(x, gamma, beta, eps, y);
+            memcpy(x, y, sizeof x);
+        } else if (norm == 2) {
+            orc_rmsnorm128(x, gamma, eps, y);
+            memcpy(x, y, sizeof x);
+        }
+        if (rope != ORC_ROPE_NONE) {
+            int32_t pos = positions[e];
             if (pos < 0 || pos >= max_pos) { ++bad; continue; }
             orc_rope128(x, cos_sin + (int64_t)pos * 64, rope);
         }

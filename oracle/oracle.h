@@ -63,6 +63,19 @@ int orc_k_store(const uint16_t* k, int64_t n_rows, int64_t k_row_stride,
                 const float* gamma, const float* beta, float eps, int dtype,
                 uint8_t* pool, int64_t num_pages, int32_t page_size, int64_t page_stride);
 
+/* compressor front end (see oracle.c, readings R13-R16) */
+float orc_exp_neg(float a);
+void orc_rmsnorm128(const float* x, const float* gamma, float eps, float* y);
+void orc_compress_pool128(const uint16_t* k_raw, const uint16_t* gate, int64_t row_stride,
+                          int64_t lo, int64_t hi, float* out);
+int orc_compress_k_store(const uint16_t* k_raw, const uint16_t* gate, int64_t row_stride,
+                         const int64_t* boundary, const int64_t* first, int64_t n_entries,
+                         int32_t ratio, const int64_t* slot_mapping, const int32_t* positions,
+                         const float* cos_sin, int32_t max_pos, int rope, int norm,
+                         const float* gamma, const float* beta, float eps, int dtype,
+                         uint8_t* pool, int64_t num_pages, int32_t page_size,
+                         int64_t page_stride);
+
 int orc_q_quant(const uint16_t* q, int64_t T, int32_t H, const int32_t* positions,
                 const float* cos_sin, int32_t max_pos, int rope, const float* w_in,
                 float softmax_scale, float head_scale, int dtype, uint8_t* q_codes,
