@@ -84,7 +84,7 @@ def _declare(L):
     L.orc_rmsnorm128.argtypes = [vp, vp, f32, vp]; L.orc_rmsnorm128.restype = None
     L.orc_compress_pool128.argtypes = [vp, vp, i64, i64, i64, vp]
     L.orc_compress_pool128.restype = None
-    L.orc_compress_k_store.argtypes = [vp, vp, i64, vp, vp, i64, i32, vp, vp, vp, i32, C.c_int,
+    L.orc_compress_k_store.argtypes = [vp, vp, i64, i64, vp, vp, i64, i32, vp, vp, vp, i32, C.c_int,
                                        C.c_int, vp, vp, f32, C.c_int, vp, i64, i32, i64]
     L.orc_compress_k_store.restype = C.c_int
     L.orc_mqa_logits.argtypes = [vp, vp, vp, i64, i32, C.c_int, vp, i64, i32, i64, vp, i32,
@@ -300,7 +300,7 @@ def compress_k_store(pool, k_raw, gate, boundary, first, ratio, slot_mapping, po
     cs = _c(cos_sin if cos_sin is not None else np.zeros((1, 64)), np.float32)
     g = _c(np.ones(128) if gamma is None else gamma, np.float32)
     b = _c(np.zeros(128) if beta is None else beta, np.float32)
-    return lib().orc_compress_k_store(_p(k_raw), _p(gate), k_raw.shape[1], _p(bnd), _p(fst), n,
+    return lib().orc_compress_k_store(_p(k_raw), _p(gate), k_raw.shape[0], k_raw.shape[1], _p(bnd), _p(fst), n,
                                       int(ratio), _p(slot), _p(pos), _p(cs), cs.shape[0], int(rope),
                                       int(norm), _p(g), _p(b), C.c_float(eps), int(dtype), _p(pool),
                                       int(num_pages), int(page_size), int(page_stride))

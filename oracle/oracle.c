@@ -341,37 +341,35 @@ int orc_k_store(const uint16_t* k, int64_t n_rows, int64_t k_row_stride,
  *   R13 entry e pools the raw rows [max(first[e], boundary[e] - 2r + 1), boundary[e]] (its
  *       own r tokens and the previous r: width 2r, overlap r; clipped at the sequence's
  *       first token);
- *   R14 per dimension d the gates of the window go through a softmax: w_i = e_i / S with
- *       e_i = exp(g_i[d] - max_window g[d]) and S = sum of e_i in token order; the pooled
- *       value is sum_i w_i * x_i[d] in token order; fp32, every operation rounded once, no
- *       bf16 rounding of the pooled row (the fused kernel keeps it on chip);
+ *   R14 per dimension d the gates of the window weight its rows by a softmax: with
+ *       m = max_window g[d], e_i = exp(g_i[d] - m), S = sum_i e_i and P = sum_i e_i * x_i[d]
+ *       (both in token order, P by fused multiply-adds), the pooled value is P / S, one
+ *       division after the sums (the softmax-weighted sum with its normalisation taken out
+ *       of the sum); fp32, no bf16 rounding of the pooled row (the fused kernel keeps it on
+ *       chip);
  *   R15 exp is orc_exp_neg below (both sides use the same method, so the bytes agree);
  *   R16 RMSNorm: y = (p * (1 / sqrt(S(p*p) / 128 + eps))) * gamma, S the fixed tree of R2.
  */
 
 /* exp(a) for a <= 0 in fp32 by Cody and Waite's argument reduction and a Taylor polynomial:
- * n = rint(a * log2(e)); f = (a - n * ln2_hi) - n * ln2_lo, with ln2 split so that n * ln2_hi
- * is exact; e^f = 1 + f + f^2/2! + ... + f^7/7! by Horner's rule; the result is e^f * 2^n.
- * Every product and sum is one rounded fp32 operation. Below -87 (where e^a nears the smallest
- * normal fp32) the result is 0. */
+ * n = rint(a * log2(e)); f = (a - n * ln2_hi) - n * ln2_lo with ln2 split so that n * ln2_hi
+ * is exact (each step one fused multiply-add); e^f = 1 + f + f^2/2! + ... + f^7/7! by Horner's
+ * rule in fused multiply-adds; the result is e^f * 2^n. fmaf rounds once (C99), so the value
+ * is the same on every IEEE machine. Below -87 (where e^a nears the smallest normal fp32) the
+ * result is 0. */
 float orc_exp_neg(float a) {
     if (!(a > -87.0f)) return 0.0f;
     if (a > 0.0f) a = 0.0f;
     const float log2e = 1.44269504f;
     const float ln2_hi = 0.693145752f; /* 0x3f317200: 16 significant bits */
     const float ln2_lo = 1.42860677e-06f;
-    float t = a * log2e;
-    float n = rintf(t);
-    float f = a - n * ln2_hi;
-    float nl = n * ln2_lo;
-    f = f - nl;
+    float n = rintf(a * log2e);
+    float f = fmaf(-n, ln2_hi, a);
+    f = fmaf(-n, ln2_lo, f);
     const float c[8] = {1.0f, 1.0f, 0.5f, 1.0f / 6.0f, 1.0f / 24.0f, 1.0f / 120.0f, 1.0f / 720.0f,
                         1.0f / 5040.0f};
     float p = c[7];
-    for (int i = 6; i >= 0; --i) {
-        float pf = p * f;
-        p = pf + c[i];
-    }
+    for (int i = 6; i >= 0; --i) p = fmaf(p, f, c[i]);
     int ni = (int)n;
     float two_n = bits_to_f32((uint32_t)(ni + 127) << 23); /* n >= -126 here */
     return p * two_n;
@@ -397,30 +395,24 @@ void orc_compress_pool128(const uint16_t* k_raw, const uint16_t* gate, int64_t r
                           int64_t lo, int64_t hi, float* out) {
     for (int d = 0; d < 128; ++d) {
         float m = bf16_to_f32(gate[lo * row_stride + d]);
-        for (int64_t i = lo + 1; i <= hi; ++i) {
-            float g = bf16_to_f32(gate[i * row_stride + d]);
-            if (g > m) m = g;
-        }
-        float sum = 0.0f;
+        for (int64_t i = lo + 1; i <= hi; ++i) m = fmaxf(m, bf16_to_f32(gate[i * row_stride + d]));
+        float sum = 0.0f, acc = 0.0f;
         for (int64_t i = lo; i <= hi; ++i) {
-            float g = bf16_to_f32(gate[i * row_stride + d]);
-            sum = sum + orc_exp_neg(g - m);
+            float e = orc_exp_neg(bf16_to_f32(gate[i * row_stride + d]) - m);
+            sum = sum + e;
+            acc = fmaf(e, bf16_to_f32(k_raw[i * row_stride + d]), acc);
         }
-        float p = 0.0f;
-        for (int64_t i = lo; i <= hi; ++i) {
-            float g = bf16_to_f32(gate[i * row_stride + d]);
-            float w = orc_exp_neg(g - m) / sum;
-            float wx = w * bf16_to_f32(k_raw[i * row_stride + d]);
-            p = p + wx;
-        }
-        out[d] = p;
+        out[d] = acc / sum;
     }
 }
 
 /* The compressed K store: for entry e, pool the window of reading R13, normalise (norm 0
  * none, 1 LayerNorm (R2), 2 RMSNorm (R16)), RoPE at positions[e], quantise and write at
- * slot_mapping[e] as orc_k_store does. Returns the number of rejected entries. */
-int orc_compress_k_store(const uint16_t* k_raw, const uint16_t* gate, int64_t row_stride,
+ * slot_mapping[e] as orc_k_store does. An entry whose slot is negative is skipped; one whose
+ * slot is past the pool, whose position is outside the table, or whose window is not inside
+ * the n_raw rows (0 <= first[e] <= boundary[e] < n_raw) is rejected. Returns the number of
+ * rejected entries. */
+int orc_compress_k_store(const uint16_t* k_raw, const uint16_t* gate, int64_t n_raw, int64_t row_stride,
                          const int64_t* boundary, const int64_t* first, int64_t n_entries,
                          int32_t ratio, const int64_t* slot_mapping, const int32_t* positions,
                          const float* cos_sin, int32_t max_pos, int rope, int norm,
@@ -435,6 +427,7 @@ int orc_compress_k_store(const uint16_t* k_raw, const uint16_t* gate, int64_t ro
         int s = (int)(slot % page_size);
         if (page >= num_pages) { ++bad; continue; }
         int64_t hi = boundary[e];
+        if (first[e] < 0 || first[e] > hi || hi >= n_raw) { ++bad; continue; }
         int64_t lo = hi - 2 * (int64_t)ratio + 1;
         if (lo < first[e]) lo = first[e];
         float x[128], y[128];

@@ -68,7 +68,7 @@ float orc_exp_neg(float a);
 void orc_rmsnorm128(const float* x, const float* gamma, float eps, float* y);
 void orc_compress_pool128(const uint16_t* k_raw, const uint16_t* gate, int64_t row_stride,
                           int64_t lo, int64_t hi, float* out);
-int orc_compress_k_store(const uint16_t* k_raw, const uint16_t* gate, int64_t row_stride,
+int orc_compress_k_store(const uint16_t* k_raw, const uint16_t* gate, int64_t n_raw, int64_t row_stride,
                          const int64_t* boundary, const int64_t* first, int64_t n_entries,
                          int32_t ratio, const int64_t* slot_mapping, const int32_t* positions,
                          const float* cos_sin, int32_t max_pos, int rope, int norm,
