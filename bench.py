@@ -387,6 +387,8 @@ def run_gpu(args, rank, world):
     if is_decode(wl) and args.config == "decode_b64" and not args.no_prefill:
         line["prefill"] = prefill_block(args, dev, peaks, peak_kind)
         line["qk_prep_sweep"] = qk_prep_sweep(args, dev, peaks)
+    if args.config == "decode_b64" and not args.no_compress:
+        line["compress"] = compress_block(args, dev, peaks)
     if not args.no_probe:
         line["tensor_probe"] = tensor_probe(torch, stream)
         if "prefill" in line:
@@ -456,6 +458,70 @@ def prefill_block(args, dev, peaks, peak_kind):
            "roofline": prefill_roofline(wl, kernel_ms["scorer"], peaks, peak_kind),
            "l2": f"inputs rotate over {copies} copies of cache+Q"}
     del rep
+    torch.cuda.empty_cache()
+    return out
+
+
+# thread instructions of the pooling per (window row, dimension): gate max 1, difference 1,
+# exp 14 (product, rint, 2 reduction and 7 Horner fused multiply-adds, 2 to build 2^n, product),
+# sum 1, fused multiply-add of the weighted row 1
+COMPRESS_OPS_PER_ROW_DIM = 18
+
+
+def compress_block(args, dev, peaks):
+    """The compressed K store (idx_compress_k_store) over whole contexts: 256 sequences of raw
+    length uniform in [1024, 9472], ratio 4, RMSNorm, NeoX RoPE, MXFP4 into 64-entry pages.
+    Inputs (bf16 K and gate rows, 512 B per raw row) are larger than L2."""
+    import torch
+    from sparse_attention_indexer_mqa_gb300 import binding as Bn
+    cw = W.compress_b256(seed=args.seed)
+
+    def d(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+
+    k_raw, gate = d(cw.k_raw), d(cw.gate)
+    bnd, fst, slot, pos = d(cw.boundary), d(cw.first), d(cw.slot_mapping), d(cw.positions)
+    cs, gam = d(cw.cos_sin), d(cw.gamma)
+    pool = torch.zeros(cw.pool_pages * cw.page_stride, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call(i=0):
+        Bn.idx_compress_k_store(k_raw, gate, bnd, fst, cw.ratio, slot, pos, cs, cw.rope, cw.norm,
+                                cw.dtype, pool, cw.pool_pages, cw.page_size, cw.page_stride,
+                                gamma=gam, dev_status=status)
+
+    for i in range(3):
+        call()
+    torch.cuda.synchronize()
+    k = max(3, min(args.steps, 20))
+    g = capture(torch, call, k)
+    g.replay()
+    torch.cuda.synchronize()
+    ms = time_graph(torch, g, stream) / k
+    n_raw, E = int(cw.k_raw.shape[0]), cw.n_entries
+    win_rows = int(np.sum(cw.boundary - np.maximum(cw.first, cw.boundary - 2 * cw.ratio + 1) + 1))
+    # every raw row once (K and gate), the entry's indices (slot, boundary, first, position) and
+    # its 68 B store; the overlapping windows re-read rows from cache, not from HBM
+    ab = n_raw * 512 + E * (8 + 8 + 8 + 4 + 68)
+    ops = float(win_rows) * 128 * COMPRESS_OPS_PER_ROW_DIM
+    t = ms / 1e3
+    out = {"workload": cw.name, "raw_rows": n_raw, "entries": E, "window_rows": win_rows, "steps": k,
+           "us": round(ms * 1e3, 2), "entries_per_s": round(E / t, 1),
+           "raw_rows_per_s": round(n_raw / t, 1),
+           "roofline": {"kernel": "compress", "bound": "alu",
+                        "achieved": round(ops / t / 1e12, 2), "peak": round(alu_peak_ops(peaks) / 1e12, 2),
+                        "unit": "T instr/s", "frac": round(ops / t / alu_peak_ops(peaks), 4),
+                        "algorithmic_ops": ops, "ops_per_row_dim": COMPRESS_OPS_PER_ROW_DIM,
+                        "peak_source": "issue rate 4x32 lanes x 152 SMs x measured max SM clock",
+                        "hbm": {"achieved_gbs": round(ab / t / 1e9, 1), "peak_gbs": peaks["hbm_gbs"],
+                                "frac": round(ab / t / 1e9 / peaks["hbm_gbs"], 4),
+                                "algorithmic_bytes": ab},
+                        "traffic": profile_traffic("compress:compress_b256", COMPRESS_SOURCES)},
+           "status": int(status.item()),
+           "l2": f"inputs {2 * n_raw * 256 / 2**20:.0f} MiB > L2"}
+    del k_raw, gate, pool, g
     torch.cuda.empty_cache()
     return out
 
@@ -721,6 +787,9 @@ SCORER_SOURCES = ["sparse_attention_indexer_mqa_gb300/csrc/scorer_decode.cu",
                   "sparse_attention_indexer_mqa_gb300/csrc/common.cuh",
                   "sparse_attention_indexer_mqa_gb300/csrc/select.cuh",
                   "sparse_attention_indexer_mqa_gb300/csrc/kernels.h"]
+COMPRESS_SOURCES = ["sparse_attention_indexer_mqa_gb300/csrc/quant.cu",
+                    "sparse_attention_indexer_mqa_gb300/csrc/common.cuh",
+                    "sparse_attention_indexer_mqa_gb300/csrc/kernels.h"]
 
 
 def main():
@@ -736,6 +805,7 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=8)
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill block of the default run")
     ap.add_argument("--no-probe", action="store_true", help="skip the tensor-core rate probe")
+    ap.add_argument("--no-compress", action="store_true", help="skip the compressed K store block")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

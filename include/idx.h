@@ -145,6 +145,41 @@ int idx_q_quant(const uint16_t* q, int64_t T, int32_t H, const int32_t* position
                 void* q_scales, float* w_out, int32_t* dev_status, cudaStream_t stream);
 
 /*
+ * Compressed K store, the DeepSeek-V4 indexer's K write ([P2] "Changes / K write": the
+ * indexer K comes from its own compressor; one fused kernel pools the raw rows by
+ * softmax-gated overlap pooling, applies RMSNorm, RoPE and the quantisation, and stores,
+ * with nothing before the norm reaching memory; [P2] "Purpose": compress ratio 4, 64-entry
+ * pages). One cache entry per boundary token:
+ *   k_raw, gate: bf16 [n_raw][row_stride] (the first 128 of each row used), 16-byte aligned,
+ *     row_stride >= 128 and a multiple of 8 (the two share the stride);
+ *   boundary, first: int64 [n_entries]; entry e pools rows lo..hi with hi = boundary[e] and
+ *     lo = max(first[e], hi - 2*ratio + 1) (its own ratio rows and the ratio rows before them,
+ *     clipped at first[e], the first raw row of the entry's sequence);
+ *   per dimension d: m = max of gate[i][d] over the window, w_i = exp(gate[i][d] - m),
+ *     pooled[d] = (sum_i w_i * k_raw[i][d]) / (sum_i w_i), sums in row order;
+ *   then norm (0 none, 1 LayerNorm as in idx_k_store, 2 RMSNorm:
+ *     y = (x * (1 / sqrt(sum(x^2) / 128 + eps))) * gamma), RoPE at positions[e], the
+ *     quantisation and the paged write at slot_mapping[e], all as in idx_k_store.
+ * Arithmetic: fp32, the pooled row is not rounded to bf16; exp is Cody-Waite reduction plus a
+ *   degree-7 Taylor polynomial in fused multiply-adds (<= 1 ulp on [-87, 0], 0 below -87);
+ *   the sum of w_i * k_raw by fused multiply-adds, every other operation rounded once; the
+ *   bytes are a function of the inputs alone (the launch shape does not change them).
+ * ratio: 1..128 (IDX_EUNSUPPORTED otherwise). slot_mapping[e] < 0 skips the entry. An entry
+ *   whose slot is past the pool sets IDX_STATUS_BAD_SLOT, whose window is not inside the raw
+ *   rows (first[e] < 0, first[e] > boundary[e] or boundary[e] >= n_raw) sets
+ *   IDX_STATUS_BAD_LEN, whose position is outside [0, max_pos) sets IDX_STATUS_BAD_POS; such
+ *   entries are not written. Other arguments as in idx_k_store (gamma/beta may be NULL:
+ *   1 and 0). Reads k_raw, gate and the index arrays; writes only the entries' slots.
+ */
+int idx_compress_k_store(const uint16_t* k_raw, const uint16_t* gate, int64_t n_raw, int64_t row_stride,
+                         const int64_t* boundary, const int64_t* first, int64_t n_entries,
+                         int32_t ratio, const int64_t* slot_mapping, const int32_t* positions,
+                         const float* cos_sin, int32_t max_pos, int32_t rope, int32_t norm,
+                         const float* gamma, const float* beta, float eps, int32_t dtype, void* pool,
+                         int64_t num_pages, int32_t page_size, int64_t page_stride,
+                         int32_t* dev_status, cudaStream_t stream);
+
+/*
  * K store and Q quant in one launch ([P3] "Purpose": the indexer's QK pre-processing as a
  * single fused kernel instead of separate launches). Computes exactly what idx_k_store(k,
  * n_rows, k_row_stride, slot_mapping, k_positions, cos_sin, max_pos, k_rope, apply_norm,

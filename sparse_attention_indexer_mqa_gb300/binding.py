@@ -85,9 +85,11 @@ def _declare(L):
     L.idx_debug_mma_rate.argtypes = [i32, i32, vp, C.POINTER(C.c_double), vp]
     L.idx_mqa_topk_paged_noalloc.argtypes = [vp, vp, vp, i64, i32, i32, vp, i64, i32, i64, vp, i32,
                                              vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
+    L.idx_compress_k_store.argtypes = [vp, vp, i64, i64, vp, vp, i64, i32, vp, vp, vp, i32, i32, i32,
+                                       vp, vp, f32, i32, vp, i64, i32, i64, vp, vp]
     for n in ("idx_cache_layout", "idx_k_store", "idx_q_quant", "idx_qk_prep", "idx_mqa_logits_paged",
               "idx_topk", "idx_debug_encode", "idx_mqa_topk_workspace_bytes", "idx_mqa_topk_paged",
-              "idx_debug_mma_rate", "idx_mqa_topk_paged_noalloc"):
+              "idx_debug_mma_rate", "idx_mqa_topk_paged_noalloc", "idx_compress_k_store"):
         getattr(L, n).restype = C.c_int
 
 
@@ -136,6 +138,20 @@ def idx_k_store(k, slot_mapping, positions, cos_sin, rope, apply_norm, dtype, po
         _ptr(k), n, stride, _ptr(slot_mapping), _ptr(positions), _ptr(cos_sin), max_pos, rope,
         int(apply_norm), _ptr(gamma), _ptr(beta), eps, dtype, _ptr(pool), num_pages, page_size,
         page_stride, _ptr(dev_status), _stream(stream)))
+
+
+def idx_compress_k_store(k_raw, gate, boundary, first, ratio, slot_mapping, positions, cos_sin, rope,
+                         norm, dtype, pool, num_pages, page_size, page_stride, gamma=None, beta=None,
+                         eps=1e-6, dev_status=None, stream=None, n_entries=None):
+    """k_raw / gate: bf16 (int16/uint16 storage) [n_raw, >=128] sharing one row stride."""
+    assert k_raw.stride(0) == gate.stride(0) and k_raw.shape[0] == gate.shape[0]
+    n = boundary.shape[0] if n_entries is None else n_entries
+    max_pos = cos_sin.shape[0] if cos_sin is not None else 0
+    _check("idx_compress_k_store", load().idx_compress_k_store(
+        _ptr(k_raw), _ptr(gate), k_raw.shape[0], k_raw.stride(0), _ptr(boundary), _ptr(first), n,
+        int(ratio), _ptr(slot_mapping), _ptr(positions), _ptr(cos_sin), max_pos, rope, int(norm),
+        _ptr(gamma), _ptr(beta), eps, dtype, _ptr(pool), num_pages, page_size, page_stride,
+        _ptr(dev_status), _stream(stream)))
 
 
 def idx_q_quant(q, positions, cos_sin, rope, w_in, softmax_scale, head_scale, dtype, q_codes,

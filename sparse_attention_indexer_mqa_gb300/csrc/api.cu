@@ -144,6 +144,36 @@ int idx_k_store(const uint16_t* k, int64_t n_rows, int64_t k_row_stride,
     return cuda_status(idx::launch_k_store(a, stream));
 }
 
+int idx_compress_k_store(const uint16_t* k_raw, const uint16_t* gate, int64_t n_raw, int64_t row_stride,
+                         const int64_t* boundary, const int64_t* first, int64_t n_entries,
+                         int32_t ratio, const int64_t* slot_mapping, const int32_t* positions,
+                         const float* cos_sin, int32_t max_pos, int32_t rope, int32_t norm,
+                         const float* gamma, const float* beta, float eps, int32_t dtype, void* pool,
+                         int64_t num_pages, int32_t page_size, int64_t page_stride,
+                         int32_t* dev_status, cudaStream_t stream) {
+    Range r("idx_compress_k_store");
+    if (n_raw < 0 || n_entries < 0 || !valid_rope(rope) || norm < 0 || norm > 2) return IDX_EINVAL;
+    const int st = check_pool(dtype, pool, num_pages, page_size, page_stride);
+    if (st != IDX_OK) return st;
+    if (ratio < 1 || ratio > 128) return IDX_EUNSUPPORTED;
+    if (n_entries == 0) return IDX_OK;
+    if (!boundary || !first || !slot_mapping) return IDX_EINVAL;
+    if (n_raw > 0 && (!k_raw || !gate || !aligned(k_raw, 16) || !aligned(gate, 16))) return IDX_EINVAL;
+    if (row_stride < 128 || row_stride % 8 != 0) return IDX_EINVAL;
+    if (rope != IDX_ROPE_NONE && (!positions || !cos_sin || !aligned(cos_sin, 16) || max_pos <= 0))
+        return IDX_EINVAL;
+    if (norm && !(eps >= 0.0f && std::isfinite(eps))) return IDX_EINVAL;
+    idx::CompressArgs a{};
+    a.k_raw = k_raw; a.gate = gate; a.n_raw = n_raw; a.row_stride = row_stride;
+    a.boundary = boundary; a.first = first; a.n_entries = n_entries; a.ratio = ratio;
+    a.slot_mapping = slot_mapping; a.positions = positions; a.cos_sin = cos_sin;
+    a.max_pos = max_pos; a.rope = rope; a.norm = norm; a.dtype = dtype;
+    a.gamma = gamma; a.beta = beta; a.eps = eps;
+    a.pool = static_cast<uint8_t*>(pool); a.num_pages = num_pages; a.page_size = page_size;
+    a.page_stride = page_stride; a.dev_status = dev_status;
+    return cuda_status(idx::launch_compress(a, stream));
+}
+
 int idx_q_quant(const uint16_t* q, int64_t T, int32_t H, const int32_t* positions,
                 const float* cos_sin, int32_t max_pos, int32_t rope, const float* w_in,
                 float softmax_scale, float head_scale, int32_t dtype, uint8_t* q_codes,

@@ -24,6 +24,29 @@ struct KStoreArgs {
     int32_t* dev_status;
 };
 
+// Compressed K store: entries pool raw rows (see idx_compress_k_store).
+struct CompressArgs {
+    const uint16_t* k_raw;
+    const uint16_t* gate;
+    int64_t n_raw, row_stride;
+    const int64_t* boundary;
+    const int64_t* first;
+    int64_t n_entries;
+    int32_t ratio;
+    const int64_t* slot_mapping;
+    const int32_t* positions;
+    const float* cos_sin;
+    int32_t max_pos, rope, norm, dtype;
+    const float* gamma;
+    const float* beta;
+    float eps;
+    uint8_t* pool;
+    int64_t num_pages;
+    int32_t page_size;
+    int64_t page_stride;
+    int32_t* dev_status;
+};
+
 struct QQuantArgs {
     const uint16_t* q;
     int64_t T;  // tokens; each has H heads (Hq = H rounded up to 8 in the image)
@@ -79,6 +102,7 @@ struct TopkArgs {
 cudaError_t launch_k_store(const KStoreArgs& a, cudaStream_t st);
 cudaError_t launch_q_quant(const QQuantArgs& a, cudaStream_t st);
 cudaError_t launch_qk_prep(const KStoreArgs& ka, const QQuantArgs& qa, cudaStream_t st);
+cudaError_t launch_compress(const CompressArgs& a, cudaStream_t st);
 cudaError_t launch_debug_encode(int kind, const float* in, int64_t n, uint8_t* out, cudaStream_t st);
 cudaError_t launch_scorer(const ScoreArgs& a, cudaStream_t st);
 cudaError_t launch_scorer_decode(const ScoreArgs& a, cudaStream_t st);

@@ -7,7 +7,10 @@
 // them with one fused kernel; vllm PR 60834 "Changes / K write" and "Q quant" do the same
 // for MXFP4 (norm -> RoPE -> MXFP4 -> preshuffled pages; RoPE -> MXFP4 with the softmax
 // and head scales folded into fp32 weights). Each of the two steps is one kernel, and
-// qk_prep_kernel runs both in a single launch (one block range each).
+// qk_prep_kernel runs both in a single launch (one block range each). compress_kernel is the
+// DeepSeek-V4 form of the K store (vllm PR 60834 "Changes / K write": the indexer's own
+// compressor pools raw rows, then RMSNorm -> RoPE -> MXFP4 -> store in one kernel, nothing
+// before the norm reaching memory): one entry per compress-ratio boundary token.
 //
 // Mapping: 16 threads per 128-element row, 8 consecutive elements (one 16-byte load of
 // bf16) per thread; a 256-thread CTA handles 16 rows. Reductions use a fixed tree (group
@@ -59,6 +62,42 @@ __device__ __forceinline__ void layernorm(float* x, int l16, const float* gamma,
         float b = beta ? __ldg(beta + 8 * l16 + i) : 0.0f;
         x[i] = __fadd_rn(__fmul_rn(__fmul_rn(d[i], rstd), g), b);
     }
+}
+
+// RMSNorm: x * (1 / sqrt(mean(x^2) + eps)) * gamma, each op rounded, the same fixed tree.
+__device__ __forceinline__ void rmsnorm(float* x, int l16, const float* gamma, float eps) {
+    const float inv_d = 0.0078125f;
+    float sq[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sq[i] = __fmul_rn(x[i], x[i]);
+    const float ms = __fmul_rn(row_sum(sq), inv_d);
+    const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float g = gamma ? __ldg(gamma + 8 * l16 + i) : 1.0f;
+        x[i] = __fmul_rn(__fmul_rn(x[i], rstd), g);
+    }
+}
+
+// exp(a) for a <= 0 by Cody and Waite's argument reduction and a degree-7 Taylor polynomial
+// (one fused multiply-add per step): n = rint(a log2 e), f = (a - n ln2_hi) - n ln2_lo with
+// ln2_hi holding 16 significant bits so that n ln2_hi is exact, e^f by Horner's rule, the
+// result e^f * 2^n. At most 0.86 ulp from exp over [-87, 0]; 0 below -87.
+__device__ __forceinline__ float exp_neg(float a) {
+    if (!(a > -87.0f)) return 0.0f;
+    if (a > 0.0f) a = 0.0f;
+    const float n = rintf(__fmul_rn(a, 1.44269504f));
+    float f = __fmaf_rn(-n, 0.693145752f, a);
+    f = __fmaf_rn(-n, 1.42860677e-06f, f);
+    float p = 1.0f / 5040.0f;
+    p = __fmaf_rn(p, f, 1.0f / 720.0f);
+    p = __fmaf_rn(p, f, 1.0f / 120.0f);
+    p = __fmaf_rn(p, f, 1.0f / 24.0f);
+    p = __fmaf_rn(p, f, 1.0f / 6.0f);
+    p = __fmaf_rn(p, f, 0.5f);
+    p = __fmaf_rn(p, f, 1.0f);
+    p = __fmaf_rn(p, f, 1.0f);
+    return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));  // n >= -126 here
 }
 
 // RoPE on dims 0..63 (lanes 0..7 of the row). NeoX pairs dims (i, i+32): lane l < 4 holds
@@ -138,6 +177,46 @@ __device__ __forceinline__ void unpack8(const uint4 v, float* x) {
     x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
 }
 
+// Quantise a row held 8 values per lane by 16 lanes and, if ok, write its codes and scale(s)
+// into slot s of the page at base. Every lane of the row takes part (shuffles).
+template <int kDtype>
+__device__ __forceinline__ void quant_store(const float* x, int l16, bool ok, uint8_t* base, int page_size,
+                                            int s) {
+    if (kDtype == IDX_MXFP4) {
+        uint32_t word, sbyte;
+        mx_quant(x, word, sbyte);
+        pdl_wait();  // the cache may still be read by the previous kernel
+        pdl_launch_dependents();
+        // gather the 4 words of a 16-byte chunk (= one scale block) into its first lane
+        uint32_t w1 = __shfl_down_sync(kFull, word, 1);
+        uint32_t w2 = __shfl_down_sync(kFull, word, 2);
+        uint32_t w3 = __shfl_down_sync(kFull, word, 3);
+        uint32_t s1 = __shfl_down_sync(kFull, sbyte, 4);
+        uint32_t s2 = __shfl_down_sync(kFull, sbyte, 8);
+        uint32_t s3 = __shfl_down_sync(kFull, sbyte, 12);
+        if (ok && (l16 & 3) == 0) {
+            *reinterpret_cast<uint4*>(base + mx_chunk_off(page_size, s, l16 >> 2)) =
+                make_uint4(word, w1, w2, w3);
+        }
+        if (ok && l16 == 0) {
+            *reinterpret_cast<uint32_t*>(base + mx_scale_off(page_size, s)) =
+                sbyte | (s1 << 8) | (s2 << 16) | (s3 << 24);
+        }
+    } else {
+        uint32_t lo, hi;
+        float scale;
+        f8_quant(x, lo, hi, scale);
+        pdl_wait();
+        pdl_launch_dependents();
+        uint32_t plo = __shfl_down_sync(kFull, lo, 1);
+        uint32_t phi = __shfl_down_sync(kFull, hi, 1);
+        if (ok && (l16 & 1) == 0) {
+            *reinterpret_cast<uint4*>(base + f8_chunk_off(s, l16 >> 1)) = make_uint4(lo, hi, plo, phi);
+        }
+        if (ok && l16 == 0) *reinterpret_cast<float*>(base + f8_scale_off(page_size, s)) = scale;
+    }
+}
+
 // K store of the 16 rows of block `blk` (one row per 16 lanes).
 template <int kDtype>
 __device__ __forceinline__ void k_store_rows(const KStoreArgs& a, int64_t blk) {
@@ -168,40 +247,79 @@ __device__ __forceinline__ void k_store_rows(const KStoreArgs& a, int64_t blk) {
     if (a.apply_norm) layernorm(x, l16, a.gamma, a.beta, a.eps);
     if (a.rope != IDX_ROPE_NONE) rope(x, l16, a.cos_sin + (int64_t)pos * 64, a.rope);
 
-    uint8_t* base = a.pool + page * a.page_stride;  // 64-bit page rebasing
-    if (kDtype == IDX_MXFP4) {
-        uint32_t word, sbyte;
-        mx_quant(x, word, sbyte);
-        pdl_wait();  // the cache may still be read by the previous kernel
-        pdl_launch_dependents();
-        // gather the 4 words of a 16-byte chunk (= one scale block) into its first lane
-        uint32_t w1 = __shfl_down_sync(kFull, word, 1);
-        uint32_t w2 = __shfl_down_sync(kFull, word, 2);
-        uint32_t w3 = __shfl_down_sync(kFull, word, 3);
-        uint32_t s1 = __shfl_down_sync(kFull, sbyte, 4);
-        uint32_t s2 = __shfl_down_sync(kFull, sbyte, 8);
-        uint32_t s3 = __shfl_down_sync(kFull, sbyte, 12);
-        if (ok && (l16 & 3) == 0) {
-            *reinterpret_cast<uint4*>(base + mx_chunk_off(a.page_size, s, l16 >> 2)) =
-                make_uint4(word, w1, w2, w3);
-        }
-        if (ok && l16 == 0) {
-            *reinterpret_cast<uint32_t*>(base + mx_scale_off(a.page_size, s)) =
-                sbyte | (s1 << 8) | (s2 << 16) | (s3 << 24);
-        }
-    } else {
-        uint32_t lo, hi;
-        float scale;
-        f8_quant(x, lo, hi, scale);
-        pdl_wait();
-        pdl_launch_dependents();
-        uint32_t plo = __shfl_down_sync(kFull, lo, 1);
-        uint32_t phi = __shfl_down_sync(kFull, hi, 1);
-        if (ok && (l16 & 1) == 0) {
-            *reinterpret_cast<uint4*>(base + f8_chunk_off(s, l16 >> 1)) = make_uint4(lo, hi, plo, phi);
-        }
-        if (ok && l16 == 0) *reinterpret_cast<float*>(base + f8_scale_off(a.page_size, s)) = scale;
+    quant_store<kDtype>(x, l16, ok, a.pool + page * a.page_stride, a.page_size, s);  // 64-bit page rebasing
+}
+
+// Compressed K store of the 16 entries of block `blk` (one entry per 16 lanes, 8 dims per
+// lane). Entry e pools the raw rows lo..hi, hi = boundary[e], lo = max(first[e], hi - 2r + 1):
+// per dimension m = max of the window's gates, e_i = exp(g_i - m), S = sum e_i and
+// P = sum e_i x_i in row order (P by fused multiply-adds), pooled = P / S; then the norm
+// (none, LayerNorm or RMSNorm), RoPE at positions[e], quantisation and the paged write.
+template <int kDtype>
+__device__ __forceinline__ void compress_rows(const CompressArgs& a, int64_t blk) {
+    const int l16 = threadIdx.x & 15;
+    const int64_t e = blk * kRowsPerCta + (threadIdx.x >> 4);
+    const bool in = e < a.n_entries;
+    const int64_t slot = in ? __ldg(a.slot_mapping + e) : -1;
+    int64_t hi = in ? __ldg(a.boundary + e) : 0;
+    const int64_t fst = in ? __ldg(a.first + e) : 0;
+    int32_t pos = (in && a.rope != IDX_ROPE_NONE) ? __ldg(a.positions + e) : 0;
+    bool ok = in && slot >= 0;
+    const int lp = a.page_size == 128 ? 7 : 6;  // page sizes are 64 or 128
+    const int64_t page = ok ? slot >> lp : 0;
+    const int s = ok ? (int)(slot & (a.page_size - 1)) : 0;
+    if (ok && page >= a.num_pages) {
+        if (l16 == 0) report(a.dev_status, IDX_STATUS_BAD_SLOT);
+        ok = false;
     }
+    if (ok && (fst < 0 || fst > hi || hi >= a.n_raw)) {
+        if (l16 == 0) report(a.dev_status, IDX_STATUS_BAD_LEN);
+        ok = false;
+    }
+    if (a.rope != IDX_ROPE_NONE && ok && (pos < 0 || pos >= a.max_pos)) {
+        if (l16 == 0) report(a.dev_status, IDX_STATUS_BAD_POS);
+        ok = false;
+    }
+    if (!ok) pos = 0;
+    int64_t lo = hi - 2 * (int64_t)a.ratio + 1;
+    if (lo < fst) lo = fst;
+    if (!ok) lo = 0, hi = -1;  // no rows: the lanes still reach the shuffles below
+
+    const uint16_t* kr = a.k_raw + 8 * l16;
+    const uint16_t* gr = a.gate + 8 * l16;
+    float m[8], x[8];
+    if (ok) {
+        unpack8(__ldg(reinterpret_cast<const uint4*>(gr + lo * a.row_stride)), m);
+        for (int64_t i = lo + 1; i <= hi; ++i) {
+            float g[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(gr + i * a.row_stride)), g);
+#pragma unroll
+            for (int d = 0; d < 8; ++d) m[d] = fmaxf(m[d], g[d]);
+        }
+        float S[8], P[8];
+#pragma unroll
+        for (int d = 0; d < 8; ++d) S[d] = P[d] = 0.0f;
+        for (int64_t i = lo; i <= hi; ++i) {
+            float g[8], v[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(gr + i * a.row_stride)), g);
+            unpack8(__ldg(reinterpret_cast<const uint4*>(kr + i * a.row_stride)), v);
+#pragma unroll
+            for (int d = 0; d < 8; ++d) {
+                const float w = exp_neg(__fsub_rn(g[d], m[d]));
+                S[d] = __fadd_rn(S[d], w);
+                P[d] = __fmaf_rn(w, v[d], P[d]);
+            }
+        }
+#pragma unroll
+        for (int d = 0; d < 8; ++d) x[d] = __fdiv_rn(P[d], S[d]);
+    } else {
+#pragma unroll
+        for (int d = 0; d < 8; ++d) x[d] = 0.0f;
+    }
+    if (a.norm == 1) layernorm(x, l16, a.gamma, a.beta, a.eps);
+    else if (a.norm == 2) rmsnorm(x, l16, a.gamma, a.eps);
+    if (a.rope != IDX_ROPE_NONE) rope(x, l16, a.cos_sin + (int64_t)pos * 64, a.rope);
+    quant_store<kDtype>(x, l16, ok, a.pool + page * a.page_stride, a.page_size, s);
 }
 
 // Q rows: CTA (t, y) takes token t's heads 16y .. 16y+15 of the Hq = H rounded up to 8
@@ -297,6 +415,11 @@ __global__ void __launch_bounds__(kThreads) qk_prep_kernel(KStoreArgs ka, QQuant
     }
 }
 
+template <int kDtype>
+__global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
+    compress_rows<kDtype>(a, blockIdx.x);
+}
+
 __global__ void debug_encode_kernel(int kind, const float* in, int64_t n, uint8_t* out) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -333,6 +456,14 @@ cudaError_t launch_qk_prep(const KStoreArgs& ka, const QQuantArgs& qa, cudaStrea
     return ka.dtype == IDX_MXFP4
                ? launch_pdl(qk_prep_kernel<IDX_MXFP4>, dim3((unsigned)grid), dim3(kThreads), 0, st, ka, qa, nk, ny)
                : launch_pdl(qk_prep_kernel<IDX_FP8>, dim3((unsigned)grid), dim3(kThreads), 0, st, ka, qa, nk, ny);
+}
+
+cudaError_t launch_compress(const CompressArgs& a, cudaStream_t st) {
+    if (a.n_entries == 0) return cudaSuccess;
+    const int64_t grid = (a.n_entries + kRowsPerCta - 1) / kRowsPerCta;
+    if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
+    return a.dtype == IDX_MXFP4 ? launch_pdl(compress_kernel<IDX_MXFP4>, dim3((unsigned)grid), dim3(kThreads), 0, st, a)
+                                : launch_pdl(compress_kernel<IDX_FP8>, dim3((unsigned)grid), dim3(kThreads), 0, st, a);
 }
 
 cudaError_t launch_debug_encode(int kind, const float* in, int64_t n, uint8_t* out, cudaStream_t st) {

@@ -282,6 +282,75 @@ def prefill_fp8(seed=0, B=8, cached=28672, new=4096, H=32, **over) -> Workload:
     )
 
 
+@dataclasses.dataclass
+class CompressWork:
+    """Inputs of the compressed K store: raw rows of several sequences back to back, one
+    entry per compress-ratio boundary token of each sequence."""
+    name: str
+    dtype: int
+    ratio: int
+    page_size: int
+    pool_pages: int
+    page_stride: int
+    raw_lens: np.ndarray        # int64 [B], raw rows per sequence
+    k_raw: np.ndarray           # uint16 [N_raw, row_stride] (bf16; columns past 128 unused)
+    gate: np.ndarray            # uint16 [N_raw, row_stride]
+    boundary: np.ndarray        # int64 [E], raw row of each entry's boundary token
+    first: np.ndarray           # int64 [E], first raw row of the entry's sequence
+    slot_mapping: np.ndarray    # int64 [E]
+    positions: np.ndarray       # int32 [E], boundary position within its sequence
+    rope: int
+    norm: int                   # 0 none, 1 LayerNorm, 2 RMSNorm
+    gamma: np.ndarray           # float32 [128]
+    cos_sin: np.ndarray
+
+    @property
+    def n_entries(self) -> int:
+        return int(self.boundary.shape[0])
+
+
+def compress_work(seed=0, raw_lens=(37, 64, 130), ratio=4, page_size=64, dtype=MXFP4,
+                  rope=ROPE_NEOX, norm=2, row_stride=128, name=None, spare_pages=1) -> CompressWork:
+    """Raw K and gate rows bf16 N(0, 1); per sequence the entries are its tokens
+    r*j + r - 1 (j = 0 .. len//r - 1; a ragged tail of fewer than r tokens has none), stored
+    in pages of a shuffled pool in entry order, RoPE'd at that in-sequence position; RMSNorm
+    weight uniform in [0.5, 1.5]."""
+    rk, rg, rp, rw = _streams(seed, 4)
+    lens = np.asarray(raw_lens, np.int64)
+    n = int(lens.sum())
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]]).astype(np.int64)
+    ents = (lens // ratio).astype(np.int32)
+    P = page_size
+    pool = int(sum((int(e) + P - 1) // P for e in ents)) + spare_pages
+    pt = _assign_pages(rp, pool, ents, P) if ents.sum() > 0 else np.zeros((len(lens), 1), np.int32)
+    slots = _slots(pt, ents, P) if ents.sum() > 0 else np.zeros(0, np.int64)
+    j = [np.arange(int(e), dtype=np.int64) for e in ents]
+    boundary = np.concatenate([starts[b] + ratio * j[b] + ratio - 1 for b in range(len(lens))])
+    first = np.concatenate([np.full(int(ents[b]), starts[b], np.int64) for b in range(len(lens))])
+    positions = np.concatenate([(ratio * j[b] + ratio - 1) for b in range(len(lens))]).astype(np.int32)
+    k_raw = np.zeros((n, row_stride), np.uint16)
+    gate = np.zeros((n, row_stride), np.uint16)
+    k_raw[:, :128] = _normal_bf16(rk, (n, 128))
+    gate[:, :128] = _normal_bf16(rg, (n, 128))
+    max_pos = int(max(lens.max(), 1))
+    return CompressWork(
+        name=name or f"compress_r{ratio}_{len(lens)}seq_{n}raw", dtype=dtype, ratio=ratio,
+        page_size=P, pool_pages=pool, page_stride=page_bytes(dtype, P), raw_lens=lens,
+        k_raw=k_raw, gate=gate, boundary=boundary.astype(np.int64), first=first,
+        slot_mapping=slots.astype(np.int64), positions=positions, rope=rope, norm=norm,
+        gamma=rw.uniform(0.5, 1.5, 128).astype(np.float32), cos_sin=rope_table(max_pos))
+
+
+def compress_b256(seed=0, B=256, **over) -> CompressWork:
+    """The compressed-indexer decode workload's contexts through the compressor: B raw
+    contexts uniform in [1024, 9472] tokens, ratio 4, 64-entry MXFP4 pages, NeoX RoPE,
+    RMSNorm (the whole context compressed, as a prefill of those sequences does)."""
+    rl = _streams(seed, 5)[4]
+    raw = rl.integers(over.pop("raw_lo", 1024), over.pop("raw_hi", 9472) + 1, size=B)
+    return compress_work(seed, raw_lens=raw, ratio=4, page_size=64, dtype=MXFP4, rope=ROPE_NEOX,
+                         norm=2, name=f"compress_mxfp4_r4_b{B}_raw1024-9472", **over)
+
+
 BUILDERS = {
     "tiny_decode": tiny_decode,
     "decode_b64": decode_b64,
