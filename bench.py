@@ -792,6 +792,23 @@ COMPRESS_SOURCES = ["sparse_attention_indexer_mqa_gb300/csrc/quant.cu",
                     "sparse_attention_indexer_mqa_gb300/csrc/kernels.h"]
 
 
+def run_block(args):
+    """One block of the default run, alone on cuda:0 (for a profiler's launch list)."""
+    import torch
+    from sparse_attention_indexer_mqa_gb300 import binding as Bn
+    Bn.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, peak_kind = measured_peaks()
+    if args.only == "compress":
+        return compress_block(args, dev, peaks)
+    if args.only == "prefill":
+        return prefill_block(args, dev, peaks, peak_kind)
+    if args.only == "qk_prep_sweep":
+        return qk_prep_sweep(args, dev, peaks)
+    return tensor_probe(torch, torch.cuda.current_stream())
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -806,6 +823,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill block of the default run")
     ap.add_argument("--no-probe", action="store_true", help="skip the tensor-core rate probe")
     ap.add_argument("--no-compress", action="store_true", help="skip the compressed K store block")
+    ap.add_argument("--only", choices=["compress", "prefill", "qk_prep_sweep", "tensor_probe"],
+                    help="run one block of the default run alone and print it (profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -815,6 +834,9 @@ def main():
         line = run_reference(args, rank, world)
         if line is not None:
             print(json.dumps(line), flush=True)
+        return
+    if args.only:
+        print(json.dumps({"only": args.only, args.only: run_block(args)}), flush=True)
         return
     if world > 1:
         import torch

@@ -82,12 +82,15 @@ __device__ __forceinline__ void rmsnorm(float* x, int l16, const float* gamma, f
 // exp(a) for a <= 0 by Cody and Waite's argument reduction and a degree-7 Taylor polynomial
 // (one fused multiply-add per step): n = rint(a log2 e), f = (a - n ln2_hi) - n ln2_lo with
 // ln2_hi holding 16 significant bits so that n ln2_hi is exact, e^f by Horner's rule, the
-// result e^f * 2^n. At most 0.86 ulp from exp over [-87, 0]; 0 below -87.
+// result e^f * 2^n. At most 0.86 ulp from exp over [-87, 0]; 0 below -87 (and for NaN).
+// Branch-free: the argument is clamped to -87 and the result selected. rint is the add and
+// subtract of 1.5 * 2^23 (round to nearest even, exact for |t| < 2^22), and the bits of that
+// sum hold n, so 2^n = bits * 2^23 + bits(1.0) in one integer multiply-add.
 __device__ __forceinline__ float exp_neg(float a) {
-    if (!(a > -87.0f)) return 0.0f;
-    if (a > 0.0f) a = 0.0f;
-    const float n = rintf(__fmul_rn(a, 1.44269504f));
-    float f = __fmaf_rn(-n, 0.693145752f, a);
+    const float ac = fmaxf(a, -87.0f);
+    const float big = __fadd_rn(__fmul_rn(ac, 1.44269504f), 12582912.0f);
+    const float n = __fsub_rn(big, 12582912.0f);
+    float f = __fmaf_rn(-n, 0.693145752f, ac);
     f = __fmaf_rn(-n, 1.42860677e-06f, f);
     float p = 1.0f / 5040.0f;
     p = __fmaf_rn(p, f, 1.0f / 720.0f);
@@ -97,7 +100,16 @@ __device__ __forceinline__ float exp_neg(float a) {
     p = __fmaf_rn(p, f, 0.5f);
     p = __fmaf_rn(p, f, 1.0f);
     p = __fmaf_rn(p, f, 1.0f);
-    return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));  // n >= -126 here
+    const float two_n = __uint_as_float(__float_as_uint(big) * (1u << 23) + 0x3f800000u);
+    const float r = __fmul_rn(p, two_n);
+    return a > -87.0f ? r : 0.0f;
+}
+
+// elementwise max of two pairs of bf16 (exact; a NaN operand yields the other)
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
 // RoPE on dims 0..63 (lanes 0..7 of the row). NeoX pairs dims (i, i+32): lane l < 4 holds
@@ -285,24 +297,36 @@ __device__ __forceinline__ void compress_rows(const CompressArgs& a, int64_t blk
     if (lo < fst) lo = fst;
     if (!ok) lo = 0, hi = -1;  // no rows: the lanes still reach the shuffles below
 
-    const uint16_t* kr = a.k_raw + 8 * l16;
-    const uint16_t* gr = a.gate + 8 * l16;
-    float m[8], x[8];
+    float x[8];
     if (ok) {
-        unpack8(__ldg(reinterpret_cast<const uint4*>(gr + lo * a.row_stride)), m);
-        for (int64_t i = lo + 1; i <= hi; ++i) {
-            float g[8];
-            unpack8(__ldg(reinterpret_cast<const uint4*>(gr + i * a.row_stride)), g);
-#pragma unroll
-            for (int d = 0; d < 8; ++d) m[d] = fmaxf(m[d], g[d]);
+        const uint4* gr = reinterpret_cast<const uint4*>(a.gate + lo * a.row_stride) + l16;
+        const uint4* kr = reinterpret_cast<const uint4*>(a.k_raw + lo * a.row_stride) + l16;
+        const int64_t step = a.row_stride / 8;  // uint4 per row
+        const int rows = (int)(hi - lo + 1);    // 1 .. 2 * ratio
+        // pass 1: the window's gate maximum per dimension, on packed bf16 pairs
+        uint4 mx = __ldg(gr);
+        for (int i = 1; i < rows; ++i) {
+            const uint4 g = __ldg(gr + i * step);
+            mx.x = bf16x2_max(mx.x, g.x); mx.y = bf16x2_max(mx.y, g.y);
+            mx.z = bf16x2_max(mx.z, g.z); mx.w = bf16x2_max(mx.w, g.w);
         }
+        float m[8];
+        unpack8(mx, m);
+        // pass 2: weights, their sum and the weighted sum, rows in order; the next row's
+        // loads are issued before this row's arithmetic
         float S[8], P[8];
 #pragma unroll
         for (int d = 0; d < 8; ++d) S[d] = P[d] = 0.0f;
-        for (int64_t i = lo; i <= hi; ++i) {
+        uint4 gn = __ldg(gr), vn = __ldg(kr);
+        for (int i = 0; i < rows; ++i) {
+            const uint4 gc = gn, vc = vn;
+            if (i + 1 < rows) {
+                gn = __ldg(gr + (i + 1) * step);
+                vn = __ldg(kr + (i + 1) * step);
+            }
             float g[8], v[8];
-            unpack8(__ldg(reinterpret_cast<const uint4*>(gr + i * a.row_stride)), g);
-            unpack8(__ldg(reinterpret_cast<const uint4*>(kr + i * a.row_stride)), v);
+            unpack8(gc, g);
+            unpack8(vc, v);
 #pragma unroll
             for (int d = 0; d < 8; ++d) {
                 const float w = exp_neg(__fsub_rn(g[d], m[d]));
