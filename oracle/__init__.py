@@ -87,6 +87,9 @@ def _declare(L):
     L.orc_compress_k_store.argtypes = [vp, vp, i64, i64, vp, vp, i64, i32, vp, vp, vp, i32, C.c_int,
                                        C.c_int, vp, vp, f32, C.c_int, vp, i64, i32, i64]
     L.orc_compress_k_store.restype = C.c_int
+    L.orc_topk_cand.argtypes = [vp, i64, vp, vp, i32, C.c_int, vp, i64, vp, i32, vp, i32, i32, vp,
+                                C.c_int]
+    L.orc_topk_cand.restype = C.c_int
     L.orc_mqa_logits.argtypes = [vp, vp, vp, i64, i32, C.c_int, vp, i64, i32, i64, vp, i32,
                                  vp, vp, i32, C.c_int, vp, i64, vp, i64, C.c_int]
     L.orc_mqa_logits.restype = C.c_int
@@ -304,3 +307,21 @@ def compress_k_store(pool, k_raw, gate, boundary, first, ratio, slot_mapping, po
                                       int(ratio), _p(slot), _p(pos), _p(cs), cs.shape[0], int(rope),
                                       int(norm), _p(g), _p(b), C.c_float(eps), int(dtype), _p(pool),
                                       int(num_pages), int(page_size), int(page_stride))
+
+
+def topk_cand(logits, seq_lens_k, cu_seqlens_q, causal, cand, n_cand, page_size, k, rows=None,
+              n_threads=None):
+    """Top-k over each query's candidate blocks (reading R17); logits as mqa_logits returns
+    them for `rows` (all queries when None); cand int32 [T, cand_stride], n_cand int32 [T]."""
+    lg = _c(logits, np.float64)
+    sl = _c(seq_lens_k, np.int32)
+    cu = _c(cu_seqlens_q, np.int32)
+    cd = _c(cand, np.int32)
+    nc = _c(n_cand, np.int32)
+    rr = None if rows is None else _c(rows, np.int64)
+    n = lg.shape[0]
+    out = np.empty((n, k), np.int32)
+    nt = n_threads or os.cpu_count() or 1
+    lib().orc_topk_cand(_p(lg), lg.shape[1], _p(sl), _p(cu), sl.shape[0], int(causal), _p(rr), n,
+                        _p(cd), cd.shape[1], _p(nc), int(page_size), int(k), _p(out), int(nt))
+    return out

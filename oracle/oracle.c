@@ -24,6 +24,10 @@
  *                quantise -> paged store, one entry per compress-ratio boundary token.
  *                [P2] "Changes / K write" (the V4 compressor's fused pool/norm/RoPE/MXFP4
  *                store); readings R13-R16 at orc_compress_k_store.
+ *   Candidate -- the V4.1 two-level indexer's second level: per query, top-k over the
+ *                visible keys of its candidate blocks only. [P2] "Purpose" (the
+ *                candidate-pool path; the dense path calls the scorer with no candidate
+ *                blocks, [P2] "Scoring and metadata"); reading R17 at orc_topk_cand.
  *   Top-k     -- per query, indices of the k largest logits among its visible keys.
  *                [P2] "Test Result / GPQA Diamond" (sparse selection of top-k 1024 once
  *                the context passes top-k x compress ratio).
@@ -716,6 +720,89 @@ int orc_topk(const double* logits, int64_t ld, const int32_t* seq_lens_k,
     }
     for (int i = 1; i < n_threads; ++i) pthread_create(&th[i], NULL, topk_rows, &jobs[i]);
     topk_rows(&jobs[0]);
+    for (int i = 1; i < n_threads; ++i) pthread_join(th[i], NULL);
+    free(jobs);
+    free(th);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Candidate-pool top-k (the two-level indexer's second level)                          */
+/* ------------------------------------------------------------------------------------ */
+/*
+ * [P2] "Purpose": besides the dense path, which scores the whole context, the MXFP4 indexer
+ * has a candidate-pool path that exists for V4.1's two-level indexer; the dense path is the
+ * scorer called with no candidate blocks ([P2] "Scoring and metadata"). The pages do not say
+ * how the first level picks blocks or how big they are. Reading R17: a candidate block is one
+ * page-table block, block j = keys [j*P, (j+1)*P) of the sequence; query t comes with a list
+ * of n_cand[t] block ids (cand[t*cand_stride + i]); its candidate keys are the keys s with
+ * s < visible(t) whose block s / P is in the list (a set: repeated ids count once, ids that
+ * name no visible block add nothing); the result is the top-k of the query's logits over its
+ * candidate keys, (value descending, index ascending), indices being key positions in the
+ * sequence, padded with -1 when there are fewer than k. The first level itself is an input.
+ *
+ * logits: the dense logits of rows `rows` (as orc_mqa_logits computes them), [n_rows][ld].
+ */
+typedef struct {
+    const double* logits;
+    int64_t ld;
+    const int32_t *seq_lens_k, *cu_seqlens_q;
+    int32_t B;
+    int causal;
+    const int64_t* rows;
+    int64_t n_rows;
+    const int32_t *cand, *n_cand;
+    int32_t cand_stride, P, k;
+    int32_t* out;
+    int n_threads, tid;
+} cand_job;
+
+static void *cand_rows(void* arg) {
+    cand_job* j = (cand_job*)arg;
+    vi_pair* buf = NULL;
+    int64_t cap = 0;
+    for (int64_t r = j->tid; r < j->n_rows; r += j->n_threads) {
+        int64_t t = j->rows ? j->rows[r] : r;
+        int64_t vis = orc_visible(t, j->seq_lens_k, j->cu_seqlens_q, j->B, j->causal);
+        if (vis < 0) vis = 0;
+        if (vis > cap) {
+            free(buf);
+            cap = vis;
+            buf = (vi_pair*)malloc(sizeof(vi_pair) * (size_t)cap);
+        }
+        int64_t n = 0;
+        for (int64_t s = 0; s < vis; ++s) {
+            int64_t blk = s / j->P;
+            int in = 0;
+            for (int32_t i = 0; i < j->n_cand[t] && !in; ++i) in = j->cand[t * j->cand_stride + i] == blk;
+            if (!in) continue;
+            buf[n].v = j->logits[r * j->ld + s];
+            buf[n].i = (int32_t)s;
+            ++n;
+        }
+        qsort(buf, (size_t)n, sizeof(vi_pair), cmp_desc);
+        for (int32_t q = 0; q < j->k; ++q) j->out[r * j->k + q] = (q < n) ? buf[q].i : -1;
+    }
+    free(buf);
+    return NULL;
+}
+
+int orc_topk_cand(const double* logits, int64_t ld, const int32_t* seq_lens_k,
+                  const int32_t* cu_seqlens_q, int32_t B, int causal, const int64_t* rows,
+                  int64_t n_rows, const int32_t* cand, int32_t cand_stride, const int32_t* n_cand,
+                  int32_t page_size, int32_t k, int32_t* out_idx, int n_threads) {
+    if (n_threads < 1) n_threads = 1;
+    cand_job* jobs = (cand_job*)calloc((size_t)n_threads, sizeof(cand_job));
+    pthread_t* th = (pthread_t*)calloc((size_t)n_threads, sizeof(pthread_t));
+    for (int i = 0; i < n_threads; ++i) {
+        cand_job* j = &jobs[i];
+        j->logits = logits; j->ld = ld; j->seq_lens_k = seq_lens_k;
+        j->cu_seqlens_q = cu_seqlens_q; j->B = B; j->causal = causal; j->rows = rows;
+        j->n_rows = n_rows; j->cand = cand; j->n_cand = n_cand; j->cand_stride = cand_stride;
+        j->P = page_size; j->k = k; j->out = out_idx; j->n_threads = n_threads; j->tid = i;
+    }
+    for (int i = 1; i < n_threads; ++i) pthread_create(&th[i], NULL, cand_rows, &jobs[i]);
+    cand_rows(&jobs[0]);
     for (int i = 1; i < n_threads; ++i) pthread_join(th[i], NULL);
     free(jobs);
     free(th);

@@ -99,7 +99,14 @@ int orc_topk(const double* logits, int64_t ld, const int32_t* seq_lens_k,
              const int32_t* cu_seqlens_q, int32_t B, int causal, const int64_t* rows,
              int64_t n_rows, int32_t k, int32_t* out_idx, int n_threads);
 
+/* candidate-pool top-k (see oracle.c, reading R17) */
+int orc_topk_cand(const double* logits, int64_t ld, const int32_t* seq_lens_k,
+                  const int32_t* cu_seqlens_q, int32_t B, int causal, const int64_t* rows,
+                  int64_t n_rows, const int32_t* cand, int32_t cand_stride, const int32_t* n_cand,
+                  int32_t page_size, int32_t k, int32_t* out_idx, int n_threads);
+
 #ifdef __cplusplus
 }
 #endif
+
 #endif
