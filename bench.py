@@ -389,6 +389,8 @@ def run_gpu(args, rank, world):
         line["qk_prep_sweep"] = qk_prep_sweep(args, dev, peaks)
     if args.config == "decode_b64" and not args.no_compress:
         line["compress"] = compress_block(args, dev, peaks)
+    if args.config == "decode_b64" and not args.no_cand:
+        line["cand"] = cand_block(args, dev, peaks)
     if not args.no_probe:
         line["tensor_probe"] = tensor_probe(torch, stream)
         if "prefill" in line:
@@ -524,6 +526,63 @@ def compress_block(args, dev, peaks):
     del k_raw, gate, pool, g
     torch.cuda.empty_cache()
     return out
+
+
+def cand_block(args, dev, peaks):
+    """The candidate-pool path (idx_mqa_topk_cand_paged) on the decode shape (B=64, H=32, 8192
+    keys, page 128): 16 candidate blocks per query (2048 of its 8192 keys, the last block
+    always in), beside the dense scorer + top-k on the same data. Each timed call follows a
+    256 MiB write that flushes L2; only the call lies between its events."""
+    import torch
+    from sparse_attention_indexer_mqa_gb300 import binding as Bn
+    wl = W.make("decode_b64", seed=args.seed)
+    rep = Replica(wl, 1, dev)
+    rep.call("qk_prep", 0)
+    torch.cuda.synchronize()
+    cand, n_cand, max_cand = W.candidate_blocks(wl, seed=args.seed, n_blocks=16)
+    c = torch.from_numpy(cand).to(dev)
+    nc = torch.from_numpy(n_cand).to(dev)
+    max_k = int(wl.seq_lens_k.max())
+    ws = torch.zeros(Bn.idx_mqa_topk_cand_workspace_bytes(wl.T, max_cand, wl.page_size, max_k),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty((wl.T, wl.topk), dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def cand_call():
+        Bn.idx_mqa_topk_cand_paged(rep.q_codes, rep.q_scales, rep.w, wl.dtype, rep.pools[0],
+                                   wl.pool_pages, wl.page_size, wl.page_stride, rep.page_table,
+                                   rep.seq_lens_k, rep.cu, wl.causal, 1, max_k, c, nc, max_cand,
+                                   wl.topk, out, ws, dev_status=status)
+
+    def dense_call():
+        rep.call("scorer", 0)
+        rep.call("topk", 0)
+
+    def timed(fn, k):
+        for _ in range(3):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
+        for s, e in ev:
+            flush.fill_(1)
+            s.record(stream)
+            fn()
+            e.record(stream)
+        torch.cuda.synchronize()
+        return sum(s.elapsed_time(e) for s, e in ev) / k
+
+    k = max(3, min(args.steps, 20))
+    cand_ms, dense_ms = timed(cand_call, k), timed(dense_call, k)
+    keys = int(sum(min(int(n), 16) for n in n_cand)) * wl.page_size
+    out_d = {"workload": wl.name, "candidate_blocks_per_query": 16, "candidate_keys": keys,
+             "dense_keys": wl.pairs(), "steps": k, "launches_per_call": 4,
+             "cand_us": round(cand_ms * 1e3, 2), "dense_scorer_topk_us": round(dense_ms * 1e3, 2),
+             "cand_k_tokens_per_s": round(keys / (cand_ms / 1e3) / 1e3, 1),
+             "status": int(status.item()), "l2": "256 MiB write before each timed call"}
+    del rep, ws, flush
+    torch.cuda.empty_cache()
+    return out_d
 
 
 def qk_prep_sweep(args, dev, peaks):
@@ -802,6 +861,8 @@ def run_block(args):
     peaks, peak_kind = measured_peaks()
     if args.only == "compress":
         return compress_block(args, dev, peaks)
+    if args.only == "cand":
+        return cand_block(args, dev, peaks)
     if args.only == "prefill":
         return prefill_block(args, dev, peaks, peak_kind)
     if args.only == "qk_prep_sweep":
@@ -823,7 +884,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill block of the default run")
     ap.add_argument("--no-probe", action="store_true", help="skip the tensor-core rate probe")
     ap.add_argument("--no-compress", action="store_true", help="skip the compressed K store block")
-    ap.add_argument("--only", choices=["compress", "prefill", "qk_prep_sweep", "tensor_probe"],
+    ap.add_argument("--no-cand", action="store_true", help="skip the candidate-pool block")
+    ap.add_argument("--only", choices=["compress", "cand", "prefill", "qk_prep_sweep", "tensor_probe"],
                     help="run one block of the default run alone and print it (profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

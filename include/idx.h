@@ -249,6 +249,40 @@ int idx_topk(const float* logits, int64_t ld_logits, const int32_t* seq_lens_k,
              cudaStream_t stream);
 
 /*
+ * Candidate-pool scoring and top-k, the second level of DeepSeek-V4.1's two-level indexer
+ * ([P2] "Purpose": the MXFP4 indexer's candidate-pool path, beside the dense path that scores
+ * the whole context; [P2] "Scoring and metadata": the dense path is the scorer called with no
+ * candidate blocks). A candidate block is one page-table block: block j of a sequence holds its
+ * keys j*P .. j*P + P - 1. Query t lists n_cand[t] block ids at cand_blocks[t*cand_stride ..];
+ * its candidate keys are its visible keys (as in idx_mqa_logits_paged) whose block is listed
+ * (repeated ids count once; ids naming no visible block add nothing). out_idx[t*k .. t*k+k-1]
+ * holds the key positions (in the sequence) of the k largest logits among the candidate keys,
+ * -1 past their count; the logits are the ones idx_mqa_logits_paged computes. The choice of the
+ * blocks (the first level) is the caller's.
+ * Arguments as idx_mqa_topk_paged, plus: cand_blocks int32 [T][cand_stride], n_cand int32 [T],
+ *   1 <= max_cand <= 1024 with max_cand <= cand_stride: an upper bound of n_cand[t]. A row whose
+ *   n_cand is negative or above max_cand, or whose sequence breaks the length bounds, gets -1
+ *   in all k slots and sets IDX_STATUS_BAD_LEN.
+ * workspace: at least idx_mqa_topk_cand_workspace_bytes(T, max_cand, page_size, max_seq_len_k)
+ *   bytes, 256-byte aligned; nothing in it needs a starting value. One workspace serves one
+ *   call at a time. Four launches on the stream: candidate preparation, the decode scorer on
+ *   one virtual sequence per query (the candidate blocks back to back), top-k, index mapping.
+ */
+int idx_mqa_topk_cand_workspace_bytes(int64_t T, int32_t max_cand, int32_t page_size,
+                                      int32_t max_seq_len_k, size_t* bytes);
+
+int idx_mqa_topk_cand_paged(const uint8_t* q_codes, const void* q_scales, const float* w,
+                            int64_t T, int32_t H, int32_t dtype, const void* pool,
+                            int64_t num_pages, int32_t page_size, int64_t page_stride,
+                            const int32_t* page_table, int32_t pt_stride,
+                            const int32_t* seq_lens_k, const int32_t* cu_seqlens_q, int32_t B,
+                            int32_t causal, int32_t max_q_len, int32_t max_seq_len_k,
+                            const int32_t* cand_blocks, int32_t cand_stride,
+                            const int32_t* n_cand, int32_t max_cand, int32_t k, int32_t* out_idx,
+                            void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                            cudaStream_t stream);
+
+/*
  * Paged MQA logits and per-query top-k in one launch ([P2] "Purpose": the cache is scored in
  * place; [P3] "Purpose": topk_indices_buffer). out_idx[t*k .. t*k+k-1] is what
  * idx_mqa_logits_paged followed by idx_topk (same arguments, k, max_seq_len_k) would give:

@@ -85,11 +85,16 @@ def _declare(L):
     L.idx_debug_mma_rate.argtypes = [i32, i32, vp, C.POINTER(C.c_double), vp]
     L.idx_mqa_topk_paged_noalloc.argtypes = [vp, vp, vp, i64, i32, i32, vp, i64, i32, i64, vp, i32,
                                              vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
+    L.idx_mqa_topk_cand_workspace_bytes.argtypes = [i64, i32, i32, i32, C.POINTER(C.c_size_t)]
+    L.idx_mqa_topk_cand_paged.argtypes = [vp, vp, vp, i64, i32, i32, vp, i64, i32, i64, vp, i32, vp,
+                                          vp, i32, i32, i32, i32, vp, i32, vp, i32, i32, vp, vp,
+                                          C.c_size_t, vp, vp]
     L.idx_compress_k_store.argtypes = [vp, vp, i64, i64, vp, vp, i64, i32, vp, vp, vp, i32, i32, i32,
                                        vp, vp, f32, i32, vp, i64, i32, i64, vp, vp]
     for n in ("idx_cache_layout", "idx_k_store", "idx_q_quant", "idx_qk_prep", "idx_mqa_logits_paged",
               "idx_topk", "idx_debug_encode", "idx_mqa_topk_workspace_bytes", "idx_mqa_topk_paged",
-              "idx_debug_mma_rate", "idx_mqa_topk_paged_noalloc", "idx_compress_k_store"):
+              "idx_debug_mma_rate", "idx_mqa_topk_paged_noalloc", "idx_compress_k_store",
+              "idx_mqa_topk_cand_workspace_bytes", "idx_mqa_topk_cand_paged"):
         getattr(L, n).restype = C.c_int
 
 
@@ -217,6 +222,26 @@ def idx_mqa_topk_paged(q_codes, q_scales, w, dtype, pool, num_pages, page_size, 
         seq_lens_k.shape[0], int(causal), max_q_len, max_seq_len_k, k, _ptr(out_idx),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status),
         _stream(stream)))
+
+
+def idx_mqa_topk_cand_workspace_bytes(T, max_cand, page_size, max_seq_len_k) -> int:
+    n = C.c_size_t(0)
+    _check("idx_mqa_topk_cand_workspace_bytes",
+           load().idx_mqa_topk_cand_workspace_bytes(T, max_cand, page_size, max_seq_len_k, C.byref(n)))
+    return int(n.value)
+
+
+def idx_mqa_topk_cand_paged(q_codes, q_scales, w, dtype, pool, num_pages, page_size, page_stride,
+                            page_table, seq_lens_k, cu_seqlens_q, causal, max_q_len, max_seq_len_k,
+                            cand_blocks, n_cand, max_cand, k, out_idx, workspace, dev_status=None,
+                            stream=None):
+    T, H = w.shape
+    _check("idx_mqa_topk_cand_paged", load().idx_mqa_topk_cand_paged(
+        _ptr(q_codes), _ptr(q_scales), _ptr(w), T, H, dtype, _ptr(pool), num_pages, page_size,
+        page_stride, _ptr(page_table), page_table.shape[1], _ptr(seq_lens_k), _ptr(cu_seqlens_q),
+        seq_lens_k.shape[0], int(causal), max_q_len, max_seq_len_k, _ptr(cand_blocks),
+        cand_blocks.shape[1], _ptr(n_cand), max_cand, k, _ptr(out_idx), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)))
 
 
 def idx_debug_encode(kind, x, out, stream=None):

@@ -1,5 +1,6 @@
 // api.cu -- the extern "C" entry points of idx.h: argument validation, then one launch on
 // the caller's stream. Nothing here allocates, frees or synchronises.
+#include <algorithm>
 #include <cmath>
 
 #include <nvtx3/nvToolsExt.h>
@@ -305,6 +306,102 @@ int idx_debug_encode(int32_t kind, const float* in, int64_t n, uint8_t* out, cud
     if (n == 0) return IDX_OK;
     if (!in || !out) return IDX_EINVAL;
     return cuda_status(idx::launch_debug_encode(kind, in, n, out, stream));
+}
+
+}  // extern "C"
+
+namespace {
+
+// Workspace of the candidate path: cu' [T+1], vlen [T], the virtual page table and the sorted
+// block ids [T][max_cand] (int32, each 256-byte padded), then the logits [T][ld'] with
+// ld' = the longest virtual row (min(max_cand * P, max_seq_len_k)) rounded up to 4.
+struct CandLayout {
+    int64_t o_vlen, o_vpt, o_vblk, o_logits, total, ld, max_len;
+};
+
+CandLayout cand_layout(int64_t T, int32_t max_cand, int32_t page_size, int32_t max_seq_len_k) {
+    auto up = [](int64_t x) { return (x + 255) / 256 * 256; };
+    CandLayout l{};
+    l.max_len = std::min<int64_t>((int64_t)max_cand * page_size, max_seq_len_k);
+    l.ld = (std::max<int64_t>(l.max_len, 1) + 3) / 4 * 4;
+    l.o_vlen = up(4 * (T + 1));
+    l.o_vpt = l.o_vlen + up(4 * T);
+    l.o_vblk = l.o_vpt + up(4 * T * max_cand);
+    l.o_logits = l.o_vblk + up(4 * T * max_cand);
+    l.total = l.o_logits + up(4 * T * l.ld);
+    return l;
+}
+
+}  // namespace
+
+extern "C" {
+
+int idx_mqa_topk_cand_workspace_bytes(int64_t T, int32_t max_cand, int32_t page_size, int32_t max_seq_len_k,
+                                      size_t* bytes) {
+    if (!bytes || T < 0 || max_seq_len_k < 0) return IDX_EINVAL;
+    if (page_size != 64 && page_size != 128) return IDX_EUNSUPPORTED;
+    if (max_cand < 1 || max_cand > 1024 || max_seq_len_k > INT32_MAX / 32) return IDX_EUNSUPPORTED;
+    *bytes = (size_t)cand_layout(T, max_cand, page_size, max_seq_len_k).total;
+    return IDX_OK;
+}
+
+int idx_mqa_topk_cand_paged(const uint8_t* q_codes, const void* q_scales, const float* w, int64_t T, int32_t H,
+                            int32_t dtype, const void* pool, int64_t num_pages, int32_t page_size,
+                            int64_t page_stride, const int32_t* page_table, int32_t pt_stride,
+                            const int32_t* seq_lens_k, const int32_t* cu_seqlens_q, int32_t B, int32_t causal,
+                            int32_t max_q_len, int32_t max_seq_len_k, const int32_t* cand_blocks,
+                            int32_t cand_stride, const int32_t* n_cand, int32_t max_cand, int32_t k,
+                            int32_t* out_idx, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                            cudaStream_t stream) {
+    Range r("idx_mqa_topk_cand_paged");
+    int st = check_pool(dtype, pool, num_pages, page_size, page_stride);
+    if (st != IDX_OK) return st;
+    if (T < 0 || B < 0 || max_q_len < 0 || max_seq_len_k < 0 || pt_stride < 0) return IDX_EINVAL;
+    if (H < 1 || H > 64 || k < 1 || k > 4096) return IDX_EUNSUPPORTED;
+    if (max_cand < 1 || max_cand > 1024 || max_seq_len_k > INT32_MAX / 32) return IDX_EUNSUPPORTED;
+    if (cand_stride < max_cand) return IDX_EINVAL;
+    if (T == 0) return IDX_OK;
+    if (T > INT32_MAX - 1) return IDX_EUNSUPPORTED;  // one virtual sequence per query
+    if (!out_idx || !seq_lens_k || !cu_seqlens_q || !cand_blocks || !n_cand || B == 0) return IDX_EINVAL;
+    if (max_seq_len_k > 0 && (!q_codes || !w || !page_table)) return IDX_EINVAL;
+    if (dtype == IDX_MXFP4 && max_seq_len_k > 0 && (!q_scales || !aligned(q_scales, 16))) return IDX_EINVAL;
+    if ((q_codes && !aligned(q_codes, 16)) || !aligned(workspace, 256)) return IDX_EINVAL;
+    if (pt_stride < (max_seq_len_k + page_size - 1) / page_size) return IDX_EINVAL;
+    const CandLayout l = cand_layout(T, max_cand, page_size, max_seq_len_k);
+    if (!workspace || (int64_t)workspace_bytes < l.total) return IDX_EINVAL;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+
+    idx::CandArgs c{};
+    c.cu_seqlens_q = cu_seqlens_q; c.seq_lens_k = seq_lens_k; c.page_table = page_table;
+    c.pt_stride = pt_stride; c.B = B; c.causal = causal != 0; c.max_q_len = max_q_len;
+    c.max_seq_len_k = max_seq_len_k; c.page_size = page_size; c.T = T; c.cand = cand_blocks;
+    c.cand_stride = cand_stride; c.max_cand = max_cand; c.n_cand = n_cand;
+    c.vcu = reinterpret_cast<int32_t*>(ws);
+    c.vlen = reinterpret_cast<int32_t*>(ws + l.o_vlen);
+    c.vpt = reinterpret_cast<int32_t*>(ws + l.o_vpt);
+    c.vblk = reinterpret_cast<int32_t*>(ws + l.o_vblk);
+    c.dev_status = dev_status;
+    cudaError_t e = idx::launch_cand_prep(c, stream);
+    if (e != cudaSuccess) return IDX_ECUDA;
+
+    // the decode scorer over one virtual sequence per query; its prologue reads the virtual
+    // lengths and page table, so it starts after the preparation has finished
+    idx::ScoreArgs a{};
+    a.q_codes = q_codes; a.q_scales = static_cast<const uint8_t*>(q_scales); a.w = w; a.T = T;
+    a.H = H; a.dtype = dtype; a.pool = static_cast<const uint8_t*>(pool); a.num_pages = num_pages;
+    a.page_size = page_size; a.page_stride = page_stride; a.page_table = c.vpt; a.pt_stride = max_cand;
+    a.seq_lens_k = c.vlen; a.cu_seqlens_q = c.vcu; a.B = (int32_t)T; a.causal = 0; a.max_q_len = 1;
+    a.max_seq_len_k = (int32_t)l.max_len; a.logits = reinterpret_cast<float*>(ws + l.o_logits); a.ld = l.ld;
+    a.dev_status = dev_status; a.no_pdl = true;
+    e = idx::launch_scorer_decode(a, stream);
+    if (e != cudaSuccess) return IDX_ECUDA;
+
+    idx::TopkArgs tk{};
+    tk.logits = a.logits; tk.ld = l.ld; tk.seq_lens_k = c.vlen; tk.cu_seqlens_q = c.vcu; tk.B = (int32_t)T;
+    tk.T = T; tk.causal = 0; tk.max_len = (int32_t)l.max_len; tk.k = k; tk.out = out_idx; tk.dev_status = dev_status;
+    e = idx::launch_topk(tk, stream);
+    if (e != cudaSuccess) return IDX_ECUDA;
+    return cuda_status(idx::launch_cand_map(c.vblk, max_cand, page_size, T, k, out_idx, stream));
 }
 
 }  // extern "C"

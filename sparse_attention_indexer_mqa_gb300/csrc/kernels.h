@@ -85,6 +85,10 @@ struct ScoreArgs {
     int32_t topk_k;
     int32_t* out_idx;
     int32_t* counters;
+    // launch without programmatic dependent launch: set when the previous kernel on the
+    // stream writes this call's metadata (lengths, page table), which the scorer's prologue
+    // reads before its grid-dependency wait
+    bool no_pdl;
 };
 
 struct TopkArgs {
@@ -103,6 +107,29 @@ cudaError_t launch_k_store(const KStoreArgs& a, cudaStream_t st);
 cudaError_t launch_q_quant(const QQuantArgs& a, cudaStream_t st);
 cudaError_t launch_qk_prep(const KStoreArgs& ka, const QQuantArgs& qa, cudaStream_t st);
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t st);
+
+// Candidate-pool scoring (idx_mqa_topk_cand_paged): per query, its candidate blocks sorted and
+// deduplicated into a virtual page table; the decode scorer and top-k then run on one virtual
+// sequence per query, and the indices are mapped back to key positions.
+struct CandArgs {
+    const int32_t* cu_seqlens_q;
+    const int32_t* seq_lens_k;
+    const int32_t* page_table;
+    int32_t pt_stride, B, causal, max_q_len, max_seq_len_k, page_size;
+    int64_t T;
+    const int32_t* cand;
+    int32_t cand_stride, max_cand;
+    const int32_t* n_cand;
+    // workspace: cu' [T+1], vlen [T], virtual page table and sorted blocks [T][max_cand]
+    int32_t* vcu;
+    int32_t* vlen;
+    int32_t* vpt;
+    int32_t* vblk;
+    int32_t* dev_status;
+};
+cudaError_t launch_cand_prep(const CandArgs& a, cudaStream_t st);
+cudaError_t launch_cand_map(const int32_t* vblk, int32_t max_cand, int32_t page_size, int64_t T, int32_t k,
+                            int32_t* out_idx, cudaStream_t st);
 cudaError_t launch_debug_encode(int kind, const float* in, int64_t n, uint8_t* out, cudaStream_t st);
 cudaError_t launch_scorer(const ScoreArgs& a, cudaStream_t st);
 cudaError_t launch_scorer_decode(const ScoreArgs& a, cudaStream_t st);

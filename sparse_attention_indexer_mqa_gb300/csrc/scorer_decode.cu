@@ -710,7 +710,7 @@ cudaError_t launch_np(const ScoreArgs& a, cudaStream_t st) {
     const int64_t units_max = (int64_t)a.B * ((a.max_seq_len_k + 127) / 128);
     const int ctas = C::kCps * sm_count();
     const int grid = (int)(units_max < ctas ? (units_max > 0 ? units_max : 1) : ctas);
-    return launch_pdl(decode_kernel<kDtype, NP, kSel>, dim3(grid), dim3(kThreads), C::kSmem, st, a);
+    return launch_k(!a.no_pdl, decode_kernel<kDtype, NP, kSel>, dim3(grid), dim3(kThreads), C::kSmem, st, a);
 }
 
 template <int kDtype, bool kSel>

@@ -351,6 +351,38 @@ def compress_b256(seed=0, B=256, **over) -> CompressWork:
                          norm=2, name=f"compress_mxfp4_r4_b{B}_raw1024-9472", **over)
 
 
+def candidate_blocks(wl, seed=0, n_blocks=16, messy=False):
+    """A stand-in for the two-level indexer's first level: per query, n_blocks distinct block
+    ids (blocks of page_size keys) drawn uniformly from its visible blocks, always including
+    the last one (the local window); all visible blocks when there are fewer. messy: the
+    lists also carry repeats and ids naming no visible block (negative, past the visible
+    blocks, past the sequence) in shuffled order. Returns (cand int32 [T, stride], n_cand
+    int32 [T], max_cand)."""
+    rng = _streams(seed + 7919, 1)[0]
+    vis = wl.visible()
+    P = wl.page_size
+    rows = []
+    for t in range(wl.T):
+        nb = int((vis[t] + P - 1) // P)
+        if nb == 0:
+            ids = np.zeros(0, np.int64)
+        elif nb <= n_blocks:
+            ids = np.arange(nb)
+        else:
+            ids = np.concatenate([rng.choice(nb - 1, n_blocks - 1, replace=False), [nb - 1]])
+        if messy and nb > 0:
+            junk = np.array([-1, nb, nb + 5, -(1 << 20), 1 << 28])
+            ids = np.concatenate([ids, rng.choice(ids, 3), rng.choice(junk, 3)])
+        rows.append(rng.permutation(ids).astype(np.int32))
+    max_cand = max(1, max(len(r) for r in rows))
+    cand = np.full((wl.T, max_cand + 3), -1, np.int32)
+    n_cand = np.zeros(wl.T, np.int32)
+    for t, r in enumerate(rows):
+        cand[t, :len(r)] = r
+        n_cand[t] = len(r)
+    return cand, n_cand, max_cand
+
+
 BUILDERS = {
     "tiny_decode": tiny_decode,
     "decode_b64": decode_b64,
