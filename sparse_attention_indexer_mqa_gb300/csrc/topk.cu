@@ -402,6 +402,267 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
     }
 }
 
+
+// Register-resident form for aligned rows of at most kT * kPer keys: thread (w, l) holds the
+// kPer consecutive keys from (32 w + l) * kPer on, read with kPer / 4 independent 16-byte
+// loads, so warp order, lane order and element order are index order and nothing is staged.
+//   1. smallest and largest key of the row;
+//   2. a 2048-bin histogram by a monotonic bin function: linear between the row's smallest
+//      and largest value (the few bins around the k-th value hold few keys each), or the top
+//      11 key bits when that range is not finite; the bin b0 of the k-th key;
+//   3. per-warp counts of the keys in higher bins, and the list of bin b0's keys;
+//   4. the k-th key among them: by direct ranking when the list is at most kT long, else by
+//      11/11/10-bit histograms of the listed keys (or of bin b0's keys re-read from the
+//      registers when the list overflowed);
+//   5. per-warp counts of listed keys above / equal to it, one scan over the warps, and the
+//      output written lane by lane in index order.
+template <int kT, int kPer>
+__global__ void __launch_bounds__(kT) topk_reg_kernel(TopkArgs a) {
+    constexpr int kW = kT / 32;
+    constexpr int kCandR = 2048;
+    static_assert(kPer % 4 == 0 && kW <= 32 && 2048 % kT == 0, "shape");
+    __shared__ uint32_t hist[2048];
+    __shared__ int32_t cand[kCandR];
+    __shared__ uint32_t ckey[kCandR];
+    __shared__ uint32_t warp_sums[kW], warp_gt[kW], warp_eq[kW];
+    __shared__ uint32_t sel[2], scal[6];  // scal: listed, min, max, k-th key, copies, taken-min
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t t = blockIdx.x;
+    const int b = seq_of_query(a.cu_seqlens_q, a.B, t);
+    for (int i = threadIdx.x; i < 2048; i += kT) hist[i] = 0;
+    if (threadIdx.x == 0) {
+        scal[0] = 0;
+        scal[1] = 0xffffffffu;
+        scal[2] = 0;
+        scal[4] = 0;
+        scal[5] = 0xffffffffu;
+    }
+    pdl_wait();  // the logits come from the previous kernel
+    pdl_launch_dependents();
+    int vis = 0;
+    if (b >= 0) {
+        const int64_t q0 = a.cu_seqlens_q[b], nq = a.cu_seqlens_q[b + 1] - q0;
+        const int32_t len = a.seq_lens_k[b];
+        if (len < 0 || len > a.max_len) {
+            if (threadIdx.x == 0) report(a.dev_status, IDX_STATUS_BAD_LEN);
+        } else {
+            vis = (int)visible_keys(len, nq, t - q0, a.causal);  // <= max_len <= kT * kPer
+        }
+    }
+    int32_t* out = a.out + t * a.k;
+    if (vis <= a.k) {
+        for (int i = threadIdx.x; i < a.k; i += kT) out[i] = i < vis ? i : -1;
+        return;
+    }
+    // 1. the thread's keys (indices i0 .. i0 + kPer - 1; those >= vis are not keys of the row)
+    const int i0 = (int)threadIdx.x * kPer;
+    const float4* row4 = reinterpret_cast<const float4*>(a.logits + t * a.ld) + threadIdx.x * (kPer / 4);
+    uint32_t key[kPer];
+    {
+        float4 v[kPer / 4];
+#pragma unroll
+        for (int q = 0; q < kPer / 4; ++q)
+            v[q] = i0 + 4 * q < vis ? row4[q] : make_float4(0.f, 0.f, 0.f, 0.f);  // in the row (ld % 4 == 0)
+#pragma unroll
+        for (int q = 0; q < kPer / 4; ++q) {
+            key[4 * q] = order_key(v[q].x);
+            key[4 * q + 1] = order_key(v[q].y);
+            key[4 * q + 2] = order_key(v[q].z);
+            key[4 * q + 3] = order_key(v[q].w);
+        }
+    }
+    const int nv = max(0, min(kPer, vis - i0));  // this thread's keys
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+        if (e < nv) {
+            kmin = min(kmin, key[e]);
+            kmax = max(kmax, key[e]);
+        }
+    }
+    kmin = __reduce_min_sync(kFull, kmin);
+    kmax = __reduce_max_sync(kFull, kmax);
+    if (lane == 0) {
+        atomicMin(&scal[1], kmin);
+        atomicMax(&scal[2], kmax);
+    }
+    __syncthreads();
+
+    // 2. histogram by a monotonic bin function; the bin of the k-th key
+    auto value_of = [](uint32_t k) { return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k); };
+    const float lo = value_of(scal[1]), hi = value_of(scal[2]);
+    const float span = hi - lo, scale = 2048.0f / span;
+    // x - lo >= 0 and the product are rounded monotonically: equal values share a bin and a
+    // larger value never falls into a lower bin
+    const bool linear = span > 0.0f && isfinite(span) && isfinite(scale) && isfinite(lo);
+    // floor of x in [0, 2^23): the bits of x + 2^23 rounded down (no float-to-int conversion)
+    auto bin_of = [&](uint32_t k) -> uint32_t {
+        if (!linear) return k >> 21;
+        const float x = fminf((value_of(k) - lo) * scale, 2047.0f);
+        return __float_as_uint(__fadd_rd(x, 8388608.0f)) - 0x4b000000u;
+    };
+    // the bins are kept in registers when the thread's keys are few
+    constexpr bool kKeepBins = kPer <= 8;
+    uint32_t bins[kKeepBins ? kPer : 1];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+        const uint32_t bn = bin_of(key[e]);
+        if constexpr (kKeepBins) bins[e] = bn;
+        if (e < nv) atomicAdd(&hist[bn], 1u);
+    }
+    auto bin_at = [&](int e) -> uint32_t {
+        if constexpr (kKeepBins) return bins[e];
+        else return bin_of(key[e]);
+    };
+    __syncthreads();
+    uint32_t b0, above;
+    select_bin<kT>(hist, 2048, (uint32_t)a.k, warp_sums, sel, b0, above);
+    uint32_t remaining = (uint32_t)a.k - above;
+
+    // 3. keys of higher bins counted per warp; bin b0's keys listed
+    uint32_t c_hi = 0;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+        if (e < nv) {
+            const uint32_t bn = bin_at(e);
+            c_hi += bn > b0;
+            if (bn == b0) {
+                const uint32_t p = atomicAdd(&scal[0], 1u);
+                if (p < (uint32_t)kCandR) {
+                    cand[p] = i0 + e;
+                    ckey[p] = key[e];
+                }
+            }
+        }
+    }
+    c_hi = __reduce_add_sync(kFull, c_hi);
+    if (lane == 0) {
+        warp_gt[warp] = c_hi;
+        warp_eq[warp] = 0;
+    }
+    __syncthreads();
+    const uint32_t nc = scal[0];
+    const bool listed = nc <= (uint32_t)kCandR;
+    constexpr int kChunk = 32 * kPer;  // keys per warp
+    auto for_each_cand = [&](auto&& f) {
+        if (listed) {
+            for (uint32_t j = threadIdx.x; j < nc; j += kT) f(cand[j], ckey[j]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < kPer; ++e)
+                if (e < nv && bin_at(e) == b0) f(i0 + e, key[e]);
+        }
+    };
+
+    // 4. the k-th key: the remaining-th largest among bin b0's keys
+    uint32_t kth;
+    if (listed && nc <= (uint32_t)kT) {
+        if (threadIdx.x < nc) {
+            const uint32_t mine = ckey[threadIdx.x];
+            uint32_t gt = 0, ge = 0;
+            for (uint32_t j = 0; j < nc; ++j) {
+                const uint32_t o = ckey[j];
+                gt += o > mine;
+                ge += o >= mine;
+            }
+            if (gt < remaining && remaining <= ge) {
+                scal[3] = mine;
+                scal[4] = remaining - gt;  // copies of the k-th key taken
+            }
+        }
+        __syncthreads();
+        kth = scal[3];
+        remaining = scal[4];
+    } else {
+        // histograms of the key bits [31:21], [20:10], [9:0] (the top 11 are bin b0's when
+        // the bins are the top key bits); when every key of a prefix is taken the k-th key is
+        // their minimum
+        uint32_t prefix = linear ? 0u : (b0 << 21);
+        uint32_t fixed = linear ? 0u : 0xffe00000u;
+        bool done = false;
+        for (int level = linear ? 0 : 1; level < 3 && !done; ++level) {
+            const int shift = level == 0 ? 21 : level == 1 ? 10 : 0;
+            const int nb = level == 2 ? 1024 : 2048;
+            for (int i = threadIdx.x; i < nb; i += kT) hist[i] = 0;
+            __syncthreads();
+            for_each_cand([&](int, uint32_t k) {
+                if ((k & fixed) == prefix) atomicAdd(&hist[(k >> shift) & (uint32_t)(nb - 1)], 1u);
+            });
+            __syncthreads();
+            uint32_t bin, ab;
+            select_bin<kT>(hist, nb, remaining, warp_sums, sel, bin, ab);
+            const uint32_t cnt = hist[bin];
+            prefix |= bin << shift;
+            fixed |= (uint32_t)(nb - 1) << shift;
+            remaining -= ab;
+            if (level < 2 && cnt == remaining) {
+                for_each_cand([&](int, uint32_t k) {
+                    if ((k & fixed) == prefix) atomicMin(&scal[5], k);
+                });
+                __syncthreads();
+                const uint32_t mn = scal[5];
+                for_each_cand([&](int, uint32_t k) {
+                    if (k == mn) atomicAdd(&scal[4], 1u);
+                });
+                __syncthreads();
+                prefix = mn;
+                remaining = scal[4];
+                done = true;
+            }
+        }
+        kth = prefix;
+    }
+
+    // 5. listed keys above / equal to the k-th complete the per-warp counts
+    for_each_cand([&](int i, uint32_t k) {
+        if (k > kth) atomicAdd(&warp_gt[i / kChunk], 1u);
+        else if (k == kth) atomicAdd(&warp_eq[i / kChunk], 1u);
+    });
+    __syncthreads();
+    if (warp == 0) {  // exclusive scans of the warps' counts
+        const uint32_t g = lane < kW ? warp_gt[lane] : 0u, q = lane < kW ? warp_eq[lane] : 0u;
+        uint32_t ig = g, iq = q;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t yg = __shfl_up_sync(kFull, ig, o), yq = __shfl_up_sync(kFull, iq, o);
+            if (lane >= o) {
+                ig += yg;
+                iq += yq;
+            }
+        }
+        if (lane < kW) {
+            warp_gt[lane] = ig - g;
+            warp_eq[lane] = iq - q;
+        }
+    }
+    __syncthreads();
+    uint32_t fg = 0, fe = 0;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+        fg |= (uint32_t)(e < nv && key[e] > kth) << e;
+        fe |= (uint32_t)(e < nv && key[e] == kth) << e;
+    }
+    const uint32_t cnt = (uint32_t)__popc(fg) | ((uint32_t)__popc(fe) << 16);
+    uint32_t inc = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += y;
+    }
+    const uint32_t ex = inc - cnt;
+    const uint32_t n_gt = (uint32_t)a.k - remaining;
+    uint32_t pg = warp_gt[warp] + (ex & 0xffffu), pe = warp_eq[warp] + (ex >> 16);
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+        if ((fg >> e) & 1u) out[pg++] = i0 + e;
+        if ((fe >> e) & 1u) {
+            if (pe < remaining) out[n_gt + pe] = i0 + e;
+            ++pe;
+        }
+    }
+}
+
 template <int kThreads, int kCand, bool kVec>
 cudaError_t launch_form(const TopkArgs& a, cudaStream_t st) {
     const int keys = (int)(a.ld < kSmemKeysMax ? a.ld : kSmemKeysMax);
@@ -421,6 +682,11 @@ cudaError_t launch_threads(const TopkArgs& a, cudaStream_t st) {
 
 }  // namespace
 
+template <int kT, int kPer>
+cudaError_t launch_reg(const TopkArgs& a, cudaStream_t st) {
+    return launch_pdl(topk_reg_kernel<kT, kPer>, dim3((unsigned)a.T), dim3(kT), 0, st, a);
+}
+
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
     if (a.T == 0) return cudaSuccess;
     // more rows than SMs and short rows: narrower CTAs, several resident per SM; otherwise
@@ -429,6 +695,12 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
+    // at most one row per SM, aligned rows of at most 16K keys: the register-resident form,
+    // whose shorter phase chain finishes a row sooner (16-byte loads need ld % 4 == 0 and a
+    // 16-byte aligned base; a row's keys past max_len are never read). With more rows the
+    // shared-memory form keeps more rows resident per SM.
+    if (a.T <= sms && a.ld % 4 == 0 && ((uintptr_t)a.logits & 15) == 0 && a.max_len <= 16384)
+        return a.max_len <= 8192 ? launch_reg<1024, 8>(a, st) : launch_reg<1024, 16>(a, st);
     return (a.T > sms && a.ld <= kNarrowKeysMax) ? launch_threads<512, 1024>(a, st)
                                                  : launch_threads<1024, 2048>(a, st);
 }

@@ -145,3 +145,21 @@ def test_topk_causal_prefill_rows(torch):
         mat = rng.standard_normal((int(nq.sum()), ld)).astype(np.float32)
         _, got = run_rows(torch, mat, 512, causal=1, cu=cu, seq_lens=lens)
         check(mat, got, lens, cu, 1, 512)
+
+
+@pytest.mark.parametrize("lens,n_rows", [((8191, 8192, 100), 8), ((8193, 16384, 9000), 8),
+                                         ((16385, 20000), 4), ((8192, 3000, 5000), 300)])
+def test_topk_form_boundaries(torch, lens, n_rows):
+    """Each launch shape on aligned rows: up to 8192 keys with few rows (1024 threads, 8 keys
+    each) or many rows (512 threads, 16 each), up to 16384 keys (1024 x 16), and longer rows
+    (the shared-memory form); the many-row case mixes in tied rows whose candidates overflow."""
+    rng = np.random.default_rng(8)
+    rows = []
+    for i in range(n_rows):
+        n = lens[i % len(lens)]
+        r = rng.standard_normal(n).astype(np.float32) * rng.uniform(0.1, 50)
+        if i % 7 == 3:
+            r = rng.integers(0, 4, n).astype(np.float32)
+        rows.append(r)
+    L = max(len(r) for r in rows)
+    _decode(torch, rows, 1024, ld=(L + 3) // 4 * 4)
