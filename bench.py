@@ -203,6 +203,8 @@ class Replica:
         self.w = torch.zeros((T, H), dtype=torch.float32, device=device)
         self.logits = torch.empty((T, wl.ld_logits), dtype=torch.float32, device=device)
         self.topk = torch.empty((T, wl.topk), dtype=torch.int32, device=device)
+        # the scorer's scheduling workspace (zeroed once; every call leaves it zero)
+        self.sched_ws = torch.zeros(Bn.idx_mqa_logits_workspace_bytes(), dtype=torch.uint8, device=device)
         # workspace of the fused scorer -> top-k (zeroed once: its counters start at zero)
         n_ws = Bn.idx_mqa_topk_workspace_bytes(T, H, wl.B, self.max_q, self.max_k)
         self.workspace = torch.zeros(max(n_ws, 256), dtype=torch.uint8, device=device)
@@ -234,7 +236,7 @@ class Replica:
             Bn.idx_mqa_logits_paged(self.q_codes, self.q_scales, self.w, wl.dtype, pool,
                                     wl.pool_pages, wl.page_size, wl.page_stride, self.page_table,
                                     self.seq_lens_k, self.cu, wl.causal, self.max_q, self.max_k,
-                                    self.logits)
+                                    self.logits, workspace=self.sched_ws)
         elif name == "scorer_topk":
             Bn.idx_mqa_topk_paged(self.q_codes, self.q_scales, self.w, wl.dtype, pool, wl.pool_pages,
                                   wl.page_size, wl.page_stride, self.page_table, self.seq_lens_k,

@@ -218,14 +218,23 @@ int idx_qk_prep(const uint16_t* k, int64_t n_rows, int64_t k_row_stride, const i
  * INT32_MAX / 32 (IDX_EUNSUPPORTED otherwise); logits fp32, 16-byte aligned.
  * Products are exact in the tensor core; sums are fp32. Accuracy against the exact
  * (fp64) scores: |error| <= 1e-4 * max_s |logit[t,s]| per row.
+ * workspace (optional, may be NULL): at least idx_mqa_logits_workspace_bytes() bytes of device
+ *   memory, 16-byte aligned, zero-filled by the caller before its first use; every call leaves
+ *   it zero again. With it, a decode call (max_q_len <= 1) with at most 256 sequences hands the
+ *   (sequence, 128-key tile) units out dynamically: each CTA claims small jobs from a counter
+ *   there, so CTAs that start late take less work. The logits are the same either way. One
+ *   workspace serves one call at a time (calls that overlap on the GPU need their own).
  */
+int idx_mqa_logits_workspace_bytes(size_t* bytes);
+
 int idx_mqa_logits_paged(const uint8_t* q_codes, const void* q_scales, const float* w,
                          int64_t T, int32_t H, int32_t dtype, const void* pool,
                          int64_t num_pages, int32_t page_size, int64_t page_stride,
                          const int32_t* page_table, int32_t pt_stride,
                          const int32_t* seq_lens_k, const int32_t* cu_seqlens_q, int32_t B,
                          int32_t causal, int32_t max_q_len, int32_t max_seq_len_k,
-                         float* logits, int64_t ld_logits, int32_t* dev_status,
+                         float* logits, int64_t ld_logits, void* workspace,
+                         size_t workspace_bytes, int32_t* dev_status,
                          cudaStream_t stream);
 
 /*

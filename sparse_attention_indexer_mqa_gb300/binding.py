@@ -76,7 +76,8 @@ def _declare(L):
     L.idx_qk_prep.argtypes = [vp, i64, i64, vp, vp, i32, i32, vp, vp, f32, vp, i64, i32, i64,
                               vp, i64, i32, vp, i32, vp, f32, f32, vp, vp, vp, vp, i32, i32, vp, vp]
     L.idx_mqa_logits_paged.argtypes = [vp, vp, vp, i64, i32, i32, vp, i64, i32, i64, vp, i32, vp,
-                                       vp, i32, i32, i32, i32, vp, i64, vp, vp]
+                                       vp, i32, i32, i32, i32, vp, i64, vp, C.c_size_t, vp, vp]
+    L.idx_mqa_logits_workspace_bytes.argtypes = [C.POINTER(C.c_size_t)]
     L.idx_topk.argtypes = [vp, i64, vp, vp, i32, i64, i32, i32, i32, vp, vp, vp]
     L.idx_debug_encode.argtypes = [i32, vp, i64, vp, vp]
     L.idx_mqa_topk_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, C.POINTER(C.c_size_t)]
@@ -94,7 +95,8 @@ def _declare(L):
     for n in ("idx_cache_layout", "idx_k_store", "idx_q_quant", "idx_qk_prep", "idx_mqa_logits_paged",
               "idx_topk", "idx_debug_encode", "idx_mqa_topk_workspace_bytes", "idx_mqa_topk_paged",
               "idx_debug_mma_rate", "idx_mqa_topk_paged_noalloc", "idx_compress_k_store",
-              "idx_mqa_topk_cand_workspace_bytes", "idx_mqa_topk_cand_paged"):
+              "idx_mqa_topk_cand_workspace_bytes", "idx_mqa_topk_cand_paged",
+              "idx_mqa_logits_workspace_bytes"):
         getattr(L, n).restype = C.c_int
 
 
@@ -187,13 +189,20 @@ def idx_qk_prep(k, slot_mapping, k_positions, k_rope, apply_norm, pool, num_page
 
 def idx_mqa_logits_paged(q_codes, q_scales, w, dtype, pool, num_pages, page_size, page_stride,
                          page_table, seq_lens_k, cu_seqlens_q, causal, max_q_len, max_seq_len_k,
-                         logits, dev_status=None, stream=None):
+                         logits, dev_status=None, stream=None, workspace=None):
     T, H = w.shape
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("idx_mqa_logits_paged", load().idx_mqa_logits_paged(
         _ptr(q_codes), _ptr(q_scales), _ptr(w), T, H, dtype, _ptr(pool), num_pages, page_size,
         page_stride, _ptr(page_table), page_table.shape[1], _ptr(seq_lens_k), _ptr(cu_seqlens_q),
         seq_lens_k.shape[0], int(causal), max_q_len, max_seq_len_k, _ptr(logits),
-        logits.stride(0), _ptr(dev_status), _stream(stream)))
+        logits.stride(0), _ptr(workspace), wsb, _ptr(dev_status), _stream(stream)))
+
+
+def idx_mqa_logits_workspace_bytes() -> int:
+    n = C.c_size_t(0)
+    _check("idx_mqa_logits_workspace_bytes", load().idx_mqa_logits_workspace_bytes(C.byref(n)))
+    return int(n.value)
 
 
 def idx_topk(logits, seq_lens_k, cu_seqlens_q, causal, max_seq_len_k, k, out_idx,

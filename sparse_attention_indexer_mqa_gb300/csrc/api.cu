@@ -25,6 +25,7 @@ inline bool valid_rope(int32_t r) {
 }
 inline int64_t page_bytes(int32_t dtype, int32_t P) { return (dtype == IDX_MXFP4 ? 68 : 132) * (int64_t)P; }
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? IDX_OK : IDX_ECUDA; }
+constexpr size_t kLogitsWorkspaceBytes = 256;  // the decode schedule's two counters, padded
 
 // common pool checks: page size, stride, alignment
 int check_pool(int32_t dtype, const void* pool, int64_t num_pages, int32_t page_size,
@@ -215,8 +216,8 @@ int idx_mqa_logits_paged(const uint8_t* q_codes, const void* q_scales, const flo
                          const int32_t* page_table, int32_t pt_stride,
                          const int32_t* seq_lens_k, const int32_t* cu_seqlens_q, int32_t B,
                          int32_t causal, int32_t max_q_len, int32_t max_seq_len_k,
-                         float* logits, int64_t ld_logits, int32_t* dev_status,
-                         cudaStream_t stream) {
+                         float* logits, int64_t ld_logits, void* workspace, size_t workspace_bytes,
+                         int32_t* dev_status, cudaStream_t stream) {
     Range r("idx_mqa_logits_paged");
     int st = check_pool(dtype, pool, num_pages, page_size, page_stride);
     if (st != IDX_OK) return st;
@@ -237,7 +238,17 @@ int idx_mqa_logits_paged(const uint8_t* q_codes, const void* q_scales, const flo
     a.pt_stride = pt_stride; a.seq_lens_k = seq_lens_k; a.cu_seqlens_q = cu_seqlens_q; a.B = B;
     a.causal = causal != 0; a.max_q_len = max_q_len; a.max_seq_len_k = max_seq_len_k;
     a.logits = logits; a.ld = ld_logits; a.dev_status = dev_status;
+    if (workspace) {
+        if (!aligned(workspace, 16) || workspace_bytes < kLogitsWorkspaceBytes) return IDX_EINVAL;
+        a.counters = static_cast<int32_t*>(workspace);  // the dynamic decode schedule's counters
+    }
     return cuda_status(idx::launch_scorer(a, stream));
+}
+
+int idx_mqa_logits_workspace_bytes(size_t* bytes) {
+    if (!bytes) return IDX_EINVAL;
+    *bytes = kLogitsWorkspaceBytes;
+    return IDX_OK;
 }
 
 int idx_topk(const float* logits, int64_t ld_logits, const int32_t* seq_lens_k,

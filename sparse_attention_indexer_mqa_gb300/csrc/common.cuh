@@ -26,9 +26,14 @@ __device__ __forceinline__ void report(int32_t* status, int32_t bit) {
 // the stream finishes. Before pdl_wait() a kernel only reads caller inputs that no kernel of
 // the path writes (lengths, page table, positions, RoPE table, bf16 q / k, head weights) and
 // sets up shared and tensor memory; it writes nothing. pdl_wait() returns once the previous
-// grid has completed and its memory is visible (at once when there is no such grid);
-// pdl_launch_dependents(), issued only after pdl_wait(), lets the next kernel start early, so
-// at most two consecutive kernels overlap and the earlier one has finished all its waiting.
+// grid has completed and its memory is visible (at once when there is no such grid).
+// pdl_launch_dependents() lets the next kernel start early. The scorers and the top-k issue it
+// after their pdl_wait(); the pre-processing kernels (K store, Q quant, both, compressor),
+// whose own work all follows their wait, issue it at entry, so that the scorer's prologue also
+// overlaps the kernel before them. Either way every CTA of a kernel is resident before its
+// dependent launches (no dependent can hold the resources a CTA of it still needs), and a
+// kernel's pdl_wait() returning means its predecessor, and everything that one waited for,
+// has completed.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

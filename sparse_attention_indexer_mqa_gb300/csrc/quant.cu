@@ -198,7 +198,6 @@ __device__ __forceinline__ void quant_store(const float* x, int l16, bool ok, ui
         uint32_t word, sbyte;
         mx_quant(x, word, sbyte);
         pdl_wait();  // the cache may still be read by the previous kernel
-        pdl_launch_dependents();
         // gather the 4 words of a 16-byte chunk (= one scale block) into its first lane
         uint32_t w1 = __shfl_down_sync(kFull, word, 1);
         uint32_t w2 = __shfl_down_sync(kFull, word, 2);
@@ -219,7 +218,6 @@ __device__ __forceinline__ void quant_store(const float* x, int l16, bool ok, ui
         float scale;
         f8_quant(x, lo, hi, scale);
         pdl_wait();
-        pdl_launch_dependents();
         uint32_t plo = __shfl_down_sync(kFull, lo, 1);
         uint32_t phi = __shfl_down_sync(kFull, hi, 1);
         if (ok && (l16 & 1) == 0) {
@@ -375,7 +373,6 @@ __device__ __forceinline__ void q_quant_rows(const QQuantArgs& a, int64_t t, int
         uint32_t word, sbyte;
         mx_quant(x, word, sbyte);
         pdl_wait();  // the Q image and weights may still be read by the previous kernel
-        pdl_launch_dependents();
         const uint32_t s1 = __shfl_down_sync(kFull, sbyte, 4);
         const uint32_t s2 = __shfl_down_sync(kFull, sbyte, 8);
         const uint32_t s3 = __shfl_down_sync(kFull, sbyte, 12);
@@ -399,7 +396,6 @@ __device__ __forceinline__ void q_quant_rows(const QQuantArgs& a, int64_t t, int
         float scale;
         f8_quant(x, lo, hi, scale);
         pdl_wait();
-        pdl_launch_dependents();
         const uint32_t plo = __shfl_down_sync(kFull, lo, 1);
         const uint32_t phi = __shfl_down_sync(kFull, hi, 1);
         if (ok || !real) {
@@ -414,13 +410,17 @@ __device__ __forceinline__ void q_quant_rows(const QQuantArgs& a, int64_t t, int
     }
 }
 
+// The pre-processing kernels let their dependents launch at entry (see common.cuh): all their
+// own work follows their wait, and the next kernel's prologue then overlaps the one before.
 template <int kDtype>
 __global__ void __launch_bounds__(kThreads) k_store_kernel(KStoreArgs a) {
+    pdl_launch_dependents();
     k_store_rows<kDtype>(a, blockIdx.x);
 }
 
 template <int kDtype>
 __global__ void __launch_bounds__(kThreads) q_quant_kernel(QQuantArgs a) {
+    pdl_launch_dependents();
     q_quant_rows<kDtype>(a, blockIdx.x, blockIdx.y);
 }
 
@@ -428,6 +428,7 @@ __global__ void __launch_bounds__(kThreads) q_quant_kernel(QQuantArgs a) {
 // nk + t*ny + y takes token t's head block y). The two halves touch disjoint buffers.
 template <int kDtype>
 __global__ void __launch_bounds__(kThreads) qk_prep_kernel(KStoreArgs ka, QQuantArgs qa, int64_t nk, int ny) {
+    pdl_launch_dependents();
     const int64_t b = blockIdx.x;
     if (b < nk) {
         k_store_rows<kDtype>(ka, b);
@@ -441,6 +442,7 @@ __global__ void __launch_bounds__(kThreads) qk_prep_kernel(KStoreArgs ka, QQuant
 
 template <int kDtype>
 __global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
+    pdl_launch_dependents();
     compress_rows<kDtype>(a, blockIdx.x);
 }
 

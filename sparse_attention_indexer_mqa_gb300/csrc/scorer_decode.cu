@@ -688,6 +688,402 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
     }
 }
 
+
+// ---- dynamic schedule ---------------------------------------------------------------------
+// With a caller workspace and at most kDynB sequences, the units are handed out as jobs of up
+// to kJob tiles of one sequence: CTA i starts with job i and claims further jobs from a
+// counter in the workspace, so CTAs that start late (their SM still busy with the previous
+// kernel) or run slow take fewer tiles and the launch ends when the work does, not when the
+// last static slice does. The producer publishes each job (sequence, first tile, tile count)
+// in a ring of kJR records that the MMA thread and the epilogue warps read in order; every
+// job loads its query into its own Q slot. The CTA that finishes last (a second counter)
+// zeroes both counters for the next call.
+constexpr int kDynB = 256;  // sequences the job tables hold
+constexpr int kJob = 2;     // tiles per job
+constexpr int kJR = 8;      // job records in flight
+
+template <int kDtype, int NP>
+struct DynCfg {
+    using C = Cfg<kDtype, NP>;
+    // records (16-byte aligned int4), then (t, vis) and the job prefix
+    static constexpr int kTab = kJR * 16 + kDynB * 8 + (kDynB + 1) * 4;
+    static constexpr int kFixed = C::kQS * (C::kQImg + C::kQSf) + 64 + 16 + kTab +
+                                  8 * (2 * C::kQS + 1 + 2 * kAccG + 2 * kJR);
+    static constexpr int kSG = (C::kBudget - kFixed) / (C::kGroup + 16);
+    static constexpr int oStages = 0;
+    static constexpr int oQ = kSG * C::kGroup;
+    static constexpr int oQSf = oQ + C::kQS * C::kQImg;
+    static constexpr int oBars = oQSf + C::kQS * C::kQSf;
+    static constexpr int kBars = 2 * kSG + 2 * C::kQS + 1 + 2 * kAccG + 2 * kJR;
+    static constexpr int oMisc = oBars + 8 * kBars;
+    static constexpr int oTab = (oMisc + 64 + 15) & ~15;  // the int4 records need 16-byte alignment
+    static constexpr int kSmem = oTab + kTab;
+    static_assert(kSG >= kJob, "a job's tiles fit the stage ring at once");
+    static_assert(oTab % 16 == 0 && oBars % 8 == 0, "alignment of the records and barriers");
+    static_assert(kSmem <= C::kBudget, "shared memory of the CTAs sharing an SM");
+};
+
+template <int kDtype, int NP>
+__global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_dyn_kernel(ScoreArgs a) {
+    using C = Cfg<kDtype, NP>;
+    using D = DynCfg<kDtype, NP>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + D::oBars);
+    uint64_t* k_full = bars;
+    uint64_t* k_empty = k_full + D::kSG;
+    uint64_t* q_full = k_empty + D::kSG;
+    uint64_t* q_empty = q_full + C::kQS;
+    uint64_t* acc_full = q_empty + C::kQS;
+    uint64_t* acc_empty = acc_full + kAccG;
+    uint64_t* drain = acc_empty + kAccG;
+    uint64_t* j_full = drain + 1;     // a record was written (the producer's arrival)
+    uint64_t* j_empty = j_full + kJR;  // a record was read (MMA thread + one lane per epilogue warp)
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + D::oMisc);  // [0] tmem, [1] jobs, [2] abort
+    volatile uint32_t* abort_flag = misc + 2;
+    int4* jrec = reinterpret_cast<int4*>(smem + D::oTab);                    // [kJR] (b, first tile, tiles, -)
+    int32_t* seq_t = reinterpret_cast<int32_t*>(smem + D::oTab + kJR * 16);  // [kDynB] query row
+    int32_t* seq_vis = seq_t + kDynB;                                         // [kDynB] visible keys
+    int32_t* jpre = seq_vis + kDynB;                                          // [kDynB + 1] jobs before b
+    int32_t* counters = a.counters;  // [0] next job - gridDim.x, [1] CTAs finished
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = a.H, P = a.page_size;
+    const int lp = P == 128 ? 7 : 6;
+    const int Hq = (H + 7) & ~7;
+    const uint64_t keep = tc::policy_evict_last();
+
+    // ---- prologue: every sequence's query row, visible keys and jobs (eight per lane) -------
+    if (warp == 0) {
+        bool bad = false;
+        int32_t carry = 0;
+        SeqInfo si[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int b = 32 * k + lane;
+            si[k] = b < a.B ? seq_info(a, b, keep, &bad) : SeqInfo{0, 0, 0};
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (32 * k >= a.B) break;
+            const int b = 32 * k + lane;
+            const int32_t n = (si[k].tiles + kJob - 1) / kJob;
+            int32_t inc = n;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t y = __shfl_up_sync(kFull, inc, o);
+                if (lane >= o) inc += y;
+            }
+            if (b < a.B) {
+                seq_t[b] = si[k].t;
+                seq_vis[b] = si[k].vis;
+                jpre[b] = carry + inc - n;
+            }
+            carry += __shfl_sync(kFull, inc, 31);
+        }
+        if (lane == 0) {
+            jpre[a.B] = carry;
+            misc[1] = (uint32_t)carry;
+            misc[2] = 0;
+        }
+        if (__any_sync(kFull, bad) && blockIdx.x == 0 && lane == 0) report(a.dev_status, IDX_STATUS_BAD_LEN);
+        for (int i = lane; i < D::kSG; i += 32) {
+            tc::mbar_init(&k_full[i], 1);
+            tc::mbar_init(&k_empty[i], 1);
+        }
+        if (lane < C::kQS) {
+            tc::mbar_init(&q_full[lane], 1);
+            tc::mbar_init(&q_empty[lane], 1);
+        }
+        if (lane == 0) tc::mbar_init(drain, 1);
+        if (lane < kAccG) {
+            tc::mbar_init(&acc_full[lane], 1);
+            tc::mbar_init(&acc_empty[lane], kEpiThreads);
+        }
+        if (lane < kJR) {
+            tc::mbar_init(&j_full[lane], 1);
+            tc::mbar_init(&j_empty[lane], 5);
+        }
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(&misc[0], C::kCols);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (warp != 0) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
+    const uint32_t tbase = misc[0];
+    const int32_t n_jobs = (int32_t)misc[1];
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer warp
+        // Job c of sequence b (jpre[b] <= c < jpre[b + 1]) holds tiles kJob * (c - jpre[b]) on;
+        // lane L issues tile L of the job (its page lookups, stage wait and copies).
+        const uint64_t stream = tc::policy_evict_first();
+        int32_t c = (int32_t)blockIdx.x;  // the first job needs no claim
+        int32_t next = -1;
+        int64_t i = 0;  // tiles issued so far
+        int64_t q = 0;  // jobs published so far
+        int64_t armed_g = -1, armed_q = -1;
+        bool dep_done = false;
+        for (;;) {
+            if (__any_sync(kFull, *abort_flag != 0)) break;
+            const int slot = (int)(q % kJR);
+            const bool end = c >= n_jobs;
+            int b = 0, j0 = 0, n = 0;
+            if (!end) {
+                int lo = 0, hi = a.B;  // the sequence of job c: jpre[lo] <= c < jpre[hi]
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (jpre[mid] <= c) lo = mid; else hi = mid;
+                }
+                b = lo;
+                j0 = kJob * (c - jpre[b]);
+                n = min(kJob, (seq_vis[b] + 127) / 128 - j0);
+            }
+            // the record: wait until its slot's previous record was read by every consumer
+            if (lane == 0) {
+                if (!tc::mbar_wait(&j_empty[slot], (uint32_t)(((q / kJR) & 1) ^ 1))) {
+                    *abort_flag = 1;
+                } else {
+                    jrec[slot] = make_int4(end ? -1 : b, j0, n, 0);
+                    tc::mbar_arrive(&j_full[slot]);
+                }
+            }
+            __syncwarp();
+            if (end || *abort_flag) break;
+            int32_t pg[2] = {-1, -1};
+            int halves = 0;
+            const int vis = seq_vis[b];
+            if (lane < n) {
+                const int64_t key0 = (int64_t)(j0 + lane) * 128;
+                halves = P == 128 ? 1 : (key0 + 64 < vis ? 2 : 1);
+                const int32_t* pt = a.page_table + (int64_t)b * a.pt_stride;
+                pg[0] = tc::ld_hint(pt + (key0 >> lp), keep);
+                if (halves == 2) pg[1] = tc::ld_hint(pt + ((key0 + 64) >> lp), keep);
+            }
+            if (!dep_done) {  // Q, the cache and the counters come from the previous kernels
+                pdl_wait();
+                pdl_launch_dependents();
+                dep_done = true;
+            }
+            // claim the job after this one (its latency hides behind this job's copies)
+            if (lane == 0) next = atomicAdd(counters, 1) + (int32_t)gridDim.x;
+            if (lane == 0) {
+                const int qs = (int)(q % C::kQS);
+                if (!tc::mbar_wait(&q_empty[qs], (uint32_t)(((q / C::kQS) & 1) ^ 1))) {
+                    *abort_flag = 1;
+                } else {
+                    const uint32_t qbytes = (uint32_t)(Hq * C::kQRow);
+                    const int32_t t = seq_t[b];
+                    tc::mbar_arrive_expect_tx(&q_full[qs], qbytes + C::kQSf);
+                    tc::bulk_g2s(smem + D::oQ + qs * C::kQImg, a.q_codes + (int64_t)t * Hq * C::kQRow, qbytes,
+                                 &q_full[qs]);
+                    if (kDtype == IDX_MXFP4)
+                        tc::bulk_g2s(smem + D::oQSf + qs * C::kQSf, a.q_scales + (int64_t)t * 512, 512, &q_full[qs]);
+                }
+            }
+            if (lane < n) {
+                const int64_t it = i + lane;
+                const int grp = (int)(it % D::kSG);
+                if (*abort_flag || !tc::mbar_wait(&k_empty[grp], (uint32_t)(((it / D::kSG) & 1) ^ 1))) {
+                    *abort_flag = 1;
+                } else {
+                    uint32_t bytes = 0;
+                    for (int h = 0; h < halves; ++h) {
+                        if (pg[h] >= 0 && pg[h] < a.num_pages) {
+                            bytes += (uint32_t)(P * (C::kTileCode / 128 + C::kTileSf / 128));
+                        } else {
+                            report(a.dev_status, IDX_STATUS_BAD_PAGE);
+                            pg[h] = -1;
+                        }
+                    }
+                    tc::mbar_arrive_expect_tx(&k_full[grp], bytes);
+                    uint8_t* dK = smem + D::oStages + grp * C::kGroup;
+                    uint8_t* dS = dK + C::kTileCode;
+                    for (int h = 0; h < halves; ++h) {
+                        if (pg[h] < 0) continue;
+                        const uint8_t* src = a.pool + (int64_t)pg[h] * a.page_stride;
+                        if (P == 128) {
+                            tc::bulk_g2s_hint(dK, src, C::kTile, &k_full[grp], stream);
+                        } else if (kDtype == IDX_MXFP4) {
+                            for (int qq = 0; qq < 4; ++qq)
+                                tc::bulk_g2s_hint(dK + qq * 2048 + h * 1024, src + qq * 1024, 1024, &k_full[grp], stream);
+                            tc::bulk_g2s_hint(dS + h * 256, src + 4096, 256, &k_full[grp], stream);
+                        } else {
+                            tc::bulk_g2s_hint(dK + h * 8192, src, 8192, &k_full[grp], stream);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            armed_g = i + n - 1;
+            armed_q = q;
+            i += n;
+            ++q;
+            c = __shfl_sync(kFull, next, 0);
+        }
+        if (*abort_flag) {
+            const uint64_t deadline = tc::global_ns() + tc::kWaitLimitNs;
+            if (lane < D::kSG && armed_g >= lane) {
+                const int64_t g = armed_g - ((armed_g - lane) % D::kSG);
+                tc::mbar_wait_until(&k_full[lane], (uint32_t)((g / D::kSG) & 1), deadline);
+            }
+            if (lane < C::kQS && armed_q >= lane) {
+                const int64_t g = armed_q - ((armed_q - lane) % C::kQS);
+                tc::mbar_wait_until(&q_full[lane], (uint32_t)((g / C::kQS) & 1), deadline);
+            }
+            if (lane == 0) {
+                // the consumers stop at the abort flag or at a record that never comes
+                report(a.dev_status, IDX_STATUS_TIMEOUT);
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------------------------------------------------------- MMA issuer
+        const uint32_t t_sfa = tbase + kAccG * NP;
+        const uint32_t t_sfb = t_sfa + kAccG * 4;
+        const uint64_t dA0 = tc::smem_desc(tc::smem_u32(smem + D::oStages), 128, C::kSbo);
+        const uint64_t dB0 = tc::smem_desc(tc::smem_u32(smem + D::oQ), 128, C::kSbo);
+        const uint64_t dSA0 = tc::smem_desc(tc::smem_u32(smem + D::oStages + C::kTileCode), 128, 128);
+        const uint64_t dSB0 = tc::smem_desc(tc::smem_u32(smem + D::oQSf), 128, 128);
+        const uint32_t id0 = kDtype == IDX_MXFP4 ? tc::idesc_mxf4(128, NP, 0, 0) : tc::idesc_f8(128, NP);
+        const uint32_t id1 = kDtype == IDX_MXFP4 ? tc::idesc_mxf4(128, NP, 2, 2) : id0;
+        int grp = 0, ag = 0;
+        uint32_t kph = 0, aph = 1;
+        for (int64_t q = 0;; ++q) {
+            const int slot = (int)(q % kJR);
+            if (*abort_flag || !tc::mbar_wait(&j_full[slot], (uint32_t)((q / kJR) & 1))) {
+                *abort_flag = 1;
+                break;
+            }
+            const int4 r = jrec[slot];
+            tc::mbar_arrive(&j_empty[slot]);
+            if (r.x < 0) break;
+            const int qs = (int)(q % C::kQS);
+            if (!tc::mbar_wait(&q_full[qs], (uint32_t)((q / C::kQS) & 1))) {
+                *abort_flag = 1;
+                break;
+            }
+            tc::tc_fence_after();
+            if (kDtype == IDX_MXFP4) tc::cp_32x128b_warpx4(t_sfb + 4 * qs, dSB0 + (uint64_t)((qs * C::kQSf) >> 4));
+            for (int t = 0; t < r.z; ++t) {
+                if (!tc::mbar_wait(&k_full[grp], kph) || !tc::mbar_wait(&acc_empty[ag], aph)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                tc::tc_fence_after();
+                const uint32_t d = tbase + ag * NP;
+                const int off = grp * C::kGroup;
+                const uint64_t da = dA0 + (uint64_t)(off >> 4);
+                const uint64_t db = dB0 + (uint64_t)((qs * C::kQImg) >> 4);
+                if (kDtype == IDX_MXFP4) {
+                    const uint32_t sfa = t_sfa + 4 * ag;
+                    tc::cp_32x128b_warpx4(sfa, dSA0 + (uint64_t)(off >> 4));
+                    tc::mma_mxf4(d, da, db, id0, sfa, t_sfb + 4 * qs, 0);
+                    tc::mma_mxf4(d, da + 16, db + 16, id1, sfa, t_sfb + 4 * qs, 1);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) tc::mma_f8(d, da + 16 * k, db + 16 * k, id0, k);
+                }
+                if (t + 1 == r.z) tc::mma_commit(&q_empty[qs]);
+                tc::mma_commit(&k_empty[grp]);
+                tc::mma_commit(&acc_full[ag]);
+                if (++grp == D::kSG) { grp = 0; kph ^= 1; }
+                if (++ag == kAccG) { ag = 0; aph ^= 1; }
+            }
+            if (*abort_flag) break;
+        }
+        if (*abort_flag) {
+            report(a.dev_status, IDX_STATUS_TIMEOUT);
+            tc::mma_commit(drain);
+            tc::mbar_wait(drain, 0);
+        }
+    } else if (warp >= 2) {
+        // ---------------------------------------------------------------- epilogue
+        const int quad = warp & 3;
+        const int m = quad * 32 + lane;
+        const uint32_t lane_addr = tbase + ((uint32_t)(quad * 32) << 16);
+        const bool split = P == 64 && kDtype == IDX_MXFP4;
+        const int half = split ? ((m >> 4) & 1) : (m >> 6);
+        const int koff = split ? (64 * half + (m & 15) + 16 * (m >> 5)) : m;
+        float wr[NP];
+        int ag = 0;
+        uint32_t aph = 0;
+        for (int64_t q = 0;; ++q) {
+            const int slot = (int)(q % kJR);
+            const bool got = __all_sync(kFull, *abort_flag == 0 && tc::mbar_wait(&j_full[slot], (uint32_t)((q / kJR) & 1)));
+            if (!got) {
+                *abort_flag = 1;
+                report(a.dev_status, IDX_STATUS_TIMEOUT);
+                break;
+            }
+            const int4 r = jrec[slot];
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&j_empty[slot]);
+            if (r.x < 0) break;
+            const int32_t t_q = seq_t[r.x], vis = seq_vis[r.x];
+#pragma unroll
+            for (int h = 0; h < NP; ++h) wr[h] = h < H ? __ldg(a.w + (int64_t)t_q * H + h) : 0.0f;
+            bool stop = false;
+            for (int t = 0; t < r.z; ++t) {
+                const int64_t key = (int64_t)(r.y + t) * 128 + koff;
+                const int32_t pg = key < vis ? tc::ld_hint(a.page_table + (int64_t)r.x * a.pt_stride + (key >> lp), keep)
+                                             : -1;
+                const bool ok = __all_sync(kFull, tc::mbar_wait(&acc_full[ag], aph));
+                if (!ok) {
+                    *abort_flag = 1;
+                    report(a.dev_status, IDX_STATUS_TIMEOUT);
+                    stop = true;
+                    break;
+                }
+                tc::tc_fence_after();
+                const bool key_ok = key < vis && pg >= 0 && pg < a.num_pages;
+                float kscale = 1.0f;
+                if (kDtype == IDX_FP8 && key_ok)
+                    kscale = __ldg(reinterpret_cast<const float*>(a.pool + (int64_t)pg * a.page_stride + 128 * P +
+                                                                  4 * ((key & (P - 1)))));
+                constexpr int CH = NP < 32 ? NP : 32;
+                float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int cc = 0; cc < NP; cc += CH) {
+                    float v[CH];
+                    load_acc<CH>(lane_addr + ag * NP + cc, v);
+#pragma unroll
+                    for (int h = 0; h < CH; ++h)
+                        if (cc + h < H) part[h & 3] = fmaf(wr[cc + h], fmaxf(v[h], 0.0f), part[h & 3]);
+                }
+                const float logit = (part[0] + part[1]) + (part[2] + part[3]);
+                if (key_ok) a.logits[(int64_t)t_q * a.ld + key] = logit * kscale;
+                tc::tc_fence_before();
+                tc::mbar_arrive(&acc_empty[ag]);
+                if (++ag == kAccG) { ag = 0; aph ^= 1; }
+            }
+            if (stop) break;
+        }
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tbase, C::kCols);
+    }
+    if (tid == 0) {
+        // every claim of this CTA has returned; the last CTA to get here zeroes the counters
+        // (not before the previous kernels are done: they may still be resetting them)
+        pdl_wait();
+        __threadfence();
+        if (atomicAdd(counters + 1, 1) == (int32_t)gridDim.x - 1) {
+            counters[0] = 0;
+            counters[1] = 0;
+        }
+    }
+}
+
 int sm_count() {
     static int n = 0;
     if (n == 0) {
@@ -713,6 +1109,26 @@ cudaError_t launch_np(const ScoreArgs& a, cudaStream_t st) {
     return launch_k(!a.no_pdl, decode_kernel<kDtype, NP, kSel>, dim3(grid), dim3(kThreads), C::kSmem, st, a);
 }
 
+template <int kDtype, int NP>
+cudaError_t launch_dyn_np(const ScoreArgs& a, cudaStream_t st) {
+    using D = DynCfg<kDtype, NP>;
+    cudaError_t e = cudaFuncSetAttribute(decode_dyn_kernel<kDtype, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         D::kSmem);
+    if (e != cudaSuccess) return e;
+    // no more CTAs than jobs could exist (a CTA whose first job does not exist exits at once)
+    const int64_t jobs_max = (int64_t)a.B * (((a.max_seq_len_k + 127) / 128 + kJob - 1) / kJob);
+    const int ctas = Cfg<kDtype, NP>::kCps * sm_count();
+    const int grid = (int)(jobs_max < ctas ? (jobs_max > 0 ? jobs_max : 1) : ctas);
+    return launch_k(!a.no_pdl, decode_dyn_kernel<kDtype, NP>, dim3(grid), dim3(kThreads), D::kSmem, st, a);
+}
+
+template <int kDtype>
+cudaError_t launch_dyn_dt(const ScoreArgs& a, cudaStream_t st) {
+    if (a.H <= 16) return launch_dyn_np<kDtype, 16>(a, st);
+    if (a.H <= 32) return launch_dyn_np<kDtype, 32>(a, st);
+    return launch_dyn_np<kDtype, 64>(a, st);
+}
+
 template <int kDtype, bool kSel>
 cudaError_t launch_dt(const ScoreArgs& a, cudaStream_t st) {
     if (a.H <= 16) return launch_np<kDtype, 16, kSel>(a, st);
@@ -724,6 +1140,9 @@ cudaError_t launch_dt(const ScoreArgs& a, cudaStream_t st) {
 
 cudaError_t launch_scorer_decode(const ScoreArgs& a, cudaStream_t st) {
     if (a.T == 0 || a.max_seq_len_k == 0 || a.B == 0) return cudaSuccess;
+    // the dynamic schedule: a workspace for its counters and at most kDynB sequences
+    if (a.counters && a.B <= kDynB)
+        return a.dtype == IDX_MXFP4 ? launch_dyn_dt<IDX_MXFP4>(a, st) : launch_dyn_dt<IDX_FP8>(a, st);
     return a.dtype == IDX_MXFP4 ? launch_dt<IDX_MXFP4, false>(a, st) : launch_dt<IDX_FP8, false>(a, st);
 }
 

@@ -112,7 +112,7 @@ class Dev:
                        wl.softmax_scale, wl.head_scale, wl.dtype, self.q_codes, self.q_scales,
                        self.w, dev_status=self.status)
 
-    def score(self, page_table=None):
+    def score(self, page_table=None, workspace=None):
         from sparse_attention_indexer_mqa_gb300 import binding as Bn
         wl = self.wl
         nq = np.diff(wl.cu_seqlens_q)
@@ -120,7 +120,8 @@ class Dev:
                                 wl.pool_pages, wl.page_size, wl.page_stride,
                                 self.page_table if page_table is None else page_table,
                                 self.seq_lens_k, self.cu, wl.causal, int(nq.max()),
-                                int(wl.seq_lens_k.max()), self.logits, dev_status=self.status)
+                                int(wl.seq_lens_k.max()), self.logits, dev_status=self.status,
+                                workspace=workspace)
 
     def select(self):
         from sparse_attention_indexer_mqa_gb300 import binding as Bn

@@ -68,9 +68,14 @@ def test_host_validation(lib):
     assert lib.idx_topk(16, 8, 16, 16, 1, 1, 0, 9, 32, 16, None, None) == -1
     # scorer: ld below max_seq_len_k, page table stride too small
     assert lib.idx_mqa_logits_paged(16, 16, 16, 1, 4, 0, 16, 1, 64, 4352, 16, 1, 16, 16, 1, 0, 1,
-                                    100, 16, 64, None, None) == -1
+                                    100, 16, 64, None, 0, None, None) == -1
     assert lib.idx_mqa_logits_paged(16, 16, 16, 1, 4, 0, 16, 1, 64, 4352, 16, 1, 16, 16, 1, 0, 1,
-                                    100, 16, 128, None, None) == -1
+                                    100, 16, 128, None, 0, None, None) == -1
+    # scorer: a workspace that is misaligned or too small
+    assert lib.idx_mqa_logits_paged(16, 16, 16, 1, 4, 0, 16, 1, 64, 4352, 16, 1, 16, 16, 1, 0, 1,
+                                    64, 16, 64, 8, 256, None, None) == -1
+    assert lib.idx_mqa_logits_paged(16, 16, 16, 1, 4, 0, 16, 1, 64, 4352, 16, 1, 16, 16, 1, 0, 1,
+                                    64, 16, 64, 16, 8, None, None) == -1
     # fused K store + Q quant: bad dtype, H out of range, unsupported page size
     qk = lambda dtype, H, P: lib.idx_qk_prep(16, 1, 128, 16, None, 0, 0, None, None, 1e-6, 16, 1, P,
                                              4352, 16, 1, H, None, 0, 16, 1.0, 1.0, 16, 16, 16,
