@@ -753,6 +753,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_dyn_ke
     const uint64_t keep = tc::policy_evict_last();
 
     // ---- prologue: every sequence's query row, visible keys and jobs (eight per lane) -------
+    int32_t pre_pg[2] = {-1, -1};  // warp 0: the first job's pages (lane L: tile L)
     if (warp == 0) {
         bool bad = false;
         int32_t carry = 0;
@@ -785,7 +786,26 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_dyn_ke
             misc[1] = (uint32_t)carry;
             misc[2] = 0;
         }
+        __syncwarp();
         if (__any_sync(kFull, bad) && blockIdx.x == 0 && lane == 0) report(a.dev_status, IDX_STATUS_BAD_LEN);
+        // the first job's page lookups (job blockIdx.x) go out now: their round trip overlaps
+        // the barrier set-up and the CTA barrier below
+        if ((int32_t)blockIdx.x < carry) {
+            const int32_t c0 = (int32_t)blockIdx.x;
+            int lo = 0, hi = a.B;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (jpre[mid] <= c0) lo = mid; else hi = mid;
+            }
+            const int32_t j00 = kJob * (c0 - jpre[lo]);
+            const int32_t n0 = min(kJob, (seq_vis[lo] + 127) / 128 - j00);
+            if (lane < n0) {
+                const int64_t key0 = (int64_t)(j00 + lane) * 128;
+                const int32_t* pt = a.page_table + (int64_t)lo * a.pt_stride;
+                pre_pg[0] = tc::ld_hint(pt + (key0 >> lp), keep);
+                if (P == 64 && key0 + 64 < seq_vis[lo]) pre_pg[1] = tc::ld_hint(pt + ((key0 + 64) >> lp), keep);
+            }
+        }
         for (int i = lane; i < D::kSG; i += 32) {
             tc::mbar_init(&k_full[i], 1);
             tc::mbar_init(&k_empty[i], 1);
@@ -862,9 +882,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_dyn_ke
             if (lane < n) {
                 const int64_t key0 = (int64_t)(j0 + lane) * 128;
                 halves = P == 128 ? 1 : (key0 + 64 < vis ? 2 : 1);
-                const int32_t* pt = a.page_table + (int64_t)b * a.pt_stride;
-                pg[0] = tc::ld_hint(pt + (key0 >> lp), keep);
-                if (halves == 2) pg[1] = tc::ld_hint(pt + ((key0 + 64) >> lp), keep);
+                if (q == 0) {  // looked up in the prologue
+                    pg[0] = pre_pg[0];
+                    pg[1] = pre_pg[1];
+                } else {
+                    const int32_t* pt = a.page_table + (int64_t)b * a.pt_stride;
+                    pg[0] = tc::ld_hint(pt + (key0 >> lp), keep);
+                    if (halves == 2) pg[1] = tc::ld_hint(pt + ((key0 + 64) >> lp), keep);
+                }
             }
             if (!dep_done) {  // Q, the cache and the counters come from the previous kernels
                 pdl_wait();
