@@ -163,3 +163,25 @@ def test_topk_form_boundaries(torch, lens, n_rows):
         rows.append(r)
     L = max(len(r) for r in rows)
     _decode(torch, rows, 1024, ld=(L + 3) // 4 * 4)
+
+
+@pytest.mark.parametrize("ld_pad", [0, 1])
+def test_topk_many_rows_narrowing_fallback(torch, ld_pad):
+    """Many rows (the shared-memory form): rows where an outlier spreads the key range, rows
+    half tied at one value, rows of two values only; both the aligned and the unaligned
+    row layout."""
+    rng = np.random.default_rng(9)
+    rows = []
+    for i in range(320):
+        n = int(rng.integers(1100, 6000))
+        r = (rng.standard_normal(n) * 3).astype(np.float32)
+        if i % 3 == 0:
+            r[rng.integers(0, n)] = np.float32(1e30)
+        if i % 5 == 0:
+            r[rng.random(n) < 0.5] = np.float32(0.75)
+        if i % 7 == 0:
+            r[:] = np.float32(-2.0)
+            r[rng.integers(0, n, 50)] = np.float32(-1.0)
+        rows.append(r)
+    L = max(len(r) for r in rows)
+    _decode(torch, rows, 1024, ld=(L + 3) // 4 * 4 + ld_pad)
