@@ -133,6 +133,29 @@ def test_store_quant_fp8_full(torch, fused):
     _check_store_and_quant(W.make("prefill_fp8"), "fp8 prefill, full size", fused)
 
 
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("dtype", [W.MXFP4, W.FP8])
+def test_store_quant_many_tokens(torch, dtype, fused):
+    """Enough tokens for the Q quant's several-tokens-per-CTA launch (2501 tokens x 2 head
+    blocks; the last CTA's group is ragged), bit-exact against the oracle."""
+    rng = np.random.default_rng(77)
+    n, H, P = 2501, 32, 128
+    pages = (n + P - 1) // P + 1
+    perm = rng.permutation(pages).astype(np.int32)
+    slots = perm[np.arange(n) // P].astype(np.int64) * P + np.arange(n) % P
+    wl = W.Workload(
+        name="many", dtype=dtype, B=1, H=H, page_size=P, pool_pages=pages, base_offset_pages=0,
+        page_stride=W.page_bytes(dtype, P), seq_lens_k=np.array([n], np.int32),
+        cu_seqlens_q=np.array([0, n], np.int32), page_table=perm[None, :], causal=1, topk=8,
+        k=W.bf16_bits(rng.standard_normal((n, 128)).astype(np.float32)), slot_mapping=slots,
+        k_positions=np.arange(n, dtype=np.int32), k_rope=W.ROPE_NEOX, k_norm=1, step_rows=np.arange(n),
+        q=W.bf16_bits((rng.standard_normal((n, H, 128)) * 4).astype(np.float32)),
+        q_positions=np.arange(n, dtype=np.int32), q_rope=W.ROPE_NEOX,
+        w_in=rng.standard_normal((n, H)).astype(np.float32), softmax_scale=0.088388, head_scale=1.0,
+        cos_sin=W.rope_table(n), ld_logits=n)
+    _check_store_and_quant(wl, f"many tokens dtype={dtype} fused={fused}", fused)
+
+
 def test_qk_prep_one_side_empty(torch):
     """idx_qk_prep with no K rows only quantises Q; with no queries only stores K."""
     import torch as T
