@@ -366,6 +366,14 @@ int idx_mqa_topk_paged_noalloc(const uint8_t* q_codes, const void* q_scales, con
 int idx_debug_mma_rate(int32_t dtype, int32_t iters, int32_t* dev_status, double* flops_per_cta,
                        cudaStream_t stream);
 
+/*
+ * Test hook for the bounded waits: one CTA whose thread waits, with the wait helper every
+ * kernel of the library uses, for an mbarrier phase that nothing completes, gives up after
+ * limit_us microseconds (1 .. 1000000) of global time, sets IDX_STATUS_TIMEOUT in *dev_status
+ * and returns; the context stays usable. *dev_status: a device int32 (required).
+ */
+int idx_debug_wait_timeout(int32_t limit_us, int32_t* dev_status, cudaStream_t stream);
+
 /* Human-readable name of an idx_status value (static string). */
 const char* idx_status_string(int status);
 

@@ -90,13 +90,14 @@ def _declare(L):
     L.idx_mqa_topk_cand_paged.argtypes = [vp, vp, vp, i64, i32, i32, vp, i64, i32, i64, vp, i32, vp,
                                           vp, i32, i32, i32, i32, vp, i32, vp, i32, i32, vp, vp,
                                           C.c_size_t, vp, vp]
+    L.idx_debug_wait_timeout.argtypes = [i32, vp, vp]
     L.idx_compress_k_store.argtypes = [vp, vp, i64, i64, vp, vp, i64, i32, vp, vp, vp, i32, i32, i32,
                                        vp, vp, f32, i32, vp, i64, i32, i64, vp, vp]
     for n in ("idx_cache_layout", "idx_k_store", "idx_q_quant", "idx_qk_prep", "idx_mqa_logits_paged",
               "idx_topk", "idx_debug_encode", "idx_mqa_topk_workspace_bytes", "idx_mqa_topk_paged",
               "idx_debug_mma_rate", "idx_mqa_topk_paged_noalloc", "idx_compress_k_store",
               "idx_mqa_topk_cand_workspace_bytes", "idx_mqa_topk_cand_paged",
-              "idx_mqa_logits_workspace_bytes"):
+              "idx_mqa_logits_workspace_bytes", "idx_debug_wait_timeout"):
         getattr(L, n).restype = C.c_int
 
 
@@ -256,6 +257,11 @@ def idx_mqa_topk_cand_paged(q_codes, q_scales, w, dtype, pool, num_pages, page_s
 def idx_debug_encode(kind, x, out, stream=None):
     _check("idx_debug_encode", load().idx_debug_encode(kind, _ptr(x), x.numel(), _ptr(out),
                                                        _stream(stream)))
+
+
+def idx_debug_wait_timeout(limit_us, dev_status, stream=None):
+    _check("idx_debug_wait_timeout", load().idx_debug_wait_timeout(int(limit_us), _ptr(dev_status),
+                                                                   _stream(stream)))
 
 
 def idx_debug_mma_rate(dtype, iters, dev_status=None, stream=None) -> float:

@@ -50,6 +50,11 @@ int idx_debug_mma_rate(int32_t dtype, int32_t iters, int32_t* dev_status, double
     return cuda_status(idx::launch_mma_rate(dtype, iters, dev_status, stream));
 }
 
+int idx_debug_wait_timeout(int32_t limit_us, int32_t* dev_status, cudaStream_t stream) {
+    if (!dev_status || limit_us < 1 || limit_us > 1000000) return IDX_EINVAL;
+    return cuda_status(idx::launch_wait_timeout(limit_us, dev_status, stream));
+}
+
 const char* idx_status_string(int status) {
     switch (status) {
         case IDX_OK: return "ok";

@@ -144,6 +144,9 @@ cudaError_t launch_scorer_prefill_select(const ScoreArgs& a, cudaStream_t st);
 int prefill_queries_per_block(int32_t H);
 int device_sm_count();
 
+// Bounded-wait test hook (idx_debug_wait_timeout).
+cudaError_t launch_wait_timeout(int32_t limit_us, int32_t* status, cudaStream_t st);
+
 // Dense tensor-core rate probe (idx_debug_mma_rate): one CTA per SM, `iters` loop iterations.
 cudaError_t launch_mma_rate(int32_t dtype, int32_t iters, int32_t* status, cudaStream_t st);
 int mma_rate_flops_per_iter(int32_t dtype);

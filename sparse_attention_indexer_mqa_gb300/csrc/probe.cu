@@ -68,7 +68,23 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, int32_t* st
     }
 }
 
+// One thread waits for phase 0 of an mbarrier whose arrival count is never reached (nothing
+// arrives on it), gives up at the deadline and reports the timeout.
+__global__ void wait_timeout_kernel(int64_t limit_ns, int32_t* status) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    tc::mbar_init(&bar, 1);
+    tc::fence_mbar_init();
+    const uint64_t deadline = tc::global_ns() + (uint64_t)limit_ns;
+    if (!tc::mbar_wait_until(&bar, 0, deadline)) report(status, IDX_STATUS_TIMEOUT);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_timeout(int32_t limit_us, int32_t* status, cudaStream_t st) {
+    wait_timeout_kernel<<<1, 32, 0, st>>>((int64_t)limit_us * 1000, status);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_mma_rate(int32_t dtype, int32_t iters, int32_t* status, cudaStream_t st) {
     int dev = 0, sms = 0;

@@ -119,3 +119,19 @@ def test_sched_length_and_page_faults(torch):
     assert out["dynamic"][1] == st
     np.testing.assert_array_equal(out["dynamic"][0], out["static"][0])
     assert np.isnan(out["static"][0][3]).all()
+
+
+def test_bounded_wait_gives_up_and_reports(torch):
+    """A wait on an mbarrier that nothing completes (the wait helper all kernels use) gives
+    up after its limit, sets IDX_STATUS_TIMEOUT and returns; the context stays usable (a
+    scorer call right after runs normally)."""
+    import time
+    from sparse_attention_indexer_mqa_gb300 import binding as Bn
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    Bn.idx_debug_wait_timeout(20000, status)  # 20 ms
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert int(status.item()) == Bn.IDX_STATUS_TIMEOUT
+    assert 0.015 < dt < 5.0
+    _static_vs_dynamic(torch, W.make("tiny_decode"), "after a timeout")
