@@ -549,17 +549,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                                     for (int i = 0; i < kColsQ / 4; ++i) {
                                         const float4 w4 = w4p[i];
                                         const uint32_t* x = r + 16 * sc + qq * kColsQ + 4 * i;
+                                        // chain 0: ReLU by max (ALU pipe); chain 1: by x + |x| = 2 ReLU(x)
+                                        // (FMA pipe), so chain 1 holds twice its sum, halved below:
+                                        // both scalings by 2 are exact, the sum is the same
+                                        const float x2 = __uint_as_float(x[2]), x3 = __uint_as_float(x[3]);
                                         acc[qq][0] = __ffma2_rn(make_float2(w4.x, w4.y),
                                                                 make_float2(fmaxf(__uint_as_float(x[0]), 0.0f),
                                                                             fmaxf(__uint_as_float(x[1]), 0.0f)),
                                                                 acc[qq][0]);
                                         acc[qq][1] = __ffma2_rn(make_float2(w4.z, w4.w),
-                                                                make_float2(fmaxf(__uint_as_float(x[2]), 0.0f),
-                                                                            fmaxf(__uint_as_float(x[3]), 0.0f)),
+                                                                make_float2(x2 + fabsf(x2), x3 + fabsf(x3)),
                                                                 acc[qq][1]);
                                     }
                                     if (h0 + kColsQ == HP) {
-                                        const float2 s2 = __fadd2_rn(acc[qq][0], acc[qq][1]);
+                                        const float2 s2 = __ffma2_rn(acc[qq][1], make_float2(0.5f, 0.5f), acc[qq][0]);
                                         lrow[q * ld + key] = (s2.x + s2.y) * kscale;
                                     }
                                 }
