@@ -352,7 +352,7 @@ def run_gpu(args, rank, world):
         achieved = ab["scorer"] / sc_s / 1e9
         roof = {"kernel": "scorer", "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": profile_traffic(f"scorer:{args.config}", SCORER_SOURCES),
+                "traffic": profile_traffic(f"scorer:{args.config}", DECODE_SOURCES),
                 "algorithmic_bytes": ab["scorer"], "peak_source": f"{peak_kind} (hbm_gbs)"}
     else:
         roof = prefill_roofline(wl, per_kernel_ms["scorer"], peaks, peak_kind)
@@ -423,7 +423,7 @@ def prefill_roofline(wl, scorer_ms, peaks, peak_kind):
     return {"kernel": "scorer", "bound": "alu", "achieved": round(alu / 1e12, 2),
             "peak": round(alu_peak_ops(peaks) / 1e12, 2), "unit": "T instr/s",
             "frac": round(alu / alu_peak_ops(peaks), 4),
-            "traffic": profile_traffic(f"scorer:{wl_key(wl)}", SCORER_SOURCES),
+            "traffic": profile_traffic(f"scorer:{wl_key(wl)}", PREFILL_SOURCES),
             "algorithmic_ops": scorer_alu_ops(wl),
             "peak_source": "issue rate 4x32 lanes x 152 SMs x measured max SM clock",
             "tensor": {"achieved_tflops": round(scorer_flops(wl) / sc_s / 1e12, 1),
@@ -842,15 +842,18 @@ def run_reference(args, rank, world):
     }
 
 
-SCORER_SOURCES = ["sparse_attention_indexer_mqa_gb300/csrc/scorer_decode.cu",
-                  "sparse_attention_indexer_mqa_gb300/csrc/scorer_prefill.cu",
+# the sources each kernel is built from (a stored DRAM-traffic figure counts only while they
+# are unchanged)
+DECODE_SOURCES = ["sparse_attention_indexer_mqa_gb300/csrc/scorer_decode.cu",
                   "sparse_attention_indexer_mqa_gb300/csrc/tc.cuh",
                   "sparse_attention_indexer_mqa_gb300/csrc/common.cuh",
-                  "sparse_attention_indexer_mqa_gb300/csrc/select.cuh",
-                  "sparse_attention_indexer_mqa_gb300/csrc/kernels.h"]
+                  "sparse_attention_indexer_mqa_gb300/csrc/select.cuh"]
+PREFILL_SOURCES = ["sparse_attention_indexer_mqa_gb300/csrc/scorer_prefill.cu",
+                   "sparse_attention_indexer_mqa_gb300/csrc/tc.cuh",
+                   "sparse_attention_indexer_mqa_gb300/csrc/common.cuh",
+                   "sparse_attention_indexer_mqa_gb300/csrc/select.cuh"]
 COMPRESS_SOURCES = ["sparse_attention_indexer_mqa_gb300/csrc/quant.cu",
-                    "sparse_attention_indexer_mqa_gb300/csrc/common.cuh",
-                    "sparse_attention_indexer_mqa_gb300/csrc/kernels.h"]
+                    "sparse_attention_indexer_mqa_gb300/csrc/common.cuh"]
 
 
 def run_block(args):
