@@ -71,6 +71,9 @@ def alu_peak_ops(peaks):
     return 4 * 32 * 152 * peaks.get("sm_max_mhz", 2070.0) * 1e6
 
 
+# nominal HBM3e bandwidth of the part (the roofline's peak is the measured copy rate)
+HBM_SPEC_GBS = 7900.0
+
 # nominal dense tensor rates relative to bf16 (2.25 PF bf16, 4.5 PF fp8, 13.5 PF fp4)
 TENSOR_RATIO = {W.MXFP4: 6.0, W.FP8: 2.0}
 
@@ -352,6 +355,8 @@ def run_gpu(args, rank, world):
         achieved = ab["scorer"] / sc_s / 1e9
         roof = {"kernel": "scorer", "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "frac_of_spec": round(achieved / HBM_SPEC_GBS, 4),
+                "cache_tokens_per_s": round(int(wl.seq_lens_k.sum()) / sc_s, 1),
                 "traffic": profile_traffic(f"scorer:{args.config}", DECODE_SOURCES),
                 "algorithmic_bytes": ab["scorer"], "peak_source": f"{peak_kind} (hbm_gbs)"}
     else:
@@ -806,11 +811,18 @@ def cpu_baseline(wl, budget_s=15.0, rows_per_step=None):
         if time.perf_counter() - t0 > budget_s or reps >= 50:
             break
     dt = time.perf_counter() - t0
+    # the same step on one core (one step, or a quarter of the sampled rows when that is long)
+    rows1 = rows if len(rows) <= 16 else rows[:: max(1, len(rows) // 16)]
+    t1 = time.perf_counter()
+    pairs1 = oracle_step(wl, pool, rows1, 1)
+    dt1 = time.perf_counter() - t1
     return {"value": round(pairs / dt / 1e3, 3), "unit": "K-tokens/s", "cores": n_threads,
             "kind": "oracle",
             "sample": f"{reps} oracle step(s): K store of {len(wl.step_rows)} new keys, Q quant, "
                       f"fp64 scoring and top-k of {len(rows)} of {wl.T} queries spread evenly "
-                      f"({pairs // reps} pairs per step), {dt:.1f} s"}
+                      f"({pairs // reps} pairs per step), {dt:.1f} s",
+            "single_core": {"value": round(pairs1 / dt1 / 1e3, 3), "unit": "K-tokens/s",
+                            "sample": f"one step on one thread, {len(rows1)} query rows, {dt1:.1f} s"}}
 
 
 def run_reference(args, rank, world):
