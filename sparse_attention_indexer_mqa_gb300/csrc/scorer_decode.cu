@@ -102,6 +102,21 @@ struct SeqInfo {  // 32-bit: T <= INT32_MAX and lengths are int32 (checked by th
     int32_t t, vis, tiles;
 };
 
+// The same from the three values already loaded (cu_seqlens_q[b], cu_seqlens_q[b+1], seq_lens_k[b]).
+__device__ __forceinline__ SeqInfo seq_info_of(const ScoreArgs& a, int32_t q0, int32_t q1, int32_t len, bool* bad) {
+    SeqInfo r{0, 0, 0};
+    const int32_t nq = q1 - q0;
+    if (nq == 0) return r;
+    if (nq < 0 || nq > a.max_q_len || len < 0 || len > a.max_seq_len_k) {
+        *bad = true;
+        return r;
+    }
+    r.t = q0;
+    r.vis = (int32_t)visible_keys(len, nq, nq - 1, a.causal);
+    r.tiles = (r.vis + 127) / 128;
+    return r;
+}
+
 __device__ __forceinline__ SeqInfo seq_info(const ScoreArgs& a, int b, uint64_t keep, bool* bad = nullptr) {
     const int32_t q0 = tc::ld_hint(a.cu_seqlens_q + b, keep), q1 = tc::ld_hint(a.cu_seqlens_q + b + 1, keep);
     const int32_t len = tc::ld_hint(a.seq_lens_k + b, keep);
@@ -705,16 +720,20 @@ constexpr int kJR = 8;      // job records in flight
 template <int kDtype, int NP>
 struct DynCfg {
     using C = Cfg<kDtype, NP>;
+    // Q slots: every job loads its query into the next slot, so the slot ring bounds the jobs
+    // in flight; four for every head count (the static kernel keeps two for 64 heads)
+    static constexpr int kQS = 4;
+    static_assert(kAccG * (NP + 4) + 4 * kQS <= (int)C::kCols, "B scale slots fit the tensor memory");
     // records (16-byte aligned int4), then (t, vis) and the job prefix
     static constexpr int kTab = kJR * 16 + kDynB * 8 + (kDynB + 1) * 4;
-    static constexpr int kFixed = C::kQS * (C::kQImg + C::kQSf) + 64 + 16 + kTab +
-                                  8 * (2 * C::kQS + 1 + 2 * kAccG + 2 * kJR);
+    static constexpr int kFixed = kQS * (C::kQImg + C::kQSf) + 64 + 16 + kTab +
+                                  8 * (2 * kQS + 1 + 2 * kAccG + 2 * kJR);
     static constexpr int kSG = (C::kBudget - kFixed) / (C::kGroup + 16);
     static constexpr int oStages = 0;
     static constexpr int oQ = kSG * C::kGroup;
-    static constexpr int oQSf = oQ + C::kQS * C::kQImg;
-    static constexpr int oBars = oQSf + C::kQS * C::kQSf;
-    static constexpr int kBars = 2 * kSG + 2 * C::kQS + 1 + 2 * kAccG + 2 * kJR;
+    static constexpr int oQSf = oQ + kQS * C::kQImg;
+    static constexpr int oBars = oQSf + kQS * C::kQSf;
+    static constexpr int kBars = 2 * kSG + 2 * kQS + 1 + 2 * kAccG + 2 * kJR;
     static constexpr int oMisc = oBars + 8 * kBars;
     static constexpr int oTab = (oMisc + 64 + 15) & ~15;  // the int4 records need 16-byte alignment
     static constexpr int kSmem = oTab + kTab;
@@ -732,8 +751,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_dyn_ke
     uint64_t* k_full = bars;
     uint64_t* k_empty = k_full + D::kSG;
     uint64_t* q_full = k_empty + D::kSG;
-    uint64_t* q_empty = q_full + C::kQS;
-    uint64_t* acc_full = q_empty + C::kQS;
+    uint64_t* q_empty = q_full + D::kQS;
+    uint64_t* acc_full = q_empty + D::kQS;
     uint64_t* acc_empty = acc_full + kAccG;
     uint64_t* drain = acc_empty + kAccG;
     uint64_t* j_full = drain + 1;     // a record was written (the producer's arrival)
@@ -757,12 +776,21 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_dyn_ke
     if (warp == 0) {
         bool bad = false;
         int32_t carry = 0;
-        SeqInfo si[8];
+        // every sequence's three values are loaded before any is used: one round trip
+        int32_t q0[8], q1[8], len[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int b = 32 * k + lane;
-            si[k] = b < a.B ? seq_info(a, b, keep, &bad) : SeqInfo{0, 0, 0};
+            q0[k] = q1[k] = len[k] = 0;
+            if (b < a.B) {
+                q0[k] = tc::ld_hint(a.cu_seqlens_q + b, keep);
+                q1[k] = tc::ld_hint(a.cu_seqlens_q + b + 1, keep);
+                len[k] = tc::ld_hint(a.seq_lens_k + b, keep);
+            }
         }
+        SeqInfo si[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) si[k] = seq_info_of(a, q0[k], q1[k], len[k], &bad);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             if (32 * k >= a.B) break;
@@ -810,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_dyn_ke
             tc::mbar_init(&k_full[i], 1);
             tc::mbar_init(&k_empty[i], 1);
         }
-        if (lane < C::kQS) {
+        if (lane < D::kQS) {
             tc::mbar_init(&q_full[lane], 1);
             tc::mbar_init(&q_empty[lane], 1);
         }
@@ -899,8 +927,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_dyn_ke
             // claim the job after this one (its latency hides behind this job's copies)
             if (lane == 0) next = atomicAdd(counters, 1) + (int32_t)gridDim.x;
             if (lane == 0) {
-                const int qs = (int)(q % C::kQS);
-                if (!tc::mbar_wait(&q_empty[qs], (uint32_t)(((q / C::kQS) & 1) ^ 1))) {
+                const int qs = (int)(q % D::kQS);
+                if (!tc::mbar_wait(&q_empty[qs], (uint32_t)(((q / D::kQS) & 1) ^ 1))) {
                     *abort_flag = 1;
                 } else {
                     const uint32_t qbytes = (uint32_t)(Hq * C::kQRow);
@@ -958,9 +986,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_dyn_ke
                 const int64_t g = armed_g - ((armed_g - lane) % D::kSG);
                 tc::mbar_wait_until(&k_full[lane], (uint32_t)((g / D::kSG) & 1), deadline);
             }
-            if (lane < C::kQS && armed_q >= lane) {
-                const int64_t g = armed_q - ((armed_q - lane) % C::kQS);
-                tc::mbar_wait_until(&q_full[lane], (uint32_t)((g / C::kQS) & 1), deadline);
+            if (lane < D::kQS && armed_q >= lane) {
+                const int64_t g = armed_q - ((armed_q - lane) % D::kQS);
+                tc::mbar_wait_until(&q_full[lane], (uint32_t)((g / D::kQS) & 1), deadline);
             }
             if (lane == 0) {
                 // the consumers stop at the abort flag or at a record that never comes
@@ -988,8 +1016,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_dyn_ke
             const int4 r = jrec[slot];
             tc::mbar_arrive(&j_empty[slot]);
             if (r.x < 0) break;
-            const int qs = (int)(q % C::kQS);
-            if (!tc::mbar_wait(&q_full[qs], (uint32_t)((q / C::kQS) & 1))) {
+            const int qs = (int)(q % D::kQS);
+            if (!tc::mbar_wait(&q_full[qs], (uint32_t)((q / D::kQS) & 1))) {
                 *abort_flag = 1;
                 break;
             }
