@@ -706,7 +706,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
 
 // ---- dynamic schedule ---------------------------------------------------------------------
 // With a caller workspace and at most kDynB sequences, the units are handed out as jobs of up
-// to kJob tiles of one sequence: CTA i starts with job i and claims further jobs from a
+// to kJob tiles of one sequence (about half the stage ring; never more than the ring, since a
+// job's tiles go out at once, one per lane, and no lane may wait for a stage that a tile of the
+// same job has to free): CTA i starts with job i and claims further jobs from a
 // counter in the workspace, so CTAs that start late (their SM still busy with the previous
 // kernel) or run slow take fewer tiles and the launch ends when the work does, not when the
 // last static slice does. The producer publishes each job (sequence, first tile, tile count)
@@ -714,7 +716,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_kernel
 // job loads its query into its own Q slot. The CTA that finishes last (a second counter)
 // zeroes both counters for the next call.
 constexpr int kDynB = 256;  // sequences the job tables hold
-constexpr int kJob = 2;     // tiles per job
 constexpr int kJR = 8;      // job records in flight
 
 template <int kDtype, int NP>
@@ -729,6 +730,9 @@ struct DynCfg {
     static constexpr int kFixed = kQS * (C::kQImg + C::kQSf) + 64 + 16 + kTab +
                                   8 * (2 * kQS + 1 + 2 * kAccG + 2 * kJR);
     static constexpr int kSG = (C::kBudget - kFixed) / (C::kGroup + 16);
+    // tiles per job: about half the stage ring, so that the next job's copies overlap this
+    // one's (measured: 4 with ten stages, 2 with four; 1 was slower everywhere)
+    static constexpr int kJob = kSG >= 8 ? 4 : (kSG >= 2 ? 2 : 1);
     static constexpr int oStages = 0;
     static constexpr int oQ = kSG * C::kGroup;
     static constexpr int oQSf = oQ + kQS * C::kQImg;
@@ -795,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_dyn_ke
         for (int k = 0; k < 8; ++k) {
             if (32 * k >= a.B) break;
             const int b = 32 * k + lane;
-            const int32_t n = (si[k].tiles + kJob - 1) / kJob;
+            const int32_t n = (si[k].tiles + D::kJob - 1) / D::kJob;
             int32_t inc = n;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -825,8 +829,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_dyn_ke
                 const int mid = (lo + hi) >> 1;
                 if (jpre[mid] <= c0) lo = mid; else hi = mid;
             }
-            const int32_t j00 = kJob * (c0 - jpre[lo]);
-            const int32_t n0 = min(kJob, (seq_vis[lo] + 127) / 128 - j00);
+            const int32_t j00 = D::kJob * (c0 - jpre[lo]);
+            const int32_t n0 = min(D::kJob, (seq_vis[lo] + 127) / 128 - j00);
             if (lane < n0) {
                 const int64_t key0 = (int64_t)(j00 + lane) * 128;
                 const int32_t* pt = a.page_table + (int64_t)lo * a.pt_stride;
@@ -890,8 +894,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<kDtype, NP>::kCps) decode_dyn_ke
                     if (jpre[mid] <= c) lo = mid; else hi = mid;
                 }
                 b = lo;
-                j0 = kJob * (c - jpre[b]);
-                n = min(kJob, (seq_vis[b] + 127) / 128 - j0);
+                j0 = D::kJob * (c - jpre[b]);
+                n = min(D::kJob, (seq_vis[b] + 127) / 128 - j0);
             }
             // the record: wait until its slot's previous record was read by every consumer
             if (lane == 0) {
@@ -1169,7 +1173,7 @@ cudaError_t launch_dyn_np(const ScoreArgs& a, cudaStream_t st) {
                                          D::kSmem);
     if (e != cudaSuccess) return e;
     // no more CTAs than jobs could exist (a CTA whose first job does not exist exits at once)
-    const int64_t jobs_max = (int64_t)a.B * (((a.max_seq_len_k + 127) / 128 + kJob - 1) / kJob);
+    const int64_t jobs_max = (int64_t)a.B * (((a.max_seq_len_k + 127) / 128 + D::kJob - 1) / D::kJob);
     const int ctas = Cfg<kDtype, NP>::kCps * sm_count();
     const int grid = (int)(jobs_max < ctas ? (jobs_max > 0 ? jobs_max : 1) : ctas);
     return launch_k(!a.no_pdl, decode_dyn_kernel<kDtype, NP>, dim3(grid), dim3(kThreads), D::kSmem, st, a);
