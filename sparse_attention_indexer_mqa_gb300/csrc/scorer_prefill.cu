@@ -23,9 +23,11 @@
 // warps per scheduler hide the tensor-memory load latency, and each warp loads 64 columns per
 // tcgen05.wait::ld (a wait covers every load in flight, so a warp cannot overlap its own loads
 // with its sums; fewer, larger loads pay the latency less often). The epilogue is written to
-// issue little beyond its sums: compile-time trip counts and head offsets, 32-bit key
-// arithmetic, the causal test only on diagonal tiles, per-block row pointers, and the block's
-// head weights in shared memory read 16 bytes at a time.
+// issue little beyond its sums: compile-time trip counts, head offsets and query indices
+// (one instance per warpgroup half), 32-bit key arithmetic, no per-query test on the tiles
+// whose keys every query of the half sees (all but the diagonal and the ragged ends),
+// per-block row pointers, and the block's head weights in shared memory read 16 bytes at a
+// time.
 //
 // Work: query blocks, heaviest first (causal), in snake order over persistent CTAs (CTA c
 // takes ranks c, 2G-1-c, 2G+c, ...). Roles: warp 0 = producer (Q image of the block by bulk
@@ -185,11 +187,11 @@ __device__ __forceinline__ bool epi_barrier_or(bool pred) {
     return r != 0;
 }
 
-// kFull: H == HP, every accumulator column is a head (no per-head guard in the epilogue).
+// kAllHeads: H == HP, every accumulator column is a head (no per-head guard in the epilogue).
 // kSel: select mode (idx_mqa_topk_paged): a block's logits go to this CTA's rows of the
 // scratch, and at the end of the block the four epilogue warpgroups select the top-k of its
 // rows (one row per warpgroup at a time) and write the indices.
-template <int kDtype, int HP, bool kFull, bool kSel>
+template <int kDtype, int HP, bool kAllHeads, bool kSel>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
     using C = PCfg<kDtype>;
     constexpr int QB = kNmax / HP;  // queries per block
@@ -507,44 +509,51 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                 // this key is visible to queries q >= qmin (all of them off the diagonal)
                 const int32_t d = key - vis0 + 1;  // causal: query q sees the key iff q >= d
                 const int qmin = !key_ok ? QB : (qstep == 0 ? (key < vis0 ? 0 : QB) : (d <= 0 ? 0 : (d >= QB ? QB : (int)d)));
-                if constexpr (kFull) {
+                if constexpr (kAllHeads) {
                     // drain in 64-column chunks, one tcgen05.wait::ld each (a wait covers every
                     // load in flight, so fewer, larger loads pay the tensor-memory latency less
                     // often); the accumulator is released as soon as this half's last chunk
                     // is in registers. Sub-chunk s of chunk c holds head columns h0 .. h0+15
-                    // of query qlo + (64c + 16s) / HP (two queries when HP = 8).
-                    constexpr int CH = 64;
-                    constexpr int QPS = HP >= 16 ? 1 : 16 / HP;    // queries per 16 columns
-                    constexpr int kColsQ = HP >= 16 ? 16 : HP;     // a query's columns per 16
-                    constexpr int NCHK = (QH0 * HP + CH - 1) / CH; // chunks per half, at most
-                    const int qend = min(qhi, nqb);
-                    const int nchk = qend > qlo ? ((qend - qlo) * HP + CH - 1) / CH : 0;
-                    if (nchk == 0) {
-                        tc::tc_fence_before();
-                        tc::mbar_arrive(&acc_empty[gb]);
-                    }
-                    float2 acc[QPS][2] = {};
-#pragma unroll
-                    for (int c = 0; c < NCHK; ++c) {
-                        if (c >= nchk) break;
-                        uint32_t r[CH];
-                        tc::tmem_ld32(lane_addr + c * CH, *reinterpret_cast<uint32_t(*)[32]>(r));
-                        tc::tmem_ld32(lane_addr + c * CH + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
-                        tc::tmem_ld_wait();
-                        if (c + 1 == nchk) {  // the last chunk is in registers
+                    // of query qlo + (64c + 16s) / HP (two queries when HP = 8). The half and,
+                    // on tiles whose key every query of the half sees, the queries summed are
+                    // compile-time, so such a tile's drain tests nothing per query.
+                    auto drain = [&](auto all_c, auto half_c) {
+                        constexpr bool kAll = decltype(all_c)::value;
+                        constexpr int GH = decltype(half_c)::value;
+                        constexpr int CH = 64;
+                        constexpr int QPS = HP >= 16 ? 1 : 16 / HP;  // queries per 16 columns
+                        constexpr int kColsQ = HP >= 16 ? 16 : HP;   // a query's columns per 16
+                        constexpr int QLO = GH ? QH0 : 0, QHI = GH ? QB : QH0;
+                        constexpr int NCHK = ((QHI - QLO) * HP + CH - 1) / CH;  // chunks of the half
+                        const int qend = kAll ? QHI : min(QHI, nqb);
+                        const int nchk = kAll ? NCHK : (qend > QLO ? ((qend - QLO) * HP + CH - 1) / CH : 0);
+                        if (nchk == 0) {
                             tc::tc_fence_before();
                             tc::mbar_arrive(&acc_empty[gb]);
                         }
+                        float2 acc[QPS][2];
 #pragma unroll
-                        for (int sc = 0; sc < CH / 16; ++sc) {
+                        for (int c = 0; c < NCHK; ++c) {
+                            if (!kAll && c >= nchk) break;
+                            uint32_t r[CH];
+                            tc::tmem_ld32(lane_addr + c * CH, *reinterpret_cast<uint32_t(*)[32]>(r));
+                            tc::tmem_ld32(lane_addr + c * CH + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+                            tc::tmem_ld_wait();
+                            if (c + 1 == nchk) {  // the last chunk is in registers
+                                tc::tc_fence_before();
+                                tc::mbar_arrive(&acc_empty[gb]);
+                            }
 #pragma unroll
-                            for (int qq = 0; qq < QPS; ++qq) {
-                                const int col = c * CH + 16 * sc;     // compile-time
-                                const int q = qlo + col / HP + qq;
-                                const int h0 = col % HP;
-                                if (h0 == 0) acc[qq][0] = acc[qq][1] = make_float2(0.0f, 0.0f);
-                                if (q >= qmin && q < qend) {
-                                    const float4* w4p = reinterpret_cast<const float4*>(wsm + q * H + h0);
+                            for (int sc = 0; sc < CH / 16; ++sc) {
+#pragma unroll
+                                for (int qq = 0; qq < QPS; ++qq) {
+                                    const int col = c * CH + 16 * sc;  // compile-time
+                                    const int q = QLO + col / HP + qq;  // compile-time
+                                    const int h0 = col % HP;
+                                    if (q >= QHI) continue;
+                                    if (h0 == 0) acc[qq][0] = acc[qq][1] = make_float2(0.0f, 0.0f);
+                                    if (!kAll && !(q >= qmin && q < qend)) continue;
+                                    const float4* w4p = reinterpret_cast<const float4*>(wsm + q * HP + h0);
 #pragma unroll
                                     for (int i = 0; i < kColsQ / 4; ++i) {
                                         const float4 w4 = w4p[i];
@@ -553,13 +562,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                                         // (FMA pipe), so chain 1 holds twice its sum, halved below:
                                         // both scalings by 2 are exact, the sum is the same
                                         const float x2 = __uint_as_float(x[2]), x3 = __uint_as_float(x[3]);
-                                        acc[qq][0] = __ffma2_rn(make_float2(w4.x, w4.y),
-                                                                make_float2(fmaxf(__uint_as_float(x[0]), 0.0f),
-                                                                            fmaxf(__uint_as_float(x[1]), 0.0f)),
-                                                                acc[qq][0]);
-                                        acc[qq][1] = __ffma2_rn(make_float2(w4.z, w4.w),
-                                                                make_float2(x2 + fabsf(x2), x3 + fabsf(x3)),
-                                                                acc[qq][1]);
+                                        const float2 r0 = make_float2(fmaxf(__uint_as_float(x[0]), 0.0f),
+                                                                      fmaxf(__uint_as_float(x[1]), 0.0f));
+                                        const float2 r1 = make_float2(x2 + fabsf(x2), x3 + fabsf(x3));
+                                        acc[qq][0] = __ffma2_rn(make_float2(w4.x, w4.y), r0, acc[qq][0]);
+                                        acc[qq][1] = __ffma2_rn(make_float2(w4.z, w4.w), r1, acc[qq][1]);
                                     }
                                     if (h0 + kColsQ == HP) {
                                         const float2 s2 = __ffma2_rn(acc[qq][1], make_float2(0.5f, 0.5f), acc[qq][0]);
@@ -568,6 +575,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                                 }
                             }
                         }
+                    };
+                    using T0 = std::integral_constant<bool, false>;
+                    using T1 = std::integral_constant<bool, true>;
+                    using G0 = std::integral_constant<int, 0>;
+                    using G1 = std::integral_constant<int, 1>;
+                    const bool all = __all_sync(kFull, qmin == 0) && nqb >= (gh ? QB : QH0);
+                    if (gh) {
+                        if (all) drain(T1{}, G1{});
+                        else drain(T0{}, G1{});
+                    } else {
+                        if (all) drain(T1{}, G0{});
+                        else drain(T0{}, G0{});
                     }
                 } else {
                     // software-pipelined drain: chunk c+1 is loaded while chunk c is summed; the
@@ -590,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(ScoreArgs a) {
                             if (q < qhi && q < nqb && q >= qmin) {
                                 const float* wq = wsm + q * H;
                                 float logit;
-                                if constexpr (kFull) {
+                                if constexpr (kAllHeads) {
                                     // eight independent chains as four packed pairs (fma.rn.f32x2:
                                     // each lane an ordinary fp32 fused multiply-add)
                                     float2 acc[4] = {{0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}};
@@ -687,18 +706,18 @@ int sm_count() {
     return n;
 }
 
-template <int kDtype, int HP, bool kFull, bool kSel>
+template <int kDtype, int HP, bool kAllHeads, bool kSel>
 cudaError_t launch_hp(const ScoreArgs& a, cudaStream_t st) {
     using C = PCfg<kDtype>;
     constexpr int smem = kSel ? C::kSmemSel : C::kSmem;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kDtype, HP, kFull, kSel>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kDtype, HP, kAllHeads, kSel>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     constexpr int QB = kNmax / HP;
     const int64_t units = (int64_t)a.B * ((a.max_q_len + QB - 1) / QB);
     // select mode: every CTA runs (the orphan-row pass is strided over the whole grid)
     const int grid = kSel ? sm_count() : (int)(units < sm_count() ? (units > 0 ? units : 1) : sm_count());
-    return launch_pdl(prefill_kernel<kDtype, HP, kFull, kSel>, dim3(grid), dim3(kThreads), smem, st, a);
+    return launch_pdl(prefill_kernel<kDtype, HP, kAllHeads, kSel>, dim3(grid), dim3(kThreads), smem, st, a);
 }
 
 template <int kDtype, bool kSel>
