@@ -438,6 +438,7 @@ __global__ void __launch_bounds__(kT) topk_reg_kernel(TopkArgs a) {
         scal[4] = 0;
         scal[5] = 0xffffffffu;
     }
+    __syncthreads();  // the counters are set before any warp's atomics on them
     pdl_wait();  // the logits come from the previous kernel
     pdl_launch_dependents();
     int vis = 0;
@@ -663,6 +664,291 @@ __global__ void __launch_bounds__(kT) topk_reg_kernel(TopkArgs a) {
     }
 }
 
+// Shared-memory form with linear bins, for aligned rows that fit in shared memory: the keys
+// are staged once, then binned linearly between the row's smallest and largest value (as in
+// the register-resident form), so that the k-th key's bin holds few keys and no bin gathers
+// a large share of the row's atomic adds; the k-th key is found by direct ranking of that
+// bin's keys (or by 11/11/10-bit histograms of them when they are many). Warp w owns the
+// slice [w*chunk, (w+1)*chunk) of the row, chunk a multiple of 128, lane L the quads
+// 4L..4L+3 of each 128 keys: the output is written in index order with one warp scan per
+// 128 keys.
+template <int kThreads, int kCand>
+__global__ void __launch_bounds__(kThreads, 2048 / kThreads) topk_lin_kernel(TopkArgs a) {
+    constexpr int kWarps = kThreads / 32;
+    extern __shared__ uint32_t skeys[];
+    __shared__ uint32_t hist[2048];
+    __shared__ int32_t cand[kCand];
+    __shared__ uint32_t ckey[kCand];
+    __shared__ uint32_t warp_sums[kWarps], warp_gt[kWarps], warp_eq[kWarps];
+    __shared__ uint32_t sel[2], scal[6];  // listed, min, max, k-th key, copies, taken-min
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t t = blockIdx.x;
+    const int b = seq_of_query(a.cu_seqlens_q, a.B, t);
+    for (int i = threadIdx.x; i < 2048; i += kThreads) hist[i] = 0;
+    if (threadIdx.x == 0) {
+        scal[0] = 0;
+        scal[1] = 0xffffffffu;
+        scal[2] = 0;
+        scal[4] = 0;
+        scal[5] = 0xffffffffu;
+    }
+    __syncthreads();  // the counters are set before any warp's atomics on them
+    pdl_wait();  // the logits come from the previous kernel
+    pdl_launch_dependents();
+    int vis = 0;
+    if (b >= 0) {
+        const int64_t q0 = a.cu_seqlens_q[b], nq = a.cu_seqlens_q[b + 1] - q0;
+        const int32_t len = a.seq_lens_k[b];
+        if (len < 0 || len > a.max_len) {
+            // the scorer skipped this sequence: no logits to rank (and none past max_len <= ld)
+            if (threadIdx.x == 0) report(a.dev_status, IDX_STATUS_BAD_LEN);
+        } else {
+            vis = (int)visible_keys(len, nq, t - q0, a.causal);  // <= len <= max_len <= ld
+        }
+    }
+    int32_t* out = a.out + t * a.k;
+    const float* row = a.logits + t * a.ld;
+    if (vis <= a.k) {
+        for (int i = threadIdx.x; i < a.k; i += kThreads) out[i] = i < vis ? i : -1;
+        return;
+    }
+
+    // 1. read and stage the keys; the row's smallest and largest key
+    const int n4 = vis >> 2;
+    const float4* row4 = reinterpret_cast<const float4*>(row);
+    uint4* sk4 = reinterpret_cast<uint4*>(skeys);
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    auto put4 = [&](int j, const float4 v) {
+        const uint4 k = make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
+        sk4[j] = k;
+        kmin = min(kmin, min(min(k.x, k.y), min(k.z, k.w)));
+        kmax = max(kmax, max(max(k.x, k.y), max(k.z, k.w)));
+    };
+    {
+        int j = threadIdx.x;
+        for (; j + kThreads < n4; j += 2 * kThreads) {
+            const float4 v0 = row4[j], v1 = row4[j + kThreads];
+            put4(j, v0);
+            put4(j + kThreads, v1);
+        }
+        if (j < n4) put4(j, row4[j]);
+        if ((int)threadIdx.x < (vis & 3)) {
+            const int i = 4 * n4 + threadIdx.x;
+            const uint32_t key = order_key(row[i]);
+            skeys[i] = key;
+            kmin = min(kmin, key);
+            kmax = max(kmax, key);
+        }
+    }
+    kmin = __reduce_min_sync(kFull, kmin);
+    kmax = __reduce_max_sync(kFull, kmax);
+    if (lane == 0) {
+        atomicMin(&scal[1], kmin);
+        atomicMax(&scal[2], kmax);
+    }
+    __syncthreads();
+
+    // 2. histogram by the monotonic bin function; the bin b0 of the k-th key
+    auto value_of = [](uint32_t k) { return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k); };
+    const float vlo = value_of(scal[1]), vhi = value_of(scal[2]);
+    const float span = vhi - vlo, scale = 2048.0f / span;
+    // x - vlo >= 0 and the product are rounded monotonically: equal values share a bin and a
+    // larger value never falls into a lower bin (a NaN or an infinity at either end, or a
+    // range that overflows, leaves the top 11 key bits as the bins)
+    const bool linear = span > 0.0f && isfinite(span) && isfinite(scale) && isfinite(vlo);
+    auto bin_of = [&](uint32_t k) -> uint32_t {
+        if (!linear) return k >> 21;
+        const float x = fminf((value_of(k) - vlo) * scale, 2047.0f);
+        return __float_as_uint(__fadd_rd(x, 8388608.0f)) - 0x4b000000u;
+    };
+    for (int j = threadIdx.x; j < n4; j += kThreads) {
+        const uint4 k = sk4[j];
+        atomicAdd(&hist[bin_of(k.x)], 1u);
+        atomicAdd(&hist[bin_of(k.y)], 1u);
+        atomicAdd(&hist[bin_of(k.z)], 1u);
+        atomicAdd(&hist[bin_of(k.w)], 1u);
+    }
+    if ((int)threadIdx.x < (vis & 3)) atomicAdd(&hist[bin_of(skeys[4 * n4 + threadIdx.x])], 1u);
+    __syncthreads();
+    uint32_t b0, above;
+    select_bin<kThreads>(hist, 2048, (uint32_t)a.k, warp_sums, sel, b0, above);
+    uint32_t remaining = (uint32_t)a.k - above;
+
+    // 3. per-warp count of keys in higher bins; bin b0's keys listed
+    const int chunk = ((vis + kWarps - 1) / kWarps + 127) & ~127;
+    const int wlo = min(vis, chunk * warp), whi = min(vis, wlo + chunk);
+    uint32_t c_hi = 0;
+    for (int base = wlo; base < whi; base += 128) {
+        const int i0 = base + 4 * lane;
+        if (i0 >= whi) continue;
+        const uint4 k4 = sk4[i0 >> 2];
+        const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+        const int nv = min(4, whi - i0);  // valid keys of this quad (4 but at the row's end)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (e < nv) {
+                const uint32_t bn = bin_of(kk[e]);
+                c_hi += bn > b0;
+                if (bn == b0) {
+                    const uint32_t p = atomicAdd(&scal[0], 1u);
+                    if (p < (uint32_t)kCand) {
+                        cand[p] = i0 + e;
+                        ckey[p] = kk[e];
+                    }
+                }
+            }
+        }
+    }
+    c_hi = __reduce_add_sync(kFull, c_hi);
+    if (lane == 0) {
+        warp_gt[warp] = c_hi;
+        warp_eq[warp] = 0;
+    }
+    __syncthreads();
+    const uint32_t nc = scal[0];
+    const bool listed = nc <= (uint32_t)kCand;
+    // visit bin b0's keys: from the list, or by rescanning the staged row
+    auto for_each_cand = [&](auto&& f) {
+        if (listed) {
+            for (uint32_t j = threadIdx.x; j < nc; j += kThreads) f((int)cand[j], ckey[j]);
+        } else {
+            for (int i = threadIdx.x; i < vis; i += kThreads) {
+                const uint32_t key = skeys[i];
+                if (bin_of(key) == b0) f(i, key);
+            }
+        }
+    };
+
+    // 4. the k-th key: the remaining-th largest of bin b0's keys
+    uint32_t kth;
+    if (listed && nc <= (uint32_t)kThreads) {
+        if (threadIdx.x < nc) {
+            const uint32_t mine = ckey[threadIdx.x];
+            uint32_t gt = 0, ge = 0;
+            for (uint32_t j = 0; j < nc; ++j) {
+                const uint32_t o = ckey[j];
+                gt += o > mine;
+                ge += o >= mine;
+            }
+            if (gt < remaining && remaining <= ge) {
+                scal[3] = mine;
+                scal[4] = remaining - gt;  // copies of the k-th key taken
+            }
+        }
+        __syncthreads();
+        kth = scal[3];
+        remaining = scal[4];
+    } else {
+        // histograms of the key bits [31:21], [20:10], [9:0] (the top 11 are bin b0's when
+        // the bins are the top key bits); when every key of a prefix is taken the k-th key is
+        // their minimum
+        uint32_t prefix = linear ? 0u : (b0 << 21);
+        uint32_t fixed = linear ? 0u : 0xffe00000u;
+        bool done = false;
+        for (int level = linear ? 0 : 1; level < 3 && !done; ++level) {
+            const int shift = level == 0 ? 21 : level == 1 ? 10 : 0;
+            const int nb = level == 2 ? 1024 : 2048;
+            for (int i = threadIdx.x; i < nb; i += kThreads) hist[i] = 0;
+            __syncthreads();
+            for_each_cand([&](int, uint32_t k) {
+                if ((k & fixed) == prefix) atomicAdd(&hist[(k >> shift) & (uint32_t)(nb - 1)], 1u);
+            });
+            __syncthreads();
+            uint32_t bin, ab;
+            select_bin<kThreads>(hist, nb, remaining, warp_sums, sel, bin, ab);
+            const uint32_t cnt = hist[bin];
+            prefix |= bin << shift;
+            fixed |= (uint32_t)(nb - 1) << shift;
+            remaining -= ab;
+            if (level < 2 && cnt == remaining) {
+                for_each_cand([&](int, uint32_t k) {
+                    if ((k & fixed) == prefix) atomicMin(&scal[5], k);
+                });
+                __syncthreads();
+                const uint32_t mn = scal[5];
+                for_each_cand([&](int, uint32_t k) {
+                    if (k == mn) atomicAdd(&scal[4], 1u);
+                });
+                __syncthreads();
+                prefix = mn;
+                remaining = scal[4];
+                done = true;
+            }
+        }
+        kth = prefix;
+    }
+
+    // 5. bin b0's keys above / equal to the k-th complete the per-warp counts; one scan over
+    //    the warps places each warp's output, written in index order
+    for_each_cand([&](int i, uint32_t k) {
+        if (k > kth) atomicAdd(&warp_gt[i / chunk], 1u);
+        else if (k == kth) atomicAdd(&warp_eq[i / chunk], 1u);
+    });
+    __syncthreads();
+    uint32_t c_gt = warp_gt[warp], c_eq = warp_eq[warp];
+    __syncthreads();
+    if (warp == 0) {  // exclusive scans of the warps' counts (kWarps <= 32)
+        const uint32_t g = lane < kWarps ? warp_gt[lane] : 0u, e = lane < kWarps ? warp_eq[lane] : 0u;
+        uint32_t ig = g, ie = e;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t yg = __shfl_up_sync(kFull, ig, o), ye = __shfl_up_sync(kFull, ie, o);
+            if (lane >= o) {
+                ig += yg;
+                ie += ye;
+            }
+        }
+        if (lane < kWarps) {
+            warp_gt[lane] = ig - g;
+            warp_eq[lane] = ie - e;
+        }
+    }
+    __syncthreads();
+    const uint32_t n_gt = (uint32_t)a.k - remaining;
+    uint32_t og = warp_gt[warp], oe = warp_eq[warp];
+    for (int base = wlo; base < whi && (c_gt > 0 || (c_eq > 0 && oe < remaining)); base += 128) {
+        const int i0 = base + 4 * lane;
+        uint32_t fg = 0, fe = 0;
+        if (i0 < whi) {
+            const uint4 k4 = sk4[i0 >> 2];
+            const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+            const int nv = min(4, whi - i0);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                fg |= (uint32_t)(e < nv && kk[e] > kth) << e;
+                fe |= (uint32_t)(e < nv && kk[e] == kth) << e;
+            }
+        }
+        const uint32_t cnt = (uint32_t)__popc(fg) | ((uint32_t)__popc(fe) << 16);
+        uint32_t inc = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, inc, o);
+            if (lane >= o) inc += y;
+        }
+        const uint32_t tot = __shfl_sync(kFull, inc, 31);
+        const uint32_t ex = inc - cnt;
+        uint32_t pg = og + (ex & 0xffffu), pe = oe + (ex >> 16);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if ((fg >> e) & 1u) out[pg++] = i0 + e;
+        if (fe) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if ((fe >> e) & 1u) {
+                    if (pe < remaining) out[n_gt + pe] = i0 + e;
+                    ++pe;
+                }
+            }
+        }
+        og += tot & 0xffffu;
+        oe += tot >> 16;
+        c_gt -= tot & 0xffffu;
+        c_eq -= tot >> 16;
+    }
+}
+
 template <int kThreads, int kCand, bool kVec>
 cudaError_t launch_form(const TopkArgs& a, cudaStream_t st) {
     const int keys = (int)(a.ld < kSmemKeysMax ? a.ld : kSmemKeysMax);
@@ -675,9 +961,18 @@ cudaError_t launch_form(const TopkArgs& a, cudaStream_t st) {
 }
 
 template <int kThreads, int kCand>
+cudaError_t launch_lin(const TopkArgs& a, cudaStream_t st) {
+    const size_t smem = (size_t)a.ld * sizeof(uint32_t);
+    cudaError_t e = cudaFuncSetAttribute(topk_lin_kernel<kThreads, kCand>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(topk_lin_kernel<kThreads, kCand>, dim3((unsigned)a.T), dim3(kThreads), smem, st, a);
+}
+
+template <int kThreads, int kCand>
 cudaError_t launch_threads(const TopkArgs& a, cudaStream_t st) {
     const bool vec = a.ld % 4 == 0 && a.ld <= kSmemKeysMax && ((uintptr_t)a.logits & 15) == 0;
-    return vec ? launch_form<kThreads, kCand, true>(a, st) : launch_form<kThreads, kCand, false>(a, st);
+    return vec ? launch_lin<kThreads, kCand>(a, st) : launch_form<kThreads, kCand, false>(a, st);
 }
 
 }  // namespace
