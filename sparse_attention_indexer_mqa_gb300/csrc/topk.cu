@@ -7,11 +7,18 @@
 // indices equal to it, each group in increasing index order, so the result is
 // deterministic.
 //
-// One CTA per query row: 1024 threads, or 512 when there are more rows than SMs and the
-// rows are short (several rows then share an SM). Warp w owns the contiguous slice
-// [w*chunk, (w+1)*chunk) of the row and its lanes read consecutive keys, so global loads are
-// coalesced, shared-memory reads are conflict-free and ballots keep the index order.
+// One CTA per query row, in one of three forms chosen per launch:
+//   * register-resident (topk_reg_kernel): at most one row per SM, aligned rows of at most
+//     16K keys; each thread holds its keys in registers;
+//   * linear bins in shared memory (topk_lin_kernel): more rows than SMs, or longer rows,
+//     that fit in shared memory and are aligned; the keys are staged once;
+//   * generic (topk_kernel): any alignment and length; rows longer than shared memory are
+//     re-read from global memory.
+// 1024 threads per CTA, or 512 when there are more rows than SMs and the rows are short
+// (several rows then share an SM). Warp w owns a contiguous slice of the row and its lanes
+// read consecutive keys, so global loads are coalesced and the output keeps index order.
 //
+// The generic form:
 //   1. The row's logits are read once, mapped to order-preserving uint32 keys, kept in
 //      shared memory (rows longer than that capacity are re-read from global memory), and
 //      histogrammed on their top 11 bits: the bin b0 holding the k-th key is found.
@@ -24,6 +31,8 @@
 //   4. Per-warp counts of candidates above / equal to the k-th key complete the warps'
 //      counts; one scan over the warps places each warp's output, and a last pass writes
 //      the indices with ballots.
+// The other two forms bin linearly between the row's smallest and largest value instead
+// (few keys share the k-th key's bin) and rank that bin's keys directly.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -91,10 +100,9 @@ __device__ __forceinline__ void select_bin(const uint32_t* hist, int nb, uint32_
     above = sel[1];
 }
 
-// kVec: every row fits in shared memory and starts on a 16-byte boundary (ld % 4 == 0), so
-// the key passes move four keys per access; otherwise the generic form (rows re-read from
-// global memory when longer than shared memory, any alignment).
-template <int kThreads, int kCand, bool kVec>
+// The generic form: any alignment, rows longer than shared memory re-read from global
+// memory; bins are the top 11 key bits.
+template <int kThreads, int kCand>
 __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_keys) {
     constexpr int kWarps = kThreads / 32;
     extern __shared__ uint32_t skeys[];
@@ -138,108 +146,49 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
     __syncthreads();
 
     // 1. read, stage, histogram the top 11 bits (thread-strided, float4 where aligned)
-    if constexpr (kVec) {
-        const int n4 = vis >> 2;
-        const float4* row4 = reinterpret_cast<const float4*>(row);
-        uint4* sk4 = reinterpret_cast<uint4*>(skeys);
-        auto put4 = [&](int j, const float4 v) {
-            const uint4 k = make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
-            sk4[j] = k;
-            atomicAdd(&hist[k.x >> 21], 1u);
-            atomicAdd(&hist[k.y >> 21], 1u);
-            atomicAdd(&hist[k.z >> 21], 1u);
-            atomicAdd(&hist[k.w >> 21], 1u);
-        };
-        int j = threadIdx.x;
-        for (; j + kThreads < n4; j += 2 * kThreads) {
-            const float4 v0 = row4[j], v1 = row4[j + kThreads];
-            put4(j, v0);
-            put4(j + kThreads, v1);
-        }
-        if (j < n4) put4(j, row4[j]);
-        if ((int)threadIdx.x < (vis & 3)) {
-            const int i = 4 * n4 + threadIdx.x;
-            const uint32_t key = order_key(row[i]);
-            skeys[i] = key;
-            atomicAdd(&hist[key >> 21], 1u);
-        }
-    } else {
-        const int head = min(vis, (int)(((16u - ((uint32_t)(uintptr_t)row & 15u)) & 15u) >> 2));
-        const int n4 = (vis - head) >> 2;
-        const float4* row4 = reinterpret_cast<const float4*>(row + head);
-        auto put = [&](int i, uint32_t key) {
-            if (cached) skeys[i] = key;
-            atomicAdd(&hist[key >> 21], 1u);
-        };
-        if ((int)threadIdx.x < head) put(threadIdx.x, order_key(row[threadIdx.x]));
-        int j = threadIdx.x;
-        for (; j + kThreads < n4; j += 2 * kThreads) {
-            const float4 v0 = row4[j], v1 = row4[j + kThreads];
-            const int i0 = head + 4 * j, i1 = head + 4 * (j + kThreads);
-            put(i0, order_key(v0.x)); put(i0 + 1, order_key(v0.y));
-            put(i0 + 2, order_key(v0.z)); put(i0 + 3, order_key(v0.w));
-            put(i1, order_key(v1.x)); put(i1 + 1, order_key(v1.y));
-            put(i1 + 2, order_key(v1.z)); put(i1 + 3, order_key(v1.w));
-        }
-        for (; j < n4; j += kThreads) {
-            const float4 v0 = row4[j];
-            const int i0 = head + 4 * j;
-            put(i0, order_key(v0.x)); put(i0 + 1, order_key(v0.y));
-            put(i0 + 2, order_key(v0.z)); put(i0 + 3, order_key(v0.w));
-        }
-        for (int i = head + 4 * n4 + threadIdx.x; i < vis; i += kThreads) put(i, order_key(row[i]));
+    const int head = min(vis, (int)(((16u - ((uint32_t)(uintptr_t)row & 15u)) & 15u) >> 2));
+    const int n4 = (vis - head) >> 2;
+    const float4* row4 = reinterpret_cast<const float4*>(row + head);
+    auto put = [&](int i, uint32_t key) {
+        if (cached) skeys[i] = key;
+        atomicAdd(&hist[key >> 21], 1u);
+    };
+    if ((int)threadIdx.x < head) put(threadIdx.x, order_key(row[threadIdx.x]));
+    int j = threadIdx.x;
+    for (; j + kThreads < n4; j += 2 * kThreads) {
+        const float4 v0 = row4[j], v1 = row4[j + kThreads];
+        const int i0 = head + 4 * j, i1 = head + 4 * (j + kThreads);
+        put(i0, order_key(v0.x)); put(i0 + 1, order_key(v0.y));
+        put(i0 + 2, order_key(v0.z)); put(i0 + 3, order_key(v0.w));
+        put(i1, order_key(v1.x)); put(i1 + 1, order_key(v1.y));
+        put(i1 + 2, order_key(v1.z)); put(i1 + 3, order_key(v1.w));
     }
+    for (; j < n4; j += kThreads) {
+        const float4 v0 = row4[j];
+        const int i0 = head + 4 * j;
+        put(i0, order_key(v0.x)); put(i0 + 1, order_key(v0.y));
+        put(i0 + 2, order_key(v0.z)); put(i0 + 3, order_key(v0.w));
+    }
+    for (int i = head + 4 * n4 + threadIdx.x; i < vis; i += kThreads) put(i, order_key(row[i]));
     __syncthreads();
     uint32_t b0, above;
     select_bin<kThreads>(hist, 2048, (uint32_t)a.k, warp_sums, sel, b0, above);
     uint32_t remaining = (uint32_t)a.k - above;
 
     // 2. per-warp count of keys above bin b0; gather bin b0's indices
-    constexpr int kStep = kVec ? 128 : 32;  // keys per warp iteration
+    constexpr int kStep = 32;  // keys per warp iteration
     const int chunk = ((vis + kWarps - 1) / kWarps + kStep - 1) & ~(kStep - 1);
     const int lo = min(vis, chunk * warp), hi = min(vis, lo + chunk);
     uint32_t c_hi = 0;
-    if constexpr (kVec) {
-        const uint4* sk4 = reinterpret_cast<const uint4*>(skeys);
-        // bin b0 holds the keys [lo_t, lo_t + 2^21); lo is a multiple of 128 whenever lo < hi
-        const uint32_t lo_t = b0 << 21, hi_t = lo_t + ((1u << 21) - 1u);
-        for (int base = lo; base < hi; base += 128) {
-            const int i0 = base + 4 * lane;
-            if (i0 >= hi) continue;
-            const uint4 k4 = sk4[i0 >> 2];
-            const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
-            const int nv = min(4, hi - i0);  // valid keys of this quad (4 but at the chunk's end)
-            uint32_t m = 0;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const bool valid = e < nv;
-                c_hi += valid && kk[e] > hi_t;
-                m |= (uint32_t)(valid && kk[e] - lo_t < (1u << 21)) << e;
-            }
-            if (m) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    if ((m >> e) & 1u) {
-                        const uint32_t p = atomicAdd(&n_cand, 1u);
-                        if (p < (uint32_t)kCand) {
-                            cand[p] = i0 + e;
-                            ckey[p] = kk[e];
-                        }
-                    }
-                }
-            }
-        }
-    } else {
-        for (int i = lo + lane; i < hi; i += 32) {
-            const uint32_t key = key_at(i);
-            const uint32_t bin = key >> 21;
-            c_hi += bin > b0;
-            if (bin == b0) {
-                const uint32_t p = atomicAdd(&n_cand, 1u);
-                if (p < (uint32_t)kCand) {
-                    cand[p] = i;
-                    ckey[p] = key;
-                }
+    for (int i = lo + lane; i < hi; i += 32) {
+        const uint32_t key = key_at(i);
+        const uint32_t bin = key >> 21;
+        c_hi += bin > b0;
+        if (bin == b0) {
+            const uint32_t p = atomicAdd(&n_cand, 1u);
+            if (p < (uint32_t)kCand) {
+                cand[p] = i;
+                ckey[p] = key;
             }
         }
     }
@@ -338,52 +287,6 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
     __syncthreads();
     const uint32_t n_gt = (uint32_t)a.k - remaining;
     uint32_t og = warp_gt[warp], oe = warp_eq[warp];
-    if constexpr (kVec) {
-        // lane L of an iteration holds keys 4L..4L+3 of the warp's next 128: per-lane counts
-        // and one warp scan place them in index order
-        const uint4* sk4 = reinterpret_cast<const uint4*>(skeys);
-        for (int base = lo; base < hi && (c_gt > 0 || (c_eq > 0 && oe < remaining)); base += 128) {
-            const int i0 = base + 4 * lane;
-            uint32_t fg = 0, fe = 0;
-            if (i0 < hi) {
-                const uint4 k4 = sk4[i0 >> 2];
-                const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
-                const int nv = min(4, hi - i0);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    fg |= (uint32_t)(e < nv && kk[e] > kth) << e;
-                    fe |= (uint32_t)(e < nv && kk[e] == kth) << e;
-                }
-            }
-            const uint32_t cnt = (uint32_t)__popc(fg) | ((uint32_t)__popc(fe) << 16);
-            uint32_t inc = cnt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(kFull, inc, o);
-                if (lane >= o) inc += y;
-            }
-            const uint32_t tot = __shfl_sync(kFull, inc, 31);
-            const uint32_t ex = inc - cnt;
-            uint32_t pg = og + (ex & 0xffffu), pe = oe + (ex >> 16);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if ((fg >> e) & 1u) out[pg++] = i0 + e;
-            if (fe) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    if ((fe >> e) & 1u) {
-                        if (pe < remaining) out[n_gt + pe] = i0 + e;
-                        ++pe;
-                    }
-                }
-            }
-            og += tot & 0xffffu;
-            oe += tot >> 16;
-            c_gt -= tot & 0xffffu;
-            c_eq -= tot >> 16;
-        }
-        return;
-    }
     const uint32_t below = (1u << lane) - 1u;
     for (int base = lo; base < hi && (c_gt > 0 || (c_eq > 0 && oe < remaining)); base += 32) {
         const int i = base + lane;
@@ -949,14 +852,14 @@ __global__ void __launch_bounds__(kThreads, 2048 / kThreads) topk_lin_kernel(Top
     }
 }
 
-template <int kThreads, int kCand, bool kVec>
+template <int kThreads, int kCand>
 cudaError_t launch_form(const TopkArgs& a, cudaStream_t st) {
     const int keys = (int)(a.ld < kSmemKeysMax ? a.ld : kSmemKeysMax);
     const size_t smem = (size_t)keys * sizeof(uint32_t);
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel<kThreads, kCand, kVec>,
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel<kThreads, kCand>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(topk_kernel<kThreads, kCand, kVec>, dim3((unsigned)a.T), dim3(kThreads), smem, st, a,
+    return launch_pdl(topk_kernel<kThreads, kCand>, dim3((unsigned)a.T), dim3(kThreads), smem, st, a,
                       keys);
 }
 
@@ -972,7 +875,7 @@ cudaError_t launch_lin(const TopkArgs& a, cudaStream_t st) {
 template <int kThreads, int kCand>
 cudaError_t launch_threads(const TopkArgs& a, cudaStream_t st) {
     const bool vec = a.ld % 4 == 0 && a.ld <= kSmemKeysMax && ((uintptr_t)a.logits & 15) == 0;
-    return vec ? launch_lin<kThreads, kCand>(a, st) : launch_form<kThreads, kCand, false>(a, st);
+    return vec ? launch_lin<kThreads, kCand>(a, st) : launch_form<kThreads, kCand>(a, st);
 }
 
 }  // namespace
