@@ -17,7 +17,9 @@
 //   top-k             over the virtual rows;
 //   cand_map_kernel   virtual position v -> key position blk[v / P] * P + v % P.
 // The scorer's prologue reads lengths and the page table before its grid-dependency wait, so
-// here it is launched as an ordinary stream-ordered launch after cand_prep_kernel.
+// here it is launched as an ordinary stream-ordered launch after cand_prep_kernel. The top-k,
+// whose prologue reads the virtual lengths too, starts no earlier than the scorer, so
+// cand_prep_kernel has completed by then.
 #include "common.cuh"
 #include "kernels.h"
 

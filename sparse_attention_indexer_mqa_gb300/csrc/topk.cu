@@ -115,19 +115,19 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t t = blockIdx.x;
     const int b = seq_of_query(a.cu_seqlens_q, a.B, t);
-    pdl_wait();  // the logits come from the previous kernel
-    pdl_launch_dependents();
+    // the row's length (a caller input, read before the wait so that the row's loads follow it
+    // at once)
     int vis = 0;
+    bool bad = false;  // the scorer skipped this sequence: no logits to rank
     if (b >= 0) {
         const int64_t q0 = a.cu_seqlens_q[b], nq = a.cu_seqlens_q[b + 1] - q0;
         const int32_t len = a.seq_lens_k[b];
-        if (len < 0 || len > a.max_len) {
-            // the scorer skipped this sequence: no logits to rank (and none past max_len <= ld)
-            if (threadIdx.x == 0) report(a.dev_status, IDX_STATUS_BAD_LEN);
-        } else {
-            vis = (int)visible_keys(len, nq, t - q0, a.causal);  // <= len <= max_len <= ld
-        }
+        if (len < 0 || len > a.max_len) bad = true;
+        else vis = (int)visible_keys(len, nq, t - q0, a.causal);  // <= len <= max_len <= ld
     }
+    pdl_wait();  // the logits come from the previous kernel
+    pdl_launch_dependents();
+    if (bad && threadIdx.x == 0) report(a.dev_status, IDX_STATUS_BAD_LEN);
     int32_t* out = a.out + t * a.k;
     const float* row = a.logits + t * a.ld;
     if (vis <= a.k) {
@@ -342,18 +342,19 @@ __global__ void __launch_bounds__(kT) topk_reg_kernel(TopkArgs a) {
         scal[5] = 0xffffffffu;
     }
     __syncthreads();  // the counters are set before any warp's atomics on them
-    pdl_wait();  // the logits come from the previous kernel
-    pdl_launch_dependents();
+    // the row's length (a caller input, read before the wait so that the row's loads follow it
+    // at once)
     int vis = 0;
+    bool bad = false;  // the scorer skipped this sequence: no logits to rank
     if (b >= 0) {
         const int64_t q0 = a.cu_seqlens_q[b], nq = a.cu_seqlens_q[b + 1] - q0;
         const int32_t len = a.seq_lens_k[b];
-        if (len < 0 || len > a.max_len) {
-            if (threadIdx.x == 0) report(a.dev_status, IDX_STATUS_BAD_LEN);
-        } else {
-            vis = (int)visible_keys(len, nq, t - q0, a.causal);  // <= max_len <= kT * kPer
-        }
+        if (len < 0 || len > a.max_len) bad = true;
+        else vis = (int)visible_keys(len, nq, t - q0, a.causal);  // <= max_len <= kT * kPer
     }
+    pdl_wait();  // the logits come from the previous kernel
+    pdl_launch_dependents();
+    if (bad && threadIdx.x == 0) report(a.dev_status, IDX_STATUS_BAD_LEN);
     int32_t* out = a.out + t * a.k;
     if (vis <= a.k) {
         for (int i = threadIdx.x; i < a.k; i += kT) out[i] = i < vis ? i : -1;
@@ -597,19 +598,19 @@ __global__ void __launch_bounds__(kThreads, 2048 / kThreads) topk_lin_kernel(Top
         scal[5] = 0xffffffffu;
     }
     __syncthreads();  // the counters are set before any warp's atomics on them
-    pdl_wait();  // the logits come from the previous kernel
-    pdl_launch_dependents();
+    // the row's length (a caller input, read before the wait so that the row's loads follow it
+    // at once)
     int vis = 0;
+    bool bad = false;  // the scorer skipped this sequence: no logits to rank
     if (b >= 0) {
         const int64_t q0 = a.cu_seqlens_q[b], nq = a.cu_seqlens_q[b + 1] - q0;
         const int32_t len = a.seq_lens_k[b];
-        if (len < 0 || len > a.max_len) {
-            // the scorer skipped this sequence: no logits to rank (and none past max_len <= ld)
-            if (threadIdx.x == 0) report(a.dev_status, IDX_STATUS_BAD_LEN);
-        } else {
-            vis = (int)visible_keys(len, nq, t - q0, a.causal);  // <= len <= max_len <= ld
-        }
+        if (len < 0 || len > a.max_len) bad = true;
+        else vis = (int)visible_keys(len, nq, t - q0, a.causal);  // <= len <= max_len <= ld
     }
+    pdl_wait();  // the logits come from the previous kernel
+    pdl_launch_dependents();
+    if (bad && threadIdx.x == 0) report(a.dev_status, IDX_STATUS_BAD_LEN);
     int32_t* out = a.out + t * a.k;
     const float* row = a.logits + t * a.ld;
     if (vis <= a.k) {
