@@ -100,6 +100,21 @@ __device__ __forceinline__ void select_bin(const uint32_t* hist, int nb, uint32_
     above = sel[1];
 }
 
+// The sequence of query row t (-1 when t lies in none). With more than two sequences the
+// whole CTA looks: thread i tests the sequences i, i + kT, ... (cu[j] <= t < cu[j + 1]), one
+// round of coalesced loads instead of a binary search's chain of dependent ones; with one or
+// two the binary search takes at most two rounds and no barrier.
+template <int kT>
+__device__ __forceinline__ int seq_of_row(const int32_t* cu, int B, int64_t t, int* s_b) {
+    if (B <= 2) return seq_of_query(cu, B, t);  // uniform over the CTA
+    if (threadIdx.x == 0) *s_b = -1;
+    __syncthreads();
+    for (int i = threadIdx.x; i < B; i += kT)
+        if (cu[i] <= t && t < cu[i + 1]) *s_b = i;
+    __syncthreads();
+    return *s_b;
+}
+
 // The generic form: any alignment, rows longer than shared memory re-read from global
 // memory; bins are the top 11 key bits.
 template <int kThreads, int kCand>
@@ -111,10 +126,11 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
     __shared__ uint32_t ckey[kCand];  // the candidates' keys, in list order
     __shared__ uint32_t warp_sums[kWarps], warp_gt[kWarps], warp_eq[kWarps];
     __shared__ uint32_t sel[2], n_cand, bin_min, bin_eq;
+    __shared__ int s_b;
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t t = blockIdx.x;
-    const int b = seq_of_query(a.cu_seqlens_q, a.B, t);
+    const int b = seq_of_row<kThreads>(a.cu_seqlens_q, a.B, t, &s_b);
     // the row's length (a caller input, read before the wait so that the row's loads follow it
     // at once)
     int vis = 0;
@@ -329,10 +345,11 @@ __global__ void __launch_bounds__(kT) topk_reg_kernel(TopkArgs a) {
     __shared__ uint32_t ckey[kCandR];
     __shared__ uint32_t warp_sums[kW], warp_gt[kW], warp_eq[kW];
     __shared__ uint32_t sel[2], scal[6];  // scal: listed, min, max, k-th key, copies, taken-min
+    __shared__ int s_b;
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t t = blockIdx.x;
-    const int b = seq_of_query(a.cu_seqlens_q, a.B, t);
+    const int b = seq_of_row<kT>(a.cu_seqlens_q, a.B, t, &s_b);
     for (int i = threadIdx.x; i < 2048; i += kT) hist[i] = 0;
     if (threadIdx.x == 0) {
         scal[0] = 0;
@@ -585,10 +602,11 @@ __global__ void __launch_bounds__(kThreads, 2048 / kThreads) topk_lin_kernel(Top
     __shared__ uint32_t ckey[kCand];
     __shared__ uint32_t warp_sums[kWarps], warp_gt[kWarps], warp_eq[kWarps];
     __shared__ uint32_t sel[2], scal[6];  // listed, min, max, k-th key, copies, taken-min
+    __shared__ int s_b;
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t t = blockIdx.x;
-    const int b = seq_of_query(a.cu_seqlens_q, a.B, t);
+    const int b = seq_of_row<kThreads>(a.cu_seqlens_q, a.B, t, &s_b);
     for (int i = threadIdx.x; i < 2048; i += kThreads) hist[i] = 0;
     if (threadIdx.x == 0) {
         scal[0] = 0;
