@@ -71,17 +71,16 @@ __device__ __forceinline__ void select_bin(const uint32_t* hist, int nb, uint32_
     }
     if (lane == 31) warp_sums[w] = x;
     __syncthreads();
-    if (w == 0) {
-        uint32_t s = lane < kWarps ? warp_sums[lane] : 0u;
+    // every warp scans the warps' totals itself (no second barrier); lane w - 1 of the scan
+    // holds the bins owned by the warps before this one
+    uint32_t s = lane < kWarps ? warp_sums[lane] : 0u;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(kFull, s, o);
-            if (lane >= o) s += y;
-        }
-        if (lane < kWarps) warp_sums[lane] = s;
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, s, o);
+        if (lane >= o) s += y;
     }
-    __syncthreads();
-    const uint32_t incl = x + (w > 0 ? warp_sums[w - 1] : 0u);
+    const uint32_t wbefore = __shfl_sync(kFull, s, (w + 31) & 31);
+    const uint32_t incl = x + (w > 0 ? wbefore : 0u);
     const uint32_t before = incl - local;
     if (before < remaining && remaining <= incl) {
         uint32_t run = before;
@@ -282,9 +281,10 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
         });
         __syncthreads();
     }
-    uint32_t c_gt = warp_gt[warp], c_eq = warp_eq[warp];
-    __syncthreads();
-    if (warp == 0) {  // exclusive scans of the warps' counts (kWarps <= 32)
+    // every warp scans the warps' counts itself: og / oe = the outputs of the warps before
+    // this one, c_gt / c_eq = this warp's own counts
+    uint32_t og, oe, c_gt, c_eq;
+    {
         const uint32_t g = lane < kWarps ? warp_gt[lane] : 0u, e = lane < kWarps ? warp_eq[lane] : 0u;
         uint32_t ig = g, ie = e;
 #pragma unroll
@@ -295,14 +295,12 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a, int smem_key
                 ie += ye;
             }
         }
-        if (lane < kWarps) {
-            warp_gt[lane] = ig - g;
-            warp_eq[lane] = ie - e;
-        }
+        og = __shfl_sync(kFull, ig - g, warp);
+        oe = __shfl_sync(kFull, ie - e, warp);
+        c_gt = __shfl_sync(kFull, g, warp);
+        c_eq = __shfl_sync(kFull, e, warp);
     }
-    __syncthreads();
     const uint32_t n_gt = (uint32_t)a.k - remaining;
-    uint32_t og = warp_gt[warp], oe = warp_eq[warp];
     const uint32_t below = (1u << lane) - 1u;
     for (int base = lo; base < hi && (c_gt > 0 || (c_eq > 0 && oe < remaining)); base += 32) {
         const int i = base + lane;
@@ -542,7 +540,10 @@ __global__ void __launch_bounds__(kT) topk_reg_kernel(TopkArgs a) {
         else if (k == kth) atomicAdd(&warp_eq[i / kChunk], 1u);
     });
     __syncthreads();
-    if (warp == 0) {  // exclusive scans of the warps' counts
+    // every warp scans the warps' counts itself: og / oe = the outputs of the warps before
+    // this one, c_gt / c_eq = this warp's own counts
+    uint32_t og, oe, c_gt, c_eq;
+    {
         const uint32_t g = lane < kW ? warp_gt[lane] : 0u, q = lane < kW ? warp_eq[lane] : 0u;
         uint32_t ig = g, iq = q;
 #pragma unroll
@@ -553,12 +554,11 @@ __global__ void __launch_bounds__(kT) topk_reg_kernel(TopkArgs a) {
                 iq += yq;
             }
         }
-        if (lane < kW) {
-            warp_gt[lane] = ig - g;
-            warp_eq[lane] = iq - q;
-        }
+        og = __shfl_sync(kFull, ig - g, warp);
+        oe = __shfl_sync(kFull, iq - q, warp);
+        c_gt = __shfl_sync(kFull, g, warp);
+        c_eq = __shfl_sync(kFull, q, warp);
     }
-    __syncthreads();
     uint32_t fg = 0, fe = 0;
 #pragma unroll
     for (int e = 0; e < kPer; ++e) {
@@ -574,7 +574,7 @@ __global__ void __launch_bounds__(kT) topk_reg_kernel(TopkArgs a) {
     }
     const uint32_t ex = inc - cnt;
     const uint32_t n_gt = (uint32_t)a.k - remaining;
-    uint32_t pg = warp_gt[warp] + (ex & 0xffffu), pe = warp_eq[warp] + (ex >> 16);
+    uint32_t pg = og + (ex & 0xffffu), pe = oe + (ex >> 16);
 #pragma unroll
     for (int e = 0; e < kPer; ++e) {
         if ((fg >> e) & 1u) out[pg++] = i0 + e;
@@ -808,9 +808,10 @@ __global__ void __launch_bounds__(kThreads, 2048 / kThreads) topk_lin_kernel(Top
         else if (k == kth) atomicAdd(&warp_eq[i / chunk], 1u);
     });
     __syncthreads();
-    uint32_t c_gt = warp_gt[warp], c_eq = warp_eq[warp];
-    __syncthreads();
-    if (warp == 0) {  // exclusive scans of the warps' counts (kWarps <= 32)
+    // every warp scans the warps' counts itself: og / oe = the outputs of the warps before
+    // this one, c_gt / c_eq = this warp's own counts
+    uint32_t og, oe, c_gt, c_eq;
+    {
         const uint32_t g = lane < kWarps ? warp_gt[lane] : 0u, e = lane < kWarps ? warp_eq[lane] : 0u;
         uint32_t ig = g, ie = e;
 #pragma unroll
@@ -821,14 +822,12 @@ __global__ void __launch_bounds__(kThreads, 2048 / kThreads) topk_lin_kernel(Top
                 ie += ye;
             }
         }
-        if (lane < kWarps) {
-            warp_gt[lane] = ig - g;
-            warp_eq[lane] = ie - e;
-        }
+        og = __shfl_sync(kFull, ig - g, warp);
+        oe = __shfl_sync(kFull, ie - e, warp);
+        c_gt = __shfl_sync(kFull, g, warp);
+        c_eq = __shfl_sync(kFull, e, warp);
     }
-    __syncthreads();
     const uint32_t n_gt = (uint32_t)a.k - remaining;
-    uint32_t og = warp_gt[warp], oe = warp_eq[warp];
     for (int base = wlo; base < whi && (c_gt > 0 || (c_eq > 0 && oe < remaining)); base += 128) {
         const int i0 = base + 4 * lane;
         uint32_t fg = 0, fe = 0;
