@@ -99,7 +99,7 @@ def test_topk_wide_uncached_rows(torch):
 
 
 def test_topk_narrow_ctas_many_rows(torch):
-    """More rows than SMs with short rows: the narrow CTA shape."""
+    """More rows than SMs with rows of up to 9000 keys: the 512-thread CTA shape."""
     rng = np.random.default_rng(3)
     rows = [rng.standard_normal(int(n)).astype(np.float32) for n in rng.integers(1, 9000, 400)]
     _decode(torch, rows, 512)
@@ -150,9 +150,10 @@ def test_topk_causal_prefill_rows(torch):
 @pytest.mark.parametrize("lens,n_rows", [((8191, 8192, 100), 8), ((8193, 16384, 9000), 8),
                                          ((16385, 20000), 4), ((8192, 3000, 5000), 300)])
 def test_topk_form_boundaries(torch, lens, n_rows):
-    """Each launch shape on aligned rows: up to 8192 keys with few rows (1024 threads, 8 keys
-    each) or many rows (512 threads, 16 each), up to 16384 keys (1024 x 16), and longer rows
-    (the shared-memory form); the many-row case mixes in tied rows whose candidates overflow."""
+    """Each launch shape on aligned rows: up to 8192 keys with few rows (registers: 1024
+    threads, 8 keys each) or many rows (shared memory, 256 threads), up to 16384 keys (1024 x
+    16), and longer rows (shared memory, 1024 threads); the many-row case mixes in tied rows
+    whose candidates overflow."""
     rng = np.random.default_rng(8)
     rows = []
     for i in range(n_rows):
