@@ -10,8 +10,9 @@
 // One CTA per query row, in one of three forms chosen per launch:
 //   * register-resident (topk_reg_kernel): at most one row per SM, aligned rows of at most
 //     16K keys; each thread holds its keys in registers;
-//   * linear bins in shared memory (topk_lin_kernel): more rows than SMs, or longer rows,
-//     that fit in shared memory and are aligned; the keys are staged once;
+//   * linear bins (topk_lin_kernel): aligned rows, more rows than SMs or longer rows; the
+//     keys are staged once in shared memory when they fit, and with many rows longer than
+//     12K keys each pass re-reads the row instead (four rows per SM);
 //   * generic (topk_kernel): any alignment and length; rows longer than shared memory are
 //     re-read from global memory.
 // 1024 threads per CTA, or 512 (rows up to 12K keys) or 256 (up to 8K) when there are more
@@ -595,8 +596,9 @@ __global__ void __launch_bounds__(kT) topk_reg_kernel(TopkArgs a) {
 // bin's keys (or by 11/11/10-bit histograms of them when they are many). Warp w owns the
 // slice [w*chunk, (w+1)*chunk) of the row, chunk a multiple of 128, lane L the quads
 // 4L..4L+3 of each 128 keys: the output is written in index order with one warp scan per
-// 128 keys.
-template <int kThreads, int kCand>
+// 128 keys. kStaged false (many rows too long to stage several per SM): nothing is staged and
+// each pass re-reads the row (from L2 after the first), so that several rows share an SM.
+template <int kThreads, int kCand, bool kStaged>
 __global__ void __launch_bounds__(kThreads, 2048 / kThreads) topk_lin_kernel(TopkArgs a) {
     constexpr int kWarps = kThreads / 32;
     extern __shared__ uint32_t skeys[];
@@ -643,10 +645,23 @@ __global__ void __launch_bounds__(kThreads, 2048 / kThreads) topk_lin_kernel(Top
     const int n4 = vis >> 2;
     const float4* row4 = reinterpret_cast<const float4*>(row);
     uint4* sk4 = reinterpret_cast<uint4*>(skeys);
+    // the keys of quad j / key i: staged, or read again
+    auto key4 = [&](int j) -> uint4 {
+        if constexpr (kStaged) {
+            return sk4[j];
+        } else {
+            const float4 v = row4[j];
+            return make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
+        }
+    };
+    auto key_at = [&](int i) -> uint32_t {
+        if constexpr (kStaged) return skeys[i];
+        else return order_key(row[i]);
+    };
     uint32_t kmin = 0xffffffffu, kmax = 0u;
     auto put4 = [&](int j, const float4 v) {
         const uint4 k = make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
-        sk4[j] = k;
+        if constexpr (kStaged) sk4[j] = k;
         kmin = min(kmin, min(min(k.x, k.y), min(k.z, k.w)));
         kmax = max(kmax, max(max(k.x, k.y), max(k.z, k.w)));
     };
@@ -661,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 2048 / kThreads) topk_lin_kernel(Top
         if ((int)threadIdx.x < (vis & 3)) {
             const int i = 4 * n4 + threadIdx.x;
             const uint32_t key = order_key(row[i]);
-            skeys[i] = key;
+            if constexpr (kStaged) skeys[i] = key;
             kmin = min(kmin, key);
             kmax = max(kmax, key);
         }
@@ -688,13 +703,13 @@ __global__ void __launch_bounds__(kThreads, 2048 / kThreads) topk_lin_kernel(Top
         return __float_as_uint(__fadd_rd(x, 8388608.0f)) - 0x4b000000u;
     };
     for (int j = threadIdx.x; j < n4; j += kThreads) {
-        const uint4 k = sk4[j];
+        const uint4 k = key4(j);
         atomicAdd(&hist[bin_of(k.x)], 1u);
         atomicAdd(&hist[bin_of(k.y)], 1u);
         atomicAdd(&hist[bin_of(k.z)], 1u);
         atomicAdd(&hist[bin_of(k.w)], 1u);
     }
-    if ((int)threadIdx.x < (vis & 3)) atomicAdd(&hist[bin_of(skeys[4 * n4 + threadIdx.x])], 1u);
+    if ((int)threadIdx.x < (vis & 3)) atomicAdd(&hist[bin_of(key_at(4 * n4 + threadIdx.x))], 1u);
     __syncthreads();
     uint32_t b0, above;
     select_bin<kThreads>(hist, 2048, (uint32_t)a.k, warp_sums, sel, b0, above);
@@ -707,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 2048 / kThreads) topk_lin_kernel(Top
     for (int base = wlo; base < whi; base += 128) {
         const int i0 = base + 4 * lane;
         if (i0 >= whi) continue;
-        const uint4 k4 = sk4[i0 >> 2];
+        const uint4 k4 = key4(i0 >> 2);
         const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
         const int nv = min(4, whi - i0);  // valid keys of this quad (4 but at the row's end)
 #pragma unroll
@@ -739,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 2048 / kThreads) topk_lin_kernel(Top
             for (uint32_t j = threadIdx.x; j < nc; j += kThreads) f((int)cand[j], ckey[j]);
         } else {
             for (int i = threadIdx.x; i < vis; i += kThreads) {
-                const uint32_t key = skeys[i];
+                const uint32_t key = key_at(i);
                 if (bin_of(key) == b0) f(i, key);
             }
         }
@@ -835,7 +850,7 @@ __global__ void __launch_bounds__(kThreads, 2048 / kThreads) topk_lin_kernel(Top
         const int i0 = base + 4 * lane;
         uint32_t fg = 0, fe = 0;
         if (i0 < whi) {
-            const uint4 k4 = sk4[i0 >> 2];
+            const uint4 k4 = key4(i0 >> 2);
             const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
             const int nv = min(4, whi - i0);
 #pragma unroll
@@ -884,19 +899,19 @@ cudaError_t launch_form(const TopkArgs& a, cudaStream_t st) {
                       keys);
 }
 
-template <int kThreads, int kCand>
+template <int kThreads, int kCand, bool kStaged>
 cudaError_t launch_lin(const TopkArgs& a, cudaStream_t st) {
-    const size_t smem = (size_t)a.ld * sizeof(uint32_t);
-    cudaError_t e = cudaFuncSetAttribute(topk_lin_kernel<kThreads, kCand>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    const size_t smem = kStaged ? (size_t)a.ld * sizeof(uint32_t) : 0;
+    cudaError_t e = cudaFuncSetAttribute(topk_lin_kernel<kThreads, kCand, kStaged>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(topk_lin_kernel<kThreads, kCand>, dim3((unsigned)a.T), dim3(kThreads), smem, st, a);
+    return launch_pdl(topk_lin_kernel<kThreads, kCand, kStaged>, dim3((unsigned)a.T), dim3(kThreads), smem, st, a);
 }
 
 template <int kThreads, int kCand>
 cudaError_t launch_threads(const TopkArgs& a, cudaStream_t st) {
     const bool vec = a.ld % 4 == 0 && a.ld <= kSmemKeysMax && ((uintptr_t)a.logits & 15) == 0;
-    return vec ? launch_lin<kThreads, kCand>(a, st) : launch_form<kThreads, kCand>(a, st);
+    return vec ? launch_lin<kThreads, kCand, true>(a, st) : launch_form<kThreads, kCand>(a, st);
 }
 
 }  // namespace
@@ -921,6 +936,11 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
     if (a.T <= sms && a.ld % 4 == 0 && ((uintptr_t)a.logits & 15) == 0 && a.max_len <= 16384)
         return a.max_len <= 8192 ? launch_reg<1024, 8>(a, st) : launch_reg<1024, 16>(a, st);
     if (a.T > sms && a.ld <= kNarrowestKeysMax) return launch_threads<256, 512>(a, st);
+    // many rows too long to stage several per SM: four 512-thread rows per SM re-read their
+    // rows from L2 (measured on 32768 rows of up to 36K keys: 3.21 ms against 3.64 ms staged,
+    // one row per SM; 3.24 / 3.63 ms with 256 / 1024 threads)
+    if (a.T > sms && a.ld > kNarrowKeysMax && a.ld % 4 == 0 && ((uintptr_t)a.logits & 15) == 0)
+        return launch_lin<512, 1024, false>(a, st);
     return (a.T > sms && a.ld <= kNarrowKeysMax) ? launch_threads<512, 1024>(a, st)
                                                  : launch_threads<1024, 2048>(a, st);
 }

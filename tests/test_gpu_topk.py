@@ -186,3 +186,22 @@ def test_topk_many_rows_narrowing_fallback(torch, ld_pad):
         rows.append(r)
     L = max(len(r) for r in rows)
     _decode(torch, rows, 1024, ld=(L + 3) // 4 * 4 + ld_pad)
+
+
+@pytest.mark.parametrize("ld_pad", [0, 1])
+def test_topk_many_long_rows(torch, ld_pad):
+    """More rows than SMs, rows longer than 12K keys: aligned rows take the form that stages
+    nothing and re-reads the row on each pass (several rows per SM), unaligned ones the generic
+    form; rows with an outlier, rows of few distinct values (overflowing candidates)."""
+    rng = np.random.default_rng(10)
+    rows = []
+    for i in range(200):
+        n = int(rng.integers(12289, 20000))
+        r = (rng.standard_normal(n) * 2).astype(np.float32)
+        if i % 4 == 1:
+            r[rng.integers(0, n)] = np.float32(-1e30)
+        if i % 6 == 2:
+            r = rng.integers(0, 5, n).astype(np.float32)
+        rows.append(r)
+    L = max(len(r) for r in rows)
+    _decode(torch, rows, 2048, ld=(L + 3) // 4 * 4 + ld_pad)
