@@ -13,7 +13,8 @@
 // before the norm reaching memory): one entry per compress-ratio boundary token.
 //
 // Mapping: 16 threads per 128-element row, 8 consecutive elements (one 16-byte load of
-// bf16) per thread; a 256-thread CTA handles 16 rows. Reductions use a fixed tree (group
+// bf16) per thread; a 256-thread CTA handles 16 K rows, or 32 Q rows of one token (two per
+// 16 threads, sharing the position and the RoPE table row). Reductions use a fixed tree (group
 // of 8 in registers, then xor-butterfly over the 16 lanes), so the result does not depend
 // on the launch shape. Every float operation is an explicitly rounded intrinsic (no FMA
 // contraction), which makes the bytes reproducible on any IEEE implementation.
@@ -26,6 +27,7 @@ namespace {
 
 constexpr int kRowsPerCta = 16;
 constexpr int kThreads = 16 * kRowsPerCta;
+constexpr int kQHeadsPerCta = 2 * kRowsPerCta;  // Q: two rows per 16 lanes
 
 __device__ __forceinline__ float sum8(const float* e) {
     float a = __fadd_rn(e[0], e[1]);
@@ -114,38 +116,78 @@ __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
 
 // RoPE on dims 0..63 (lanes 0..7 of the row). NeoX pairs dims (i, i+32): lane l < 4 holds
 // the first element of its pairs, lane l+4 the second. Interleaved pairs (2i, 2i+1) lie
-// inside one lane. cs = the table row [cos f0..f0+31, sin f0..f0+31] (16-byte aligned).
-__device__ __forceinline__ void rope(float* x, int l16, const float* cs, int mode) {
+// inside one lane. cs = the table row [cos f0..f0+31, sin f0..f0+31] (16-byte aligned). The
+// table loads and the rotation are apart, so that rows of one position share the loads.
+struct RopeCS {
+    float c[8], sn[8];
+};
+
+__device__ __forceinline__ void rope_load(int l16, const float* cs, int mode, RopeCS& r) {
     if (mode == IDX_ROPE_NEOX) {
-        float p[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) p[i] = __shfl_xor_sync(kFull, x[i], 4);
         if (l16 < 8) {
             const int f0 = (8 * l16) & 31;
             const float4 c0 = __ldg(reinterpret_cast<const float4*>(cs + f0));
             const float4 c1 = __ldg(reinterpret_cast<const float4*>(cs + f0 + 4));
             const float4 s0 = __ldg(reinterpret_cast<const float4*>(cs + 32 + f0));
             const float4 s1 = __ldg(reinterpret_cast<const float4*>(cs + 32 + f0 + 4));
-            const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-            const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                if (l16 < 4) x[i] = __fsub_rn(__fmul_rn(x[i], c[i]), __fmul_rn(p[i], sn[i]));  // a' = ac - bs
-                else         x[i] = __fadd_rn(__fmul_rn(x[i], c[i]), __fmul_rn(p[i], sn[i]));  // b' = bc + as
-            }
+            r.c[0] = c0.x; r.c[1] = c0.y; r.c[2] = c0.z; r.c[3] = c0.w;
+            r.c[4] = c1.x; r.c[5] = c1.y; r.c[6] = c1.z; r.c[7] = c1.w;
+            r.sn[0] = s0.x; r.sn[1] = s0.y; r.sn[2] = s0.z; r.sn[3] = s0.w;
+            r.sn[4] = s1.x; r.sn[5] = s1.y; r.sn[6] = s1.z; r.sn[7] = s1.w;
         }
     } else if (mode == IDX_ROPE_INTERLEAVED) {
         if (l16 < 8) {
             const float4 c4 = __ldg(reinterpret_cast<const float4*>(cs + 4 * l16));
             const float4 s4 = __ldg(reinterpret_cast<const float4*>(cs + 32 + 4 * l16));
-            const float c[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
+            r.c[0] = c4.x; r.c[1] = c4.y; r.c[2] = c4.z; r.c[3] = c4.w;
+            r.sn[0] = s4.x; r.sn[1] = s4.y; r.sn[2] = s4.z; r.sn[3] = s4.w;
+        }
+    }
+}
+
+__device__ __forceinline__ void rope_apply(float* x, int l16, int mode, const RopeCS& r) {
+    if (mode == IDX_ROPE_NEOX) {
+        float p[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) p[i] = __shfl_xor_sync(kFull, x[i], 4);
+        if (l16 < 8) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (l16 < 4) x[i] = __fsub_rn(__fmul_rn(x[i], r.c[i]), __fmul_rn(p[i], r.sn[i]));  // a' = ac - bs
+                else         x[i] = __fadd_rn(__fmul_rn(x[i], r.c[i]), __fmul_rn(p[i], r.sn[i]));  // b' = bc + as
+            }
+        }
+    } else if (mode == IDX_ROPE_INTERLEAVED) {
+        if (l16 < 8) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float a = x[2 * q], b = x[2 * q + 1];
-                x[2 * q] = __fsub_rn(__fmul_rn(a, c[q]), __fmul_rn(b, sn[q]));
-                x[2 * q + 1] = __fadd_rn(__fmul_rn(b, c[q]), __fmul_rn(a, sn[q]));
+                x[2 * q] = __fsub_rn(__fmul_rn(a, r.c[q]), __fmul_rn(b, r.sn[q]));
+                x[2 * q + 1] = __fadd_rn(__fmul_rn(b, r.c[q]), __fmul_rn(a, r.sn[q]));
             }
         }
+    }
+}
+
+// One row: the partner elements are exchanged before the table loads (fewer live registers).
+__device__ __forceinline__ void rope(float* x, int l16, const float* cs, int mode) {
+    if (mode == IDX_ROPE_NEOX) {
+        float p[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) p[i] = __shfl_xor_sync(kFull, x[i], 4);
+        if (l16 < 8) {
+            RopeCS r;
+            rope_load(l16, cs, mode, r);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (l16 < 4) x[i] = __fsub_rn(__fmul_rn(x[i], r.c[i]), __fmul_rn(p[i], r.sn[i]));  // a' = ac - bs
+                else         x[i] = __fadd_rn(__fmul_rn(x[i], r.c[i]), __fmul_rn(p[i], r.sn[i]));  // b' = bc + as
+            }
+        }
+    } else if (mode == IDX_ROPE_INTERLEAVED) {
+        RopeCS r;
+        rope_load(l16, cs, mode, r);
+        rope_apply(x, l16, mode, r);
     }
 }
 
@@ -344,31 +386,15 @@ __device__ __forceinline__ void compress_rows(const CompressArgs& a, int64_t blk
     quant_store<kDtype>(x, l16, ok, a.pool + page * a.page_stride, a.page_size, s);
 }
 
-// Q rows: CTA (t, y) takes token t's heads 16y .. 16y+15 of the Hq = H rounded up to 8
-// heads; heads past H write the zero/neutral padding of the tensor-core image (see idx.h
-// for the layout). Hq is a multiple of 8, so the two rows of a warp are live together.
-// Q quant of token t's heads 16y .. 16y+15.
+// Quantise and store Q row (t, h) held 8 values per lane by 16 lanes (x after RoPE); w_in is
+// the row's head weight (lane 0). Heads past H write the zero/neutral padding of the
+// tensor-core image (see idx.h for the layout); a real row whose position was rejected (ok
+// false) writes nothing.
 template <int kDtype>
-__device__ __forceinline__ void q_quant_rows(const QQuantArgs& a, int64_t t, int y) {
+__device__ __forceinline__ void q_store_row(const QQuantArgs& a, int64_t t, int h, int Hq, bool real, bool ok,
+                                            const float* x, float w_in) {
     const int l16 = threadIdx.x & 15;
-    const int Hq = (a.H + 7) & ~7;
-    const int h = y * kRowsPerCta + (threadIdx.x >> 4);
-    if (h >= Hq) return;
-    const bool real = h < a.H;
     const int64_t row = t * a.H + h;  // index of (t, h) in q, w_in, w_out
-    // the Q row and the position are independent loads: issue them together
-    const uint4 raw = real ? __ldg(reinterpret_cast<const uint4*>(a.q + row * 128 + 8 * l16))
-                           : make_uint4(0, 0, 0, 0);
-    int32_t pos = (real && a.rope != IDX_ROPE_NONE) ? __ldg(a.positions + t) : 0;
-    bool ok = real;
-    if (a.rope != IDX_ROPE_NONE && ok && (pos < 0 || pos >= a.max_pos)) {
-        if (l16 == 0) report(a.dev_status, IDX_STATUS_BAD_POS);
-        ok = false;
-    }
-    if (!ok) pos = 0;
-    float x[8];
-    unpack8(ok ? raw : make_uint4(0, 0, 0, 0), x);
-    if (a.rope != IDX_ROPE_NONE) rope(x, l16, a.cos_sin + (int64_t)pos * 64, a.rope);
     if (kDtype == IDX_MXFP4) {
         uint32_t word, sbyte;
         mx_quant(x, word, sbyte);
@@ -388,7 +414,7 @@ __device__ __forceinline__ void q_quant_rows(const QQuantArgs& a, int64_t t, int
             if (l16 == 0) {
                 uint8_t* atom = reinterpret_cast<uint8_t*>(a.q_scales) + t * 512 + (h & 31) * 16 + (h >> 5) * 4;
                 *reinterpret_cast<uint32_t*>(atom) = real ? (sbyte | (s1 << 8) | (s2 << 16) | (s3 << 24)) : 0x7f7f7f7fu;
-                if (real) a.w_out[row] = __fmul_rn(__ldg(a.w_in + row), a.fold);
+                if (real) a.w_out[row] = __fmul_rn(w_in, a.fold);
             }
         }
     } else {
@@ -404,9 +430,50 @@ __device__ __forceinline__ void q_quant_rows(const QQuantArgs& a, int64_t t, int
                 *reinterpret_cast<uint4*>(img) = real ? make_uint4(lo, hi, plo, phi) : make_uint4(0, 0, 0, 0);
             if (l16 == 0 && real) {
                 if (a.q_scales) reinterpret_cast<float*>(a.q_scales)[row] = scale;
-                a.w_out[row] = __fmul_rn(__fmul_rn(__ldg(a.w_in + row), a.fold), scale);
+                a.w_out[row] = __fmul_rn(__fmul_rn(w_in, a.fold), scale);
             }
         }
+    }
+}
+
+// Q rows: CTA (t, y) takes token t's heads hpc*y .. hpc*y + hpc-1 of the Hq = H rounded up to
+// 8 heads, hpc = 16 (one row per 16 lanes) or 32 (two: heads h and h + 16, whose loads -- the
+// two rows, their weights, the position and the RoPE table row they share -- all go out
+// before either row is worked on; more rows in flight per SM, a longer chain per CTA). Hq is
+// a multiple of 8, so the rows of a warp are live together.
+template <int kDtype>
+__device__ __forceinline__ void q_quant_rows(const QQuantArgs& a, int64_t t, int y, int hpc) {
+    const int l16 = threadIdx.x & 15;
+    const int Hq = (a.H + 7) & ~7;
+    const int h0 = y * hpc + (threadIdx.x >> 4), h1 = h0 + 16;
+    if (h0 >= Hq) return;
+    const bool two = hpc == kQHeadsPerCta && h1 < Hq;
+    const bool real0 = h0 < a.H, real1 = two && h1 < a.H;  // real1 implies real0
+    const int64_t row0 = t * a.H + h0, row1 = t * a.H + h1;
+    const uint4 raw0 = real0 ? __ldg(reinterpret_cast<const uint4*>(a.q + row0 * 128 + 8 * l16))
+                             : make_uint4(0, 0, 0, 0);
+    const uint4 raw1 = real1 ? __ldg(reinterpret_cast<const uint4*>(a.q + row1 * 128 + 8 * l16))
+                             : make_uint4(0, 0, 0, 0);
+    const float w0 = (real0 && l16 == 0) ? __ldg(a.w_in + row0) : 0.0f;
+    const float w1 = (real1 && l16 == 0) ? __ldg(a.w_in + row1) : 0.0f;
+    int32_t pos = (real0 && a.rope != IDX_ROPE_NONE) ? __ldg(a.positions + t) : 0;
+    bool pos_ok = true;
+    if (a.rope != IDX_ROPE_NONE && real0 && (pos < 0 || pos >= a.max_pos)) {
+        if (l16 == 0) report(a.dev_status, IDX_STATUS_BAD_POS);
+        pos_ok = false;
+    }
+    const bool ok0 = real0 && pos_ok, ok1 = real1 && pos_ok;
+    if (!ok0) pos = 0;  // a rejected or padding row is zeros, rotated by the table's row 0
+    RopeCS cs;
+    if (a.rope != IDX_ROPE_NONE) rope_load(l16, a.cos_sin + (int64_t)pos * 64, a.rope, cs);
+    float x[8];
+    unpack8(ok0 ? raw0 : make_uint4(0, 0, 0, 0), x);
+    if (a.rope != IDX_ROPE_NONE) rope_apply(x, l16, a.rope, cs);
+    q_store_row<kDtype>(a, t, h0, Hq, real0, ok0, x, w0);
+    if (two) {
+        unpack8(ok1 ? raw1 : make_uint4(0, 0, 0, 0), x);
+        if (a.rope != IDX_ROPE_NONE) rope_apply(x, l16, a.rope, cs);
+        q_store_row<kDtype>(a, t, h1, Hq, real1, ok1, x, w1);
     }
 }
 
@@ -419,15 +486,16 @@ __global__ void __launch_bounds__(kThreads) k_store_kernel(KStoreArgs a) {
 }
 
 template <int kDtype>
-__global__ void __launch_bounds__(kThreads) q_quant_kernel(QQuantArgs a) {
+__global__ void __launch_bounds__(kThreads) q_quant_kernel(QQuantArgs a, int hpc) {
     pdl_launch_dependents();
-    q_quant_rows<kDtype>(a, blockIdx.x, blockIdx.y);
+    q_quant_rows<kDtype>(a, blockIdx.x, blockIdx.y, hpc);
 }
 
 // K store and Q quant in one launch: blocks [0, nk) store K rows, the rest quantise Q (block
 // nk + t*ny + y takes token t's head block y). The two halves touch disjoint buffers.
 template <int kDtype>
-__global__ void __launch_bounds__(kThreads) qk_prep_kernel(KStoreArgs ka, QQuantArgs qa, int64_t nk, int ny) {
+__global__ void __launch_bounds__(kThreads) qk_prep_kernel(KStoreArgs ka, QQuantArgs qa, int64_t nk, int ny,
+                                                           int hpc) {
     pdl_launch_dependents();
     const int64_t b = blockIdx.x;
     if (b < nk) {
@@ -436,7 +504,7 @@ __global__ void __launch_bounds__(kThreads) qk_prep_kernel(KStoreArgs ka, QQuant
         // ny = 1..4 and the grid is below 2^31: a 32-bit divide by a constant
         const uint32_t i = (uint32_t)(b - nk);
         const uint32_t t = ny == 1 ? i : (ny == 2 ? i >> 1 : (ny == 4 ? i >> 2 : i / 3u));
-        q_quant_rows<kDtype>(qa, t, (int)(i - t * (uint32_t)ny));
+        q_quant_rows<kDtype>(qa, t, (int)(i - t * (uint32_t)ny), hpc);
     }
 }
 
@@ -464,24 +532,41 @@ cudaError_t launch_k_store(const KStoreArgs& a, cudaStream_t st) {
                                 : launch_pdl(k_store_kernel<IDX_FP8>, dim3((unsigned)grid), dim3(kThreads), 0, st, a);
 }
 
+namespace {
+
+// Heads per Q CTA: 16 while the Q CTAs fit on the GPU at once (one row per 16 lanes, the
+// shortest chain: decode steps), else 32 (two rows per 16 lanes, more rows in flight: prefill).
+// Measured: 8192 tokens x 32 heads 40.5 -> 33.5 us with 32; 64 tokens 1.3 -> 1.6 us.
+int q_heads_per_cta(int64_t T, int Hq) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 1;
+    const int64_t ctas16 = T * ((Hq + kRowsPerCta - 1) / kRowsPerCta);
+    return ctas16 <= (int64_t)4 * sms ? kRowsPerCta : kQHeadsPerCta;
+}
+
+}  // namespace
+
 cudaError_t launch_q_quant(const QQuantArgs& a, cudaStream_t st) {
     if (a.T == 0) return cudaSuccess;
     const int Hq = (a.H + 7) & ~7;
-    const dim3 grid((unsigned)a.T, (unsigned)((Hq + kRowsPerCta - 1) / kRowsPerCta));
-    return a.dtype == IDX_MXFP4 ? launch_pdl(q_quant_kernel<IDX_MXFP4>, grid, dim3(kThreads), 0, st, a)
-                                : launch_pdl(q_quant_kernel<IDX_FP8>, grid, dim3(kThreads), 0, st, a);
+    const int hpc = q_heads_per_cta(a.T, Hq);
+    const dim3 grid((unsigned)a.T, (unsigned)((Hq + hpc - 1) / hpc));
+    return a.dtype == IDX_MXFP4 ? launch_pdl(q_quant_kernel<IDX_MXFP4>, grid, dim3(kThreads), 0, st, a, hpc)
+                                : launch_pdl(q_quant_kernel<IDX_FP8>, grid, dim3(kThreads), 0, st, a, hpc);
 }
 
 cudaError_t launch_qk_prep(const KStoreArgs& ka, const QQuantArgs& qa, cudaStream_t st) {
     const int64_t nk = (ka.n_rows + kRowsPerCta - 1) / kRowsPerCta;
     const int Hq = (qa.H + 7) & ~7;
-    const int ny = (Hq + kRowsPerCta - 1) / kRowsPerCta;
+    const int hpc = q_heads_per_cta(qa.T, Hq);
+    const int ny = (Hq + hpc - 1) / hpc;
     const int64_t grid = nk + qa.T * ny;
     if (grid == 0) return cudaSuccess;
     if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
     return ka.dtype == IDX_MXFP4
-               ? launch_pdl(qk_prep_kernel<IDX_MXFP4>, dim3((unsigned)grid), dim3(kThreads), 0, st, ka, qa, nk, ny)
-               : launch_pdl(qk_prep_kernel<IDX_FP8>, dim3((unsigned)grid), dim3(kThreads), 0, st, ka, qa, nk, ny);
+               ? launch_pdl(qk_prep_kernel<IDX_MXFP4>, dim3((unsigned)grid), dim3(kThreads), 0, st, ka, qa, nk, ny, hpc)
+               : launch_pdl(qk_prep_kernel<IDX_FP8>, dim3((unsigned)grid), dim3(kThreads), 0, st, ka, qa, nk, ny, hpc);
 }
 
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t st) {

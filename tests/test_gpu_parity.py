@@ -156,6 +156,78 @@ def test_store_quant_many_tokens(torch, dtype, fused):
     _check_store_and_quant(wl, f"many tokens dtype={dtype} fused={fused}", fused)
 
 
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("H", [20, 64])
+@pytest.mark.parametrize("rope", [W.ROPE_NEOX, W.ROPE_INTERLEAVED])
+@pytest.mark.parametrize("dtype", [W.MXFP4, W.FP8])
+def test_store_quant_two_q_rows_per_lanes(torch, dtype, rope, H, fused):
+    """Enough tokens for the Q launch that gives each 16 lanes two heads (h, h + 16) sharing one
+    position: padded head counts (20 -> 24, the second rows partly padding) and 64 heads (two
+    head blocks per token), both RoPE layouts, bit-exact against the oracle."""
+    rng = np.random.default_rng(78 + H)
+    n, P = 700, 64
+    pages = (n + P - 1) // P + 1
+    perm = rng.permutation(pages).astype(np.int32)
+    slots = perm[np.arange(n) // P].astype(np.int64) * P + np.arange(n) % P
+    wl = W.Workload(
+        name="two_rows", dtype=dtype, B=1, H=H, page_size=P, pool_pages=pages, base_offset_pages=0,
+        page_stride=W.page_bytes(dtype, P), seq_lens_k=np.array([n], np.int32),
+        cu_seqlens_q=np.array([0, n], np.int32), page_table=perm[None, :], causal=1, topk=8,
+        k=W.bf16_bits(rng.standard_normal((n, 128)).astype(np.float32)), slot_mapping=slots,
+        k_positions=rng.integers(0, 3000, n).astype(np.int32), k_rope=rope, k_norm=1, step_rows=np.arange(n),
+        q=W.bf16_bits((rng.standard_normal((n, H, 128)) * 3).astype(np.float32)),
+        q_positions=rng.integers(0, 3000, n).astype(np.int32), q_rope=rope,
+        w_in=rng.standard_normal((n, H)).astype(np.float32), softmax_scale=0.088388, head_scale=0.75,
+        cos_sin=W.rope_table(3000), ld_logits=n)
+    _check_store_and_quant(wl, f"two rows H={H} rope={rope} dtype={dtype} fused={fused}", fused)
+
+
+@pytest.mark.parametrize("n", [8, 700])
+@pytest.mark.parametrize("dtype", [W.MXFP4, W.FP8])
+def test_q_bad_position_sets_status(torch, dtype, n):
+    """A query token whose position lies beyond the RoPE table: IDX_STATUS_BAD_POS, its real
+    head rows and weights left untouched, its padding rows written; every other token
+    bit-exact. Few tokens (one Q row per 16 lanes) and many (two per 16 lanes)."""
+    from sparse_attention_indexer_mqa_gb300 import binding as Bn
+    rng = np.random.default_rng(90 + n)
+    H, P, bad = 20, 64, 3
+    pages = (n + P - 1) // P + 1
+    perm = rng.permutation(pages).astype(np.int32)
+    slots = perm[np.arange(n) // P].astype(np.int64) * P + np.arange(n) % P
+    wl = W.Workload(
+        name="badq", dtype=dtype, B=1, H=H, page_size=P, pool_pages=pages, base_offset_pages=0,
+        page_stride=W.page_bytes(dtype, P), seq_lens_k=np.array([n], np.int32),
+        cu_seqlens_q=np.array([0, n], np.int32), page_table=perm[None, :], causal=1, topk=8,
+        k=W.bf16_bits(rng.standard_normal((n, 128)).astype(np.float32)), slot_mapping=slots,
+        k_positions=np.arange(n, dtype=np.int32), k_rope=W.ROPE_NEOX, k_norm=1, step_rows=np.arange(n),
+        q=W.bf16_bits(rng.standard_normal((n, H, 128)).astype(np.float32)),
+        q_positions=rng.integers(0, 1000, n).astype(np.int32), q_rope=W.ROPE_NEOX,
+        w_in=rng.standard_normal((n, H)).astype(np.float32), softmax_scale=0.088388, head_scale=1.0,
+        cos_sin=W.rope_table(1000), ld_logits=n)
+    qc, qs, w = oracle_q(wl)
+    d = Dev(wl)
+    d.qpos[bad] = 10 ** 6
+    d.w.fill_(-3.0)
+    d.quant()
+    assert int(d.host("status")[0]) & Bn.IDX_STATUS_BAD_POS
+    codes = d.host("q_codes")
+    Hq = (H + 7) // 8 * 8
+    kc = 4 if dtype == W.MXFP4 else 8
+    plain = codes.reshape(n, Hq // 8, kc, 8, 16).transpose(0, 1, 3, 2, 4).reshape(n, Hq, kc * 16)
+    assert (plain[bad, :H] == 0xEE).all(), "the rejected token's rows were written"
+    assert not plain[bad, H:].any(), "the rejected token's padding rows must be zero"
+    assert (d.host("w")[bad] == -3.0).all(), "the rejected token's weights were written"
+    ok = np.setdiff1d(np.arange(n), [bad])
+    codes[bad] = 0  # the rejected token is checked above; the rest through the plain layout
+    gc, gs = q_image_to_plain(codes, d.host("q_scales"), H, dtype)
+    np.testing.assert_array_equal(gc[ok], qc[ok])
+    if dtype == W.MXFP4:
+        np.testing.assert_array_equal(gs[ok], qs[ok])
+    else:
+        np.testing.assert_array_equal(d.host("q_scales").view(np.uint32)[ok], qs.view(np.uint32)[ok])
+    np.testing.assert_array_equal(d.host("w").view(np.uint32)[ok], w.view(np.uint32)[ok])
+
+
 def test_qk_prep_one_side_empty(torch):
     """idx_qk_prep with no K rows only quantises Q; with no queries only stores K."""
     import torch as T
