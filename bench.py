@@ -653,11 +653,11 @@ def run_e2e(rep, args, torch, stream, world, dev):
     rows, slots, positions, Q, positions, weights: one packed pinned host buffer) to the device
     in one H2D copy and reads its top-k indices back in one D2H copy.
 
-    Pipelined (the reported value): uploads and read-backs run on two more streams with two
-    device input buffers and two top-k buffers used in turn, so step i+1's upload and step
-    i's read-back overlap each other and step i's kernels, which stay in order on the
-    compute stream. Serial (reported
-    beside it): upload, kernels and read-back of each step one after the other."""
+    Pipelined: uploads and read-backs run on two more streams with two device input buffers
+    and two top-k buffers used in turn, so step i+1's upload and step i's read-back overlap each
+    other and step i's kernels, which stay in order on the compute stream. Serial: upload,
+    kernels and read-back of each step one after the other. Both are timed; the value is the
+    faster."""
     wl = rep.wl
     sr = wl.step_rows
     parts = [("k", wl.k[sr].view(np.int16), torch.int16), ("slot", wl.slot_mapping[sr], torch.int64),
@@ -747,14 +747,20 @@ def run_e2e(rep, args, torch, stream, world, dev):
     for h in h_tops[: min(2, args.steps)]:
         if not torch.equal(h, ref):
             raise RuntimeError("pipelined end-to-end steps returned a different top-k")
-    return {"value": round(job_rate(wl.pairs(), ms, world), 1), "unit": "K-tokens/s",
-            "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(h2d),
+    # the value is the faster of the two schedules (both copy every step's inputs and results;
+    # with very large copies the overlapped one can lose)
+    best = min(ms, ms_serial)
+    return {"value": round(job_rate(wl.pairs(), best, world), 1), "unit": "K-tokens/s",
+            "ms_per_step": round(best, 5), "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h),
+            "schedule": "pipelined" if ms <= ms_serial else "serial",
+            "pipelined_ms_per_step": round(ms, 5),
             "serial_ms_per_step": round(ms_serial, 5),
             "how": "K steps in one CUDA graph; each step: one packed H2D of its inputs from pinned "
-                   "host, 3 library calls, one D2H of its top-k; uploads and read-backs on their "
-                   "own streams with double-buffered inputs/outputs overlap each other and the "
-                   "neighbouring steps' kernels (serial_ms_per_step: the same with no overlap)"}
+                   "host, 3 library calls, one D2H of its top-k. pipelined: uploads and read-backs "
+                   "on their own streams with double-buffered inputs/outputs overlap each other and "
+                   "the neighbouring steps' kernels; serial: upload, kernels and read-back one after "
+                   "the other; value and ms_per_step: the faster of the two"}
 
 
 # ----------------------------------------------------------------------------------------
