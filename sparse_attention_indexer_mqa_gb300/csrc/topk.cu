@@ -762,7 +762,8 @@ __global__ void __launch_bounds__(kThreads, 2048 / kThreads) topk_lin_kernel(Top
 
     // 4. the k-th key: the remaining-th largest of bin b0's keys
     uint32_t kth;
-    if (listed && nc <= (uint32_t)kThreads) {
+    const bool ranked = listed && nc <= (uint32_t)kThreads;  // the k-th key by direct ranking
+    if (ranked) {
         if (threadIdx.x < nc) {
             const uint32_t mine = ckey[threadIdx.x];
             uint32_t gt = 0, ge = 0;
@@ -819,6 +820,60 @@ __global__ void __launch_bounds__(kThreads, 2048 / kThreads) topk_lin_kernel(Top
         kth = prefix;
     }
 
+    if (ranked) {
+        // 5'. the keys equal to the k-th are all listed: the first `remaining` of them by index
+        //     go to the end of the output, each placed by its rank among them; the pass over
+        //     the row then writes only the keys above the k-th
+        const uint32_t n_gt = (uint32_t)a.k - remaining;
+        if (threadIdx.x < nc && ckey[threadIdx.x] == kth) {
+            const int mine = cand[threadIdx.x];
+            uint32_t r = 0;
+            for (uint32_t j = 0; j < nc; ++j) r += ckey[j] == kth && cand[j] < mine;
+            if (r < remaining) out[n_gt + r] = mine;
+        }
+        for_each_cand([&](int i, uint32_t k) {
+            if (k > kth) atomicAdd(&warp_gt[i / chunk], 1u);
+        });
+        __syncthreads();
+        uint32_t og, c_gt;
+        {
+            const uint32_t g = lane < kWarps ? warp_gt[lane] : 0u;
+            uint32_t ig = g;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(kFull, ig, o);
+                if (lane >= o) ig += y;
+            }
+            og = __shfl_sync(kFull, ig - g, warp);
+            c_gt = __shfl_sync(kFull, g, warp);
+        }
+        for (int base = wlo; base < whi && c_gt > 0; base += 128) {
+            const int i0 = base + 4 * lane;
+            const int nv = i0 < whi ? min(4, whi - i0) : 0;
+            uint32_t fg = 0;
+            if (nv > 0) {
+                const uint4 k4 = key4(i0 >> 2);
+                fg = ((uint32_t)(k4.x > kth) | ((uint32_t)(k4.y > kth) << 1) | ((uint32_t)(k4.z > kth) << 2) |
+                      ((uint32_t)(k4.w > kth) << 3)) & ((1u << nv) - 1u);
+            }
+            const uint32_t cnt = (uint32_t)__popc(fg);
+            uint32_t inc = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(kFull, inc, o);
+                if (lane >= o) inc += y;
+            }
+            const uint32_t tot = __shfl_sync(kFull, inc, 31);
+            int32_t* dst = out + og + (inc - cnt);
+            if (fg & 1u) *dst++ = i0;
+            if (fg & 2u) *dst++ = i0 + 1;
+            if (fg & 4u) *dst++ = i0 + 2;
+            if (fg & 8u) *dst = i0 + 3;
+            og += tot;
+            c_gt -= tot;
+        }
+        return;
+    }
     // 5. bin b0's keys above / equal to the k-th complete the per-warp counts; one scan over
     //    the warps places each warp's output, written in index order
     for_each_cand([&](int i, uint32_t k) {
