@@ -702,14 +702,25 @@ __global__ void __launch_bounds__(kThreads, 2048 / kThreads) topk_lin_kernel(Top
         const float x = fminf((value_of(k) - vlo) * scale, 2047.0f);
         return __float_as_uint(__fadd_rd(x, 8388608.0f)) - 0x4b000000u;
     };
-    for (int j = threadIdx.x; j < n4; j += kThreads) {
-        const uint4 k = key4(j);
-        atomicAdd(&hist[bin_of(k.x)], 1u);
-        atomicAdd(&hist[bin_of(k.y)], 1u);
-        atomicAdd(&hist[bin_of(k.z)], 1u);
-        atomicAdd(&hist[bin_of(k.w)], 1u);
-    }
-    if ((int)threadIdx.x < (vis & 3)) atomicAdd(&hist[bin_of(key_at(4 * n4 + threadIdx.x))], 1u);
+    // the histogram and candidate passes run in one of two instances, linear bins or top key
+    // bits, so that the per-key bin function has no branch
+    auto bin_lin = [&](uint32_t k) -> uint32_t {
+        const float x = fminf((value_of(k) - vlo) * scale, 2047.0f);
+        return __float_as_uint(__fadd_rd(x, 8388608.0f)) - 0x4b000000u;
+    };
+    auto bin_top = [](uint32_t k) -> uint32_t { return k >> 21; };
+    auto hist_pass = [&](auto binf) {
+        for (int j = threadIdx.x; j < n4; j += kThreads) {
+            const uint4 k = key4(j);
+            atomicAdd(&hist[binf(k.x)], 1u);
+            atomicAdd(&hist[binf(k.y)], 1u);
+            atomicAdd(&hist[binf(k.z)], 1u);
+            atomicAdd(&hist[binf(k.w)], 1u);
+        }
+        if ((int)threadIdx.x < (vis & 3)) atomicAdd(&hist[binf(key_at(4 * n4 + threadIdx.x))], 1u);
+    };
+    if (linear) hist_pass(bin_lin);
+    else hist_pass(bin_top);
     __syncthreads();
     uint32_t b0, above;
     select_bin<kThreads>(hist, 2048, (uint32_t)a.k, warp_sums, sel, b0, above);
@@ -719,27 +730,34 @@ __global__ void __launch_bounds__(kThreads, 2048 / kThreads) topk_lin_kernel(Top
     const int chunk = ((vis + kWarps - 1) / kWarps + 127) & ~127;
     const int wlo = min(vis, chunk * warp), whi = min(vis, wlo + chunk);
     uint32_t c_hi = 0;
-    for (int base = wlo; base < whi; base += 128) {
-        const int i0 = base + 4 * lane;
-        if (i0 >= whi) continue;
-        const uint4 k4 = key4(i0 >> 2);
-        const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
-        const int nv = min(4, whi - i0);  // valid keys of this quad (4 but at the row's end)
+    auto cand_pass = [&](auto binf) {
+        for (int base = wlo; base < whi; base += 128) {
+            const int i0 = base + 4 * lane;
+            if (i0 >= whi) continue;
+            const uint4 k4 = key4(i0 >> 2);
+            const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+            const int nv = min(4, whi - i0);  // valid keys of this quad (4 but at the row's end)
+            uint32_t bn[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            if (e < nv) {
-                const uint32_t bn = bin_of(kk[e]);
-                c_hi += bn > b0;
-                if (bn == b0) {
-                    const uint32_t p = atomicAdd(&scal[0], 1u);
-                    if (p < (uint32_t)kCand) {
-                        cand[p] = i0 + e;
-                        ckey[p] = kk[e];
+            for (int e = 0; e < 4; ++e) bn[e] = e < nv ? binf(kk[e]) : 0u;  // bin 0 <= b0: not counted
+#pragma unroll
+            for (int e = 0; e < 4; ++e) c_hi += bn[e] > b0;
+            if (((bn[0] == b0) | (bn[1] == b0) | (bn[2] == b0) | (bn[3] == b0)) != 0) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (e < nv && bn[e] == b0) {
+                        const uint32_t p = atomicAdd(&scal[0], 1u);
+                        if (p < (uint32_t)kCand) {
+                            cand[p] = i0 + e;
+                            ckey[p] = kk[e];
+                        }
                     }
                 }
             }
         }
-    }
+    };
+    if (linear) cand_pass(bin_lin);
+    else cand_pass(bin_top);
     c_hi = __reduce_add_sync(kFull, c_hi);
     if (lane == 0) {
         warp_gt[warp] = c_hi;
