@@ -205,3 +205,23 @@ def test_topk_many_long_rows(torch, ld_pad):
         rows.append(r)
     L = max(len(r) for r in rows)
     _decode(torch, rows, 2048, ld=(L + 3) // 4 * 4 + ld_pad)
+
+
+@pytest.mark.parametrize("n_rows", [64, 300])
+def test_topk_kth_value_repeated(torch, n_rows):
+    """The k-th value has several copies and k cuts through them (few enough for the direct
+    ranking): the lowest-indexed copies are taken, placed after the keys above it. Few rows
+    (the register form) and many (the shared-memory linear form)."""
+    rng = np.random.default_rng(11)
+    k = 1024
+    rows = []
+    for i in range(n_rows):
+        n = int(rng.integers(3000, 8000))
+        r = rng.standard_normal(n).astype(np.float32)
+        order = np.argsort(-r, kind="stable")
+        v = r[order[k - 3]]                       # 3rd value from the cut
+        lower = order[k + 10:]                    # positions holding smaller values
+        r[rng.choice(lower, size=2 + i % 5, replace=False)] = v  # extra copies of v
+        rows.append(r)
+    L = max(len(r) for r in rows)
+    _decode(torch, rows, k, ld=(L + 3) // 4 * 4)
