@@ -837,7 +837,8 @@ def run_reference(args, rank, world):
     wl = W.make(args.config, seed=args.seed)
     n_threads = os.cpu_count() or 1
     pool = oracle_pool(wl)
-    rows = sample_rows(wl, args.ref_rows)
+    # decode: every query of the step (the GPU arm's exact workload); prefill: an even sample
+    rows = sample_rows(wl, None if is_decode(wl) else args.ref_rows)
     for _ in range(args.warmup):
         oracle_step(wl, pool, rows, n_threads)
     t0 = time.perf_counter()
@@ -903,7 +904,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ref-rows", type=int, default=8)
+    ap.add_argument("--ref-rows", type=int, default=8,
+                    help="query rows per step of the reference arm on prefill configs (decode: all)")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill block of the default run")
     ap.add_argument("--no-probe", action="store_true", help="skip the tensor-core rate probe")
     ap.add_argument("--no-compress", action="store_true", help="skip the compressed K store block")
